@@ -1,0 +1,620 @@
+"""Benchmark of one EAGLE-3 draft-and-verify round on synthetic data.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config 8b|tiny|batched|long|70b] [--impl ours|reference]
+
+A step is one whole round: fuse -> expand x D -> tree_build_mask -> tree_verify_attn
+x L -> lmhead_logits -> spec_accept -> kv_compact (all L layers), over one batch of
+synthetic input that is resident in HBM.  The K timed steps are one CUDA graph of K
+rounds (each round first resets kv_len, so every step does the same work).  Inputs
+exceed L2: the per-layer KV (276 MB at 8B) and the 1.05 GB LM head stream from HBM
+in every step.  --impl reference times the CPU oracle on a bounded sample instead.
+Multi-GPU: replicas only (independent requests per GPU, no collective on the path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+CONFIGS = {
+    "tiny": dict(B=1, P=[128], N=14, D=3, k=2, W=1 << 20, H=4, KVH=4, hd=64, d=256, V=1024, L=1, dtype="f32",
+                 temps=[1.0], noise=1.0,
+                 workload="tiny fp32 single-layer target: d=256, 4x64 heads, vocab 1024, batch 1, prefix 128, "
+                          "depth 3, top-k 2 (14 nodes)"),
+    "8b": dict(B=1, P=[2048], N=60, D=6, k=10, W=10, H=32, KVH=8, hd=128, d=4096, V=128256, L=32, dtype="bf16",
+               temps=[1.0], noise=1.0,
+               workload="Llama-3.1-8B-shaped verify round, bf16: d=4096, 32/8 heads x 128, vocab 128256, batch 1, "
+                        "prefix 2048, 60-node depth-6 tree, top-k 10, 32 layers, fusion 12288->4096, temp 1"),
+    "batched": dict(B=32, P="uniform:512:8192", N=60, D=6, k=10, W=10, H=32, KVH=8, hd=128, d=4096, V=128256,
+                    L=32, dtype="bf16", temps="mixed", noise=1.0,
+                    workload="batched serving, 8B shape, bf16: 32 requests, prefix U[512,8192], 60-node depth-6 "
+                             "trees, mixed greedy/temp-1, ragged 64-token pages"),
+    "long": dict(B=1, P=[65536], N=32, D=7, k=4, W=4, H=32, KVH=8, hd=128, d=4096, V=128256, L=32, dtype="bf16",
+                 temps=[0.7], noise=2.0,
+                 workload="long-context agent shape, 8B dims, bf16: batch 1, prefix 65536, 32-node depth-7 tree, "
+                          "top-k 4, draft noise N(0,2), temp 0.7"),
+    "70b": dict(B=8, P=[4096] * 8, N=60, D=6, k=10, W=10, H=64, KVH=8, hd=128, d=8192, V=128256, L=80,
+                dtype="bf16", temps=[1.0], noise=1.0,
+                workload="Llama-3-70B-shaped verify round, bf16: d=8192, 64/8 heads x 128, vocab 128256, batch 8, "
+                         "prefix 4096, fusion 24576->8192, 60-node depth-6 tree, temp 1, 80 layers"),
+}
+METRIC = "tree-verify rounds/s & nodes/s (8B-shape, 60-node tree); % HBM/tensor roofline"
+TAB_ROWS = 4096  # token-keyed Q/K/V tables of the synthetic target (token id modulo this)
+
+
+def cfg_values(name, seed):
+    c = dict(CONFIGS[name])
+    rng = np.random.default_rng(seed)
+    if isinstance(c["P"], str):
+        lo, hi = (int(x) for x in c["P"].split(":")[1:])
+        c["P"] = [int(x) for x in rng.integers(lo, hi + 1, c["B"])]
+    if c["temps"] == "mixed":
+        c["temps"] = [0.0 if b % 2 == 0 else 1.0 for b in range(c["B"])]
+    return c
+
+
+# ---------------------------------------------------------------------------
+# synthetic workload on the GPU
+# ---------------------------------------------------------------------------
+
+class Workload:
+    def __init__(self, name, seed=0, device="cuda"):
+        import torch
+
+        from eagle_speculative_decoding_round_gb300 import eagle3 as e3
+        from eagle_speculative_decoding_round_gb300 import synth
+        from eagle_speculative_decoding_round_gb300.round import RoundBuffers, RoundConfig
+
+        self.torch, self.e3, self.synth = torch, e3, synth
+        c = cfg_values(name, seed)
+        self.name, self.c, self.seed = name, c, seed
+        R = c["N"] + 1
+        self.cfg = RoundConfig(B=c["B"], N=c["N"], D=c["D"], k=c["k"], W=c["W"], H=c["H"], KVH=c["KVH"],
+                               hd=c["hd"], d=c["d"], V=c["V"], L=c["L"], max_kv_len=max(c["P"]), dtype=c["dtype"])
+        pt, npages = synth.page_table(seed, [p + R for p in c["P"]], self.cfg.page_size)
+        self.pt = pt
+        self.bufs = b = RoundBuffers(self.cfg, torch.from_numpy(pt), npages, device)
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        self.gen = g
+        td = self.cfg.tdtype
+
+        def randn(shape, std):
+            return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std).to(td)
+
+        for l in range(c["L"]):
+            b.K[l].copy_(randn(b.K[l].shape, 1.0))
+            b.Vc[l].copy_(randn(b.Vc[l].shape, 1.0))
+        for t in b.h:
+            t.copy_(randn(t.shape, 0.02))
+        b.W_f.copy_(randn(b.W_f.shape, 0.02))
+        b.W_lm.copy_(randn(b.W_lm.shape, 1.0 / math.sqrt(self.cfg.H * self.cfg.hd)))
+        self.Qtab = randn((TAB_ROWS, c["H"], c["hd"]), 1.0)
+        self.Ktab = randn((TAB_ROWS, c["KVH"], c["hd"]), 1.0)
+        self.Vtab = randn((TAB_ROWS, c["KVH"], c["hd"]), 1.0)
+        self.kv_len0 = torch.tensor(c["P"], dtype=torch.int32, device=device)
+        b.kv_len.copy_(self.kv_len0)
+        rt = np.random.default_rng(seed + 1).integers(0, c["V"], c["B"]).astype(np.int32)
+        b.root_tok.copy_(torch.from_numpy(rt))
+        b.set_temperature(torch.tensor(c["temps"], dtype=torch.float32))
+        b.u_acc.copy_(torch.from_numpy(synth.uniforms(seed, synth.PURPOSE_ACCEPT, c["B"], R).view(np.int32)))
+        b.u_bonus.copy_(torch.from_numpy(synth.uniforms(seed, synth.PURPOSE_BONUS, c["B"], R).view(np.int32)))
+        self.calibrate_and_draft()
+
+    # -- token-keyed tree Q/K/V of the synthetic target -----------------------
+    def write_nodes(self, toks, layers, R):
+        """toks [B, R] int64 (device): write Q (given layers) and K/V at slots P..P+R-1."""
+        torch, b, c = self.torch, self.bufs, self.cfg
+        key = toks % TAB_ROWS
+        q = self.Qtab[key]                      # [B, R, H, hd]
+        kk, vv = self.Ktab[key], self.Vtab[key]  # [B, R, KVH, hd]
+        P = self.kv_len0.long()[:, None] + torch.arange(R, device=toks.device)[None]
+        page = torch.gather(b.page_table.long(), 1, P // c.page_size)
+        slot = P % c.page_size
+        for l in layers:
+            if l < len(b.Q) and b.Q[l].shape[1] == R:
+                b.Q[l].copy_(q)
+            b.K[l][page, :, slot, :] = kk
+            b.Vc[l][page, :, slot, :] = vv
+        return q
+
+    def target_logits_of(self, node_tok, node_par, rows):
+        """Target logits of selected nodes of per-request mini-trees, by the library's
+        own verify (last layer) + LM head.  node_tok/node_par: numpy [B, R'];
+        rows: list of (b, i) in output order."""
+        torch, e3, b, c = self.torch, self.e3, self.bufs, self.cfg
+        B, Rm = node_tok.shape
+        q = self.write_nodes(torch.from_numpy(node_tok).long().cuda(), [c.L - 1], Rm)
+        mask = np.zeros((B, Rm, (Rm + 63) // 64), np.uint64)
+        for bb in range(B):
+            for i in range(Rm):
+                j = i
+                while j >= 0:
+                    mask[bb, i, j >> 6] |= np.uint64(1 << (j & 63))
+                    j = int(node_par[bb, j])
+        maskt = torch.from_numpy(mask.view(np.int64)).cuda()
+        O = torch.empty((B, Rm, c.H, c.hd), dtype=c.tdtype, device="cuda")
+        lse = torch.empty((B, Rm, c.H), device="cuda")
+        wsb = e3.eagle3_verify_workspace_bytes(B, Rm, c.H, c.KVH, c.hd, c.max_kv_len, c.dt)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+        e3.tree_verify_attn(q.contiguous(), b.kv[c.L - 1], b.kv_len, maskt, B, Rm, c.H, c.max_kv_len,
+                            1.0 / math.sqrt(c.hd), O, lse, b.dev_err, ws, wsb)
+        sel = torch.tensor([bb * Rm + i for bb, i in rows], device="cuda")
+        h = O.view(B * Rm, c.H * c.hd)[sel].contiguous()
+        M = h.shape[0]
+        z = torch.empty((M, c.V), device="cuda")
+        e3.lmhead_logits(h, b.W_lm, M, c.H * c.hd, c.V, torch.ones(M, device="cuda"), z,
+                         torch.empty(M, device="cuda"), torch.empty(M, dtype=torch.int64, device="cuda"),
+                         torch.empty(M, dtype=torch.int32, device="cuda"), b.dev_err, c.dt)
+        return z
+
+    def calibrate_and_draft(self):
+        """Draft stand-in: at each depth the frontier nodes' target logits (verify +
+        LM head on the frontier's own mini-tree) plus N(0, noise^2) are the draft
+        logits.  W_lm is first scaled so that target logits have std ~ 4."""
+        torch, e3, b, c = self.torch, self.e3, self.bufs, self.cfg
+        B = c.B
+        roots = b.root_tok.cpu().numpy()
+        z = self.target_logits_of(roots[:, None].astype(np.int64), np.full((B, 1), -1), [(bb, 0) for bb in range(B)])
+        scale = 4.0 / float(z.float().std())
+        b.W_lm.copy_((b.W_lm.float() * scale).to(c.tdtype))
+        sizes, n_cand = c.frontier_sizes()
+        paths = [{-1: [int(roots[bb])]} for bb in range(B)]
+        for di, (F, off) in enumerate(sizes):
+            fid = b.f_id[di].cpu().numpy()[:, :F]
+            # per request: mini-tree = root + frontier nodes' ancestors + frontier nodes
+            node_lists = []
+            for bb in range(B):
+                nodes = {(): -1}
+                order = [()]
+                for f in fid[bb]:
+                    p = paths[bb][int(f)][1:]
+                    for depth in range(1, len(p) + 1):
+                        key = tuple(p[:depth])
+                        if key not in nodes:
+                            nodes[key] = len(order)
+                            order.append(key)
+                order.sort(key=lambda t: (len(t), t))
+                node_lists.append(order)
+            Rm = max(len(o) for o in node_lists)
+            tok = np.zeros((B, Rm), np.int64)
+            par = np.full((B, Rm), -1, np.int64)
+            rows = []
+            for bb, order in enumerate(node_lists):
+                index = {key: i for i, key in enumerate(order)}
+                for i, key in enumerate(order):
+                    tok[bb, i] = key[-1] if key else roots[bb]
+                    par[bb, i] = index[key[:-1]] if key else -1
+                for i in range(len(order), Rm):  # padding nodes hang off the root
+                    par[bb, i] = 0
+                for f in fid[bb]:
+                    rows.append((bb, index[tuple(paths[bb][int(f)][1:])]))
+            zt = self.target_logits_of(tok, par, rows).view(B, F, c.V)
+            noise = torch.randn(zt.shape, generator=self.gen, device="cuda") * self.c["noise"]
+            b.draft_logits[di].copy_(zt + noise)
+            e3.eagle3_expand(b.draft_logits[di], B, F, c.V, c.k, c.W, 1.0, b.f_score[di], b.f_id[di], di + 1, off,
+                             b.cand, b.f_id[di + 1], b.f_score[di + 1], b.dev_err)
+            ct, cp = b.c_tok.cpu().numpy(), b.c_parent.cpu().numpy()
+            for bb in range(B):
+                for i in range(off, off + F * c.k):
+                    paths[bb][i] = paths[bb][int(cp[bb, i])] + [int(ct[bb, i])]
+        # the final tree (same every step) and its Q/K/V in every layer
+        e3.tree_build_mask(b.cand, B, n_cand, c.N, b.root_tok, b.kv_len, b.tok, b.parent, b.depth, b.pos, b.mask)
+        self.write_nodes(b.tok.long(), range(c.L), c.R)
+        torch.cuda.synchronize()
+        assert int(b.dev_err.item()) == 0, "device error during setup"
+
+    def round(self, stream=None):
+        from eagle_speculative_decoding_round_gb300.round import run_round
+        self.bufs.kv_len.copy_(self.kv_len0)
+        run_round(self.bufs, stream=stream)
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per round (the units of the roofline)
+# ---------------------------------------------------------------------------
+
+def work_model(w):
+    c, cfg = w.c, w.cfg
+    esz = 2 if cfg.dtype == "bf16" else 4
+    B, R, H, KVH, hd, d, V, L = cfg.B, cfg.R, cfg.H, cfg.KVH, cfg.hd, cfg.d, cfg.V, cfg.L
+    P = c["P"]
+    par = w.bufs.parent.cpu().numpy()
+    anc = 0
+    for bb in range(B):
+        for i in range(R):
+            j = i
+            while j >= 0:
+                anc += 1
+                j = int(par[bb, j])
+    verify_bytes = sum(2 * KVH * hd * esz * (p + R) for p in P) + 2 * B * R * H * hd * esz + B * R * H * 4
+    verify_flops = 4 * H * hd * (sum(R * p for p in P) + anc)
+    M = B * R
+    lm_bytes = V * d * esz + M * d * esz + M * V * 4
+    lm_flops = 2 * M * d * V
+    fuse_bytes = 3 * d * d * esz + 4 * cfg.M * d * esz
+    return dict(verify_bytes=verify_bytes, verify_flops=verify_flops, lm_bytes=lm_bytes, lm_flops=lm_flops,
+                fuse_bytes=fuse_bytes, fuse_flops=2 * cfg.M * 3 * d * d)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ---------------------------------------------------------------------------
+
+def oracle_sample(w, budget_s=20.0):
+    """Time the oracle on a bounded sample of one round of the same workload and
+    scale to a whole round.  Sample: fusion, all expansion depths, tree build,
+    accept and compaction in full; verify attention of request 0 on 1 layer
+    (scaled by L and by the number of requests); LM head on a 1/8 slice of the
+    vocabulary (scaled by 8)."""
+    import torch
+
+    import oracle
+    try:
+        from threadpoolctl import threadpool_info
+        blas_threads = max([x.get("num_threads", 1) for x in threadpool_info()] or [1])
+    except Exception:
+        blas_threads = os.cpu_count()
+    b, cfg = w.bufs, w.cfg
+    f = lambda t: t.float().cpu().numpy() if t.dtype == torch.bfloat16 else t.cpu().numpy()  # noqa: E731
+    B, R, V = cfg.B, cfg.R, cfg.V
+    times = {}
+    t0 = time.perf_counter()
+    hs = [f(t) for t in b.h]
+    Wf = f(b.W_f)
+    t = time.perf_counter()
+    oracle.fuse(*hs, Wf)
+    times["fuse"] = time.perf_counter() - t
+    sizes, n_cand = cfg.frontier_sizes()
+    drafts = [f(x) for x in b.draft_logits]
+    t = time.perf_counter()
+    trees = []
+    for bb in range(B if B <= 2 else 1):
+        c = oracle.new_cands(n_cand)
+        fid, fsc = np.array([-1], np.int32), np.zeros(1, np.float32)
+        for di, (F, off) in enumerate(sizes):
+            fid, fsc = oracle.expand(drafts[di][bb], cfg.k, cfg.W, fsc, fid, di + 1, off, c)
+        trees.append(oracle.build_tree(c, n_cand, cfg.N, int(b.root_tok[bb]), int(w.kv_len0[bb])))
+    times["expand_build"] = (time.perf_counter() - t) * (B / len(trees))
+    K, Vc = f(b.K[cfg.L - 1]), f(b.Vc[cfg.L - 1])
+    Q = f(b.Q[cfg.L - 1])[:1]
+    t = time.perf_counter()
+    O, _ = oracle.tree_verify_attn(Q, K, Vc, w.pt[:1], w.kv_len0.cpu().numpy()[:1], trees[0]["parent"][None],
+                                   1.0 / math.sqrt(cfg.hd))
+    p0 = int(w.c["P"][0])
+    scale_b = sum(p + R for p in w.c["P"]) / (p0 + R)
+    times["verify"] = (time.perf_counter() - t) * cfg.L * scale_b
+    Wl = f(b.W_lm)
+    h = f(b.O[cfg.L - 1]).reshape(B * R, -1)
+    sl = slice(0, V // 8)
+    t = time.perf_counter()
+    z = oracle.lmhead_logits(h, Wl[sl])
+    oracle.row_stats(z.astype(np.float32), 1.0)
+    times["lmhead"] = (time.perf_counter() - t) * 8
+    zl = f(b.logits)
+    t = time.perf_counter()
+    tt = {"tok": b.tok.cpu().numpy()[0], "parent": b.parent.cpu().numpy()[0]}
+    oracle.accept(tt, zl[:R], float(w.c["temps"][0]), b.u_acc.cpu().numpy()[0].view(np.uint32),
+                  b.u_bonus.cpu().numpy()[0].view(np.uint32), cfg.D)
+    times["accept"] = (time.perf_counter() - t) * B
+    total = sum(times.values())
+    wall = time.perf_counter() - t0
+    return {"round_s": total, "times": times, "cores": blas_threads, "wall_s": wall}
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="8b", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        return reference_arm(args, rank, world)
+    torch.cuda.set_device(local)
+    w = Workload(args.config, seed=args.seed + 1000 * rank)
+    cfg = w.cfg
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            w.round()
+    s.synchronize()
+    accepted = w.bufs.acc_len.cpu().numpy().copy()
+
+    # the timed region: one graph of K rounds, with events at the phase boundaries
+    K = args.steps
+    phases = ["fuse", "expand", "tree", "verify", "lmhead", "accept", "compact"]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)] for _ in range(K)]
+    from eagle_speculative_decoding_round_gb300 import eagle3 as e3
+    from eagle_speculative_decoding_round_gb300.round import run_round
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for k in range(K):
+            w.bufs.kv_len.copy_(w.kv_len0)
+            run_round_phased(w, ev[k], e3)
+    torch.cuda.synchronize()
+    graph.replay()  # one untimed replay of the captured work
+    torch.cuda.synchronize()
+    launches_per_step = count_launches(cfg)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(s)
+    graph.replay()
+    t1.record(s)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    # keep the GPU busy a little longer so the clock sampler sees load
+    extra = 0
+    while extra < 3 and ms * (extra + 1) < 1500:
+        graph.replay()
+        extra += 1
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / K
+    phase_ms = {p: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
+                for i, p in enumerate(phases)}
+    rounds_s = world * 1000.0 / ms_step
+    nodes_s = rounds_s * cfg.B * cfg.N
+
+    wm = work_model(w)
+    peaks = load_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    tflops = peaks.get("bf16_tflops_sustained", 1700.0)
+    lm_ms = phase_ms["lmhead"]
+    lm_gbs = wm["lm_bytes"] / (lm_ms * 1e-3) / 1e9
+    lm_tf = wm["lm_flops"] / (lm_ms * 1e-3) / 1e12
+    ver_ms = phase_ms["verify"] / cfg.L
+    ver_gbs = wm["verify_bytes"] / (ver_ms * 1e-3) / 1e9
+    lm_bound = "hbm" if wm["lm_flops"] / wm["lm_bytes"] < tflops * 1e12 / (hbm * 1e9) else "tensor"
+    if lm_bound == "hbm":
+        roofline = {"kernel": "lmhead_logits (GEMM + row statistics)", "bound": "hbm", "achieved": round(lm_gbs, 1),
+                    "peak": hbm, "unit": "GB/s", "frac": round(lm_gbs / hbm, 4), "traffic": None,
+                    "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if "hbm_gbs" in peaks else "fallback"}
+    else:
+        roofline = {"kernel": "lmhead_logits (GEMM + row statistics)", "bound": "tensor", "achieved": round(lm_tf, 1),
+                    "peak": tflops, "unit": "TFLOP/s", "frac": round(lm_tf / tflops, 4), "traffic": None,
+                    "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (of measured)"}
+    e2e = None if args.no_e2e else e2e_leg(w, s, K, args.warmup)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        o = oracle_sample(w)
+        cpu = {"value": round(1.0 / o["round_s"], 6), "unit": "rounds/s", "cores": o["cores"], "kind": "oracle",
+               "sample": "one round of the same workload: fusion, expansion, tree build, accept in full; verify on "
+                         "layer L-1 for request 0 scaled by L and by the batch's keys; LM head on 1/8 of the "
+                         f"vocabulary scaled by 8 (wall {o['wall_s']:.1f} s)",
+               "seconds_per_round": round(o["round_s"], 3),
+               "breakdown_s": {k: round(v, 3) for k, v in o["times"].items()}}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(rounds_s, 3), "unit": "rounds/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded; random-init weights)",
+            "config": {"workload": w.c["workload"], "global_batch": cfg.B * world, "prefix_lens": summarize(w.c["P"]),
+                       "nodes": cfg.N, "depth": cfg.D, "topk": cfg.k, "layers": cfg.L,
+                       "l2": "inputs larger than L2 per step (L distinct per-layer KV caches + 1 LM head)",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "nodes_per_s": round(nodes_s, 1),
+            "accepted_mean": float(np.mean(accepted)),
+            "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
+            "roofline": roofline,
+            "roofline_verify": {"bound": "hbm", "achieved": round(ver_gbs, 1), "peak": hbm, "unit": "GB/s",
+                                "frac": round(ver_gbs / hbm, 4), "per_layer_us": round(ver_ms * 1e3, 2)},
+            "gpu_launches": launches_per_step * K,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def summarize(P):
+    return P if len(P) <= 4 else {"n": len(P), "min": min(P), "max": max(P), "mean": float(np.mean(P))}
+
+
+def run_round_phased(w, evs, e3):
+    """One round with a timing event at each phase boundary (same calls as run_round)."""
+    import torch
+    b, c = w.bufs, w.cfg
+    s = torch.cuda.current_stream()
+    R = c.R
+    evs[0].record(s)
+    e3.eagle3_fuse(b.h[0], b.h[1], b.h[2], b.W_f, None, b.g, c.M, c.d, c.d, c.dt, b.fuse_ws, b.fuse_ws_bytes)
+    evs[1].record(s)
+    sizes, n_cand = c.frontier_sizes()
+    for di, (F, off) in enumerate(sizes):
+        e3.eagle3_expand(b.draft_logits[di], c.B, F, c.V, c.k, c.W, 1.0, b.f_score[di], b.f_id[di], di + 1, off,
+                         b.cand, b.f_id[di + 1], b.f_score[di + 1], b.dev_err)
+    evs[2].record(s)
+    e3.tree_build_mask(b.cand, c.B, n_cand, c.N, b.root_tok, b.kv_len, b.tok, b.parent, b.depth, b.pos, b.mask)
+    evs[3].record(s)
+    for l in range(c.L):
+        e3.tree_verify_attn(b.Q[l], b.kv[l], b.kv_len, b.mask, c.B, R, c.H, c.max_kv_len, 1.0 / math.sqrt(c.hd),
+                            b.O[l], b.lse[l], b.dev_err, b.ws, b.ws_bytes)
+    evs[4].record(s)
+    e3.lmhead_logits(b.O[c.L - 1], b.W_lm, c.B * R, c.H * c.hd, c.V, b.temp_rows, b.logits, b.row_max, b.row_Q,
+                     b.row_argmax, b.dev_err, c.dt)
+    evs[5].record(s)
+    e3.spec_accept(b.tok, b.parent, c.B, R, c.D, b.logits, b.row_max, b.row_Q, b.row_argmax, c.V, b.temp, b.u_acc,
+                   b.u_bonus, e3.E3_ACCEPT_TREE_DET, b.acc_len, b.path, b.out_tok, b.status)
+    evs[6].record(s)
+    e3.kv_compact(b.kv, c.B, b.path, b.acc_len, c.D, b.kv_len, b.dev_err)
+    evs[7].record(s)
+
+
+def count_launches(cfg):
+    """Kernels of libeagle3 per round: fuse 1, expand 2 per depth, tree 1, verify 2
+    per layer, LM head 2, accept 1, compact 2."""
+    return 1 + 2 * cfg.D + 1 + 2 * cfg.L + 2 + 1 + 2
+
+
+def e2e_leg(w, s, K, warmup):
+    """Same rounds through the C ABI, from pinned HOST buffers: each step copies the
+    round's inputs host->device (fusion inputs, draft logits, per-layer Q, uniforms,
+    temperatures, root tokens), runs the round, and copies the result (emitted
+    tokens, path, accepted length) back."""
+    import torch
+    b = w.bufs
+    ins = [*b.h, *b.draft_logits, *b.Q, b.u_acc, b.u_bonus, b.temp, b.temp_rows, b.root_tok]
+    outs = [b.out_tok, b.path, b.acc_len]
+    h_in = [t.detach().cpu().pin_memory() for t in ins]
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
+    bi = sum(t.numel() * t.element_size() for t in ins)
+    bo = sum(t.numel() * t.element_size() for t in outs)
+    g1 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g1, stream=s):
+        w.round()
+    torch.cuda.synchronize()
+
+    def step():
+        with torch.cuda.stream(s):
+            for d, h in zip(ins, h_in):
+                d.copy_(h, non_blocking=True)
+            g1.replay()
+            for h, d in zip(h_out, outs):
+                h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    z = torch.cuda.Event(enable_timing=True)
+    a.record(s)
+    for _ in range(K):
+        step()
+    z.record(s)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(z) / K
+    return {"value": round(1000.0 / ms, 3), "unit": "rounds/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "ms_per_step": round(ms, 4)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return json.load(open(p))
+    except Exception:
+        return {}
+
+
+def reference_arm(args, rank, world):
+    """The oracle, as it stands, timed on the host cores: each step is a bounded
+    sample of one round of the same workload (see oracle_sample), scaled to a round."""
+    if rank != 0:
+        return 0
+    import torch
+    w = Workload(args.config, seed=args.seed)
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle_sample(w)
+    per = []
+    cores = 1
+    for _ in range(args.steps):
+        o = oracle_sample(w)
+        per.append(o["round_s"])
+        cores = o["cores"]
+    sec = float(np.mean(per))
+    v = 1.0 / sec
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "rounds/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1000, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded; random-init weights)",
+            "config": {"workload": w.c["workload"], "global_batch": w.cfg.B},
+            "cpu_baseline": {"value": round(v, 6), "unit": "rounds/s", "cores": cores, "kind": "oracle",
+                             "sample": "per step: one round with verify on 1 layer (scaled by L) and LM head on 1/8 "
+                                       "of the vocabulary (scaled by 8)"},
+            "e2e": {"value": round(v, 6), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    main()

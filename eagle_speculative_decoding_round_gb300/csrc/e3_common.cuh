@@ -1,0 +1,201 @@
+// e3_common.cuh -- shared device helpers of libeagle3 (CUDA, sm_103a).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/eagle3.h"
+
+namespace e3 {
+
+// ---------------------------------------------------------------------------
+// host-side error reporting
+// ---------------------------------------------------------------------------
+void set_error(const char* fmt, ...);
+e3_status cuda_status(cudaError_t e, const char* what);
+
+#define E3_REQUIRE(cond, code, ...)   \
+  do {                                \
+    if (!(cond)) {                    \
+      ::e3::set_error(__VA_ARGS__);   \
+      return code;                    \
+    }                                 \
+  } while (0)
+
+#define E3_LAUNCH_CHECK(what)                                   \
+  do {                                                          \
+    cudaError_t _e = cudaGetLastError();                        \
+    if (_e != cudaSuccess) return ::e3::cuda_status(_e, what);  \
+  } while (0)
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------
+// device error word
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void dev_flag(int32_t* dev_err, int bits) {
+  if (dev_err) atomicOr(dev_err, bits);
+}
+
+// ---------------------------------------------------------------------------
+// element loads
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ld_elem(const float* p, size_t i) { return p[i]; }
+__device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, size_t i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_elem(float* p, size_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16* p, size_t i, float v) {
+  p[i] = __float2bfloat16_rn(v);
+}
+
+// ---------------------------------------------------------------------------
+// Fixed-point softmax decision arithmetic (fp32, every operation explicitly
+// rounded so that no contraction changes a result).
+//   E(x), x <= 0:  Cody-Waite reduction x = n ln2 + r (ln2 split into a 16-bit
+//   high part and a low part), Taylor polynomial of exp(r) to degree 7 with
+//   coefficients 1/k! rounded to fp32, Horner with fused multiply-add, then an
+//   exact scaling by 2^n.  E(x) = 0 for x < -32.
+//   mass(s, m) = floor(2^40 E(s - m)).
+//   ell(Q) = ln(Q 2^-40): Q -> fp32 (nearest), exponent extraction, mantissa
+//   folded into [sqrt(1/2), sqrt(2)], ln f = 2 atanh(t), t = (f-1)/(f+1), series
+//   to t^11, plus (e - 40) ln2 (split).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fx_exp(float x) {
+  if (x < -32.0f) return 0.0f;
+  const float kLog2e = 0x1.715476p+0f;
+  const float kLn2Hi = 0x1.62e4p-1f;
+  const float kLn2Lo = 0x1.7f7d1cp-20f;
+  float t = __fmul_rn(x, kLog2e);
+  float n = rintf(t);
+  float r = __fmaf_rn(-n, kLn2Hi, x);
+  r = __fmaf_rn(-n, kLn2Lo, r);
+  float p = 0x1.a01a02p-13f;
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  float scale = __int_as_float((static_cast<int>(n) + 127) << 23);
+  return __fmul_rn(p, scale);
+}
+
+__device__ __forceinline__ uint64_t fx_mass(float s, float m) {
+  float e = fx_exp(__fsub_rn(s, m));
+  return __float2ull_rz(__fmul_rn(e, 0x1p40f));
+}
+
+__device__ __forceinline__ float fx_ell(uint64_t Q) {
+  const float kLn2Hi = 0x1.62e4p-1f;
+  const float kLn2Lo = 0x1.7f7d1cp-20f;
+  float y = __ull2float_rn(Q);
+  uint32_t b = __float_as_uint(y);
+  int e = static_cast<int>(b >> 23) - 127;
+  float f = __uint_as_float((b & 0x7FFFFFu) | 0x3F800000u);
+  if (f > 0x1.6a09e6p+0f) {
+    f = __fmul_rn(f, 0.5f);
+    e += 1;
+  }
+  float t = __fdiv_rn(__fsub_rn(f, 1.0f), __fadd_rn(f, 1.0f));
+  float t2 = __fmul_rn(t, t);
+  float P = 0x1.745d18p-4f;
+  P = __fmaf_rn(P, t2, 0x1.c71c72p-4f);
+  P = __fmaf_rn(P, t2, 0x1.24924ap-3f);
+  P = __fmaf_rn(P, t2, 0x1.99999ap-3f);
+  P = __fmaf_rn(P, t2, 0x1.555556p-2f);
+  P = __fmaf_rn(P, t2, 1.0f);
+  float lnf = __fmul_rn(__fmul_rn(t, P), 2.0f);
+  float k = static_cast<float>(e - 40);
+  return __fmaf_rn(k, kLn2Hi, __fmaf_rn(k, kLn2Lo, lnf));
+}
+
+// 1/T for T > 0, else 1 (greedy rows keep s = z).
+__device__ __forceinline__ float inv_temp(float T) {
+  return T > 0.0f ? __fdiv_rn(1.0f, T) : 1.0f;
+}
+
+// (u * R) >> 32 for a uint32 uniform and a mass R < 2^57, exact.
+__device__ __forceinline__ uint64_t mulhi32(uint32_t u, uint64_t R) {
+  uint64_t lo = static_cast<uint64_t>(u) * R;  // low 64 bits of the product
+  uint64_t hi = __umul64hi(static_cast<uint64_t>(u), R);
+  return (hi << 32) | (lo >> 32);
+}
+
+// Order-preserving map of a finite float to uint32 (-0 folded onto +0).
+__device__ __forceinline__ uint32_t ord_f32(float f) {
+  f = __fadd_rn(f, 0.0f);
+  uint32_t b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float unord_f32(uint32_t o) {
+  uint32_t b = (o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o;
+  return __uint_as_float(b);
+}
+
+// (value desc, id asc) packed so that a larger key is better.
+__device__ __forceinline__ uint64_t pack_best(float v, uint32_t id) {
+  return (static_cast<uint64_t>(ord_f32(v)) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - id);
+}
+__device__ __forceinline__ uint32_t packed_id(uint64_t k) {
+  return 0xFFFFFFFFu - static_cast<uint32_t>(k & 0xFFFFFFFFull);
+}
+
+// ---------------------------------------------------------------------------
+// block reductions (blockDim.x a multiple of 32, <= 1024)
+// ---------------------------------------------------------------------------
+template <typename T, typename Op>
+__device__ __forceinline__ T warp_reduce(T v, Op op) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+template <typename T, typename Op>
+__device__ T block_reduce(T v, Op op, T* smem32 /* >= 32 */) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  v = warp_reduce(v, op);
+  __syncthreads();
+  if (lane == 0) smem32[wid] = v;
+  __syncthreads();
+  T r = smem32[0];
+  for (int i = 1; i < nw; ++i) r = op(r, smem32[i]);
+  return r;
+}
+
+struct MaxU64 {
+  __device__ __forceinline__ uint64_t operator()(uint64_t a, uint64_t b) const { return a > b ? a : b; }
+};
+struct SumU64 {
+  __device__ __forceinline__ uint64_t operator()(uint64_t a, uint64_t b) const { return a + b; }
+};
+struct MaxF {
+  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct OrI {
+  __device__ __forceinline__ int operator()(int a, int b) const { return a | b; }
+};
+
+// Block-wide bitonic sort of n (power of two) uint64 keys in shared memory,
+// descending.
+__device__ __forceinline__ void block_bitonic_desc(uint64_t* s, int n) {
+  for (int kk = 2; kk <= n; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        int ixj = i ^ j;
+        if (ixj > i) {
+          uint64_t a = s[i], b = s[ixj];
+          bool first_half = (i & kk) == 0;
+          if (first_half ? (a < b) : (a > b)) {
+            s[i] = b;
+            s[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+}  // namespace e3

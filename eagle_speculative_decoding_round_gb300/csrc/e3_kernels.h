@@ -1,0 +1,45 @@
+// e3_kernels.h -- internal launchers of libeagle3 (not part of the C ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/eagle3.h"
+
+namespace e3 {
+
+struct CompactLayers {
+  void* k[E3_MAX_LAYERS];
+  void* v[E3_MAX_LAYERS];
+};
+
+e3_status launch_expand(const float* logits, int B, int F, int V, int k, int W, float inv_temp,
+                        const float* parent_score, const int32_t* parent_id, int depth, int cand_offset,
+                        const e3_cand& c, int32_t* next_id, float* next_score, int32_t* dev_err,
+                        cudaStream_t s);
+
+e3_status launch_tree_build(const e3_cand& c, int B, int n_cand, int N, const int32_t* root_tok,
+                            const int32_t* kv_len, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* pos,
+                            uint64_t* mask, cudaStream_t s);
+
+size_t verify_workspace_bytes(int B, int R, int H, int KVH, int hd, int max_kv_len, bool mma);
+bool verify_uses_mma(e3_dtype dt, int hd);
+e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_len, const uint64_t* mask,
+                        int B, int R, int H, int max_kv_len, float sm_scale, void* O, float* lse,
+                        int32_t* dev_err, void* ws, size_t ws_bytes, cudaStream_t s);
+
+e3_status launch_gemm_simt(const void* a0, const void* a1, const void* a2, int dseg, const void* W,
+                           const float* bias, void* out, bool out_f32, int M, int N, int K, e3_dtype dt,
+                           cudaStream_t s);
+e3_status launch_row_stats(const float* logits, int M, int V, const float* temp, float* row_max,
+                           uint64_t* row_Q, int32_t* row_argmax, int32_t* dev_err, cudaStream_t s);
+
+e3_status launch_accept(const int32_t* tok, const int32_t* parent, int B, int R, int D, const float* logits,
+                        const float* row_max, const uint64_t* row_Q, const int32_t* row_argmax, int V,
+                        const float* temp, const uint32_t* u_acc, const uint32_t* u_bonus, int32_t* acc_len,
+                        int32_t* path, int32_t* out_tok, int32_t* status, cudaStream_t s);
+
+e3_status launch_compact(const CompactLayers& layers, const e3_kv_layer& geo, int L, int B, const int32_t* path,
+                         const int32_t* acc_len, int D, int32_t* kv_len, int32_t* dev_err, cudaStream_t s);
+
+}  // namespace e3

@@ -1,0 +1,161 @@
+"""ctypes binding of libeagle3 (include/eagle3.h): same names, argument
+marshalling only.  Every step runs in the library's CUDA kernels; there is no
+fallback -- importing this module fails if the library is missing.
+
+Arguments that are device buffers accept a torch CUDA tensor (its data_ptr is
+passed) or an int address.  ``stream`` defaults to torch's current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libeagle3.so")
+
+E3_OK = 0
+E3_F32, E3_BF16 = 0, 1
+E3_DEV_ERR_NONFINITE, E3_DEV_ERR_CAPACITY, E3_DEV_ERR_TIMEOUT = 1, 2, 4
+E3_ACCEPT_TREE_DET = 0
+STATUS_NAMES = {0: "E3_OK", 1: "E3_ERR_INVALID_ARG", 2: "E3_ERR_SHAPE", 3: "E3_ERR_UNSUPPORTED",
+                4: "E3_ERR_CAPACITY", 5: "E3_ERR_NONFINITE", 6: "E3_ERR_CUDA", 7: "E3_ERR_TIMEOUT"}
+SYMBOLS = ["eagle3_fuse", "eagle3_fuse_workspace_bytes", "eagle3_expand", "tree_build_mask",
+           "tree_verify_attn", "eagle3_verify_workspace_bytes", "lmhead_logits", "spec_accept",
+           "kv_compact", "eagle3_last_error", "eagle3_abi_version"]
+
+
+class E3Error(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class e3_cand(ctypes.Structure):
+    _fields_ = [("tok", ctypes.c_void_p), ("parent", ctypes.c_void_p), ("score", ctypes.c_void_p),
+                ("depth", ctypes.c_void_p), ("cap", ctypes.c_int)]
+
+
+class e3_kv_layer(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
+                ("n_pages", ctypes.c_int), ("page_size", ctypes.c_int), ("max_pages", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("dt", ctypes.c_int)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libeagle3.so is not built ({LIB_PATH}); run "
+                          "eagle_speculative_decoding_round_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "eagle3_fuse": (I, [P, P, P, P, P, P, I, I, I, I, P, S, P]),
+        "eagle3_fuse_workspace_bytes": (S, [I, I, I, I]),
+        "eagle3_expand": (I, [P, I, I, I, I, I, F, P, P, I, I, ctypes.POINTER(e3_cand), P, P, P, P]),
+        "tree_build_mask": (I, [ctypes.POINTER(e3_cand), I, I, I, P, P, P, P, P, P, P, P]),
+        "tree_verify_attn": (I, [P, ctypes.POINTER(e3_kv_layer), P, P, I, I, I, I, F, P, P, P, P, S, P]),
+        "eagle3_verify_workspace_bytes": (S, [I, I, I, I, I, I, I]),
+        "lmhead_logits": (I, [P, P, I, I, I, P, P, P, P, P, P, I, P]),
+        "spec_accept": (I, [P, P, I, I, I, P, P, P, P, I, P, P, P, I, P, P, P, P, P]),
+        "kv_compact": (I, [ctypes.POINTER(e3_kv_layer), I, I, P, P, I, P, P, P]),
+        "eagle3_last_error": (ctypes.c_char_p, []),
+        "eagle3_abi_version": (I, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def ptr(x) -> int | None:
+    """Device address of a torch tensor (or pass an int / None through)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, st: int):
+    if st != E3_OK:
+        raise E3Error(fn, st, _lib.eagle3_last_error().decode())
+
+
+def make_cand(tok, parent, score, depth, cap: int) -> e3_cand:
+    return e3_cand(ptr(tok), ptr(parent), ptr(score), ptr(depth), cap)
+
+
+def make_kv_layer(k, v, page_table, n_pages, page_size, max_pages, n_kv_heads, head_dim, dt) -> e3_kv_layer:
+    return e3_kv_layer(ptr(k), ptr(v), ptr(page_table), n_pages, page_size, max_pages, n_kv_heads, head_dim, dt)
+
+
+def abi_version() -> int:
+    return _lib.eagle3_abi_version()
+
+
+def eagle3_fuse_workspace_bytes(M, d, d_out, dt) -> int:
+    return int(_lib.eagle3_fuse_workspace_bytes(M, d, d_out, dt))
+
+
+def eagle3_fuse(h_low, h_mid, h_high, W_f, bias, g, M, d, d_out, dt, ws=None, ws_bytes=0, stream=None):
+    _check("eagle3_fuse", _lib.eagle3_fuse(ptr(h_low), ptr(h_mid), ptr(h_high), ptr(W_f), ptr(bias), ptr(g),
+                                           M, d, d_out, dt, ptr(ws), ws_bytes, _stream(stream)))
+
+
+def eagle3_expand(draft_logits, B, F, V, k, W, inv_temp, parent_score, parent_id, depth, cand_offset,
+                  cands: e3_cand, next_id, next_score, dev_err=None, stream=None):
+    _check("eagle3_expand", _lib.eagle3_expand(ptr(draft_logits), B, F, V, k, W, inv_temp, ptr(parent_score),
+                                               ptr(parent_id), depth, cand_offset, ctypes.byref(cands),
+                                               ptr(next_id), ptr(next_score), ptr(dev_err), _stream(stream)))
+
+
+def tree_build_mask(cands: e3_cand, B, n_cand, N, root_tok, kv_len, tok, parent, depth, pos, mask, stream=None):
+    _check("tree_build_mask", _lib.tree_build_mask(ctypes.byref(cands), B, n_cand, N, ptr(root_tok), ptr(kv_len),
+                                                   ptr(tok), ptr(parent), ptr(depth), ptr(pos), ptr(mask),
+                                                   _stream(stream)))
+
+
+def eagle3_verify_workspace_bytes(B, R, n_q_heads, n_kv_heads, head_dim, max_kv_len, dt) -> int:
+    return int(_lib.eagle3_verify_workspace_bytes(B, R, n_q_heads, n_kv_heads, head_dim, max_kv_len, dt))
+
+
+def tree_verify_attn(Q, kv: e3_kv_layer, kv_len, mask, B, R, n_q_heads, max_kv_len, sm_scale, O, lse,
+                     dev_err=None, ws=None, ws_bytes=0, stream=None):
+    _check("tree_verify_attn", _lib.tree_verify_attn(ptr(Q), ctypes.byref(kv), ptr(kv_len), ptr(mask), B, R,
+                                                     n_q_heads, max_kv_len, sm_scale, ptr(O), ptr(lse),
+                                                     ptr(dev_err), ptr(ws), ws_bytes, _stream(stream)))
+
+
+def lmhead_logits(h, W_lm, M, d, V, temp_per_row, logits, row_max, row_Q, row_argmax, dev_err, dt, stream=None):
+    _check("lmhead_logits", _lib.lmhead_logits(ptr(h), ptr(W_lm), M, d, V, ptr(temp_per_row), ptr(logits),
+                                               ptr(row_max), ptr(row_Q), ptr(row_argmax), ptr(dev_err), dt,
+                                               _stream(stream)))
+
+
+def spec_accept(tok, parent, B, R, D, logits, row_max, row_Q, row_argmax, V, temp, u_acc, u_bonus, mode,
+                acc_len, path, out_tok, status, stream=None):
+    _check("spec_accept", _lib.spec_accept(ptr(tok), ptr(parent), B, R, D, ptr(logits), ptr(row_max), ptr(row_Q),
+                                           ptr(row_argmax), V, ptr(temp), ptr(u_acc), ptr(u_bonus), mode,
+                                           ptr(acc_len), ptr(path), ptr(out_tok), ptr(status), _stream(stream)))
+
+
+def kv_compact(layers, B, path, acc_len, D, kv_len, dev_err=None, stream=None):
+    arr = (e3_kv_layer * len(layers))(*layers)
+    _check("kv_compact", _lib.kv_compact(arr, len(layers), B, ptr(path), ptr(acc_len), D, ptr(kv_len),
+                                         ptr(dev_err), _stream(stream)))

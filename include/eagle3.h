@@ -1,0 +1,259 @@
+/*
+ * eagle3.h -- C ABI of libeagle3, one EAGLE-3 draft-and-verify round on one GPU.
+ *
+ * The round (sources are web pages on EAGLE-3, cited by title and section):
+ *   eagle3_fuse      g = W_f [h_low; h_mid; h_high]
+ *                    ("论文专题讲解：EAGLE-3", 推理流程：多层特征融合 + 单层 draft decoder;
+ *                     "SpecForge：把 EAGLE3 从训练样本交付到 SGLang", 多层特征融合到底融合了什么)
+ *   eagle3_expand    one depth of the EAGLE-2 dynamic draft tree: top-k children
+ *                    per frontier node, cumulative confidence, next frontier
+ *                    ("EAGLE 系列与 DFlash", §二 EAGLE-2 阶段一; "论文专题讲解：EAGLE-3",
+ *                     Draft tree 配置)
+ *   tree_build_mask  keep the N most confident nodes, flatten breadth first,
+ *                    positions and the ancestor-only 0/1 mask
+ *                    ("EAGLE 系列与 DFlash", §二 阶段二, 关键新增步骤① and ②)
+ *   tree_verify_attn one tree-masked attention layer of the single verify pass
+ *                    ("EAGLE 系列与 DFlash", §二 阶段三; "Thinking Budget 与 EAGLE-3",
+ *                     一棵候选树怎样被验证; prefix and tree segments merged by
+ *                     log-sum-exp as in "EAGLE-3 投机解码与 USP 长序列训练优化",
+ *                     USP 核心设计：三步走)
+ *   lmhead_logits    per-node target logits and softmax statistics
+ *                    ("SpecForge…", 先看 checkpoint 最终要参与什么计算: the target
+ *                     computes the true probabilities of the tree)
+ *   spec_accept      speculative-sampling accept/reject along the tree, residual
+ *                    correction at the rejection point, longest accepted path
+ *                    ("EAGLE 系列与 DFlash", §四 DFlash worked example and §二 阶段三;
+ *                     "SpecForge…", 接受连续前缀，拒绝处进行校正)
+ *   kv_compact       commit only the accepted path's KV
+ *                    ("Thinking Budget 与 EAGLE-3", 一棵候选树怎样被验证, step 5)
+ *
+ * Conventions (every call):
+ *  - All data pointers are DEVICE pointers owned by the caller, unless a
+ *    parameter says "host".  The library keeps no allocation across calls.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and return after enqueue.
+ *  - Shape and argument errors are detected on the host before any launch and
+ *    return a non-OK status without touching device memory;
+ *    eagle3_last_error() then gives a message (thread local).
+ *  - Data-dependent errors found on the device (non-finite logits, a page
+ *    table too short for kv_len + R, a wait that ran out) are OR-ed into the
+ *    caller's `dev_err` word (int32, device, nullable) with the E3_DEV_ERR_*
+ *    bits; kernels never trap.
+ *  - Row-major layouts, innermost dimension last.  bf16 is IEEE bfloat16.
+ */
+#ifndef EAGLE3_H
+#define EAGLE3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define E3_API __attribute__((visibility("default")))
+#else
+#define E3_API
+#endif
+
+typedef struct CUstream_st* e3_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  E3_OK = 0,
+  E3_ERR_INVALID_ARG = 1, /* null pointer, bad enum, misaligned pointer */
+  E3_ERR_SHAPE = 2,       /* sizes out of the supported range or inconsistent */
+  E3_ERR_UNSUPPORTED = 3, /* valid request this build does not implement */
+  E3_ERR_CAPACITY = 4,    /* a buffer or workspace is too small */
+  E3_ERR_NONFINITE = 5,   /* reserved for synchronous callers; see E3_DEV_ERR_NONFINITE */
+  E3_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed */
+  E3_ERR_TIMEOUT = 7      /* reserved for synchronous callers; see E3_DEV_ERR_TIMEOUT */
+} e3_status;
+
+typedef enum { E3_F32 = 0, E3_BF16 = 1 } e3_dtype;
+
+/* bits of the device error word */
+#define E3_DEV_ERR_NONFINITE 1 /* a logit was NaN or +-Inf */
+#define E3_DEV_ERR_CAPACITY 2  /* kv_len + R exceeds the request's pages */
+#define E3_DEV_ERR_TIMEOUT 4   /* a bounded on-device wait ran out; outputs invalid */
+
+/* Limits of this build. */
+#define E3_MAX_TOPK 32     /* k of eagle3_expand */
+#define E3_MAX_FRONTIER 64 /* W of eagle3_expand */
+#define E3_MAX_NODES 255   /* N of tree_build_mask; R = N + 1 <= 256 */
+#define E3_MAX_DEPTH 16    /* D */
+#define E3_MAX_CAND 4096   /* candidates per request */
+#define E3_MAX_LAYERS 128  /* L of kv_compact */
+
+/* Candidate list of the dynamic tree, structure of arrays, [B][cap] each
+ * (device).  Candidate c of request b lives at index b*cap + c. */
+typedef struct {
+  int32_t* tok;    /* token id */
+  int32_t* parent; /* candidate index of the parent within the request; -1 = root */
+  float* score;    /* cumulative draft log-probability (confidence) */
+  int32_t* depth;  /* 1 for the root's children */
+  int cap;         /* candidates per request */
+} e3_cand;
+
+/* One layer's paged KV cache.  k and v: [n_pages][n_kv_heads][page_size][head_dim]
+ * of dtype dt (device).  Logical token t of request b is slot t % page_size of
+ * page page_table[b*max_pages + t / page_size]. */
+typedef struct {
+  void* k;
+  void* v;
+  const int32_t* page_table; /* [B][max_pages], device */
+  int n_pages;
+  int page_size;
+  int max_pages;
+  int n_kv_heads;
+  int head_dim;
+  e3_dtype dt;
+} e3_kv_layer;
+
+/* ---------------------------------------------------------------------------
+ * eagle3_fuse: g[m, o] = sum_j W_f[o, j] x[m, j] (+ bias[o]),
+ *   x[m] = [h_low[m]; h_mid[m]; h_high[m]] (3*d values), fp32 accumulation.
+ * h_low/h_mid/h_high: [M][d] dtype dt; W_f: [d_out][3*d] dtype dt;
+ * bias: [d_out] fp32 or NULL; g: [M][d_out] dtype dt.
+ * Limits: 1 <= M <= 65536; d % 64 == 0 and d_out % 128 == 0 for bf16
+ * (any positive d, d_out for fp32).  Pointers 16-byte aligned.
+ * ws: scratch of eagle3_fuse_workspace_bytes() bytes (device), or NULL if that is 0.
+ * ------------------------------------------------------------------------- */
+E3_API e3_status eagle3_fuse(const void* h_low, const void* h_mid, const void* h_high,
+                      const void* W_f, const float* bias, void* g, int M, int d,
+                      int d_out, e3_dtype dt, void* ws, size_t ws_bytes,
+                      e3_stream_t stream);
+E3_API size_t eagle3_fuse_workspace_bytes(int M, int d, int d_out, e3_dtype dt);
+
+/* ---------------------------------------------------------------------------
+ * eagle3_expand: one depth of the dynamic draft tree, B requests at once.
+ * draft_logits: [B][F][V] fp32, row f = frontier node f of the request.
+ * parent_score: [B][F] fp32 (the root has 0); parent_id: [B][F] int32
+ *   (candidate index of the frontier node, -1 = root).
+ * For each row: s_j = z_j * inv_temp (fp32), m = max s,
+ *   Q = sum_j floor(2^40 E(s_j - m)), ell = ln(Q 2^-40) (fixed-point recipe),
+ *   the k largest s (ties -> lower token id) become children r = 0..k-1 at
+ *   candidate index cand_offset + f*k + r with
+ *   score = (parent_score + (s_c - m)) - ell and depth = `depth`.
+ * Next frontier: the first Wn = min(W, F*k) of these children in the order
+ *   (score descending, candidate index ascending) -> next_id [B][Wn] (candidate
+ *   index) and next_score [B][Wn].
+ * Non-finite logits set E3_DEV_ERR_NONFINITE.
+ * Limits: 1 <= k <= E3_MAX_TOPK, k <= V, 1 <= W <= E3_MAX_FRONTIER or W >= F*k,
+ *   F*k <= 2048, cand_offset + F*k <= cands->cap <= E3_MAX_CAND.
+ * ------------------------------------------------------------------------- */
+E3_API e3_status eagle3_expand(const float* draft_logits, int B, int F, int V, int k, int W,
+                        float inv_temp, const float* parent_score,
+                        const int32_t* parent_id, int depth, int cand_offset,
+                        const e3_cand* cands /* host struct, device arrays */,
+                        int32_t* next_id, float* next_score, int32_t* dev_err,
+                        e3_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * tree_build_mask: per request, keep the N best of the first n_cand candidates
+ * in the order (score descending, candidate index ascending) -- closed under
+ * parents because a child's score never exceeds its parent's -- and flatten
+ * with the root as node 0, then depth by depth ordered by (parent's flat
+ * index, candidate index).  R = N + 1.
+ * Outputs ([B][R] int32 each): tok (root = root_tok[b]), parent (root -1),
+ * depth (root 0), pos = kv_len[b] + depth; mask [B][R][W64] uint64 with
+ * W64 = ceil(R/64): bit j of row i set iff node j is node i or an ancestor.
+ * Limits: 1 <= N <= min(n_cand, E3_MAX_NODES), n_cand <= cands->cap.
+ * ------------------------------------------------------------------------- */
+E3_API e3_status tree_build_mask(const e3_cand* cands, int B, int n_cand, int N,
+                          const int32_t* root_tok, const int32_t* kv_len, int32_t* tok,
+                          int32_t* parent, int32_t* depth, int32_t* pos, uint64_t* mask,
+                          e3_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * tree_verify_attn: one attention layer of the verify pass.
+ * For request b (P = kv_len[b]), node i < R, query head h < n_q_heads:
+ *   keys = prefix [0, P) and tree slots {P + j : bit j of mask[b][i]},
+ *   o = softmax(sm_scale * q . k) v,  lse = ln(sum exp(sm_scale * q . k)).
+ * The caller has written the tree nodes' K/V at logical slots P .. P+R-1.
+ * Query head h reads KV head h / (n_q_heads / n_kv_heads).
+ * Q: [B][R][n_q_heads][head_dim] dtype kv->dt; O: same shape and dtype;
+ * lse: [B][R][n_q_heads] fp32.  Pages must cover P + R tokens, else
+ * E3_DEV_ERR_CAPACITY and the request's outputs are left unwritten.
+ * Limits: head_dim 64 or 128 (fp32: any multiple of 32 up to 256); R <= 256;
+ *   n_q_heads % n_kv_heads == 0; page_size % 16 == 0.
+ * ws: eagle3_verify_workspace_bytes(B, R, n_q_heads, n_kv_heads, head_dim,
+ *   max_kv_len, dt) bytes (device scratch), where max_kv_len bounds every kv_len[b].
+ * ------------------------------------------------------------------------- */
+E3_API e3_status tree_verify_attn(const void* Q, const e3_kv_layer* kv /* host struct */,
+                           const int32_t* kv_len, const uint64_t* mask, int B, int R,
+                           int n_q_heads, int max_kv_len, float sm_scale, void* O,
+                           float* lse, int32_t* dev_err, void* ws, size_t ws_bytes,
+                           e3_stream_t stream);
+E3_API size_t eagle3_verify_workspace_bytes(int B, int R, int n_q_heads, int n_kv_heads,
+                                     int head_dim, int max_kv_len, e3_dtype dt);
+
+/* ---------------------------------------------------------------------------
+ * lmhead_logits: logits[m][v] = sum_j h[m][j] W_lm[v][j] (fp32 accumulation),
+ * then the softmax statistics of each row at temperature T = temp_per_row[m]:
+ *   s_v = z_v * (1/T) (s_v = z_v when T <= 0), row_max[m] = max s,
+ *   row_argmax[m] = argmax s (lowest id on ties),
+ *   row_Q[m] = sum_v floor(2^40 E(s_v - row_max)) (fixed-point recipe).
+ * h: [M][d] dtype dt; W_lm: [V][d] dtype dt; temp_per_row: [M] fp32;
+ * logits: [M][V] fp32; row_max [M] fp32; row_Q [M] uint64; row_argmax [M] int32.
+ * Non-finite logits set E3_DEV_ERR_NONFINITE.
+ * Limits: 1 <= M <= 65536; bf16: d % 64 == 0, V % 4 == 0.
+ * ------------------------------------------------------------------------- */
+E3_API e3_status lmhead_logits(const void* h, const void* W_lm, int M, int d, int V,
+                        const float* temp_per_row, float* logits, float* row_max,
+                        uint64_t* row_Q, int32_t* row_argmax, int32_t* dev_err,
+                        e3_dtype dt, e3_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * spec_accept: accept/reject along each request's flattened tree.
+ * Rows of logits/row_* are b*R + i.  temp: [B]; row statistics must have been
+ * computed with temp[b] for the rows of request b.  u_acc, u_bonus: [B][R]
+ * uint32 uniforms (u_acc[c] tests child c; u_bonus[u] draws the bonus at u).
+ * mode E3_ACCEPT_TREE_DET (deterministic top-k children): starting at the root
+ * u, for each child c of u in flattened order with token t:
+ *   T > 0:  accept iff (u_acc[c] * Rmass) >> 32 < q_t,  q_t = floor(2^40 E(s_t - m_u));
+ *           on reject Rmass -= q_t and t leaves the residual (Rmass starts at
+ *           row_Q[u] at every node);
+ *   T <= 0: accept iff t == row_argmax[u].
+ * An accepted child becomes u.  When no child of u is accepted (or u is a
+ * leaf), the bonus token is drawn at u: greedy -> row_argmax[u]; sampled ->
+ * the smallest token id whose cumulative residual mass exceeds
+ * (u_bonus[u] * Rmass) >> 32 (ascending token ids).
+ * Outputs: acc_len [B]; path [B][D+1] (flat node ids, root first, -1 padded);
+ * out_tok [B][D+1] (accepted tokens then the bonus token, -1 padded);
+ * status [B] (0, or E3_DEV_ERR_* bits for that request).
+ * Limits: R <= 256, D <= E3_MAX_DEPTH, depth of every node <= D.
+ * ------------------------------------------------------------------------- */
+#define E3_ACCEPT_TREE_DET 0
+E3_API e3_status spec_accept(const int32_t* tok, const int32_t* parent, int B, int R, int D,
+                      const float* logits, const float* row_max, const uint64_t* row_Q,
+                      const int32_t* row_argmax, int V, const float* temp,
+                      const uint32_t* u_acc, const uint32_t* u_bonus, int mode,
+                      int32_t* acc_len, int32_t* path, int32_t* out_tok, int32_t* status,
+                      e3_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * kv_compact: for every layer l < L, request b (P = kv_len[b]) and accepted
+ * node j = 1..acc_len[b], K and V of logical slot P + path[b][j] move to slot
+ * P + j (all KV heads).  Every source is read before any destination is
+ * written, so a slot that is both (path [0,3,4,5]) is handled.  Afterwards
+ * kv_len[b] += 1 + acc_len[b] (root + accepted tokens; the bonus token becomes
+ * the next root and has no KV yet).
+ * layers: host array of L descriptors (same page_table/page_size/heads/dtype in
+ * all layers).  path: [B][D+1].
+ * Limits: 1 <= L <= E3_MAX_LAYERS, D <= E3_MAX_DEPTH.
+ * ------------------------------------------------------------------------- */
+E3_API e3_status kv_compact(const e3_kv_layer* layers, int L, int B, const int32_t* path,
+                     const int32_t* acc_len, int D, int32_t* kv_len, int32_t* dev_err,
+                     e3_stream_t stream);
+
+/* Last error message of the calling thread ("" if none). */
+E3_API const char* eagle3_last_error(void);
+
+/* ABI version: 1. */
+E3_API int eagle3_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EAGLE3_H */

@@ -1,0 +1,86 @@
+"""CPU-side checks of the C ABI: the library loads, exports exactly what
+include/eagle3.h declares, and rejects bad arguments on the host (no launch)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "eagle3.h")
+
+
+@pytest.fixture(scope="module")
+def e3():
+    from eagle_speculative_decoding_round_gb300 import build
+    build.build()
+    from eagle_speculative_decoding_round_gb300 import eagle3
+    return eagle3
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"E3_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_header_declares_the_seven_steps():
+    names = declared_functions()
+    for n in ["eagle3_fuse", "eagle3_expand", "tree_build_mask", "tree_verify_attn", "lmhead_logits",
+              "spec_accept", "kv_compact"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(e3):
+    out = subprocess.run(["nm", "-D", "--defined-only", e3.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (\w+)$", out, re.M))
+    for n in declared_functions():
+        assert n in exported, n
+        assert hasattr(e3.lib(), n)
+    assert set(e3.SYMBOLS) == set(declared_functions())
+    assert e3.abi_version() == 1
+
+
+def test_host_validation_rejects_bad_arguments(e3):
+    # every call below fails its host checks before touching the device
+    with pytest.raises(e3.E3Error) as ei:
+        e3.lmhead_logits(0, 0, 1, 1, 1, 0, 0, 0, 0, 0, None, 0, stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(e3.E3Error) as ei:
+        e3.lmhead_logits(8, 8, 0, 1, 1, 8, 8, 8, 8, 8, None, 0, stream=0)  # M = 0
+    assert ei.value.status == 2
+    cand = e3.make_cand(16, 16, 16, 16, 100)
+    with pytest.raises(e3.E3Error) as ei:  # k > E3_MAX_TOPK
+        e3.eagle3_expand(16, 1, 1, 1000, 40, 10, 1.0, 16, 16, 1, 0, cand, 16, 16, None, stream=0)
+    assert ei.value.status == 2
+    with pytest.raises(e3.E3Error) as ei:  # candidates past the capacity
+        e3.eagle3_expand(16, 1, 10, 1000, 10, 10, 1.0, 16, 16, 2, 95, cand, 16, 16, None, stream=0)
+    assert ei.value.status == 4
+    with pytest.raises(e3.E3Error) as ei:  # N > E3_MAX_NODES
+        e3.tree_build_mask(e3.make_cand(16, 16, 16, 16, 4000), 1, 4000, 300, 16, 16, 16, 16, 16, 16, 16, stream=0)
+    assert ei.value.status == 2
+    kv = e3.make_kv_layer(16, 16, 16, 10, 64, 4, 8, 128, e3.E3_BF16)
+    with pytest.raises(e3.E3Error) as ei:  # pages cannot hold max_kv_len + R
+        e3.tree_verify_attn(16, kv, 16, 16, 1, 61, 32, 250, 0.1, 16, 16, None, 16, 1 << 30, stream=0)
+    assert ei.value.status == 4
+    bad = e3.make_kv_layer(16, 16, 16, 10, 64, 40, 8, 100, e3.E3_BF16)  # head_dim 100
+    with pytest.raises(e3.E3Error) as ei:
+        e3.tree_verify_attn(16, bad, 16, 16, 1, 61, 32, 250, 0.1, 16, 16, None, 16, 1 << 30, stream=0)
+    assert ei.value.status == 2
+    with pytest.raises(e3.E3Error) as ei:  # unknown accept mode
+        e3.spec_accept(*([16] * 2), 1, 15, 3, *([16] * 4), 1000, *([16] * 3), 7, *([16] * 4), stream=0)
+    assert ei.value.status == 3
+    with pytest.raises(e3.E3Error) as ei:  # too many layers
+        e3.kv_compact([kv] * 200, 1, 16, 16, 6, 16, None, stream=0)
+    assert ei.value.status == 2
+    assert "kv_compact" in e3.lib().eagle3_last_error().decode()
+
+
+def test_product_path_does_not_reference_the_oracle():
+    pkg = os.path.join(ROOT, "eagle_speculative_decoding_round_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "eagle3_oracle" not in text, f
