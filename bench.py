@@ -402,7 +402,7 @@ def main():
     # the timed region: one graph of K rounds, with events at the phase boundaries
     K = args.steps
     phases = ["fuse", "expand", "tree", "verify", "lmhead", "accept", "compact"]
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(phases) + 1)] for _ in range(K)]
+    ev = [[graph_event() for _ in range(len(phases) + 1)] for _ in range(K)]
     from eagle_speculative_decoding_round_gb300 import eagle3 as e3
     from eagle_speculative_decoding_round_gb300.round import run_round
     graph = torch.cuda.CUDAGraph()
@@ -411,7 +411,8 @@ def main():
             w.bufs.kv_len.copy_(w.kv_len0)
             run_round_phased(w, ev[k], e3)
     torch.cuda.synchronize()
-    graph.replay()  # one untimed replay of the captured work
+    with torch.cuda.stream(s):
+        graph.replay()  # one untimed replay of the captured work
     torch.cuda.synchronize()
     launches_per_step = count_launches(cfg)
     clocks = ClockSampler(local)
@@ -422,15 +423,17 @@ def main():
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(s)
-    graph.replay()
-    t1.record(s)
+    with torch.cuda.stream(s):
+        t0.record(s)
+        graph.replay()
+        t1.record(s)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1)
     # keep the GPU busy a little longer so the clock sampler sees load
     extra = 0
     while extra < 3 and ms * (extra + 1) < 1500:
-        graph.replay()
+        with torch.cuda.stream(s):
+            graph.replay()
         extra += 1
     torch.cuda.synchronize()
     clk = clocks.stop()
@@ -495,6 +498,15 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def graph_event():
+    """A timing event that becomes an event-record node when captured in a graph."""
+    import torch
+    try:
+        return torch.cuda.Event(enable_timing=True, external=True)
+    except TypeError:  # older torch without graph event-record nodes
+        return torch.cuda.Event(enable_timing=True)
 
 
 def summarize(P):

@@ -149,7 +149,7 @@ E3_API e3_status lmhead_logits(const void* h, const void* W_lm, int M, int d, in
   E3_REQUIRE(h && W_lm && temp_per_row && logits && row_max && row_Q && row_argmax, E3_ERR_INVALID_ARG,
              "lmhead_logits: null pointer");
   E3_REQUIRE(valid_dtype(dt), E3_ERR_INVALID_ARG, "lmhead_logits: bad dtype");
-  E3_REQUIRE(M >= 1 && M <= 65536 && d >= 1 && V >= 1, E3_ERR_SHAPE, "lmhead_logits: M=%d d=%d V=%d", M, d, V);
+  E3_REQUIRE(M >= 1 && M <= 4000000 && d >= 1 && V >= 1, E3_ERR_SHAPE, "lmhead_logits: M=%d d=%d V=%d", M, d, V);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   e3_status st = launch_gemm_simt(h, h, h, d, W_lm, nullptr, logits, true, M, V, d, dt, s);
   if (st != E3_OK) return st;

@@ -197,7 +197,7 @@ E3_API size_t eagle3_verify_workspace_bytes(int B, int R, int n_q_heads, int n_k
  * h: [M][d] dtype dt; W_lm: [V][d] dtype dt; temp_per_row: [M] fp32;
  * logits: [M][V] fp32; row_max [M] fp32; row_Q [M] uint64; row_argmax [M] int32.
  * Non-finite logits set E3_DEV_ERR_NONFINITE.
- * Limits: 1 <= M <= 65536; bf16: d % 64 == 0, V % 4 == 0.
+ * Limits: 1 <= M <= 4000000; bf16: d % 64 == 0, V % 4 == 0.
  * ------------------------------------------------------------------------- */
 E3_API e3_status lmhead_logits(const void* h, const void* W_lm, int M, int d, int V,
                         const float* temp_per_row, float* logits, float* row_max,

@@ -213,8 +213,8 @@ def test_tree_build_page_example():
         sc.append(-1.0 * dmap[n] - 0.001 * i)
         dep.append(dmap[n])
     C = len(tok)
-    cand = e3.make_cand(*(to_dev(np.array(a, t)) for a, t in ((tok, np.int32), (par, np.int32), (sc, np.float32),
-                                                               (dep, np.int32))), C)
+    keep = [to_dev(np.array(a, t)) for a, t in ((tok, np.int32), (par, np.int32), (sc, np.float32), (dep, np.int32))]
+    cand = e3.make_cand(*keep, C)  # make_cand keeps raw addresses: `keep` holds the tensors alive
     R = C + 1
     out = {x: i32((1, R)) for x in ("tok", "parent", "depth", "pos")}
     mask = torch.zeros((1, R, 1), dtype=torch.int64, device="cuda")
