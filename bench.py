@@ -520,7 +520,7 @@ def run_round_phased(w, evs, e3):
     s = torch.cuda.current_stream()
     R = c.R
     evs[0].record(s)
-    e3.eagle3_fuse(b.h[0], b.h[1], b.h[2], b.W_f, None, b.g, c.M, c.d, c.d, c.dt, b.fuse_ws, b.fuse_ws_bytes)
+    e3.eagle3_fuse(b.h[0], b.h[1], b.h[2], b.W_f, None, b.g, c.M, c.d, c.d, c.dt, b.fuse_ws, b.fuse_ws_bytes, b.dev_err)
     evs[1].record(s)
     sizes, n_cand = c.frontier_sizes()
     for di, (F, off) in enumerate(sizes):

@@ -64,7 +64,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> 
             raise RuntimeError("nvcc failed")
     if force or jobs or not os.path.exists(LIB):
         tmp = LIB + f".tmp{os.getpid()}"
-        r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"], capture_output=True, text=True)
+        r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
         if r.returncode != 0:
             sys.stderr.write(r.stdout + r.stderr)
             raise RuntimeError("link failed")

@@ -49,27 +49,29 @@ E3_API const char* eagle3_last_error(void) { return g_err; }
 
 E3_API int eagle3_abi_version(void) { return 1; }
 
+static bool fuse_uses_tc(int d, int d_out, e3_dtype dt) { return dt == E3_BF16 && d % 64 == 0 && d_out >= 1; }
+
 E3_API size_t eagle3_fuse_workspace_bytes(int M, int d, int d_out, e3_dtype dt) {
-  (void)M;
-  (void)d;
-  (void)d_out;
-  (void)dt;
-  return 0;
+  if (M < 1 || d < 1 || d_out < 1) return 0;
+  return fuse_uses_tc(d, d_out, dt) ? tc_fuse_workspace_bytes(M, d, d_out) : 0;
 }
 
 E3_API e3_status eagle3_fuse(const void* h_low, const void* h_mid, const void* h_high, const void* W_f,
-                      const float* bias, void* g, int M, int d, int d_out, e3_dtype dt, void* ws,
-                      size_t ws_bytes, e3_stream_t stream) {
+                             const float* bias, void* g, int M, int d, int d_out, e3_dtype dt, void* ws,
+                             size_t ws_bytes, int32_t* dev_err, e3_stream_t stream) {
   g_err[0] = 0;
-  (void)ws;
-  (void)ws_bytes;
   E3_REQUIRE(h_low && h_mid && h_high && W_f && g, E3_ERR_INVALID_ARG, "eagle3_fuse: null pointer");
   E3_REQUIRE(valid_dtype(dt), E3_ERR_INVALID_ARG, "eagle3_fuse: bad dtype");
   E3_REQUIRE(M >= 1 && M <= 65536 && d >= 1 && d_out >= 1, E3_ERR_SHAPE, "eagle3_fuse: bad sizes M=%d d=%d d_out=%d",
              M, d, d_out);
   E3_REQUIRE(static_cast<long>(d) * 3 < (1L << 30), E3_ERR_SHAPE, "eagle3_fuse: d too large");
-  return launch_gemm_simt(h_low, h_mid, h_high, d, W_f, bias, g, dt == E3_F32, M, d_out, 3 * d, dt,
-                          reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (fuse_uses_tc(d, d_out, dt)) {
+    E3_REQUIRE(aligned16(h_low) && aligned16(h_mid) && aligned16(h_high) && aligned16(W_f), E3_ERR_INVALID_ARG,
+               "eagle3_fuse: bf16 operands must be 16-byte aligned");
+    return launch_fuse_tc(h_low, h_mid, h_high, W_f, bias, g, M, d, d_out, ws, ws_bytes, dev_err, s);
+  }
+  return launch_gemm_simt(h_low, h_mid, h_high, d, W_f, bias, g, dt == E3_F32, M, d_out, 3 * d, dt, s);
 }
 
 E3_API e3_status eagle3_expand(const float* draft_logits, int B, int F, int V, int k, int W, float inv_temp,
@@ -151,6 +153,10 @@ E3_API e3_status lmhead_logits(const void* h, const void* W_lm, int M, int d, in
   E3_REQUIRE(valid_dtype(dt), E3_ERR_INVALID_ARG, "lmhead_logits: bad dtype");
   E3_REQUIRE(M >= 1 && M <= 4000000 && d >= 1 && V >= 1, E3_ERR_SHAPE, "lmhead_logits: M=%d d=%d V=%d", M, d, V);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (dt == E3_BF16 && d % 64 == 0 && V % 4 == 0 && aligned16(logits)) {
+    E3_REQUIRE(aligned16(h) && aligned16(W_lm), E3_ERR_INVALID_ARG, "lmhead_logits: bf16 operands must be 16-byte aligned");
+    return launch_lmhead_tc(h, W_lm, M, d, V, temp_per_row, logits, row_max, row_Q, row_argmax, dev_err, s);
+  }
   e3_status st = launch_gemm_simt(h, h, h, d, W_lm, nullptr, logits, true, M, V, d, dt, s);
   if (st != E3_OK) return st;
   return launch_row_stats(logits, M, V, temp_per_row, row_max, row_Q, row_argmax, dev_err, s);

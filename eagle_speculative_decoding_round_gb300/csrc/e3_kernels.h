@@ -34,6 +34,14 @@ e3_status launch_gemm_simt(const void* a0, const void* a1, const void* a2, int d
 e3_status launch_row_stats(const float* logits, int M, int V, const float* temp, float* row_max,
                            uint64_t* row_Q, int32_t* row_argmax, int32_t* dev_err, cudaStream_t s);
 
+bool tc_gemm_supported(int d_k, int n_rows);
+size_t tc_fuse_workspace_bytes(int M, int d, int d_out);
+e3_status launch_fuse_tc(const void* h_low, const void* h_mid, const void* h_high, const void* W_f, const float* bias,
+                         void* g, int M, int d, int d_out, void* ws, size_t ws_bytes, int32_t* dev_err,
+                         cudaStream_t s);
+e3_status launch_lmhead_tc(const void* h, const void* W_lm, int M, int d, int V, const float* temp, float* logits,
+                           float* row_max, uint64_t* row_Q, int32_t* row_argmax, int32_t* dev_err, cudaStream_t s);
+
 e3_status launch_accept(const int32_t* tok, const int32_t* parent, int B, int R, int D, const float* logits,
                         const float* row_max, const uint64_t* row_Q, const int32_t* row_argmax, int V,
                         const float* temp, const uint32_t* u_acc, const uint32_t* u_bonus, int32_t* acc_len,

@@ -48,7 +48,7 @@ def _load() -> ctypes.CDLL:
     lib = ctypes.CDLL(LIB_PATH)
     P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     sig = {
-        "eagle3_fuse": (I, [P, P, P, P, P, P, I, I, I, I, P, S, P]),
+        "eagle3_fuse": (I, [P, P, P, P, P, P, I, I, I, I, P, S, P, P]),
         "eagle3_fuse_workspace_bytes": (S, [I, I, I, I]),
         "eagle3_expand": (I, [P, I, I, I, I, I, F, P, P, I, I, ctypes.POINTER(e3_cand), P, P, P, P]),
         "tree_build_mask": (I, [ctypes.POINTER(e3_cand), I, I, I, P, P, P, P, P, P, P, P]),
@@ -113,9 +113,10 @@ def eagle3_fuse_workspace_bytes(M, d, d_out, dt) -> int:
     return int(_lib.eagle3_fuse_workspace_bytes(M, d, d_out, dt))
 
 
-def eagle3_fuse(h_low, h_mid, h_high, W_f, bias, g, M, d, d_out, dt, ws=None, ws_bytes=0, stream=None):
+def eagle3_fuse(h_low, h_mid, h_high, W_f, bias, g, M, d, d_out, dt, ws=None, ws_bytes=0, dev_err=None,
+                stream=None):
     _check("eagle3_fuse", _lib.eagle3_fuse(ptr(h_low), ptr(h_mid), ptr(h_high), ptr(W_f), ptr(bias), ptr(g),
-                                           M, d, d_out, dt, ptr(ws), ws_bytes, _stream(stream)))
+                                           M, d, d_out, dt, ptr(ws), ws_bytes, ptr(dev_err), _stream(stream)))
 
 
 def eagle3_expand(draft_logits, B, F, V, k, W, inv_temp, parent_score, parent_id, depth, cand_offset,

@@ -150,7 +150,7 @@ def run_round(bufs: RoundBuffers, stream=None, write_tree_qkv=None, sm_scale=Non
     s = stream
     sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(c.hd)
     e3.eagle3_fuse(bufs.h[0], bufs.h[1], bufs.h[2], bufs.W_f, None, bufs.g, c.M, c.d, c.d, c.dt,
-                   bufs.fuse_ws, bufs.fuse_ws_bytes, stream=s)
+                   bufs.fuse_ws, bufs.fuse_ws_bytes, bufs.dev_err, stream=s)
     sizes, n_cand = c.frontier_sizes()
     for di, (F, off) in enumerate(sizes):
         e3.eagle3_expand(bufs.draft_logits[di], c.B, F, c.V, c.k, c.W, 1.0, bufs.f_score[di], bufs.f_id[di],

@@ -117,12 +117,14 @@ typedef struct {
  * bias: [d_out] fp32 or NULL; g: [M][d_out] dtype dt.
  * Limits: 1 <= M <= 65536; d % 64 == 0 and d_out % 128 == 0 for bf16
  * (any positive d, d_out for fp32).  Pointers 16-byte aligned.
- * ws: scratch of eagle3_fuse_workspace_bytes() bytes (device), or NULL if that is 0.
+ * ws: scratch of eagle3_fuse_workspace_bytes() bytes (device), or NULL if that is 0
+ * (bf16 with d % 64 == 0 runs split-K on the tensor cores and needs it).
+ * dev_err: E3_DEV_ERR_TIMEOUT if a bounded on-device wait ran out.
  * ------------------------------------------------------------------------- */
 E3_API e3_status eagle3_fuse(const void* h_low, const void* h_mid, const void* h_high,
                       const void* W_f, const float* bias, void* g, int M, int d,
                       int d_out, e3_dtype dt, void* ws, size_t ws_bytes,
-                      e3_stream_t stream);
+                      int32_t* dev_err, e3_stream_t stream);
 E3_API size_t eagle3_fuse_workspace_bytes(int M, int d, int d_out, e3_dtype dt);
 
 /* ---------------------------------------------------------------------------

@@ -26,7 +26,8 @@ def i32(n, fill=0):
 # ------------------------------------------------------------------ fusion ----
 
 @pytest.mark.parametrize("M,d,dout,dt", [(3, 256, 256, "f32"), (1, 256, 256, "f32"), (7, 4096, 4096, "bf16"),
-                                         (13, 256, 384, "bf16"), (130, 512, 256, "bf16")])
+                                         (13, 256, 384, "bf16"), (130, 512, 256, "bf16"), (1, 64, 128, "bf16"),
+                                         (300, 128, 200, "bf16"), (5, 96, 256, "bf16")])
 def test_fuse(M, d, dout, dt):
     hs = [synth.normal(M * d + dout, f"h{i}", (M, d), 0.02) for i in range(3)]
     W = synth.normal(M * d + dout, "Wf", (dout, 3 * d), 0.02)
@@ -46,8 +47,10 @@ def test_fuse(M, d, dout, dt):
     ws_b = e3.eagle3_fuse_workspace_bytes(M, d, dout, code)
     ws = torch.empty(max(ws_b, 16), dtype=torch.uint8, device="cuda")
     bt = to_dev(bias) if bias is not None else None
-    e3.eagle3_fuse(hd_[0], hd_[1], hd_[2], Wt, bt, g, M, d, dout, code, ws, ws_b)
+    err = i32(1)
+    e3.eagle3_fuse(hd_[0], hd_[1], hd_[2], Wt, bt, g, M, d, dout, code, ws, ws_b, err)
     torch.cuda.synchronize()
+    assert int(err.item()) == 0
     ref = oracle.fuse(hs[0], hs[1], hs[2], W, bias)
     assert_close(host(g), ref, tol, "fuse")
 
@@ -55,7 +58,8 @@ def test_fuse(M, d, dout, dt):
 # ----------------------------------------------------------------- LM head ----
 
 @pytest.mark.parametrize("M,d,V,dt", [(15, 256, 1024, "f32"), (61, 4096, 128256, "bf16"), (3, 128, 1000, "bf16"),
-                                      (200, 256, 4096, "bf16")])
+                                      (200, 256, 4096, "bf16"), (300, 192, 2048, "bf16"), (1, 64, 256, "bf16"),
+                                      (20, 256, 1000, "bf16"), (40, 100, 512, "bf16")])
 def test_lmhead_logits_and_stats(M, d, V, dt):
     h = synth.normal(V + M, "h", (M, d), 1.0)
     W = synth.normal(V + M, "Wlm", (V, d), 4.0 / math.sqrt(d))
