@@ -134,6 +134,12 @@ __device__ __forceinline__ float unord_f32(uint32_t o) {
   return __uint_as_float(b);
 }
 
+// Two floats -> packed bf16x2 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
 // (value desc, id asc) packed so that a larger key is better.
 __device__ __forceinline__ uint64_t pack_best(float v, uint32_t id) {
   return (static_cast<uint64_t>(ord_f32(v)) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - id);

@@ -15,8 +15,8 @@
 //
 // One CTA per request.  Thread 0 walks the tree (at most D+1 rows); the bonus
 // draw is an inverse-CDF search over the whole vocabulary done by all threads:
-// per-thread chunk sums of the fixed-point masses, a block exclusive scan, and
-// a rescan of the one chunk that holds the target.
+// per-warp segment sums of the fixed-point masses, an exclusive scan of the
+// warp sums, and a rescan of the one segment that holds the target.
 #include "e3_common.cuh"
 #include "e3_kernels.h"
 
@@ -24,7 +24,7 @@ namespace e3 {
 
 namespace {
 
-constexpr int kAcceptThreads = 256;
+constexpr int kAcceptThreads = 1024;
 
 __device__ __forceinline__ bool is_removed(const int* removed, int nrem, int j) {
   for (int q = 0; q < nrem; ++q)
@@ -43,7 +43,7 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
   __shared__ int s_removed[256];
   __shared__ int s_nrem, s_u, s_acc, s_bonus, s_err;
   __shared__ unsigned long long s_x;
-  __shared__ uint64_t s_scan[kAcceptThreads / 32];
+  __shared__ uint64_t s_scan[32];
   __shared__ int s_path[E3_MAX_DEPTH + 1];
   const int b = blockIdx.x;
   const float T = temp[b];
@@ -51,6 +51,20 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
   for (int i = threadIdx.x; i < R; i += blockDim.x) {
     s_tok[i] = tok[static_cast<size_t>(b) * R + i];
     s_par[i] = parent[static_cast<size_t>(b) * R + i];
+  }
+  // prefetch, in parallel, everything the walk reads: each node's statistics and
+  // each child's logit under its parent's row
+  __shared__ float s_m[256], s_zc[256];
+  __shared__ unsigned long long s_Q[256];
+  __shared__ int s_am[256];
+  __syncthreads();
+  for (int i = threadIdx.x; i < R; i += blockDim.x) {
+    const size_t row = static_cast<size_t>(b) * R + i;
+    s_m[i] = row_max[row];
+    s_Q[i] = row_Q[row];
+    s_am[i] = row_argmax[row];
+    const int p = s_par[i], t = s_tok[i];
+    s_zc[i] = (i > 0 && p >= 0 && p < R && t >= 0 && t < V) ? logits[(static_cast<size_t>(b) * R + p) * V + t] : 0.0f;
   }
   if (threadIdx.x == 0) {
     s_err = 0;
@@ -62,10 +76,9 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
   if (threadIdx.x == 0) {
     int u = 0, a = 0;
     for (;;) {
-      const size_t row = static_cast<size_t>(b) * R + u;
-      const float m = row_max[row];
-      uint64_t Rm = row_Q[row];
-      const int am = row_argmax[row];
+      const float m = s_m[u];
+      uint64_t Rm = s_Q[u];
+      const int am = s_am[u];
       if (am < 0 || !isfinite(m)) {
         s_err = E3_DEV_ERR_NONFINITE;
         break;
@@ -82,7 +95,7 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
           continue;
         }
         if (t < 0 || t >= V) continue;
-        const uint64_t q = fx_mass(__fmul_rn(logits[row * V + t], it), m);
+        const uint64_t q = fx_mass(__fmul_rn(s_zc[c], it), m);
         if (mulhi32(u_acc[static_cast<size_t>(b) * R + c], Rm) < q) {
           accepted = c;
           break;
@@ -109,39 +122,47 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
   __syncthreads();
   const int err = s_err;
   if (!err && T > 0.0f) {
-    // inverse CDF over the residual, ascending token ids
+    // inverse CDF over the residual, ascending token ids.  Warp w owns the
+    // contiguous segment [w*seg, (w+1)*seg) and sums it with lane-strided loads;
+    // an exclusive scan of the 32 warp sums locates the segment holding x, which
+    // its warp rescans 32 tokens at a time (warp scan + ballot).
     const int u = s_u, nrem = s_nrem;
     const uint64_t x = s_x;
     const size_t row = static_cast<size_t>(b) * R + u;
     const float m = row_max[row];
     const float* z = logits + row * V;
-    const int chunk = (V + blockDim.x - 1) / blockDim.x;
-    const int j0 = threadIdx.x * chunk, j1 = min(V, j0 + chunk);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int seg = (V + nw - 1) / nw;
+    const int j0 = min(V, wid * seg), j1 = min(V, j0 + seg);
     uint64_t local = 0;
-    for (int j = j0; j < j1; ++j)
-      if (!is_removed(s_removed, nrem, j)) local += fx_mass(__fmul_rn(z[j], it), m);
-    // block exclusive scan of the chunk sums
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    uint64_t incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= o) incl += y;
+#pragma unroll 8
+    for (int j = j0 + lane; j < j1; j += 32) {
+      const float zj = z[j];
+      if (!is_removed(s_removed, nrem, j)) local += fx_mass(__fmul_rn(zj, it), m);
     }
-    if (lane == 31) s_scan[wid] = incl;
+    local = warp_reduce(local, SumU64());
+    if (lane == 0) s_scan[wid] = local;
     __syncthreads();
-    uint64_t wbase = 0;
-    for (int w = 0; w < wid; ++w) wbase += s_scan[w];
-    const uint64_t excl = wbase + incl - local;
-    if (x >= excl && x < excl + local) {
-      uint64_t cum = excl;
-      for (int j = j0; j < j1; ++j) {
-        if (is_removed(s_removed, nrem, j)) continue;
-        cum += fx_mass(__fmul_rn(z[j], it), m);
-        if (cum > x) {
-          s_bonus = j;
+    uint64_t excl = 0;
+    for (int w = 0; w < wid; ++w) excl += s_scan[w];
+    if (x >= excl && x < excl + local) {  // uniform within the warp
+      uint64_t base = excl;
+      for (int c0 = j0; c0 < j1; c0 += 32) {
+        const int j = c0 + lane;
+        uint64_t q = 0;
+        if (j < j1 && !is_removed(s_removed, nrem, j)) q = fx_mass(__fmul_rn(z[j], it), m);
+        uint64_t incl = q;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, base + incl > x);
+        if (hit) {
+          if (lane == __ffs(hit) - 1) s_bonus = j;
           break;
         }
+        base += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
     }
     __syncthreads();

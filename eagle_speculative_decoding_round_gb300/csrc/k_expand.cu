@@ -4,12 +4,15 @@
 // tokens as children; "论文专题讲解：EAGLE-3", Draft tree 配置: 10 nodes are
 // chosen per expansion, by draft confidence.
 //
-// Kernel 1 (one CTA per frontier row): stream the row once for the maximum, a
-// per-thread top-KMAX list (packed (value, id) keys, so ties go to the lower
-// token id) and the non-finite check; merge the lists warp by warp; stream the
-// row again (L2-resident) for the fixed-point mass Q; write the k children.
+// Kernel 1 (one 8-CTA cluster per frontier row): each CTA reads its eighth of
+// the row once into shared memory while building a per-thread top-KMAX list
+// (packed (value, id) keys, so ties go to the lower token id); the row maximum,
+// the fixed-point mass Q and the top-k lists are combined through distributed
+// shared memory; CTA 0 writes the k children.
 // Kernel 2 (one CTA per request): sort the F*k children by (score desc,
 // candidate index asc) in shared memory and emit the next frontier.
+#include <cooperative_groups.h>
+
 #include "e3_common.cuh"
 #include "e3_kernels.h"
 
@@ -17,7 +20,8 @@ namespace e3 {
 
 namespace {
 
-constexpr int kExpandThreads = 512;
+constexpr int kExpandThreads = 256;
+constexpr int kCluster = 8;  // CTAs per frontier row
 
 template <int KMAX>
 __device__ __forceinline__ void topk_insert(uint64_t (&keys)[KMAX], uint64_t key) {
@@ -47,85 +51,130 @@ __device__ void warp_merge_topk(uint64_t (&keys)[KMAX], int k, uint64_t* out) {
   }
 }
 
+// One 8-CTA cluster per frontier row.  CTA r keeps chunk r of the row in shared
+// memory; the row maximum, the non-finite flag, the fixed-point mass and the
+// per-CTA top-k lists are exchanged through distributed shared memory.
 template <int KMAX>
-__global__ void __launch_bounds__(kExpandThreads)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kExpandThreads)
 expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float it,
                    const float* __restrict__ parent_score, const int32_t* __restrict__ parent_id,
                    int depth, int cand_offset, e3_cand c, int32_t* dev_err) {
-  const int row = blockIdx.x;  // b * F + f
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int row = blockIdx.x / kCluster;  // b * F + f
   const int b = row / F, f = row % F;
   const float* z = logits + static_cast<size_t>(row) * V;
+  extern __shared__ float4 chunk4[];
   __shared__ uint64_t warp_lists[kExpandThreads / 32][E3_MAX_TOPK];
+  __shared__ uint64_t ltop[E3_MAX_TOPK];   // this CTA's best k keys
+  __shared__ uint64_t lbest;               // this CTA's best key
+  __shared__ uint64_t lQ;                  // this CTA's mass
+  __shared__ int lbad;
   __shared__ uint64_t red64[32];
   __shared__ int redi[32];
+  __shared__ uint64_t all_top[kCluster * E3_MAX_TOPK];
 
+  // chunk of this CTA, in float4 units (the row is 16-byte aligned and V % 4 == 0
+  // on the vector path; otherwise element-wise)
+  const bool vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
+  const int nvec = vec ? (V >> 2) : V;
+  const int per = (nvec + kCluster - 1) / kCluster;
+  const int v0 = min(nvec, rank * per), v1 = min(nvec, v0 + per);
+  float* chunk = reinterpret_cast<float*>(chunk4);
+
+  // stage the chunk (scaled by 1/T) in shared memory with independent, unrolled loads
+  if (vec) {
+    const float4* z4 = reinterpret_cast<const float4*>(z);
+#pragma unroll 8
+    for (int q = v0 + threadIdx.x; q < v1; q += blockDim.x) {
+      float4 v = __ldg(z4 + q);
+      v.x = __fmul_rn(v.x, it);
+      v.y = __fmul_rn(v.y, it);
+      v.z = __fmul_rn(v.z, it);
+      v.w = __fmul_rn(v.w, it);
+      chunk4[q - v0] = v;
+    }
+  } else {
+#pragma unroll 8
+    for (int j = v0 + threadIdx.x; j < v1; j += blockDim.x) chunk[j - v0] = __fmul_rn(__ldg(z + j), it);
+  }
+  __syncthreads();
+  const int e0 = vec ? 4 * v0 : v0;  // token id of chunk[0]
+  const int n_local = vec ? 4 * (v1 - v0) : (v1 - v0);
   uint64_t keys[KMAX];
 #pragma unroll
   for (int i = 0; i < KMAX; ++i) keys[i] = 0ull;
   int bad = 0;
-  const bool vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
-  if (vec) {
-    const float4* z4 = reinterpret_cast<const float4*>(z);
-    for (int q = threadIdx.x; q < (V >> 2); q += blockDim.x) {
-      float4 v = __ldg(z4 + q);
-      float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        bad |= !isfinite(e[u]);
-        topk_insert(keys, pack_best(__fmul_rn(e[u], it), static_cast<uint32_t>(4 * q + u)));
-      }
-    }
-  } else {
-    for (int j = threadIdx.x; j < V; j += blockDim.x) {
-      float v = __ldg(z + j);
-      bad |= !isfinite(v);
-      topk_insert(keys, pack_best(__fmul_rn(v, it), static_cast<uint32_t>(j)));
-    }
+  for (int j = threadIdx.x; j < n_local; j += blockDim.x) {
+    const float sj = chunk[j];
+    bad |= !isfinite(sj);
+    topk_insert(keys, pack_best(sj, static_cast<uint32_t>(e0 + j)));
   }
   bad = block_reduce(bad, OrI(), redi);
-  if (bad) {
-    if (threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_NONFINITE);
-    return;
-  }
   const int warp = threadIdx.x >> 5;
   warp_merge_topk(keys, k, warp_lists[warp]);
   __syncthreads();
-  __shared__ uint64_t top[E3_MAX_TOPK];
   if (warp == 0) {
     const int nw = blockDim.x >> 5;
     uint64_t lk[KMAX];
 #pragma unroll
     for (int i = 0; i < KMAX; ++i)
       lk[i] = (static_cast<int>(threadIdx.x) < nw && i < k) ? warp_lists[threadIdx.x][i] : 0ull;
-    warp_merge_topk(lk, k, top);
+    warp_merge_topk(lk, k, ltop);
   }
   __syncthreads();
-  const float m = unord_f32(static_cast<uint32_t>(top[0] >> 32));
-  // second pass: fixed-point mass of the row
+  if (threadIdx.x == 0) {
+    lbest = ltop[0];
+    lbad = bad;
+  }
+  cluster.sync();  // every CTA's maximum and flag are visible
+  uint64_t gbest = 0;
+  int gbad = 0;
+  for (int r = 0; r < kCluster; ++r) {
+    gbest = max(gbest, static_cast<uint64_t>(*cluster.map_shared_rank(&lbest, r)));
+    gbad |= *cluster.map_shared_rank(&lbad, r);
+  }
+  if (gbad) {
+    if (rank == 0 && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_NONFINITE);
+    cluster.sync();  // nobody leaves while a peer may still read its shared memory
+    return;
+  }
+  const float m = unord_f32(static_cast<uint32_t>(gbest >> 32));
   uint64_t Q = 0;
-  if (vec) {
-    const float4* z4 = reinterpret_cast<const float4*>(z);
-    for (int q = threadIdx.x; q < (V >> 2); q += blockDim.x) {
-      float4 v = __ldg(z4 + q);
-      Q += fx_mass(__fmul_rn(v.x, it), m) + fx_mass(__fmul_rn(v.y, it), m) +
-           fx_mass(__fmul_rn(v.z, it), m) + fx_mass(__fmul_rn(v.w, it), m);
-    }
-  } else {
-    for (int j = threadIdx.x; j < V; j += blockDim.x) Q += fx_mass(__fmul_rn(__ldg(z + j), it), m);
-  }
+  for (int j = threadIdx.x; j < n_local; j += blockDim.x) Q += fx_mass(chunk[j], m);
   Q = block_reduce(Q, SumU64(), red64);
-  if (threadIdx.x < k) {
-    const int r = threadIdx.x;
-    const float ell = fx_ell(Q);
-    const uint32_t t = packed_id(top[r]);
-    const float sc = unord_f32(static_cast<uint32_t>(top[r] >> 32));
-    const float ps = parent_score[row];
-    const size_t ci = static_cast<size_t>(b) * c.cap + cand_offset + f * k + r;
-    c.tok[ci] = static_cast<int32_t>(t);
-    c.parent[ci] = parent_id[row];
-    c.score[ci] = __fsub_rn(__fadd_rn(ps, __fsub_rn(sc, m)), ell);
-    c.depth[ci] = depth;
+  if (threadIdx.x == 0) lQ = Q;
+  cluster.sync();  // masses and top-k lists are visible
+  if (rank == 0) {
+    for (int i = threadIdx.x; i < kCluster * k; i += blockDim.x)
+      all_top[i] = *cluster.map_shared_rank(&ltop[i % k], i / k);
+    uint64_t Qt = 0;
+    for (int r = 0; r < kCluster; ++r) Qt += *cluster.map_shared_rank(&lQ, r);
+    __syncthreads();
+    __shared__ uint64_t top[E3_MAX_TOPK];
+    if (warp == 0) {
+      uint64_t lk[KMAX];
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i)
+        lk[i] = (static_cast<int>(threadIdx.x) < kCluster && i < k) ? all_top[threadIdx.x * k + i] : 0ull;
+      warp_merge_topk(lk, k, top);
+    }
+    __syncthreads();
+    if (threadIdx.x < k) {
+      const int r = threadIdx.x;
+      const float ell = fx_ell(Qt);
+      const uint32_t t = packed_id(top[r]);
+      const float sc = unord_f32(static_cast<uint32_t>(top[r] >> 32));
+      const float ps = parent_score[row];
+      const size_t ci = static_cast<size_t>(b) * c.cap + cand_offset + f * k + r;
+      c.tok[ci] = static_cast<int32_t>(t);
+      c.parent[ci] = parent_id[row];
+      c.score[ci] = __fsub_rn(__fadd_rn(ps, __fsub_rn(sc, m)), ell);
+      c.depth[ci] = depth;
+    }
   }
+  cluster.sync();  // rank 0 is done reading the peers' shared memory
 }
 
 }  // namespace
@@ -163,10 +212,22 @@ e3_status launch_expand(const float* logits, int B, int F, int V, int k, int W, 
                         int cand_offset, const e3_cand& c, int32_t* next_id, float* next_score,
                         int32_t* dev_err, cudaStream_t s) {
   const int rows = B * F;
-  dim3 grid(rows), block(kExpandThreads);
-#define E3_EXPAND_CASE(KM)                                                                   \
-  expand_rows_kernel<KM><<<grid, block, 0, s>>>(logits, F, V, k, inv_temp, parent_score,     \
-                                                parent_id, depth, cand_offset, c, dev_err)
+  dim3 grid(rows * kCluster), block(kExpandThreads);
+  const bool vec = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
+  const int nvec = vec ? V / 4 : V;
+  const int per = (nvec + kCluster - 1) / kCluster;
+  const size_t smem = static_cast<size_t>(per) * (vec ? 16 : 4) + 16;
+  if (smem > 200 * 1024) return E3_ERR_SHAPE;
+#define E3_EXPAND_CASE(KM)                                                                               \
+  do {                                                                                                   \
+    static bool attr_done = false;                                                                       \
+    if (!attr_done) {                                                                                    \
+      cudaFuncSetAttribute(expand_rows_kernel<KM>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024); \
+      attr_done = true;                                                                                  \
+    }                                                                                                    \
+    expand_rows_kernel<KM><<<grid, block, smem, s>>>(logits, F, V, k, inv_temp, parent_score, parent_id,  \
+                                                     depth, cand_offset, c, dev_err);                    \
+  } while (0)
   if (k <= 2)
     E3_EXPAND_CASE(2);
   else if (k <= 4)

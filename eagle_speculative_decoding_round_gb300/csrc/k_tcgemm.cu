@@ -306,6 +306,7 @@ row_q_kernel(const float* __restrict__ logits, int V, const float* __restrict__ 
   uint64_t Q = 0;
   int bad = 0;
   const float4* z4 = reinterpret_cast<const float4*>(z);
+#pragma unroll 8
   for (int q = threadIdx.x; q < (V >> 2); q += blockDim.x) {
     const float4 v = z4[q];
     bad |= !isfinite(v.x) | !isfinite(v.y) | !isfinite(v.z) | !isfinite(v.w);

@@ -392,7 +392,9 @@ verify_mma_kernel(const __nv_bfloat16* __restrict__ Q, e3_kv_layer kv, const int
 }
 
 // ---------------------------------------------------------------------------
-// Merge of the segments: one warp per (b, i, h) row.
+// Merge of the segments: one warp per (b, i, h) row.  Lanes load the segments'
+// (m, l) in parallel; each lane owns HD/32 consecutive output dims and adds the
+// weighted partial vectors with independent loads.
 // ---------------------------------------------------------------------------
 template <typename T, int HD>
 __global__ void __launch_bounds__(256)
@@ -408,31 +410,46 @@ verify_merge_kernel(e3_kv_layer kv, const int32_t* __restrict__ kv_len, VerifyGe
   const int ih = static_cast<int>(row % (static_cast<long>(g.R) * g.H));
   const int P = kv_len[b];
   if (!kv_capacity_ok(kv, P, g.R, g.max_kv_len)) return;
-  const int n_pre_b = (P + g.chunk - 1) / g.chunk;  // segments that hold keys
+  const int n_pre_b = (P + g.chunk - 1) / g.chunk;  // prefix segments that hold keys
+  const int nseg = n_pre_b + 1;                     // + the tree segment
+  const size_t stride = static_cast<size_t>(g.R) * g.H;
+  const size_t base = static_cast<size_t>(b) * g.S * stride + ih;
+  auto seg_id = [&](int q) { return q < n_pre_b ? q : g.n_pre; };
   float M = -INFINITY;
-  for (int s = 0; s <= g.n_pre; ++s) {
-    if (s < g.n_pre && s >= n_pre_b) continue;
-    const float2 ml = ws_ml[(static_cast<size_t>(b) * g.S + s) * g.R * g.H + ih];
-    if (ml.y > 0.0f) M = fmaxf(M, ml.x);
+  for (int q0 = 0; q0 < nseg; q0 += 32) {
+    const int q = q0 + lane;
+    if (q < nseg) {
+      const float2 ml = ws_ml[base + seg_id(q) * stride];
+      if (ml.y > 0.0f) M = fmaxf(M, ml.x);
+    }
   }
+  M = warp_reduce(M, MaxF());
   float acc[PER];
 #pragma unroll
   for (int u = 0; u < PER; ++u) acc[u] = 0.0f;
   float den = 0.0f;
-  for (int s = 0; s <= g.n_pre; ++s) {
-    if (s < g.n_pre && s >= n_pre_b) continue;
-    const size_t rec = (static_cast<size_t>(b) * g.S + s) * g.R * g.H + ih;
-    const float2 ml = ws_ml[rec];
-    if (!(ml.y > 0.0f)) continue;
-    const float w = ml.y * exp2f(ml.x - M);
+  for (int q0 = 0; q0 < nseg; q0 += 32) {
+    const int q = q0 + lane;
+    float w = 0.0f;
+    if (q < nseg) {
+      const float2 ml = ws_ml[base + seg_id(q) * stride];
+      w = ml.y > 0.0f ? ml.y * exp2f(ml.x - M) : 0.0f;
+    }
     den += w;
+    const int nq = min(32, nseg - q0);
+#pragma unroll 4
+    for (int j = 0; j < nq; ++j) {
+      const float wj = __shfl_sync(0xFFFFFFFFu, w, j);
+      const float* src = ws_o + (base + seg_id(q0 + j) * stride) * HD + lane * PER;
 #pragma unroll
-    for (int u = 0; u < PER; ++u) acc[u] = fmaf(w, ws_o[rec * HD + lane + 32 * u], acc[u]);
+      for (int u = 0; u < PER; ++u) acc[u] = fmaf(wj, src[u], acc[u]);
+    }
   }
+  den = warp_reduce(den, [](float a, float c) { return a + c; });
   const float inv = den > 0.0f ? 1.0f / den : 0.0f;
-  T* out = O + static_cast<size_t>(row) * HD;
+  T* out = O + static_cast<size_t>(row) * HD + lane * PER;
 #pragma unroll
-  for (int u = 0; u < PER; ++u) st_elem(out, lane + 32 * u, acc[u] * inv);
+  for (int u = 0; u < PER; ++u) st_elem(out, u, acc[u] * inv);
   if (lane == 0) lse[row] = (M + log2f(den)) * kLn2;
 }
 
@@ -463,6 +480,7 @@ VerifyGeom make_geom(int B, int R, int H, int KVH, int hd, int max_kv_len, bool 
   long chunk = (max_kv_len + splits - 1) / splits;
   chunk = ((chunk + 63) / 64) * 64;
   if (chunk < 64) chunk = 64;
+  if (mma && chunk < 256) chunk = 256;  // two 128-key tiles per tensor-core CTA at least
   g.chunk = static_cast<int>(chunk);
   g.n_pre = static_cast<int>((max_kv_len + chunk - 1) / chunk);
   g.S = g.n_pre + 1;
@@ -494,7 +512,11 @@ e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_
   ml_addr = (ml_addr + 15) & ~static_cast<uintptr_t>(15);
   float2* ws_ml = reinterpret_cast<float2*>(ml_addr);
 
-  if (mma) {
+  if (mma && verify_tc_supported(kv, H)) {
+    e3_status st = launch_verify_tc(Q, kv, kv_len, mask, B, R, H, max_kv_len, sm_scale, g.n_pre, g.S, g.chunk, ws_o,
+                                    ws_ml, dev_err, s);
+    if (st != E3_OK) return st;
+  } else if (mma) {
     dim3 grid(g.RG * g.S, kv.n_kv_heads, B);
 #define E3_MMA_CASE(HDV)                                                                           \
   do {                                                                                             \

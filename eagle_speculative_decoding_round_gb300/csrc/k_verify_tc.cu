@@ -1,0 +1,511 @@
+// k_verify_tc.cu -- tree_verify_attn on the 5th-generation tensor cores (bf16,
+// head_dim 128, pages of a multiple of 64 tokens).
+//
+// Same segment decomposition as the mma.sync kernel in k_verify.cu ("EAGLE-3 投机
+// 解码与 USP 长序列训练优化", USP 核心设计：三步走: the prefix is the main segment,
+// split across CTAs, the tree is the branch segment; all are merged by their
+// log-sum-exp), and the same partial (o, m, l) records, merged by
+// verify_merge_kernel.  The mask is the ancestor-only tree mask of "EAGLE 系列与
+// DFlash", §二 关键新增步骤②.
+//
+// One CTA = (segment, 128-query-row group) of one KV head of one request.  The
+// 128 rows are the G query heads of 128/G consecutive tree nodes (a 3-D TMA box
+// over Q[B*R][H][hd]).  Keys stream in tiles of 128 (two 64-token page boxes per
+// operand):
+//   S = Q K^T    tcgen05.mma, M = 128 rows, N = 128 keys, K = head_dim (K-major)
+//   softmax      one thread per query row reads its TMEM lane; running max and
+//                sum in registers; P (bf16) written to shared memory as a K-major
+//                128-byte-swizzled operand
+//   O_t = P V    tcgen05.mma, N = head_dim, K = keys; V is used in place as an
+//                MN-major operand (rows of 64 head-dim values per key)
+//   O += O_t     accumulated in registers with the online-softmax correction.
+// Warps: 0 TMA, 1 TMEM owner + MMA issuer, 2..9 softmax/epilogue (two warps per
+// TMEM lane quarter, each owning half of the keys and half of the head dims).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "e3_common.cuh"
+#include "e3_kernels.h"
+
+namespace e3 {
+
+namespace {
+
+constexpr int kRows = 128;      // query rows per CTA
+constexpr int kKeys = 128;      // keys per tile
+constexpr int kHD = 128;        // head dim
+constexpr int kHalf = 64;       // head-dim (or key) elements per 128-byte row
+constexpr int kBox = kHalf * kHalf * 2;        // 64 x 64 bf16 = 8 KB
+constexpr int kQBytes = kRows * kHD * 2;       // 32 KB (two 16 KB halves)
+constexpr int kKVBytes = kKeys * kHD * 2;      // 32 KB per operand per tile
+constexpr int kStages = 2;
+constexpr int kPBytes = kRows * kKeys * 2;     // 32 KB
+constexpr int kSmem = 1024 + kQBytes + kStages * 2 * kKVBytes + kPBytes + 256 + 6 * 128 * 4 + 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr unsigned long long kWaitNs = 1000000000ull;
+
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(n));
+}
+__device__ __forceinline__ void bar_expect(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t par) {
+  uint32_t ok;
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(ok)
+               : "r"(su32(b)), "r"(par)
+               : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t par, volatile int* abort) {
+  if (bar_try(b, par)) return true;
+  const uint64_t t0 = gtimer();
+  for (;;) {
+    if (bar_try(b, par)) return true;
+    if (*abort) return false;
+    if (gtimer() - t0 > kWaitNs) {
+      *abort = 1;
+      return false;
+    }
+    __nanosleep(32);
+  }
+}
+__device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* m, int x, int y, uint64_t* b) {
+  asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+                   "r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(su32(b))
+               : "memory");
+}
+__device__ __forceinline__ void tma3d(void* dst, const CUtensorMap* m, int x, int y, int z, uint64_t* b) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::
+          "r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(su32(b))
+      : "memory");
+}
+// 128-byte-swizzled smem descriptor; lbo/sbo in bytes.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+// kind::f16 instruction descriptor: bf16 x bf16 -> f32, M x N, operand majors.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::
+                   "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void umma_commit(uint64_t* b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// bit j set iff lo <= T0 + j < hi (j < 32)
+__device__ __forceinline__ uint32_t range_bits32(int T0, int lo, int hi) {
+  const int a = max(lo - T0, 0), e = min(hi - T0, 32);
+  if (e <= a) return 0u;
+  const uint32_t upto = e >= 32 ? 0xFFFFFFFFu : ((1u << e) - 1u);
+  return upto & ~((1u << a) - 1u);
+}
+// bit j = mask bit (j0 + j) of an ancestor row of `words` uint64 words, 0 outside it
+__device__ __forceinline__ uint32_t mask_bits32(const uint64_t* row, int words, int j0) {
+  uint32_t out = 0;
+  const int w0 = j0 >> 6;  // floor division (j0 may be negative)
+  for (int w = w0; w <= w0 + 1; ++w) {
+    if (w < 0 || w >= words) continue;
+    const uint64_t bits = row[w];
+    const int sh = w * 64 - j0;  // position of word bit 0 in the output
+    if (sh >= 0) {
+      if (sh < 32) out |= static_cast<uint32_t>(bits << sh);
+    } else if (-sh < 64) {
+      out |= static_cast<uint32_t>(bits >> (-sh));
+    }
+  }
+  return out;
+}
+
+struct TcGeom {
+  int B, R, H, KVH, G, n_pre, S, chunk, RG, max_kv_len;
+  int page_size, max_pages, n_pages;
+  const int32_t* page_table;
+};
+
+__device__ __forceinline__ int page_of(const TcGeom& g, int b, int t, bool* ok) {
+  const int pi = t / g.page_size;
+  if (pi < 0 || pi >= g.max_pages) {
+    *ok = false;
+    return 0;
+  }
+  const int p = g.page_table[static_cast<size_t>(b) * g.max_pages + pi];
+  if (p < 0 || p >= g.n_pages) {
+    *ok = false;
+    return 0;
+  }
+  return p;
+}
+
+__global__ void __launch_bounds__(320, 1)
+verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                 const __grid_constant__ CUtensorMap tmV, TcGeom g, const int32_t* __restrict__ kv_len,
+                 const uint64_t* __restrict__ mask, float sm_scale, float* __restrict__ ws_o,
+                 float2* __restrict__ ws_ml, int32_t* dev_err) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sQ = sm;                                  // [2 halves][128 rows][128 B]
+  unsigned char* sKV = sQ + kQBytes;                       // [stage][K | V][2 halves][128 keys][128 B]
+  unsigned char* sP = sKV + kStages * 2 * kKVBytes;        // [2 key halves][128 rows][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kPBytes);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;    // [kStages]
+  uint64_t* kv_empty = bars + 3;   // [kStages]
+  uint64_t* s_full = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* o_full = bars + 7;
+  uint64_t* xch = bars + 8;        // [4] row-maximum exchange of the two halves, per lane quarter
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rg = blockIdx.x % g.RG, s = blockIdx.x / g.RG;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int P = kv_len[b];
+  const long need = static_cast<long>(P) + g.R;
+  if (P < 0 || P > g.max_kv_len || need > static_cast<long>(g.max_pages) * g.page_size) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
+    return;
+  }
+  const bool tree = (s == g.n_pre);
+  int k0, k1;  // logical key range of this segment
+  if (tree) {
+    k0 = P;
+    k1 = P + g.R;
+  } else {
+    k0 = s * g.chunk;
+    k1 = min(P, k0 + g.chunk);
+  }
+  const int t_begin = k0 & ~(kHalf - 1);  // 64-aligned start
+  const int ntile = k1 > k0 ? (k1 - t_begin + kKeys - 1) / kKeys : 0;
+  const int nodes_per_tile = kRows / g.G;
+  const int i0 = rg * nodes_per_tile;  // first node of this row group
+
+  if (threadIdx.x == 0) {
+    bar_init(q_full, 1);
+    for (int st = 0; st < kStages; ++st) {
+      bar_init(&kv_full[st], 1);
+      bar_init(&kv_empty[st], 1);
+    }
+    bar_init(s_full, 1);
+    bar_init(p_full, 256);
+    bar_init(o_full, 1);
+    for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], 64);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)), "r"(256));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  fence_before();
+  __syncthreads();
+  fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem, tO = tmem + kKeys;
+
+  if (warp == 0) {
+    if (lane == 0 && ntile > 0) {
+      bar_expect(q_full, kQBytes);
+      for (int h = 0; h < 2; ++h)
+        tma3d(sQ + h * (kQBytes / 2), &tmQ, h * kHalf, kvh * g.G, b * g.R + i0, q_full);
+      bool okp = true;
+      for (int t = 0; t < ntile; ++t) {
+        const int st = t % kStages;
+        if (!bar_wait(&kv_empty[st], ((t / kStages) & 1) ^ 1, abort)) break;
+        unsigned char* kst = sKV + st * 2 * kKVBytes;
+        unsigned char* vst = kst + kKVBytes;
+        bar_expect(&kv_full[st], 2 * kKVBytes);
+        for (int blk = 0; blk < 2; ++blk) {  // two 64-key blocks per tile
+          const int T = t_begin + t * kKeys + blk * kHalf;
+          bool ok = true;
+          int page = page_of(g, b, T, &ok);
+          const int slot = ok ? T % g.page_size : 0;
+          okp &= ok || T >= P + g.R;  // blocks past the request's tokens only load masked filler
+          const int row = (page * g.KVH + kvh) * g.page_size + slot;
+          for (int h = 0; h < 2; ++h) {
+            tma2d(kst + h * (kKVBytes / 2) + blk * kBox, &tmK, h * kHalf, row, &kv_full[st]);
+            tma2d(vst + h * (kKVBytes / 2) + blk * kBox, &tmV, h * kHalf, row, &kv_full[st]);
+          }
+        }
+      }
+      if (!okp) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && ntile > 0) {
+      constexpr uint32_t idS = idesc_bf16(kRows, kKeys, 0, 0);
+      constexpr uint32_t idO = idesc_bf16(kRows, kHD, 0, 1);
+      bool ok = bar_wait(q_full, 0, abort);
+      const uint32_t q_addr = su32(sQ), p_addr = su32(sP);
+      for (int t = 0; ok && t < ntile; ++t) {
+        const int st = t % kStages;
+        if (!bar_wait(&kv_full[st], (t / kStages) & 1, abort)) break;
+        fence_after();
+        const uint32_t k_addr = su32(sKV + st * 2 * kKVBytes);
+        const uint32_t v_addr = k_addr + kKVBytes;
+#pragma unroll
+        for (int kk = 0; kk < kHD / 16; ++kk) {  // S = Q K^T over head_dim
+          const uint32_t off = (kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32;
+          umma(tS, desc_sw128(q_addr + qoff, 16, 1024), desc_sw128(k_addr + off, 16, 1024), idS, kk > 0);
+        }
+        umma_commit(s_full);
+        if (!bar_wait(p_full, t & 1, abort)) break;
+        fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {  // O_t = P V over keys
+          const uint32_t poff = (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32;
+          const uint32_t voff = kk * 16 * 128;  // 16 keys = 16 rows of 128 bytes
+          umma(tO, desc_sw128(p_addr + poff, 16, 1024), desc_sw128(v_addr + voff, kKVBytes / 2, 1024), idO,
+               kk > 0);
+        }
+        umma_commit(o_full);
+        umma_commit(&kv_empty[st]);
+      }
+    }
+  } else {
+    // softmax / epilogue: warps 2..9.  Warp w reads TMEM lane quarter q = w % 4
+    // (query rows 32q..32q+31) and handles half hh of the keys of S and of the
+    // head dims of O; the two halves of a row exchange their maxima through
+    // shared memory, ordered by a 64-arrival mbarrier per quarter (bounded wait).
+    const int q = warp & 3;
+    const int hh = (warp - 2) >> 2;
+    const int r = q * 32 + lane;
+    const int gr = rg * kRows + r;  // row within the KV head's G*R rows
+    const bool row_ok = gr < g.G * g.R;
+    const int node = row_ok ? gr / g.G : 0;
+    const int head = kvh * g.G + (row_ok ? gr % g.G : 0);
+    const int words = (g.R + 63) >> 6;
+    const uint64_t* mrow = mask + (static_cast<size_t>(b) * g.R + node) * words;
+    const float c2 = sm_scale * kLog2e;
+    float* s_max = reinterpret_cast<float*>(tmem_slot + 4);  // [2 tile parities][2 halves][128 rows]
+    float o[kHalf];
+#pragma unroll
+    for (int d = 0; d < kHalf; ++d) o[d] = 0.0f;
+    float m = -INFINITY, l = 0.0f;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const int tid_sm = threadIdx.x - 64;  // 0..255
+    for (int t = 0; t < ntile; ++t) {
+      const int T0 = t_begin + t * kKeys;
+      const int st = t % kStages;
+      unsigned char* vst = sKV + st * 2 * kKVBytes + kKVBytes;
+      if (!bar_wait(s_full, t & 1, abort)) break;
+      fence_after();
+      // V rows of keys outside the segment are zeroed so that masked keys add exactly 0
+      if (tid_sm < kKeys) {
+        const int T = T0 + tid_sm;
+        if (T < k0 || T >= k1) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          for (int h = 0; h < 2; ++h) {
+            uint4* rowp = reinterpret_cast<uint4*>(vst + h * (kKVBytes / 2) + tid_sm * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) rowp[c] = z;
+          }
+        }
+      }
+      // validity bits of this thread's 64 keys (two 32-key chunks)
+      uint32_t valid[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int Tc = T0 + hh * 64 + c * 32;
+        valid[c] = range_bits32(Tc, k0, k1);
+        if (tree) valid[c] &= mask_bits32(mrow, words, Tc - P);
+      }
+      // pass 1: masked, scaled maximum of this half of the row
+      float hmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float v[32];
+        tmem_ld32(tS + lane_base + hh * 64 + c * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if ((valid[c] >> j) & 1u) hmax = fmaxf(hmax, v[j] * c2);
+      }
+      s_max[((t & 1) * 2 + hh) * kRows + r] = hmax;
+      bar_arrive(&xch[q]);
+      if (!bar_wait(&xch[q], t & 1, abort)) break;
+      const float tmax = fmaxf(hmax, s_max[((t & 1) * 2 + (hh ^ 1)) * kRows + r]);
+      const float mn = fmaxf(m, tmax);
+      const float corr = (mn == -INFINITY) ? 1.0f : fast_exp2(m - mn);
+      const float sub = (mn == -INFINITY) ? 0.0f : mn;
+      float rs = 0.0f;
+      // pass 2: P (bf16) for this half of the keys into the K-major swizzled operand:
+      // key chunk c8 (8 keys) of key half hh goes to 16-byte slot (c8 ^ (r & 7)) of row r
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float v[32];
+        tmem_ld32(tS + lane_base + hh * 64 + c * 32, v);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          float e[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = c4 * 8 + u;
+            e[u] = ((valid[c] >> j) & 1u) ? fast_exp2(v[j] * c2 - sub) : 0.0f;
+            rs += e[u];
+          }
+          uint4 pk;
+          pk.x = pack2_bf16(e[0], e[1]);
+          pk.y = pack2_bf16(e[2], e[3]);
+          pk.z = pack2_bf16(e[4], e[5]);
+          pk.w = pack2_bf16(e[6], e[7]);
+          const int c8 = c * 4 + c4;
+          *reinterpret_cast<uint4*>(sP + hh * (kPBytes / 2) + r * 128 + ((c8 ^ (r & 7)) << 4)) = pk;
+        }
+      }
+      l = l * corr + rs;
+      m = mn;
+      fence_async_smem();  // generic-proxy writes (P, zeroed V rows) -> tensor core
+      bar_arrive(p_full);
+      if (!bar_wait(o_full, t & 1, abort)) break;
+      fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float v[32];
+        tmem_ld32(tO + lane_base + hh * 64 + c * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[c * 32 + j] = fmaf(o[c * 32 + j], corr, v[j]);
+      }
+    }
+    // combine the two halves' sums
+    float* s_l = s_max + 4 * kRows;  // [2 halves][128 rows]
+    s_l[hh * kRows + r] = l;
+    bar_arrive(&xch[q]);
+    bar_wait(&xch[q], ntile & 1, abort);
+    const float lt = l + s_l[(hh ^ 1) * kRows + r];
+    if (row_ok && !*abort) {
+      const size_t rec = ((static_cast<size_t>(b) * g.S + s) * g.R + node) * g.H + head;
+      const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+      float4* dst = reinterpret_cast<float4*>(ws_o + rec * kHD + hh * kHalf);
+#pragma unroll
+      for (int d = 0; d < kHalf / 4; ++d)
+        dst[d] = make_float4(o[4 * d] * inv, o[4 * d + 1] * inv, o[4 * d + 2] * inv, o[4 * d + 3] * inv);
+      if (hh == 0) ws_ml[rec] = make_float2(m, lt);
+    }
+  }
+  fence_before();
+  __syncthreads();
+  if (*abort && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
+  if (warp == 1) {
+    __syncwarp();
+    fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+bool verify_tc_supported(const e3_kv_layer& kv, int H) {
+  const int G = H / kv.n_kv_heads;
+  return kv.dt == E3_BF16 && kv.head_dim == kHD && kv.page_size % kHalf == 0 && G >= 1 && G <= 16 &&
+         (kRows % G) == 0;
+}
+
+e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* kv_len, const uint64_t* mask, int B,
+                           int R, int H, int max_kv_len, float sm_scale, int n_pre, int S, int chunk, float* ws_o,
+                           float2* ws_ml, int32_t* dev_err, cudaStream_t s) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  E3_REQUIRE(enc != nullptr, E3_ERR_CUDA, "tree_verify_attn: tensor-map encoder unavailable");
+  const int G = H / kv.n_kv_heads;
+  CUtensorMap mq, mk, mv;
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHD), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B) * R};
+    cuuint64_t str[2] = {static_cast<cuuint64_t>(kHD) * 2, static_cast<cuuint64_t>(H) * kHD * 2};
+    cuuint32_t box[3] = {kHalf, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(kRows / G)};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(Q), dims, str, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    E3_REQUIRE(r == CUDA_SUCCESS, E3_ERR_INVALID_ARG, "tree_verify_attn: Q tensor map rejected (%d)", (int)r);
+  }
+  const cuuint64_t rows = static_cast<cuuint64_t>(kv.n_pages) * kv.n_kv_heads * kv.page_size;
+  for (int w = 0; w < 2; ++w) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHD), rows};
+    cuuint64_t str[1] = {static_cast<cuuint64_t>(kHD) * 2};
+    cuuint32_t box[2] = {kHalf, kHalf};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(w ? &mv : &mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w ? kv.v : kv.k, dims, str, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    E3_REQUIRE(r == CUDA_SUCCESS, E3_ERR_INVALID_ARG, "tree_verify_attn: KV tensor map rejected (%d)", (int)r);
+  }
+  TcGeom g;
+  g.B = B;
+  g.R = R;
+  g.H = H;
+  g.KVH = kv.n_kv_heads;
+  g.G = G;
+  g.n_pre = n_pre;
+  g.S = S;
+  g.chunk = chunk;
+  g.RG = (G * R + kRows - 1) / kRows;
+  g.max_kv_len = max_kv_len;
+  g.page_size = kv.page_size;
+  g.max_pages = kv.max_pages;
+  g.n_pages = kv.n_pages;
+  g.page_table = kv.page_table;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return cuda_status(e, "verify_tc_kernel smem attribute");
+    attr_done = true;
+  }
+  dim3 grid(g.RG * S, kv.n_kv_heads, B);
+  verify_tc_kernel<<<grid, 320, kSmem, s>>>(mq, mk, mv, g, kv_len, mask, sm_scale, ws_o, ws_ml, dev_err);
+  E3_LAUNCH_CHECK("verify_tc_kernel");
+  return E3_OK;
+}
+
+}  // namespace e3

@@ -276,6 +276,8 @@ def mask_from_parent(par):
     dict(dt="bf16", lens=[77], R=1, H=8, KVH=8, hd=128, ps=32, D=0),            # N = 0: plain decode
     dict(dt="f32", lens=[200, 3], R=130, H=2, KVH=1, hd=32, ps=16, D=9),        # > 64 nodes: 3 mask words
     dict(dt="bf16", lens=[100], R=256, H=4, KVH=2, hd=128, ps=64, D=16),        # maximum tree
+    dict(dt="bf16", lens=[0, 128, 64, 65], R=20, H=8, KVH=2, hd=128, ps=64, D=5),  # empty / page-aligned prefixes
+    dict(dt="bf16", lens=[300, 1], R=61, H=16, KVH=16, hd=128, ps=128, D=6),    # 128-token pages, MHA (G = 1)
 ])
 def test_verify_attention(case):
     dt, lens, R, H, KVH, hd, ps, D = (case[x] for x in ("dt", "lens", "R", "H", "KVH", "hd", "ps", "D"))
