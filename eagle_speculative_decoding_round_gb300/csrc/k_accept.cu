@@ -13,10 +13,16 @@
 // distribution, and the next sibling is tested against what remains.  With no
 // child accepted, the bonus (correction) token is drawn from the residual.
 //
-// One CTA per request.  Thread 0 walks the tree (at most D+1 rows); the bonus
-// draw is an inverse-CDF search over the whole vocabulary done by all threads:
-// per-warp segment sums of the fixed-point masses, an exclusive scan of the
-// warp sums, and a rescan of the one segment that holds the target.
+// One cluster of CL CTAs per request (16 where allowed, else 8).  Every CTA
+// builds the children lists and each child's fixed-point mass in parallel and
+// then walks the tree (integer work only).  For the bonus draw, CTA r owns a
+// contiguous chunk of the vocabulary: it computes the residual masses of its
+// chunk into shared memory; the chunk sums are exchanged through distributed
+// shared memory; the CTA whose chunk holds the target finds the token (warp
+// sums, then a warp scan of one 32-token group) and writes the request's
+// outputs.
+#include <cooperative_groups.h>
+
 #include "e3_common.cuh"
 #include "e3_kernels.h"
 
@@ -24,13 +30,8 @@ namespace e3 {
 
 namespace {
 
-constexpr int kAcceptThreads = 1024;
-
-__device__ __forceinline__ bool is_removed(const int* removed, int nrem, int j) {
-  for (int q = 0; q < nrem; ++q)
-    if (removed[q] == j) return true;
-  return false;
-}
+constexpr int kAcceptThreads = 512;
+constexpr int kMaxR = E3_MAX_NODES + 1;
 
 __global__ void __launch_bounds__(kAcceptThreads)
 accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ parent, int R, int D,
@@ -39,53 +40,78 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
               const float* __restrict__ temp, const uint32_t* __restrict__ u_acc,
               const uint32_t* __restrict__ u_bonus, int32_t* acc_len, int32_t* path, int32_t* out_tok,
               int32_t* status) {
-  __shared__ int s_tok[256], s_par[256];
-  __shared__ int s_removed[256];
-  __shared__ int s_nrem, s_u, s_acc, s_bonus, s_err;
-  __shared__ unsigned long long s_x;
-  __shared__ uint64_t s_scan[32];
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int b = blockIdx.x / CL;
+  extern __shared__ unsigned long long qbuf[];  // residual masses of this CTA's chunk
+  __shared__ int s_tok[kMaxR], s_par[kMaxR], s_nch[kMaxR], s_first[kMaxR + 1], s_child[kMaxR];
+  __shared__ unsigned long long s_qc[kMaxR];  // mass of child c under its parent's row
+  __shared__ int s_removed[kMaxR];
   __shared__ int s_path[E3_MAX_DEPTH + 1];
-  const int b = blockIdx.x;
+  __shared__ int s_nrem, s_u, s_acc, s_err, s_bonus;
+  __shared__ unsigned long long s_x, s_sum;
+  __shared__ unsigned long long s_wsum[kAcceptThreads / 32];
+
+  const size_t rb = static_cast<size_t>(b) * R;
   const float T = temp[b];
   const float it = inv_temp(T);
   for (int i = threadIdx.x; i < R; i += blockDim.x) {
-    s_tok[i] = tok[static_cast<size_t>(b) * R + i];
-    s_par[i] = parent[static_cast<size_t>(b) * R + i];
+    s_tok[i] = tok[rb + i];
+    s_par[i] = parent[rb + i];
   }
-  // prefetch, in parallel, everything the walk reads: each node's statistics and
-  // each child's logit under its parent's row
-  __shared__ float s_m[256], s_zc[256];
-  __shared__ unsigned long long s_Q[256];
-  __shared__ int s_am[256];
   __syncthreads();
-  for (int i = threadIdx.x; i < R; i += blockDim.x) {
-    const size_t row = static_cast<size_t>(b) * R + i;
-    s_m[i] = row_max[row];
-    s_Q[i] = row_Q[row];
-    s_am[i] = row_argmax[row];
-    const int p = s_par[i], t = s_tok[i];
-    s_zc[i] = (i > 0 && p >= 0 && p < R && t >= 0 && t < V) ? logits[(static_cast<size_t>(b) * R + p) * V + t] : 0.0f;
+  // children lists in CSR form (children in ascending flat order) and child masses
+  for (int u = threadIdx.x; u < R; u += blockDim.x) {
+    int n = 0;
+    for (int c = u + 1; c < R; ++c) n += (s_par[c] == u);
+    s_nch[u] = n;
   }
+  __syncthreads();
   if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int u = 0; u < R; ++u) {
+      s_first[u] = acc;
+      acc += s_nch[u];
+    }
+    s_first[R] = acc;
     s_err = 0;
-    s_acc = 0;
     s_bonus = -1;
     s_path[0] = 0;
   }
   __syncthreads();
+  for (int c = threadIdx.x; c < R; c += blockDim.x) {
+    const int p = s_par[c];
+    s_qc[c] = 0ull;
+    if (c == 0 || p < 0 || p >= c) continue;  // root, or not a forward edge
+    int rk = 0;
+    for (int c2 = p + 1; c2 < c; ++c2) rk += (s_par[c2] == p);
+    s_child[s_first[p] + rk] = c;
+    const int t = s_tok[c];
+    if (T > 0.0f && t >= 0 && t < V) {
+      const size_t prow = rb + p;
+      s_qc[c] = fx_mass(__fmul_rn(logits[prow * V + t], it), row_max[prow]);
+    }
+  }
+  __syncthreads();
+  // the walk (every CTA of the cluster does it; integer work only)
   if (threadIdx.x == 0) {
-    int u = 0, a = 0;
+    int u = 0, a = 0, nrem = 0;
+    uint64_t Rm = 0;
     for (;;) {
-      const float m = s_m[u];
-      uint64_t Rm = s_Q[u];
-      const int am = s_am[u];
+      const size_t row = rb + u;
+      const float m = row_max[row];
+      const int am = row_argmax[row];
       if (am < 0 || !isfinite(m)) {
         s_err = E3_DEV_ERR_NONFINITE;
         break;
       }
-      int nrem = 0, accepted = -1;
-      for (int c = u + 1; c < R; ++c) {
-        if (s_par[c] != u) continue;
+      Rm = row_Q[row];
+      nrem = 0;
+      int accepted = -1;
+      for (int e = s_first[u]; e < s_first[u] + s_nch[u]; ++e) {
+        const int c = s_child[e];
         const int t = s_tok[c];
         if (T <= 0.0f) {
           if (t == am) {
@@ -95,8 +121,8 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
           continue;
         }
         if (t < 0 || t >= V) continue;
-        const uint64_t q = fx_mass(__fmul_rn(s_zc[c], it), m);
-        if (mulhi32(u_acc[static_cast<size_t>(b) * R + c], Rm) < q) {
+        const uint64_t q = s_qc[c];
+        if (mulhi32(u_acc[rb + c], Rm) < q) {
           accepted = c;
           break;
         }
@@ -109,65 +135,88 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
         u = accepted;
         continue;
       }
-      s_u = u;
-      s_acc = a;
-      s_nrem = nrem;
-      if (T <= 0.0f)
-        s_bonus = am;
-      else
-        s_x = mulhi32(u_bonus[static_cast<size_t>(b) * R + u], Rm);
+      if (T <= 0.0f) s_bonus = am;
       break;
     }
+    s_u = u;
+    s_acc = a;
+    s_nrem = nrem;
+    s_x = (T > 0.0f) ? mulhi32(u_bonus[rb + u], Rm) : 0ull;
   }
   __syncthreads();
   const int err = s_err;
-  if (!err && T > 0.0f) {
-    // inverse CDF over the residual, ascending token ids.  Warp w owns the
-    // contiguous segment [w*seg, (w+1)*seg) and sums it with lane-strided loads;
-    // an exclusive scan of the 32 warp sums locates the segment holding x, which
-    // its warp rescans 32 tokens at a time (warp scan + ballot).
-    const int u = s_u, nrem = s_nrem;
+  int writer = 0;  // the CTA that writes this request's outputs
+  const bool sampled = !err && T > 0.0f;  // uniform across the cluster
+  if (sampled) {
+    const int u = s_u;
     const uint64_t x = s_x;
-    const size_t row = static_cast<size_t>(b) * R + u;
+    const size_t row = rb + u;
     const float m = row_max[row];
     const float* z = logits + row * V;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int seg = (V + nw - 1) / nw;
-    const int j0 = min(V, wid * seg), j1 = min(V, j0 + seg);
-    uint64_t local = 0;
-#pragma unroll 8
-    for (int j = j0 + lane; j < j1; j += 32) {
-      const float zj = z[j];
-      if (!is_removed(s_removed, nrem, j)) local += fx_mass(__fmul_rn(zj, it), m);
-    }
-    local = warp_reduce(local, SumU64());
-    if (lane == 0) s_scan[wid] = local;
+    const int per = (V + CL - 1) / CL;
+    const int j0 = min(V, rank * per), j1 = min(V, j0 + per);
+    const int n = j1 - j0;
+    // residual masses of the chunk (removed tokens zeroed) and the chunk sum
+#pragma unroll 4
+    for (int j = threadIdx.x; j < n; j += blockDim.x) qbuf[j] = fx_mass(__fmul_rn(z[j0 + j], it), m);
     __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int i = 0; i < s_nrem; ++i) {
+        const int t = s_removed[i];
+        if (t >= j0 && t < j1) qbuf[t - j0] = 0ull;
+      }
+    }
+    __syncthreads();
+    // per-warp sums of contiguous sub-segments
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int wseg = (n + nw - 1) / nw;
+    const int a0 = min(n, w * wseg), a1 = min(n, a0 + wseg);
+    uint64_t local = 0;
+    for (int j = a0 + lane; j < a1; j += 32) local += qbuf[j];
+    local = warp_reduce(local, SumU64());
+    if (lane == 0) s_wsum[w] = local;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint64_t tot = 0;
+      for (int i = 0; i < nw; ++i) tot += s_wsum[i];
+      s_sum = tot;
+    }
+    cluster.sync();  // chunk sums visible
     uint64_t excl = 0;
-    for (int w = 0; w < wid; ++w) excl += s_scan[w];
-    if (x >= excl && x < excl + local) {  // uniform within the warp
-      uint64_t base = excl;
-      for (int c0 = j0; c0 < j1; c0 += 32) {
-        const int j = c0 + lane;
-        uint64_t q = 0;
-        if (j < j1 && !is_removed(s_removed, nrem, j)) q = fx_mass(__fmul_rn(z[j], it), m);
-        uint64_t incl = q;
+    int found = -1;
+    for (int r = 0; r < CL; ++r) {  // the chunk sums partition [0, Rmass)
+      const uint64_t sr = *cluster.map_shared_rank(&s_sum, r);
+      if (found < 0 && x >= excl && x < excl + sr) found = r;
+      excl += sr;
+    }
+    writer = found < 0 ? 0 : found;
+    if (found == rank) {
+      uint64_t wex = 0;
+      for (int r = 0; r < rank; ++r) wex += *cluster.map_shared_rank(&s_sum, r);
+      for (int i = 0; i < w; ++i) wex += s_wsum[i];
+      if (x >= wex && x < wex + s_wsum[w]) {  // uniform within the warp
+        uint64_t base = wex;
+        for (int c0 = a0; c0 < a1; c0 += 32) {
+          const int j = c0 + lane;
+          const uint64_t q = j < a1 ? qbuf[j] : 0ull;
+          uint64_t incl = q;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += y;
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const unsigned hit = __ballot_sync(0xFFFFFFFFu, base + incl > x);
+          if (hit) {
+            if (lane == __ffs(hit) - 1) s_bonus = j0 + j;
+            break;
+          }
+          base += __shfl_sync(0xFFFFFFFFu, incl, 31);
         }
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, base + incl > x);
-        if (hit) {
-          if (lane == __ffs(hit) - 1) s_bonus = j;
-          break;
-        }
-        base += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
+  if (rank == writer && threadIdx.x == 0) {
     const int a = err ? 0 : s_acc;
     const size_t o = static_cast<size_t>(b) * (D + 1);
     for (int j = 0; j <= D; ++j) {
@@ -183,6 +232,31 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
     acc_len[b] = a;
     status[b] = err;
   }
+  cluster.sync();  // peers may still read this CTA's chunk sum
+}
+
+int accept_cluster_size() {
+  static int cl = 0;
+  if (cl == 0) {
+    cl = 8;
+    if (cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16);
+      cfg.blockDim = dim3(kAcceptThreads);
+      cfg.dynamicSmemBytes = 72 * 1024;
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = 16;
+      at.val.clusterDim.y = 1;
+      at.val.clusterDim.z = 1;
+      cfg.attrs = &at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, accept_kernel, &cfg) == cudaSuccess && n > 0) cl = 16;
+    }
+    cudaGetLastError();
+  }
+  return cl;
 }
 
 }  // namespace
@@ -191,9 +265,30 @@ e3_status launch_accept(const int32_t* tok, const int32_t* parent, int B, int R,
                         const float* row_max, const uint64_t* row_Q, const int32_t* row_argmax, int V,
                         const float* temp, const uint32_t* u_acc, const uint32_t* u_bonus, int32_t* acc_len,
                         int32_t* path, int32_t* out_tok, int32_t* status, cudaStream_t s) {
-  accept_kernel<<<B, kAcceptThreads, 0, s>>>(tok, parent, R, D, logits, row_max, row_Q, row_argmax, V, temp,
-                                            u_acc, u_bonus, acc_len, path, out_tok, status);
-  E3_LAUNCH_CHECK("accept_kernel");
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr_done = true;
+  }
+  const int CL = accept_cluster_size();
+  const size_t smem = static_cast<size_t>((V + CL - 1) / CL) * sizeof(unsigned long long) + 16;
+  E3_REQUIRE(smem <= 200 * 1024, E3_ERR_SHAPE, "spec_accept: V=%d too large", V);
+  E3_REQUIRE(static_cast<long>(B) * CL < (1L << 31), E3_ERR_SHAPE, "spec_accept: B=%d too large", B);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B * CL);
+  cfg.blockDim = dim3(kAcceptThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = CL;
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, accept_kernel, tok, parent, R, D, logits, row_max, row_Q, row_argmax, V,
+                                     temp, u_acc, u_bonus, acc_len, path, out_tok, status);
+  if (e != cudaSuccess) return cuda_status(e, "accept_kernel");
   return E3_OK;
 }
 

@@ -4,8 +4,8 @@
 // tokens as children; "论文专题讲解：EAGLE-3", Draft tree 配置: 10 nodes are
 // chosen per expansion, by draft confidence.
 //
-// Kernel 1 (one 8-CTA cluster per frontier row): each CTA reads its eighth of
-// the row once into shared memory while building a per-thread top-KMAX list
+// Kernel 1 (one 16- or 8-CTA cluster per frontier row): each CTA reads its part
+// of the row once into shared memory, then builds a per-thread top-KMAX list
 // (packed (value, id) keys, so ties go to the lower token id); the row maximum,
 // the fixed-point mass Q and the top-k lists are combined through distributed
 // shared memory; CTA 0 writes the k children.
@@ -20,8 +20,8 @@ namespace e3 {
 
 namespace {
 
-constexpr int kExpandThreads = 256;
-constexpr int kCluster = 8;  // CTAs per frontier row
+constexpr int kExpandThreads = 512;
+constexpr int kMaxCluster = 16;  // CTAs per frontier row (at most)
 
 template <int KMAX>
 __device__ __forceinline__ void topk_insert(uint64_t (&keys)[KMAX], uint64_t key) {
@@ -51,18 +51,20 @@ __device__ void warp_merge_topk(uint64_t (&keys)[KMAX], int k, uint64_t* out) {
   }
 }
 
-// One 8-CTA cluster per frontier row.  CTA r keeps chunk r of the row in shared
+// One cluster of CL CTAs per frontier row (CL = 16 where the device allows
+// clusters of that size, else 8).  CTA r stages chunk r of the row in shared
 // memory; the row maximum, the non-finite flag, the fixed-point mass and the
 // per-CTA top-k lists are exchanged through distributed shared memory.
 template <int KMAX>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kExpandThreads)
+__global__ void __launch_bounds__(kExpandThreads)
 expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float it,
                    const float* __restrict__ parent_score, const int32_t* __restrict__ parent_id,
                    int depth, int cand_offset, e3_cand c, int32_t* dev_err) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
+  const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
-  const int row = blockIdx.x / kCluster;  // b * F + f
+  const int row = blockIdx.x / CL;  // b * F + f
   const int b = row / F, f = row % F;
   const float* z = logits + static_cast<size_t>(row) * V;
   extern __shared__ float4 chunk4[];
@@ -73,20 +75,19 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   __shared__ int lbad;
   __shared__ uint64_t red64[32];
   __shared__ int redi[32];
-  __shared__ uint64_t all_top[kCluster * E3_MAX_TOPK];
+  __shared__ uint64_t all_top[kMaxCluster * E3_MAX_TOPK];
+  __shared__ uint64_t top[E3_MAX_TOPK];
 
-  // chunk of this CTA, in float4 units (the row is 16-byte aligned and V % 4 == 0
-  // on the vector path; otherwise element-wise)
   const bool vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
   const int nvec = vec ? (V >> 2) : V;
-  const int per = (nvec + kCluster - 1) / kCluster;
+  const int per = (nvec + CL - 1) / CL;
   const int v0 = min(nvec, rank * per), v1 = min(nvec, v0 + per);
   float* chunk = reinterpret_cast<float*>(chunk4);
 
   // stage the chunk (scaled by 1/T) in shared memory with independent, unrolled loads
   if (vec) {
     const float4* z4 = reinterpret_cast<const float4*>(z);
-#pragma unroll 8
+#pragma unroll 4
     for (int q = v0 + threadIdx.x; q < v1; q += blockDim.x) {
       float4 v = __ldg(z4 + q);
       v.x = __fmul_rn(v.x, it);
@@ -96,7 +97,7 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
       chunk4[q - v0] = v;
     }
   } else {
-#pragma unroll 8
+#pragma unroll 4
     for (int j = v0 + threadIdx.x; j < v1; j += blockDim.x) chunk[j - v0] = __fmul_rn(__ldg(z + j), it);
   }
   __syncthreads();
@@ -105,11 +106,15 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   uint64_t keys[KMAX];
 #pragma unroll
   for (int i = 0; i < KMAX; ++i) keys[i] = 0ull;
+  float thr = -INFINITY;  // value of this thread's KMAX-th key (cheap float pre-test)
   int bad = 0;
   for (int j = threadIdx.x; j < n_local; j += blockDim.x) {
     const float sj = chunk[j];
     bad |= !isfinite(sj);
-    topk_insert(keys, pack_best(sj, static_cast<uint32_t>(e0 + j)));
+    if (sj >= thr) {
+      topk_insert(keys, pack_best(sj, static_cast<uint32_t>(e0 + j)));
+      if (keys[KMAX - 1] != 0ull) thr = unord_f32(static_cast<uint32_t>(keys[KMAX - 1] >> 32));
+    }
   }
   bad = block_reduce(bad, OrI(), redi);
   const int warp = threadIdx.x >> 5;
@@ -131,7 +136,7 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   cluster.sync();  // every CTA's maximum and flag are visible
   uint64_t gbest = 0;
   int gbad = 0;
-  for (int r = 0; r < kCluster; ++r) {
+  for (int r = 0; r < CL; ++r) {
     gbest = max(gbest, static_cast<uint64_t>(*cluster.map_shared_rank(&lbest, r)));
     gbad |= *cluster.map_shared_rank(&lbad, r);
   }
@@ -147,17 +152,16 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   if (threadIdx.x == 0) lQ = Q;
   cluster.sync();  // masses and top-k lists are visible
   if (rank == 0) {
-    for (int i = threadIdx.x; i < kCluster * k; i += blockDim.x)
+    for (int i = threadIdx.x; i < CL * k; i += blockDim.x)
       all_top[i] = *cluster.map_shared_rank(&ltop[i % k], i / k);
     uint64_t Qt = 0;
-    for (int r = 0; r < kCluster; ++r) Qt += *cluster.map_shared_rank(&lQ, r);
+    for (int r = 0; r < CL; ++r) Qt += *cluster.map_shared_rank(&lQ, r);
     __syncthreads();
-    __shared__ uint64_t top[E3_MAX_TOPK];
     if (warp == 0) {
       uint64_t lk[KMAX];
 #pragma unroll
       for (int i = 0; i < KMAX; ++i)
-        lk[i] = (static_cast<int>(threadIdx.x) < kCluster && i < k) ? all_top[threadIdx.x * k + i] : 0ull;
+        lk[i] = (static_cast<int>(threadIdx.x) < CL && i < k) ? all_top[threadIdx.x * k + i] : 0ull;
       warp_merge_topk(lk, k, top);
     }
     __syncthreads();
@@ -175,6 +179,65 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     }
   }
   cluster.sync();  // rank 0 is done reading the peers' shared memory
+}
+
+template <int KMAX>
+int cluster_size_for() {
+  static int cl = 0;
+  if (cl == 0) {
+    cl = 8;
+    if (cudaFuncSetAttribute(expand_rows_kernel<KMAX>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16);
+      cfg.blockDim = dim3(kExpandThreads);
+      cfg.dynamicSmemBytes = 64 * 1024;
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = 16;
+      at.val.clusterDim.y = 1;
+      at.val.clusterDim.z = 1;
+      cfg.attrs = &at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, expand_rows_kernel<KMAX>, &cfg) == cudaSuccess && n > 0) cl = 16;
+    }
+    cudaGetLastError();
+  }
+  return cl;
+}
+
+template <int KMAX>
+e3_status launch_rows(const float* logits, int rows, int F, int V, int k, float inv_temp, const float* parent_score,
+                      const int32_t* parent_id, int depth, int cand_offset, const e3_cand& c, int32_t* dev_err,
+                      cudaStream_t s) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(expand_rows_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr_done = true;
+  }
+  const int CL = cluster_size_for<KMAX>();
+  const bool vec = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
+  const int nvec = vec ? V / 4 : V;
+  const int per = (nvec + CL - 1) / CL;
+  const size_t smem = static_cast<size_t>(per) * (vec ? 16 : 4) + 16;
+  E3_REQUIRE(smem <= 200 * 1024, E3_ERR_SHAPE, "eagle3_expand: V=%d too large", V);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows * CL);
+  cfg.blockDim = dim3(kExpandThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = CL;
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, expand_rows_kernel<KMAX>, logits, F, V, k, inv_temp, parent_score,
+                                     parent_id, depth, cand_offset, c, dev_err);
+  if (e != cudaSuccess) return cuda_status(e, "expand_rows_kernel");
+  return E3_OK;
 }
 
 }  // namespace
@@ -212,33 +275,18 @@ e3_status launch_expand(const float* logits, int B, int F, int V, int k, int W, 
                         int cand_offset, const e3_cand& c, int32_t* next_id, float* next_score,
                         int32_t* dev_err, cudaStream_t s) {
   const int rows = B * F;
-  dim3 grid(rows * kCluster), block(kExpandThreads);
-  const bool vec = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
-  const int nvec = vec ? V / 4 : V;
-  const int per = (nvec + kCluster - 1) / kCluster;
-  const size_t smem = static_cast<size_t>(per) * (vec ? 16 : 4) + 16;
-  if (smem > 200 * 1024) return E3_ERR_SHAPE;
-#define E3_EXPAND_CASE(KM)                                                                               \
-  do {                                                                                                   \
-    static bool attr_done = false;                                                                       \
-    if (!attr_done) {                                                                                    \
-      cudaFuncSetAttribute(expand_rows_kernel<KM>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024); \
-      attr_done = true;                                                                                  \
-    }                                                                                                    \
-    expand_rows_kernel<KM><<<grid, block, smem, s>>>(logits, F, V, k, inv_temp, parent_score, parent_id,  \
-                                                     depth, cand_offset, c, dev_err);                    \
-  } while (0)
+  e3_status st;
   if (k <= 2)
-    E3_EXPAND_CASE(2);
+    st = launch_rows<2>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
   else if (k <= 4)
-    E3_EXPAND_CASE(4);
+    st = launch_rows<4>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
   else if (k <= 8)
-    E3_EXPAND_CASE(8);
+    st = launch_rows<8>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
   else if (k <= 16)
-    E3_EXPAND_CASE(16);
+    st = launch_rows<16>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
   else
-    E3_EXPAND_CASE(32);
-#undef E3_EXPAND_CASE
+    st = launch_rows<32>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
+  if (st != E3_OK) return st;
   E3_LAUNCH_CHECK("expand_rows_kernel");
   const int n = F * k;
   const int Wn = W < n ? W : n;
