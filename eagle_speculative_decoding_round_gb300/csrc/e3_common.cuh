@@ -82,9 +82,19 @@ __device__ __forceinline__ float fx_exp(float x) {
   return __fmul_rn(p, scale);
 }
 
+// floor(e * 2^40) for 0 <= e <= 1, from the bits of e (e = 1.f x 2^E, so the
+// product is the 24-bit significand shifted by E + 17); exact, and avoids a
+// float -> 64-bit integer conversion.
+__device__ __forceinline__ uint64_t fx_scale40_floor(float e) {
+  const uint32_t b = __float_as_uint(e);
+  if (b == 0u) return 0ull;
+  const int sh = static_cast<int>(b >> 23) - 127 + 40 - 23;
+  const uint64_t mant = static_cast<uint64_t>((b & 0x7FFFFFu) | 0x800000u);
+  return sh >= 0 ? (mant << sh) : (sh > -64 ? (mant >> (-sh)) : 0ull);
+}
+
 __device__ __forceinline__ uint64_t fx_mass(float s, float m) {
-  float e = fx_exp(__fsub_rn(s, m));
-  return __float2ull_rz(__fmul_rn(e, 0x1p40f));
+  return fx_scale40_floor(fx_exp(__fsub_rn(s, m)));
 }
 
 __device__ __forceinline__ float fx_ell(uint64_t Q) {

@@ -22,6 +22,7 @@ namespace {
 
 constexpr int kExpandThreads = 512;
 constexpr int kMaxCluster = 16;  // CTAs per frontier row (at most)
+constexpr int kPreferCluster = 8;  // eight-CTA clusters keep every row of a depth in one wave
 
 template <int KMAX>
 __device__ __forceinline__ void topk_insert(uint64_t (&keys)[KMAX], uint64_t key) {
@@ -59,7 +60,7 @@ template <int KMAX>
 __global__ void __launch_bounds__(kExpandThreads)
 expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float it,
                    const float* __restrict__ parent_score, const int32_t* __restrict__ parent_id,
-                   int depth, int cand_offset, e3_cand c, int32_t* dev_err) {
+                   int depth, int cand_offset, e3_cand c, int32_t* dev_err, int cand_cap) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = static_cast<int>(cluster.num_blocks());
@@ -77,6 +78,7 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   __shared__ int redi[32];
   __shared__ uint64_t all_top[kMaxCluster * E3_MAX_TOPK];
   __shared__ uint64_t top[E3_MAX_TOPK];
+  __shared__ int s_cnt;
 
   const bool vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
   const int nvec = vec ? (V >> 2) : V;
@@ -103,30 +105,57 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   __syncthreads();
   const int e0 = vec ? 4 * v0 : v0;  // token id of chunk[0]
   const int n_local = vec ? 4 * (v1 - v0) : (v1 - v0);
-  uint64_t keys[KMAX];
-#pragma unroll
-  for (int i = 0; i < KMAX; ++i) keys[i] = 0ull;
-  float thr = -INFINITY;  // value of this thread's KMAX-th key (cheap float pre-test)
+  // (1) per-thread maximum key (value desc, token id asc) and the non-finite flag
+  uint64_t tmax = 0ull;
   int bad = 0;
   for (int j = threadIdx.x; j < n_local; j += blockDim.x) {
     const float sj = chunk[j];
     bad |= !isfinite(sj);
-    if (sj >= thr) {
-      topk_insert(keys, pack_best(sj, static_cast<uint32_t>(e0 + j)));
-      if (keys[KMAX - 1] != 0ull) thr = unord_f32(static_cast<uint32_t>(keys[KMAX - 1] >> 32));
-    }
+    const uint64_t key = pack_best(sj, static_cast<uint32_t>(e0 + j));
+    tmax = key > tmax ? key : tmax;
   }
   bad = block_reduce(bad, OrI(), redi);
-  const int warp = threadIdx.x >> 5;
-  warp_merge_topk(keys, k, warp_lists[warp]);
+  // (2) thr = k-th largest per-thread maximum: every element of this CTA's top k
+  // is >= thr, and only threads whose maximum is >= thr can hold one
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {
+    uint64_t v = tmax;
+    for (int r = 0; r < k; ++r) {
+      const uint64_t best = warp_reduce(v, MaxU64());
+      if (v == best) v = 0ull;  // keys are distinct: exactly one lane (or all-zero lanes)
+      if (lane == 0) warp_lists[warp][r] = best;
+    }
+  }
   __syncthreads();
   if (warp == 0) {
     const int nw = blockDim.x >> 5;
     uint64_t lk[KMAX];
 #pragma unroll
     for (int i = 0; i < KMAX; ++i)
-      lk[i] = (static_cast<int>(threadIdx.x) < nw && i < k) ? warp_lists[threadIdx.x][i] : 0ull;
-    warp_merge_topk(lk, k, ltop);
+      lk[i] = (lane < nw && i < k) ? warp_lists[lane][i] : 0ull;
+    warp_merge_topk(lk, k, top);
+  }
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  const uint64_t thr = top[k - 1];
+  // (3) candidates >= thr, then their exact ranks
+  uint64_t* cand = reinterpret_cast<uint64_t*>(chunk4 + (per + 1));
+  for (int j = threadIdx.x; j < n_local; j += blockDim.x) {
+    const uint64_t key = pack_best(chunk[j], static_cast<uint32_t>(e0 + j));
+    if (key >= thr && key != 0ull) {
+      const int at = atomicAdd(&s_cnt, 1);
+      if (at < cand_cap) cand[at] = key;
+    }
+  }
+  __syncthreads();
+  const int ncand = min(s_cnt, cand_cap);
+  if (threadIdx.x < E3_MAX_TOPK) ltop[threadIdx.x] = 0ull;
+  __syncthreads();
+  for (int i = threadIdx.x; i < ncand; i += blockDim.x) {
+    const uint64_t key = cand[i];
+    int rank = 0;
+    for (int j = 0; j < ncand; ++j) rank += cand[j] > key;
+    if (rank < k) ltop[rank] = key;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -134,12 +163,25 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     lbad = bad;
   }
   cluster.sync();  // every CTA's maximum and flag are visible
-  uint64_t gbest = 0;
-  int gbad = 0;
-  for (int r = 0; r < CL; ++r) {
-    gbest = max(gbest, static_cast<uint64_t>(*cluster.map_shared_rank(&lbest, r)));
-    gbad |= *cluster.map_shared_rank(&lbad, r);
+  __shared__ uint64_t s_gbest;
+  __shared__ int s_gbad;
+  if (warp == 0) {  // lane r gathers rank r, then a warp reduction
+    uint64_t v = 0ull;
+    int bd = 0;
+    if (lane < CL) {
+      v = *cluster.map_shared_rank(&lbest, lane);
+      bd = *cluster.map_shared_rank(&lbad, lane);
+    }
+    v = warp_reduce(v, MaxU64());
+    bd = warp_reduce(bd, OrI());
+    if (lane == 0) {
+      s_gbest = v;
+      s_gbad = bd;
+    }
   }
+  __syncthreads();
+  const uint64_t gbest = s_gbest;
+  const int gbad = s_gbad;
   if (gbad) {
     if (rank == 0 && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_NONFINITE);
     cluster.sync();  // nobody leaves while a peer may still read its shared memory
@@ -154,15 +196,20 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   if (rank == 0) {
     for (int i = threadIdx.x; i < CL * k; i += blockDim.x)
       all_top[i] = *cluster.map_shared_rank(&ltop[i % k], i / k);
-    uint64_t Qt = 0;
-    for (int r = 0; r < CL; ++r) Qt += *cluster.map_shared_rank(&lQ, r);
+    __shared__ uint64_t s_Qt;
+    if (warp == 0) {
+      uint64_t v = lane < CL ? static_cast<uint64_t>(*cluster.map_shared_rank(&lQ, lane)) : 0ull;
+      v = warp_reduce(v, SumU64());
+      if (lane == 0) s_Qt = v;
+    }
     __syncthreads();
+    const uint64_t Qt = s_Qt;
     if (warp == 0) {
       uint64_t lk[KMAX];
 #pragma unroll
       for (int i = 0; i < KMAX; ++i)
         lk[i] = (static_cast<int>(threadIdx.x) < CL && i < k) ? all_top[threadIdx.x * k + i] : 0ull;
-      warp_merge_topk(lk, k, top);
+      warp_merge_topk(lk, k, top);  // top[] is free again: thr was consumed above
     }
     __syncthreads();
     if (threadIdx.x < k) {
@@ -186,6 +233,7 @@ int cluster_size_for() {
   static int cl = 0;
   if (cl == 0) {
     cl = 8;
+    if (kPreferCluster == 8) return cl;
     if (cudaFuncSetAttribute(expand_rows_kernel<KMAX>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
         cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
@@ -220,7 +268,9 @@ e3_status launch_rows(const float* logits, int rows, int F, int V, int k, float 
   const bool vec = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
   const int nvec = vec ? V / 4 : V;
   const int per = (nvec + CL - 1) / CL;
-  const size_t smem = static_cast<size_t>(per) * (vec ? 16 : 4) + 16;
+  const int per_thread = ((vec ? per * 4 : per) + kExpandThreads - 1) / kExpandThreads;
+  const int cand_cap = k * per_thread + 32;
+  const size_t smem = static_cast<size_t>(per + 1) * 16 + static_cast<size_t>(cand_cap) * 8 + 16;
   E3_REQUIRE(smem <= 200 * 1024, E3_ERR_SHAPE, "eagle3_expand: V=%d too large", V);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows * CL);
@@ -235,7 +285,7 @@ e3_status launch_rows(const float* logits, int rows, int F, int V, int k, float 
   cfg.attrs = &at;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, expand_rows_kernel<KMAX>, logits, F, V, k, inv_temp, parent_score,
-                                     parent_id, depth, cand_offset, c, dev_err);
+                                     parent_id, depth, cand_offset, c, dev_err, cand_cap);
   if (e != cudaSuccess) return cuda_status(e, "expand_rows_kernel");
   return E3_OK;
 }
@@ -245,20 +295,32 @@ e3_status launch_rows(const float* logits, int rows, int F, int V, int k, float 
 namespace {
 
 __global__ void __launch_bounds__(256)
-expand_frontier_kernel(int n, int Wn, int cand_offset, e3_cand c, int32_t* next_id,
-                       float* next_score, const int32_t* dev_err) {
+expand_frontier_kernel(int n, int Wn, int cand_offset, e3_cand c, int32_t* next_id, float* next_score,
+                       const int32_t* dev_err) {
   __shared__ uint64_t keys[2048];
   const int b = blockIdx.x;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int ci = cand_offset + i;
+    keys[i] = pack_best(c.score[static_cast<size_t>(b) * c.cap + ci], static_cast<uint32_t>(ci));
+  }
+  __syncthreads();
+  if (n <= 1024) {
+    // exact rank of each child among the n (distinct keys): the first Wn ranks win
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const uint64_t key = keys[i];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += keys[j] > key;
+      if (rank < Wn) {
+        const uint32_t ci = packed_id(key);
+        next_id[static_cast<size_t>(b) * Wn + rank] = static_cast<int32_t>(ci);
+        next_score[static_cast<size_t>(b) * Wn + rank] = c.score[static_cast<size_t>(b) * c.cap + ci];
+      }
+    }
+    return;
+  }
   int np = 1;
   while (np < n) np <<= 1;
-  for (int i = threadIdx.x; i < np; i += blockDim.x) {
-    uint64_t key = 0ull;
-    if (i < n) {
-      const int ci = cand_offset + i;
-      key = pack_best(c.score[static_cast<size_t>(b) * c.cap + ci], static_cast<uint32_t>(ci));
-    }
-    keys[i] = key;
-  }
+  for (int i = n + threadIdx.x; i < np; i += blockDim.x) keys[i] = 0ull;
   __syncthreads();
   block_bitonic_desc(keys, np);
   for (int q = threadIdx.x; q < Wn; q += blockDim.x) {
