@@ -19,7 +19,8 @@ E3_DEV_ERR_NONFINITE, E3_DEV_ERR_CAPACITY, E3_DEV_ERR_TIMEOUT = 1, 2, 4
 E3_ACCEPT_TREE_DET = 0
 STATUS_NAMES = {0: "E3_OK", 1: "E3_ERR_INVALID_ARG", 2: "E3_ERR_SHAPE", 3: "E3_ERR_UNSUPPORTED",
                 4: "E3_ERR_CAPACITY", 5: "E3_ERR_NONFINITE", 6: "E3_ERR_CUDA", 7: "E3_ERR_TIMEOUT"}
-SYMBOLS = ["eagle3_fuse", "eagle3_fuse_workspace_bytes", "eagle3_expand", "tree_build_mask",
+SYMBOLS = ["eagle3_fuse", "eagle3_fuse_workspace_bytes", "eagle3_fuse_noalloc",
+           "eagle3_fuse_noalloc_max_scratch_bytes", "eagle3_expand", "tree_build_mask",
            "tree_verify_attn", "eagle3_verify_workspace_bytes", "lmhead_logits", "spec_accept",
            "kv_compact", "eagle3_last_error", "eagle3_abi_version"]
 
@@ -50,6 +51,8 @@ def _load() -> ctypes.CDLL:
     sig = {
         "eagle3_fuse": (I, [P, P, P, P, P, P, I, I, I, I, P, S, P, P]),
         "eagle3_fuse_workspace_bytes": (S, [I, I, I, I]),
+        "eagle3_fuse_noalloc": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
+        "eagle3_fuse_noalloc_max_scratch_bytes": (S, []),
         "eagle3_expand": (I, [P, I, I, I, I, I, F, P, P, I, I, ctypes.POINTER(e3_cand), P, P, P, P]),
         "tree_build_mask": (I, [ctypes.POINTER(e3_cand), I, I, I, P, P, P, P, P, P, P, P]),
         "tree_verify_attn": (I, [P, ctypes.POINTER(e3_kv_layer), P, P, I, I, I, I, F, P, P, P, P, S, P]),
@@ -117,6 +120,16 @@ def eagle3_fuse(h_low, h_mid, h_high, W_f, bias, g, M, d, d_out, dt, ws=None, ws
                 stream=None):
     _check("eagle3_fuse", _lib.eagle3_fuse(ptr(h_low), ptr(h_mid), ptr(h_high), ptr(W_f), ptr(bias), ptr(g),
                                            M, d, d_out, dt, ptr(ws), ws_bytes, ptr(dev_err), _stream(stream)))
+
+
+def eagle3_fuse_noalloc(h_low, h_mid, h_high, W_f, bias, g, M, d, d_out, dt, dev_err=None, stream=None):
+    """eagle3_fuse without caller scratch (fixed library array; see include/eagle3.h)."""
+    _check("eagle3_fuse_noalloc", _lib.eagle3_fuse_noalloc(ptr(h_low), ptr(h_mid), ptr(h_high), ptr(W_f), ptr(bias),
+                                                           ptr(g), M, d, d_out, dt, ptr(dev_err), _stream(stream)))
+
+
+def eagle3_fuse_noalloc_max_scratch_bytes() -> int:
+    return int(_lib.eagle3_fuse_noalloc_max_scratch_bytes())
 
 
 def eagle3_expand(draft_logits, B, F, V, k, W, inv_temp, parent_score, parent_id, depth, cand_offset,

@@ -128,6 +128,24 @@ E3_API e3_status eagle3_fuse(const void* h_low, const void* h_mid, const void* h
 E3_API size_t eagle3_fuse_workspace_bytes(int M, int d, int d_out, e3_dtype dt);
 
 /* ---------------------------------------------------------------------------
+ * eagle3_fuse_noalloc: eagle3_fuse for callers that cannot allocate device
+ * memory (no cudaMalloc or allocating library call may happen where they run the
+ * fusion: allocator-free serving loops, embedders without a device allocator).
+ * The pages have no counterpart: this is a library-level convenience.
+ * Same inputs, output and numerics as eagle3_fuse, but the split-K scratch is a
+ * fixed array inside the library (eagle3_fuse_noalloc_max_scratch_bytes(), 4 MiB;
+ * held on every GPU that loads the library until exit).  Shapes whose scratch
+ * (eagle3_fuse_workspace_bytes) exceeds it return E3_ERR_CAPACITY before any
+ * launch.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress), so make it before any stream capture.  All calls share
+ * the array: calls that overlap on the GPU race and must be ordered by the caller.
+ * ------------------------------------------------------------------------- */
+E3_API e3_status eagle3_fuse_noalloc(const void* h_low, const void* h_mid, const void* h_high,
+                                     const void* W_f, const float* bias, void* g, int M, int d,
+                                     int d_out, e3_dtype dt, int32_t* dev_err, e3_stream_t stream);
+E3_API size_t eagle3_fuse_noalloc_max_scratch_bytes(void);
+
+/* ---------------------------------------------------------------------------
  * eagle3_expand: one depth of the dynamic draft tree, B requests at once.
  * draft_logits: [B][F][V] fp32, row f = frontier node f of the request.
  * parent_score: [B][F] fp32 (the root has 0); parent_id: [B][F] int32
