@@ -31,7 +31,7 @@ e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_
 bool verify_tc_supported(const e3_kv_layer& kv, int H);
 e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* kv_len, const uint64_t* mask, int B,
                            int R, int H, int max_kv_len, float sm_scale, int n_pre, int S, int chunk, float* ws_o,
-                           float2* ws_ml, int32_t* dev_err, cudaStream_t s);
+                           float2* ws_ml, void* O, float* lse, bool* merged, int32_t* dev_err, cudaStream_t s);
 
 e3_status launch_gemm_simt(const void* a0, const void* a1, const void* a2, int dseg, const void* W,
                            const float* bias, void* out, bool out_f32, int M, int N, int K, e3_dtype dt,

@@ -59,17 +59,19 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait; returns false (and raises *abort) if the phase did not complete.
+// mbarrier.try_wait suspends in hardware; the clock is checked every 64 probes.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
-    if (mbar_try(bar, parity)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer() - t0 > kWaitNs) {
       *abort = 1;
       return false;
     }
-    __nanosleep(64);
   }
 }
 

@@ -481,6 +481,10 @@ VerifyGeom make_geom(int B, int R, int H, int KVH, int hd, int max_kv_len, bool 
   chunk = ((chunk + 63) / 64) * 64;
   if (chunk < 64) chunk = 64;
   if (mma && chunk < 256) chunk = 256;  // two 128-key tiles per tensor-core CTA at least
+  if (mma) {                            // at most 15 prefix segments (+ tree) per cluster
+    const long cap = ((static_cast<long>(max_kv_len) + 14) / 15 + 127) / 128 * 128;
+    if (chunk < cap) chunk = cap;
+  }
   g.chunk = static_cast<int>(chunk);
   g.n_pre = static_cast<int>((max_kv_len + chunk - 1) / chunk);
   g.S = g.n_pre + 1;
@@ -513,9 +517,11 @@ e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_
   float2* ws_ml = reinterpret_cast<float2*>(ml_addr);
 
   if (mma && verify_tc_supported(kv, H)) {
+    bool merged = false;
     e3_status st = launch_verify_tc(Q, kv, kv_len, mask, B, R, H, max_kv_len, sm_scale, g.n_pre, g.S, g.chunk, ws_o,
-                                    ws_ml, dev_err, s);
+                                    ws_ml, O, lse, &merged, dev_err, s);
     if (st != E3_OK) return st;
+    if (merged) return E3_OK;  // segments merged inside the cluster
   } else if (mma) {
     dim3 grid(g.RG * g.S, kv.n_kv_heads, B);
 #define E3_MMA_CASE(HDV)                                                                           \

@@ -19,8 +19,9 @@
 //   O_t = P V    tcgen05.mma, N = head_dim, K = keys; V is used in place as an
 //                MN-major operand (rows of 64 head-dim values per key)
 //   O += O_t     accumulated in registers with the online-softmax correction.
-// Warps: 0 TMA, 1 TMEM owner + MMA issuer, 2..9 softmax/epilogue (two warps per
-// TMEM lane quarter, each owning half of the keys and half of the head dims).
+// Warps: 0 TMA, 1 TMEM owner + MMA issuer, 2..17 softmax/epilogue (four warps per
+// TMEM lane quarter, each owning a quarter of the keys and of the head dims).
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -40,7 +41,10 @@ constexpr int kQBytes = kRows * kHD * 2;       // 32 KB (two 16 KB halves)
 constexpr int kKVBytes = kKeys * kHD * 2;      // 32 KB per operand per tile
 constexpr int kStages = 2;
 constexpr int kPBytes = kRows * kKeys * 2;     // 32 KB
-constexpr int kSmem = 1024 + kQBytes + kStages * 2 * kKVBytes + kPBytes + 256 + 6 * 128 * 4 + 64;
+constexpr int kRowCache = 128;       // KV block rows looked up ahead
+constexpr int kThreads = 576;         // warp 0 TMA, warp 1 MMA, warps 2..17 softmax
+constexpr int kSoftmaxThreads = 512;
+constexpr int kSmem = 1024 + kQBytes + kStages * 2 * kKVBytes + kPBytes + 256 + 12 * 128 * 4 + 4 * kRowCache + 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
@@ -67,17 +71,21 @@ __device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t par) {
                : "memory");
   return ok != 0;
 }
+// Bounded wait: mbarrier.try_wait suspends the thread in hardware until the phase
+// completes or a short system-dependent limit passes; the clock and the abort flag
+// are checked every 64 probes.
 __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t par, volatile int* abort) {
   if (bar_try(b, par)) return true;
   const uint64_t t0 = gtimer();
   for (;;) {
-    if (bar_try(b, par)) return true;
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (bar_try(b, par)) return true;
     if (*abort) return false;
     if (gtimer() - t0 > kWaitNs) {
       *abort = 1;
       return false;
     }
-    __nanosleep(32);
   }
 }
 __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* m, int x, int y, uint64_t* b) {
@@ -159,6 +167,7 @@ __device__ __forceinline__ uint32_t mask_bits32(const uint64_t* row, int words, 
 
 struct TcGeom {
   int B, R, H, KVH, G, n_pre, S, chunk, RG, max_kv_len;
+  int fold_tree;  // 1: segment S-1 also processes the tree slots (no separate tree segment)
   int page_size, max_pages, n_pages;
   const int32_t* page_table;
 };
@@ -177,11 +186,18 @@ __device__ __forceinline__ int page_of(const TcGeom& g, int b, int t, bool* ok) 
   return p;
 }
 
-__global__ void __launch_bounds__(320, 1)
+// CLUSTER: the S segments of one (row group, KV head, request) form one cluster;
+// after their tile loops each CTA pushes its partial (o, m, l) rows into the
+// shared memory of the CTA that owns those rows, and each CTA merges and writes
+// the final O and lse of its slice.  Otherwise partial records go to the
+// workspace for verify_merge_kernel.
+template <bool CLUSTER>
+__global__ void __launch_bounds__(kThreads, 1)
 verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, TcGeom g, const int32_t* __restrict__ kv_len,
                  const uint64_t* __restrict__ mask, float sm_scale, float* __restrict__ ws_o,
-                 float2* __restrict__ ws_ml, int32_t* dev_err) {
+                 float2* __restrict__ ws_ml, __nv_bfloat16* __restrict__ O, float* __restrict__ lse,
+                 int32_t* dev_err) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned char* sQ = sm;                                  // [2 halves][128 rows][128 B]
@@ -194,33 +210,92 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint64_t* s_full = bars + 5;
   uint64_t* p_full = bars + 6;
   uint64_t* o_full = bars + 7;
-  uint64_t* xch = bars + 8;        // [4] row-maximum exchange of the two halves, per lane quarter
+  uint64_t* xch = bars + 8;        // [4] exchange among the four parts of a row, per lane quarter
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* s_max = reinterpret_cast<float*>(tmem_slot + 4);  // [2 parities][4 parts][128 rows]
+  float* s_l = s_max + 8 * kRows;                           // [4 parts][128 rows]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rg = blockIdx.x % g.RG, s = blockIdx.x / g.RG;
+  const int rg = CLUSTER ? blockIdx.x / g.S : blockIdx.x % g.RG;
+  const int s = CLUSTER ? blockIdx.x % g.S : blockIdx.x / g.RG;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int P = kv_len[b];
   const long need = static_cast<long>(P) + g.R;
   if (P < 0 || P > g.max_kv_len || need > static_cast<long>(g.max_pages) * g.page_size) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
-    return;
+    return;  // uniform across the cluster (same request)
   }
-  const bool tree = (s == g.n_pre);
-  int k0, k1;  // logical key range of this segment
-  if (tree) {
-    k0 = P;
-    k1 = P + g.R;
+  // key ranges of this CTA: a prefix range [pk0, pk1) and, for the tree segment
+  // (or the last segment when the tree is folded in), the tree slots [P, P + R)
+  int pk0 = 0, pk1 = 0;
+  bool has_tree;
+  if (g.fold_tree) {
+    pk0 = min(P, s * g.chunk);
+    pk1 = min(P, pk0 + g.chunk);
+    has_tree = (s == g.S - 1);
+  } else if (s == g.n_pre) {
+    has_tree = true;
   } else {
-    k0 = s * g.chunk;
-    k1 = min(P, k0 + g.chunk);
+    pk0 = min(P, s * g.chunk);
+    pk1 = min(P, pk0 + g.chunk);
+    has_tree = false;
   }
-  const int t_begin = k0 & ~(kHalf - 1);  // 64-aligned start
-  const int ntile = k1 > k0 ? (k1 - t_begin + kKeys - 1) / kKeys : 0;
+  const int tA = pk0 & ~(kHalf - 1);
+  const int ntA = pk1 > pk0 ? (pk1 - tA + kKeys - 1) / kKeys : 0;
+  const int tB = P & ~(kHalf - 1);
+  const int ntB = has_tree ? (P + g.R - tB + kKeys - 1) / kKeys : 0;
+  const int ntile = ntA + ntB;
+  auto tile_T0 = [&](int t) { return t < ntA ? tA + t * kKeys : tB + (t - ntA) * kKeys; };
+  auto tile_lo = [&](int t) { return t < ntA ? pk0 : P; };
+  auto tile_hi = [&](int t) { return t < ntA ? pk1 : P + g.R; };
   const int nodes_per_tile = kRows / g.G;
   const int i0 = rg * nodes_per_tile;  // first node of this row group
 
+  // cache rows of the first kRowCache 64-key blocks, looked up by warp 0's lanes in
+  // parallel (the page table is read once, off the producer's critical path)
+  int* s_rows = reinterpret_cast<int*>(s_l + 4 * kRows);  // [kRowCache], -1 = bad page
+  if (warp == 0) {
+    for (int i = lane; i < 2 * ntile && i < kRowCache; i += 32) {
+      const int T = tile_T0(i >> 1) + (i & 1) * kHalf;
+      bool ok = true;
+      const int page = page_of(g, b, T, &ok);
+      const int slot = ok ? T % g.page_size : 0;
+      s_rows[i] = (ok || T >= P + g.R) ? (page * g.KVH + kvh) * g.page_size + slot : -1;
+    }
+    __syncwarp();
+  }
+  // TMA producer state (thread 0): it issues Q and the first stages right after
+  // initialising the barriers, so the loads overlap the TMEM allocation
+  bool okp = true;
+  auto issue_tile = [&](int t) {
+    const int st = t % kStages;
+    unsigned char* kst = sKV + st * 2 * kKVBytes;
+    unsigned char* vst = kst + kKVBytes;
+    bar_expect(&kv_full[st], 2 * kKVBytes);
+    for (int blk = 0; blk < 2; ++blk) {  // two 64-key blocks per tile
+      int row;
+      const int i = 2 * t + blk;
+      if (i < kRowCache) {
+        row = s_rows[i];
+        if (row < 0) {
+          okp = false;
+          row = 0;
+        }
+      } else {
+        const int T = tile_T0(t) + blk * kHalf;
+        bool ok = true;
+        const int page = page_of(g, b, T, &ok);
+        const int slot = ok ? T % g.page_size : 0;
+        okp &= ok || T >= P + g.R;  // blocks past the request's tokens only load masked filler
+        row = (page * g.KVH + kvh) * g.page_size + slot;
+      }
+      for (int h = 0; h < 2; ++h) {
+        tma2d(kst + h * (kKVBytes / 2) + blk * kBox, &tmK, h * kHalf, row, &kv_full[st]);
+        tma2d(vst + h * (kKVBytes / 2) + blk * kBox, &tmV, h * kHalf, row, &kv_full[st]);
+      }
+    }
+  };
   if (threadIdx.x == 0) {
     bar_init(q_full, 1);
     for (int st = 0; st < kStages; ++st) {
@@ -228,11 +303,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       bar_init(&kv_empty[st], 1);
     }
     bar_init(s_full, 1);
-    bar_init(p_full, 256);
+    bar_init(p_full, kSoftmaxThreads);
     bar_init(o_full, 1);
-    for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], 64);
+    for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], kSoftmaxThreads / 4);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (ntile > 0) {
+      bar_expect(q_full, kQBytes);
+      for (int h = 0; h < 2; ++h)
+        tma3d(sQ + h * (kQBytes / 2), &tmQ, h * kHalf, kvh * g.G, b * g.R + i0, q_full);
+      for (int t = 0; t < ntile && t < kStages; ++t) issue_tile(t);
+    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)), "r"(256));
@@ -246,28 +327,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 
   if (warp == 0) {
     if (lane == 0 && ntile > 0) {
-      bar_expect(q_full, kQBytes);
-      for (int h = 0; h < 2; ++h)
-        tma3d(sQ + h * (kQBytes / 2), &tmQ, h * kHalf, kvh * g.G, b * g.R + i0, q_full);
-      bool okp = true;
-      for (int t = 0; t < ntile; ++t) {
+      for (int t = kStages; t < ntile; ++t) {
         const int st = t % kStages;
         if (!bar_wait(&kv_empty[st], ((t / kStages) & 1) ^ 1, abort)) break;
-        unsigned char* kst = sKV + st * 2 * kKVBytes;
-        unsigned char* vst = kst + kKVBytes;
-        bar_expect(&kv_full[st], 2 * kKVBytes);
-        for (int blk = 0; blk < 2; ++blk) {  // two 64-key blocks per tile
-          const int T = t_begin + t * kKeys + blk * kHalf;
-          bool ok = true;
-          int page = page_of(g, b, T, &ok);
-          const int slot = ok ? T % g.page_size : 0;
-          okp &= ok || T >= P + g.R;  // blocks past the request's tokens only load masked filler
-          const int row = (page * g.KVH + kvh) * g.page_size + slot;
-          for (int h = 0; h < 2; ++h) {
-            tma2d(kst + h * (kKVBytes / 2) + blk * kBox, &tmK, h * kHalf, row, &kv_full[st]);
-            tma2d(vst + h * (kKVBytes / 2) + blk * kBox, &tmV, h * kHalf, row, &kv_full[st]);
-          }
-        }
+        issue_tile(t);
       }
       if (!okp) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
     }
@@ -303,35 +366,41 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         umma_commit(&kv_empty[st]);
       }
     }
-  } else {
-    // softmax / epilogue: warps 2..9.  Warp w reads TMEM lane quarter q = w % 4
-    // (query rows 32q..32q+31) and handles half hh of the keys of S and of the
-    // head dims of O; the two halves of a row exchange their maxima through
-    // shared memory, ordered by a 64-arrival mbarrier per quarter (bounded wait).
-    const int q = warp & 3;
-    const int hh = (warp - 2) >> 2;
-    const int r = q * 32 + lane;
-    const int gr = rg * kRows + r;  // row within the KV head's G*R rows
-    const bool row_ok = gr < g.G * g.R;
-    const int node = row_ok ? gr / g.G : 0;
-    const int head = kvh * g.G + (row_ok ? gr % g.G : 0);
+  }
+  // softmax warps 2..17: warp w reads TMEM lane quarter q = w % 4 (query rows
+  // 32q..32q+31) and owns part pp of the row: keys [32pp, 32pp+32) of S and
+  // head dims [32pp, 32pp+32) of O.  The four parts of a row exchange maxima and
+  // sums through shared memory, ordered by a per-quarter mbarrier (bounded wait).
+  const bool softmax = warp >= 2;
+  const int q = warp & 3;
+  const int pp = softmax ? (warp - 2) >> 2 : 0;
+  const int r = q * 32 + lane;
+  const int gr = rg * kRows + r;  // row within the KV head's G*R rows
+  const bool row_ok = softmax && gr < g.G * g.R;
+  const int node = row_ok ? gr / g.G : 0;
+  const int head = kvh * g.G + (row_ok ? gr % g.G : 0);
+  float o[32];
+#pragma unroll
+  for (int d = 0; d < 32; ++d) o[d] = 0.0f;
+  float m = -INFINITY, lt = 0.0f;
+  if (softmax) {
     const int words = (g.R + 63) >> 6;
     const uint64_t* mrow = mask + (static_cast<size_t>(b) * g.R + node) * words;
     const float c2 = sm_scale * kLog2e;
-    float* s_max = reinterpret_cast<float*>(tmem_slot + 4);  // [2 tile parities][2 halves][128 rows]
-    float o[kHalf];
-#pragma unroll
-    for (int d = 0; d < kHalf; ++d) o[d] = 0.0f;
-    float m = -INFINITY, l = 0.0f;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    const int tid_sm = threadIdx.x - 64;  // 0..255
+    const int tid_sm = threadIdx.x - 64;  // 0..511
+    float l = 0.0f;
     for (int t = 0; t < ntile; ++t) {
-      const int T0 = t_begin + t * kKeys;
+      const int T0 = tile_T0(t);
+      const int k0 = tile_lo(t), k1 = tile_hi(t);
+      const bool tree = t >= ntA;
       const int st = t % kStages;
       unsigned char* vst = sKV + st * 2 * kKVBytes + kKVBytes;
       if (!bar_wait(s_full, t & 1, abort)) break;
       fence_after();
-      // V rows of keys outside the segment are zeroed so that masked keys add exactly 0
+      float v[32];
+      tmem_ld32(tS + lane_base + pp * 32, v);  // this part's 32 scores (kept in registers)
+      // V rows of keys outside the range are zeroed so that masked keys add exactly 0
       if (tid_sm < kKeys) {
         const int T = T0 + tid_sm;
         if (T < k0 || T >= k1) {
@@ -343,55 +412,41 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
         }
       }
-      // validity bits of this thread's 64 keys (two 32-key chunks)
-      uint32_t valid[2];
+      const int Tc = T0 + pp * 32;
+      uint32_t valid = range_bits32(Tc, k0, k1);
+      if (tree) valid &= mask_bits32(mrow, words, Tc - P);
+      float pmax = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int Tc = T0 + hh * 64 + c * 32;
-        valid[c] = range_bits32(Tc, k0, k1);
-        if (tree) valid[c] &= mask_bits32(mrow, words, Tc - P);
-      }
-      // pass 1: masked, scaled maximum of this half of the row
-      float hmax = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tmem_ld32(tS + lane_base + hh * 64 + c * 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if ((valid[c] >> j) & 1u) hmax = fmaxf(hmax, v[j] * c2);
-      }
-      s_max[((t & 1) * 2 + hh) * kRows + r] = hmax;
+      for (int j = 0; j < 32; ++j)
+        if ((valid >> j) & 1u) pmax = fmaxf(pmax, v[j] * c2);
+      s_max[((t & 1) * 4 + pp) * kRows + r] = pmax;
       bar_arrive(&xch[q]);
       if (!bar_wait(&xch[q], t & 1, abort)) break;
-      const float tmax = fmaxf(hmax, s_max[((t & 1) * 2 + (hh ^ 1)) * kRows + r]);
+      float tmax = s_max[((t & 1) * 4) * kRows + r];
+#pragma unroll
+      for (int x = 1; x < 4; ++x) tmax = fmaxf(tmax, s_max[((t & 1) * 4 + x) * kRows + r]);
       const float mn = fmaxf(m, tmax);
       const float corr = (mn == -INFINITY) ? 1.0f : fast_exp2(m - mn);
       const float sub = (mn == -INFINITY) ? 0.0f : mn;
       float rs = 0.0f;
-      // pass 2: P (bf16) for this half of the keys into the K-major swizzled operand:
-      // key chunk c8 (8 keys) of key half hh goes to 16-byte slot (c8 ^ (r & 7)) of row r
+      // P for keys [32pp, 32pp+32): key half pp/2, 8-key chunks (pp%2)*4 + c4, each
+      // at 16-byte slot (chunk ^ (r & 7)) of row r (K-major, 128-byte swizzle)
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tmem_ld32(tS + lane_base + hh * 64 + c * 32, v);
+      for (int c4 = 0; c4 < 4; ++c4) {
+        float e[8];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          float e[8];
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int j = c4 * 8 + u;
-            e[u] = ((valid[c] >> j) & 1u) ? fast_exp2(v[j] * c2 - sub) : 0.0f;
-            rs += e[u];
-          }
-          uint4 pk;
-          pk.x = pack2_bf16(e[0], e[1]);
-          pk.y = pack2_bf16(e[2], e[3]);
-          pk.z = pack2_bf16(e[4], e[5]);
-          pk.w = pack2_bf16(e[6], e[7]);
-          const int c8 = c * 4 + c4;
-          *reinterpret_cast<uint4*>(sP + hh * (kPBytes / 2) + r * 128 + ((c8 ^ (r & 7)) << 4)) = pk;
+        for (int u = 0; u < 8; ++u) {
+          const int j = c4 * 8 + u;
+          e[u] = ((valid >> j) & 1u) ? fast_exp2(v[j] * c2 - sub) : 0.0f;
+          rs += e[u];
         }
+        uint4 pk;
+        pk.x = pack2_bf16(e[0], e[1]);
+        pk.y = pack2_bf16(e[2], e[3]);
+        pk.z = pack2_bf16(e[4], e[5]);
+        pk.w = pack2_bf16(e[6], e[7]);
+        const int c8 = (pp & 1) * 4 + c4;
+        *reinterpret_cast<uint4*>(sP + (pp >> 1) * (kPBytes / 2) + r * 128 + ((c8 ^ (r & 7)) << 4)) = pk;
       }
       l = l * corr + rs;
       m = mn;
@@ -399,33 +454,80 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       bar_arrive(p_full);
       if (!bar_wait(o_full, t & 1, abort)) break;
       fence_after();
+      tmem_ld32(tO + lane_base + pp * 32, v);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tmem_ld32(tO + lane_base + hh * 64 + c * 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) o[c * 32 + j] = fmaf(o[c * 32 + j], corr, v[j]);
-      }
+      for (int j = 0; j < 32; ++j) o[j] = fmaf(o[j], corr, v[j]);
     }
-    // combine the two halves' sums
-    float* s_l = s_max + 4 * kRows;  // [2 halves][128 rows]
-    s_l[hh * kRows + r] = l;
+    // total of the four parts' sums
+    s_l[pp * kRows + r] = l;
     bar_arrive(&xch[q]);
     bar_wait(&xch[q], ntile & 1, abort);
-    const float lt = l + s_l[(hh ^ 1) * kRows + r];
-    if (row_ok && !*abort) {
+    lt = s_l[r] + s_l[kRows + r] + s_l[2 * kRows + r] + s_l[3 * kRows + r];
+    if (!CLUSTER && row_ok && !*abort) {
       const size_t rec = ((static_cast<size_t>(b) * g.S + s) * g.R + node) * g.H + head;
       const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
-      float4* dst = reinterpret_cast<float4*>(ws_o + rec * kHD + hh * kHalf);
+      float4* dst = reinterpret_cast<float4*>(ws_o + rec * kHD + pp * 32);
 #pragma unroll
-      for (int d = 0; d < kHalf / 4; ++d)
+      for (int d = 0; d < 8; ++d)
         dst[d] = make_float4(o[4 * d] * inv, o[4 * d + 1] * inv, o[4 * d + 2] * inv, o[4 * d + 3] * inv);
-      if (hh == 0) ws_ml[rec] = make_float2(m, lt);
+      if (pp == 0) ws_ml[rec] = make_float2(m, lt);
     }
   }
   fence_before();
   __syncthreads();
   if (*abort && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
+  if (CLUSTER) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = g.S;
+    const int rpc = (kRows + S - 1) / S;  // rows owned (merged and written) per CTA
+    // receive area (in the now idle KV buffers of every CTA): [S][rpc][128] floats + [S][rpc] (m, l)
+    float* recv_o = reinterpret_cast<float*>(sKV);
+    float2* recv_ml = reinterpret_cast<float2*>(sKV + static_cast<size_t>(S) * rpc * kHD * 4);
+    __syncwarp();
+    cluster.sync();  // every CTA of the cluster is past its tile loop
+    if (softmax) {
+      const int owner = r / rpc, li = r - owner * rpc;
+      const bool ok = row_ok && !*abort;
+      const float inv = (ok && lt > 0.0f) ? 1.0f / lt : 0.0f;
+      float4* dst = cluster.map_shared_rank(reinterpret_cast<float4*>(recv_o + (static_cast<size_t>(s) * rpc + li) * kHD + pp * 32), owner);
+#pragma unroll
+      for (int d = 0; d < 8; ++d)
+        dst[d] = make_float4(o[4 * d] * inv, o[4 * d + 1] * inv, o[4 * d + 2] * inv, o[4 * d + 3] * inv);
+      if (pp == 0) *cluster.map_shared_rank(recv_ml + s * rpc + li, owner) = make_float2(m, ok ? lt : 0.0f);
+    }
+    cluster.sync();  // every partial row has landed at its owner
+    const int nwarps = blockDim.x >> 5;
+    for (int li = warp; li < rpc; li += nwarps) {
+      const int rr = s * rpc + li;
+      if (rr >= kRows) break;
+      const int grr = rg * kRows + rr;
+      if (grr >= g.G * g.R) continue;
+      const int nd = grr / g.G, hh = kvh * g.G + grr % g.G;
+      float2 ml = make_float2(-INFINITY, 0.0f);
+      if (lane < S) ml = recv_ml[lane * rpc + li];
+      float M = ml.y > 0.0f ? ml.x : -INFINITY;
+      M = warp_reduce(M, MaxF());
+      const float w = ml.y > 0.0f ? ml.y * fast_exp2(ml.x - M) : 0.0f;
+      const float den = warp_reduce(w, [](float a, float c) { return a + c; });
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int sg = 0; sg < S; ++sg) {
+        const float wj = __shfl_sync(0xFFFFFFFFu, w, sg);
+        const float4 vv = reinterpret_cast<const float4*>(recv_o + (static_cast<size_t>(sg) * rpc + li) * kHD)[lane];
+        acc.x = fmaf(wj, vv.x, acc.x);
+        acc.y = fmaf(wj, vv.y, acc.y);
+        acc.z = fmaf(wj, vv.z, acc.z);
+        acc.w = fmaf(wj, vv.w, acc.w);
+      }
+      const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+      const size_t orow = (static_cast<size_t>(b) * g.R + nd) * g.H + hh;
+      uint2 pk;
+      pk.x = pack2_bf16(acc.x * inv, acc.y * inv);
+      pk.y = pack2_bf16(acc.z * inv, acc.w * inv);
+      *reinterpret_cast<uint2*>(O + orow * kHD + lane * 4) = pk;
+      if (lane == 0) lse[orow] = (M + __log2f(den)) * 0.6931471805599453f;
+    }
+  }
   if (warp == 1) {
     __syncwarp();
     fence_after();
@@ -445,6 +547,43 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
+// How many clusters of S verify CTAs (one per SM) can be resident at once
+// (0 if such clusters cannot be launched).
+int max_active_clusters(int S) {
+  static int cache[17] = {0};  // -1: not launchable
+  if (S < 1 || S > 16) return 0;
+  if (cache[S] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = S;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    cache[S] = (cudaOccupancyMaxActiveClusters(&n, verify_tc_kernel<true>, &cfg) == cudaSuccess && n > 0) ? n : -1;
+    cudaGetLastError();
+  }
+  return cache[S] > 0 ? cache[S] : 0;
+}
+
+// Segments per cluster: the largest S (<= 16) whose clusters all fit in one wave
+// and still give every CTA at least two 128-key tiles; 1 when the groups alone
+// fill the GPU; 0 if no cluster can be launched.
+int pick_cluster_segments(int groups, int max_kv_len) {
+  if (max_active_clusters(1) == 0) return 0;
+  if (groups >= max_active_clusters(1)) return 1;
+  for (int S = 16; S >= 2; --S) {
+    const int n = max_active_clusters(S);
+    if (n >= groups && (max_kv_len + S - 1) / S >= 2 * kKeys) return S;
+  }
+  return 1;
+}
+
 }  // namespace
 
 bool verify_tc_supported(const e3_kv_layer& kv, int H) {
@@ -455,7 +594,7 @@ bool verify_tc_supported(const e3_kv_layer& kv, int H) {
 
 e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* kv_len, const uint64_t* mask, int B,
                            int R, int H, int max_kv_len, float sm_scale, int n_pre, int S, int chunk, float* ws_o,
-                           float2* ws_ml, int32_t* dev_err, cudaStream_t s) {
+                           float2* ws_ml, void* O, float* lse, bool* merged, int32_t* dev_err, cudaStream_t s) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   E3_REQUIRE(enc != nullptr, E3_ERR_CUDA, "tree_verify_attn: tensor-map encoder unavailable");
   const int G = H / kv.n_kv_heads;
@@ -496,14 +635,48 @@ e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* 
   g.max_pages = kv.max_pages;
   g.n_pages = kv.n_pages;
   g.page_table = kv.page_table;
+  g.fold_tree = 0;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(verify_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return cuda_status(e, "verify_tc_kernel smem attribute");
+    cudaFuncSetAttribute(verify_tc_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaGetLastError();
     attr_done = true;
   }
+  *merged = false;
+  const int Sc = pick_cluster_segments(g.RG * kv.n_kv_heads * B, max_kv_len);
+  if (Sc >= 1) {
+    // cluster mode: Sc prefix segments, the tree folded into the last one
+    S = Sc;
+    g.S = Sc;
+    g.n_pre = Sc;
+    g.fold_tree = 1;
+    g.chunk = ((max_kv_len + Sc - 1) / Sc + kHalf - 1) / kHalf * kHalf;
+    if (g.chunk < kHalf) g.chunk = kHalf;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g.RG * S, kv.n_kv_heads, B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = S;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, verify_tc_kernel<true>, mq, mk, mv, g, kv_len, mask, sm_scale, ws_o,
+                                       ws_ml, static_cast<__nv_bfloat16*>(O), lse, dev_err);
+    if (e != cudaSuccess) return cuda_status(e, "verify_tc_kernel (cluster)");
+    *merged = true;
+    return E3_OK;
+  }
   dim3 grid(g.RG * S, kv.n_kv_heads, B);
-  verify_tc_kernel<<<grid, 320, kSmem, s>>>(mq, mk, mv, g, kv_len, mask, sm_scale, ws_o, ws_ml, dev_err);
+  verify_tc_kernel<false><<<grid, kThreads, kSmem, s>>>(mq, mk, mv, g, kv_len, mask, sm_scale, ws_o, ws_ml,
+                                                   static_cast<__nv_bfloat16*>(O), lse, dev_err);
   E3_LAUNCH_CHECK("verify_tc_kernel");
   return E3_OK;
 }
