@@ -39,12 +39,11 @@ constexpr int kHalf = 64;       // head-dim (or key) elements per 128-byte row
 constexpr int kBox = kHalf * kHalf * 2;        // 64 x 64 bf16 = 8 KB
 constexpr int kQBytes = kRows * kHD * 2;       // 32 KB (two 16 KB halves)
 constexpr int kKVBytes = kKeys * kHD * 2;      // 32 KB per operand per tile
-constexpr int kStages = 2;
 constexpr int kPBytes = kRows * kKeys * 2;     // 32 KB
 constexpr int kRowCache = 128;       // KV block rows looked up ahead
 constexpr int kThreads = 576;         // warp 0 TMA, warp 1 MMA, warps 2..17 softmax
 constexpr int kSoftmaxThreads = 512;
-constexpr int kSmem = 1024 + kQBytes + kStages * 2 * kKVBytes + kPBytes + 256 + 12 * 128 * 4 + 4 * kRowCache + 64;
+constexpr int kSmem = 1024 + kQBytes + 4 * kKVBytes + kPBytes + 256 + 12 * 128 * 4 + 4 * kRowCache + 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
@@ -200,18 +199,24 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
                  int32_t* dev_err) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // Tile t uses K stage, V stage and TMEM S/O buffer t % 2.  K(t) is released as
+  // soon as S(t) has been computed and V(t) once PV(t) has run, so the next tiles'
+  // loads start early; P has its own buffer, rewritten only after PV(t-1).
   unsigned char* sQ = sm;                                  // [2 halves][128 rows][128 B]
-  unsigned char* sKV = sQ + kQBytes;                       // [stage][K | V][2 halves][128 keys][128 B]
-  unsigned char* sP = sKV + kStages * 2 * kKVBytes;        // [2 key halves][128 rows][128 B]
+  unsigned char* sK = sQ + kQBytes;                        // [2 stages][2 hd halves][128 keys][128 B]
+  unsigned char* sV = sK + 2 * kKVBytes;                   // [2 stages][2 hd halves][128 keys][128 B]
+  unsigned char* sP = sV + 2 * kKVBytes;                   // [2 key halves][128 rows][128 B]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kPBytes);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;    // [kStages]
-  uint64_t* kv_empty = bars + 3;   // [kStages]
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* o_full = bars + 7;
-  uint64_t* xch = bars + 8;        // [4] exchange among the four parts of a row, per lane quarter
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* k_full = bars + 1;     // [2]
+  uint64_t* k_empty = bars + 3;    // [2]
+  uint64_t* v_full = bars + 5;     // [2]
+  uint64_t* v_empty = bars + 7;    // [2]
+  uint64_t* s_full = bars + 9;     // [2]
+  uint64_t* p_full = bars + 11;    // [2]
+  uint64_t* o_full = bars + 13;    // [2]
+  uint64_t* xch = bars + 15;       // [4] exchange among the four parts of a row, per lane quarter
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* s_max = reinterpret_cast<float*>(tmem_slot + 4);  // [2 parities][4 parts][128 rows]
   float* s_l = s_max + 8 * kRows;                           // [4 parts][128 rows]
@@ -252,8 +257,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int nodes_per_tile = kRows / g.G;
   const int i0 = rg * nodes_per_tile;  // first node of this row group
 
-  // cache rows of the first kRowCache 64-key blocks, looked up by warp 0's lanes in
-  // parallel (the page table is read once, off the producer's critical path)
+  // rows of the first kRowCache 64-key blocks, looked up by warp 0's lanes in parallel
   int* s_rows = reinterpret_cast<int*>(s_l + 4 * kRows);  // [kRowCache], -1 = bad page
   if (warp == 0) {
     for (int i = lane; i < 2 * ntile && i < kRowCache; i += 32) {
@@ -265,72 +269,80 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
     __syncwarp();
   }
-  // TMA producer state (thread 0): it issues Q and the first stages right after
-  // initialising the barriers, so the loads overlap the TMEM allocation
-  bool okp = true;
-  auto issue_tile = [&](int t) {
-    const int st = t % kStages;
-    unsigned char* kst = sKV + st * 2 * kKVBytes;
-    unsigned char* vst = kst + kKVBytes;
-    bar_expect(&kv_full[st], 2 * kKVBytes);
-    for (int blk = 0; blk < 2; ++blk) {  // two 64-key blocks per tile
-      int row;
-      const int i = 2 * t + blk;
-      if (i < kRowCache) {
-        row = s_rows[i];
-        if (row < 0) {
-          okp = false;
-          row = 0;
-        }
-      } else {
-        const int T = tile_T0(t) + blk * kHalf;
-        bool ok = true;
-        const int page = page_of(g, b, T, &ok);
-        const int slot = ok ? T % g.page_size : 0;
-        okp &= ok || T >= P + g.R;  // blocks past the request's tokens only load masked filler
-        row = (page * g.KVH + kvh) * g.page_size + slot;
+  auto block_row = [&](int i, bool* okp) {  // cache row of 64-key block i
+    if (i < kRowCache) {
+      const int row = s_rows[i];
+      if (row < 0) {
+        *okp = false;
+        return 0;
       }
-      for (int h = 0; h < 2; ++h) {
-        tma2d(kst + h * (kKVBytes / 2) + blk * kBox, &tmK, h * kHalf, row, &kv_full[st]);
-        tma2d(vst + h * (kKVBytes / 2) + blk * kBox, &tmV, h * kHalf, row, &kv_full[st]);
-      }
+      return row;
+    }
+    const int T = tile_T0(i >> 1) + (i & 1) * kHalf;
+    bool ok = true;
+    const int page = page_of(g, b, T, &ok);
+    const int slot = ok ? T % g.page_size : 0;
+    if (!ok && T < P + g.R) *okp = false;
+    return (page * g.KVH + kvh) * g.page_size + slot;
+  };
+  // load tile t's K (which = 0) or V (which = 1) into stage t % 2
+  auto issue_kv = [&](int t, int which, bool* okp) {
+    const int st = t & 1;
+    unsigned char* base = (which ? sV : sK) + st * kKVBytes;
+    uint64_t* bar = which ? &v_full[st] : &k_full[st];
+    const CUtensorMap* map = which ? &tmV : &tmK;
+    bar_expect(bar, kKVBytes);
+    for (int blk = 0; blk < 2; ++blk) {
+      const int row = block_row(2 * t + blk, okp);
+      for (int h = 0; h < 2; ++h) tma2d(base + h * (kKVBytes / 2) + blk * kBox, map, h * kHalf, row, bar);
     }
   };
   if (threadIdx.x == 0) {
     bar_init(q_full, 1);
-    for (int st = 0; st < kStages; ++st) {
-      bar_init(&kv_full[st], 1);
-      bar_init(&kv_empty[st], 1);
+    for (int bb = 0; bb < 2; ++bb) {
+      bar_init(&k_full[bb], 1);
+      bar_init(&k_empty[bb], 1);
+      bar_init(&v_full[bb], 1);
+      bar_init(&v_empty[bb], 1);
+      bar_init(&s_full[bb], 1);
+      bar_init(&p_full[bb], kSoftmaxThreads);
+      bar_init(&o_full[bb], 1);
     }
-    bar_init(s_full, 1);
-    bar_init(p_full, kSoftmaxThreads);
-    bar_init(o_full, 1);
     for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], kSoftmaxThreads / 4);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (ntile > 0) {
+    if (ntile > 0) {  // Q and the first two tiles' K and V, before the TMEM allocation
+      bool okp = true;
       bar_expect(q_full, kQBytes);
       for (int h = 0; h < 2; ++h)
         tma3d(sQ + h * (kQBytes / 2), &tmQ, h * kHalf, kvh * g.G, b * g.R + i0, q_full);
-      for (int t = 0; t < ntile && t < kStages; ++t) issue_tile(t);
+      for (int t = 0; t < ntile && t < 2; ++t) {
+        issue_kv(t, 0, &okp);
+        issue_kv(t, 1, &okp);
+      }
+      if (!okp) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
     }
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)), "r"(256));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)), "r"(512));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   fence_before();
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem, tO = tmem + kKeys;
+  // TMEM: S buffers at columns [0,128) and [128,256), O buffers at [256,384), [384,512)
+  auto tS = [&](int bb) { return tmem + bb * kKeys; };
+  auto tO = [&](int bb) { return tmem + 2 * kKeys + bb * kHD; };
 
   if (warp == 0) {
-    if (lane == 0 && ntile > 0) {
-      for (int t = kStages; t < ntile; ++t) {
-        const int st = t % kStages;
-        if (!bar_wait(&kv_empty[st], ((t / kStages) & 1) ^ 1, abort)) break;
-        issue_tile(t);
+    // lane 0 streams K, lane 1 streams V: a slow V release never delays the next K
+    if (lane < 2 && ntile > 2) {
+      bool okp = true;
+      for (int t = 2; t < ntile; ++t) {
+        uint64_t* empty = lane == 0 ? &k_empty[t & 1] : &v_empty[t & 1];
+        if (!bar_wait(empty, ((t >> 1) & 1) ^ 1, abort)) break;
+        issue_kv(t, lane, &okp);
       }
       if (!okp) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
     }
@@ -338,32 +350,48 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (lane == 0 && ntile > 0) {
       constexpr uint32_t idS = idesc_bf16(kRows, kKeys, 0, 0);
       constexpr uint32_t idO = idesc_bf16(kRows, kHD, 0, 1);
-      bool ok = bar_wait(q_full, 0, abort);
       const uint32_t q_addr = su32(sQ), p_addr = su32(sP);
-      for (int t = 0; ok && t < ntile; ++t) {
-        const int st = t % kStages;
-        if (!bar_wait(&kv_full[st], (t / kStages) & 1, abort)) break;
-        fence_after();
-        const uint32_t k_addr = su32(sKV + st * 2 * kKVBytes);
-        const uint32_t v_addr = k_addr + kKVBytes;
+      auto issue_S = [&](int t) {  // S(t) = Q K(t)^T into S buffer t % 2; frees K stage t % 2
+        const int bb = t & 1;
+        const uint32_t k_addr = su32(sK + bb * kKVBytes);
 #pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk) {  // S = Q K^T over head_dim
+        for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32;
-          umma(tS, desc_sw128(q_addr + qoff, 16, 1024), desc_sw128(k_addr + off, 16, 1024), idS, kk > 0);
+          umma(tS(bb), desc_sw128(q_addr + qoff, 16, 1024), desc_sw128(k_addr + off, 16, 1024), idS, kk > 0);
         }
-        umma_commit(s_full);
-        if (!bar_wait(p_full, t & 1, abort)) break;
+        umma_commit(&s_full[bb]);
+        umma_commit(&k_empty[bb]);
+      };
+      bool ok = bar_wait(q_full, 0, abort);
+      for (int t = 0; ok && t < ntile && t < 2; ++t) {
+        if (!bar_wait(&k_full[t], 0, abort)) {
+          ok = false;
+          break;
+        }
         fence_after();
+        issue_S(t);
+      }
+      for (int t = 0; ok && t < ntile; ++t) {
+        const int bb = t & 1;
+        if (!bar_wait(&p_full[bb], (t >> 1) & 1, abort)) break;
+        if (!bar_wait(&v_full[bb], (t >> 1) & 1, abort)) break;
+        fence_after();
+        const uint32_t v_addr = su32(sV + bb * kKVBytes);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {  // O_t = P V over keys
+        for (int kk = 0; kk < kKeys / 16; ++kk) {  // O(t) = P(t) V(t) over keys
           const uint32_t poff = (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32;
           const uint32_t voff = kk * 16 * 128;  // 16 keys = 16 rows of 128 bytes
-          umma(tO, desc_sw128(p_addr + poff, 16, 1024), desc_sw128(v_addr + voff, kKVBytes / 2, 1024), idO,
+          umma(tO(bb), desc_sw128(p_addr + poff, 16, 1024), desc_sw128(v_addr + voff, kKVBytes / 2, 1024), idO,
                kk > 0);
         }
-        umma_commit(o_full);
-        umma_commit(&kv_empty[st]);
+        umma_commit(&o_full[bb]);   // O(t) ready; the P buffer and V stage t % 2 are free
+        umma_commit(&v_empty[bb]);
+        if (t + 2 < ntile) {
+          if (!bar_wait(&k_full[bb], ((t + 2) >> 1) & 1, abort)) break;
+          fence_after();
+          issue_S(t + 2);
+        }
       }
     }
   }
@@ -390,20 +418,95 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int tid_sm = threadIdx.x - 64;  // 0..511
     float l = 0.0f;
+    float corr_prev = 1.0f;  // correction of the previous tile, applied when its O is folded in
+    auto fold_O = [&](int t) {  // wait PV(t); o = o * corr(t) + O(t)
+      const int bb = t & 1;
+      if (!bar_wait(&o_full[bb], (t >> 1) & 1, abort)) return false;
+      fence_after();
+      float v[32];
+      tmem_ld32(tO(bb) + lane_base + pp * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = fmaf(o[j], corr_prev, v[j]);
+      return true;
+    };
+    bool live = true;
     for (int t = 0; t < ntile; ++t) {
       const int T0 = tile_T0(t);
       const int k0 = tile_lo(t), k1 = tile_hi(t);
       const bool tree = t >= ntA;
-      const int st = t % kStages;
-      unsigned char* vst = sKV + st * 2 * kKVBytes + kKVBytes;
-      if (!bar_wait(s_full, t & 1, abort)) break;
+      const int bb = t & 1;
+      if (!bar_wait(&s_full[bb], (t >> 1) & 1, abort)) {
+        live = false;
+        break;
+      }
       fence_after();
       float v[32];
-      tmem_ld32(tS + lane_base + pp * 32, v);  // this part's 32 scores (kept in registers)
+      tmem_ld32(tS(bb) + lane_base + pp * 32, v);  // this part's 32 scores
+      const int Tc = T0 + pp * 32;
+      uint32_t valid = range_bits32(Tc, k0, k1);
+      if (tree) valid &= mask_bits32(mrow, words, Tc - P);
+      const bool full = valid == 0xFFFFFFFFu;  // interior chunk: no per-element tests
+      float pmax = -INFINITY;
+      if (full) {
+        float a0 = fmaxf(v[0], v[1]), a1 = fmaxf(v[2], v[3]), a2 = fmaxf(v[4], v[5]), a3 = fmaxf(v[6], v[7]);
+#pragma unroll
+        for (int j = 8; j < 32; j += 8) {
+          a0 = fmaxf(a0, fmaxf(v[j], v[j + 1]));
+          a1 = fmaxf(a1, fmaxf(v[j + 2], v[j + 3]));
+          a2 = fmaxf(a2, fmaxf(v[j + 4], v[j + 5]));
+          a3 = fmaxf(a3, fmaxf(v[j + 6], v[j + 7]));
+        }
+        pmax = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c2;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if ((valid >> j) & 1u) pmax = fmaxf(pmax, v[j] * c2);
+      }
+      s_max[((t & 1) * 4 + pp) * kRows + r] = pmax;
+      bar_arrive(&xch[q]);
+      if (!bar_wait(&xch[q], t & 1, abort)) {
+        live = false;
+        break;
+      }
+      float tmax = s_max[((t & 1) * 4) * kRows + r];
+#pragma unroll
+      for (int x = 1; x < 4; ++x) tmax = fmaxf(tmax, s_max[((t & 1) * 4 + x) * kRows + r]);
+      const float mn = fmaxf(m, tmax);
+      const float corr = (mn == -INFINITY) ? 1.0f : fast_exp2(m - mn);
+      const float nsub = (mn == -INFINITY) ? 0.0f : -mn;
+      // probabilities of this part's 32 keys, packed to bf16 pairs
+      uint32_t pk[16];
+      float rs = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        float e0, e1;
+        if (full) {
+          e0 = fast_exp2(fmaf(v[j], c2, nsub));
+          e1 = fast_exp2(fmaf(v[j + 1], c2, nsub));
+        } else {
+          e0 = ((valid >> j) & 1u) ? fast_exp2(fmaf(v[j], c2, nsub)) : 0.0f;
+          e1 = ((valid >> (j + 1)) & 1u) ? fast_exp2(fmaf(v[j + 1], c2, nsub)) : 0.0f;
+        }
+        rs += e0 + e1;
+        pk[j >> 1] = pack2_bf16(e0, e1);
+      }
+      l = l * corr + rs;
+      m = mn;
+      // PV(t-1) must have read the P buffer (and O(t-1) is then ready to fold)
+      if (t > 0 && !fold_O(t - 1)) {
+        live = false;
+        break;
+      }
+      corr_prev = corr;
       // V rows of keys outside the range are zeroed so that masked keys add exactly 0
       if (tid_sm < kKeys) {
         const int T = T0 + tid_sm;
         if (T < k0 || T >= k1) {
+          if (!bar_wait(&v_full[bb], (t >> 1) & 1, abort)) {
+            live = false;
+            break;
+          }
+          unsigned char* vst = sV + bb * kKVBytes;
           const uint4 z = make_uint4(0, 0, 0, 0);
           for (int h = 0; h < 2; ++h) {
             uint4* rowp = reinterpret_cast<uint4*>(vst + h * (kKVBytes / 2) + tid_sm * 128);
@@ -412,52 +515,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
         }
       }
-      const int Tc = T0 + pp * 32;
-      uint32_t valid = range_bits32(Tc, k0, k1);
-      if (tree) valid &= mask_bits32(mrow, words, Tc - P);
-      float pmax = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if ((valid >> j) & 1u) pmax = fmaxf(pmax, v[j] * c2);
-      s_max[((t & 1) * 4 + pp) * kRows + r] = pmax;
-      bar_arrive(&xch[q]);
-      if (!bar_wait(&xch[q], t & 1, abort)) break;
-      float tmax = s_max[((t & 1) * 4) * kRows + r];
-#pragma unroll
-      for (int x = 1; x < 4; ++x) tmax = fmaxf(tmax, s_max[((t & 1) * 4 + x) * kRows + r]);
-      const float mn = fmaxf(m, tmax);
-      const float corr = (mn == -INFINITY) ? 1.0f : fast_exp2(m - mn);
-      const float sub = (mn == -INFINITY) ? 0.0f : mn;
-      float rs = 0.0f;
-      // P for keys [32pp, 32pp+32): key half pp/2, 8-key chunks (pp%2)*4 + c4, each
-      // at 16-byte slot (chunk ^ (r & 7)) of row r (K-major, 128-byte swizzle)
+      // P(t) for keys [32pp, 32pp+32): key half pp/2, 8-key chunks (pp%2)*4 + c4,
+      // each at 16-byte slot (chunk ^ (r & 7)) of row r (K-major, 128-byte swizzle)
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
-        float e[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = c4 * 8 + u;
-          e[u] = ((valid >> j) & 1u) ? fast_exp2(v[j] * c2 - sub) : 0.0f;
-          rs += e[u];
-        }
-        uint4 pk;
-        pk.x = pack2_bf16(e[0], e[1]);
-        pk.y = pack2_bf16(e[2], e[3]);
-        pk.z = pack2_bf16(e[4], e[5]);
-        pk.w = pack2_bf16(e[6], e[7]);
         const int c8 = (pp & 1) * 4 + c4;
-        *reinterpret_cast<uint4*>(sP + (pp >> 1) * (kPBytes / 2) + r * 128 + ((c8 ^ (r & 7)) << 4)) = pk;
+        *reinterpret_cast<uint4*>(sP + (pp >> 1) * (kPBytes / 2) + r * 128 + ((c8 ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
       }
-      l = l * corr + rs;
-      m = mn;
       fence_async_smem();  // generic-proxy writes (P, zeroed V rows) -> tensor core
-      bar_arrive(p_full);
-      if (!bar_wait(o_full, t & 1, abort)) break;
-      fence_after();
-      tmem_ld32(tO + lane_base + pp * 32, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = fmaf(o[j], corr, v[j]);
+      bar_arrive(&p_full[bb]);
     }
+    if (live && ntile > 0) fold_O(ntile - 1);
     // total of the four parts' sums
     s_l[pp * kRows + r] = l;
     bar_arrive(&xch[q]);
@@ -482,8 +551,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const int S = g.S;
     const int rpc = (kRows + S - 1) / S;  // rows owned (merged and written) per CTA
     // receive area (in the now idle KV buffers of every CTA): [S][rpc][128] floats + [S][rpc] (m, l)
-    float* recv_o = reinterpret_cast<float*>(sKV);
-    float2* recv_ml = reinterpret_cast<float2*>(sKV + static_cast<size_t>(S) * rpc * kHD * 4);
+    float* recv_o = reinterpret_cast<float*>(sK);  // K and V rings: 128 KB, contiguous
+    float2* recv_ml = reinterpret_cast<float2*>(sK + static_cast<size_t>(S) * rpc * kHD * 4);
     __syncwarp();
     cluster.sync();  // every CTA of the cluster is past its tile loop
     if (softmax) {
@@ -531,7 +600,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (warp == 1) {
     __syncwarp();
     fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
   }
 }
 
