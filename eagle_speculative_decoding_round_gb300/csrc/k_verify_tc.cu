@@ -13,11 +13,11 @@
 // over Q[B*R][H][hd]).  Keys stream in tiles of 128 (two 64-token page boxes per
 // operand):
 //   S = Q K^T    tcgen05.mma, M = 128 rows, N = 128 keys, K = head_dim (K-major)
-//   softmax      one thread per query row reads its TMEM lane; running max and
-//                sum in registers; P (bf16) written to shared memory as a K-major
-//                128-byte-swizzled operand
-//   O_t = P V    tcgen05.mma, N = head_dim, K = keys; V is used in place as an
-//                MN-major operand (rows of 64 head-dim values per key)
+//   softmax      the threads of a query row read its TMEM lane; running max and
+//                sum in registers; P (bf16) is written back over S in TMEM
+//   O_t = P V    tcgen05.mma with A (P) from TMEM, N = head_dim, K = keys; V is
+//                used in place as an MN-major operand (rows of 64 head-dim values
+//                per key)
 //   O += O_t     accumulated in registers with the online-softmax correction.
 // Warps: 0 TMA, 1 TMEM owner + MMA issuer, 2..17 softmax/epilogue (four warps per
 // TMEM lane quarter, each owning a quarter of the keys and of the head dims).
@@ -39,11 +39,10 @@ constexpr int kHalf = 64;       // head-dim (or key) elements per 128-byte row
 constexpr int kBox = kHalf * kHalf * 2;        // 64 x 64 bf16 = 8 KB
 constexpr int kQBytes = kRows * kHD * 2;       // 32 KB (two 16 KB halves)
 constexpr int kKVBytes = kKeys * kHD * 2;      // 32 KB per operand per tile
-constexpr int kPBytes = kRows * kKeys * 2;     // 32 KB
 constexpr int kRowCache = 128;       // KV block rows looked up ahead
 constexpr int kThreads = 576;         // warp 0 TMA, warp 1 MMA, warps 2..17 softmax
 constexpr int kSoftmaxThreads = 512;
-constexpr int kSmem = 1024 + kQBytes + 4 * kKVBytes + kPBytes + 256 + 12 * 128 * 4 + 4 * kRowCache + 64;
+constexpr int kSmem = 1024 + kQBytes + 4 * kKVBytes + 256 + 12 * 128 * 4 + 4 * kRowCache + 64;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
@@ -113,6 +112,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
   asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::
                    "r"(d), "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+// D = A(TMEM) * B(smem): A is M x K with row i in TMEM lane i and two 16-bit
+// K elements per 32-bit column (the lower half is the lower K index).
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t id, uint32_t acc) {
+  asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::
+                   "r"(d), "r"(a_tmem), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]));
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void umma_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b)) : "memory");
@@ -201,12 +213,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // Tile t uses K stage, V stage and TMEM S/O buffer t % 2.  K(t) is released as
   // soon as S(t) has been computed and V(t) once PV(t) has run, so the next tiles'
-  // loads start early; P has its own buffer, rewritten only after PV(t-1).
+  // loads start early.  P(t) is written (bf16) over S(t) in tensor memory.
   unsigned char* sQ = sm;                                  // [2 halves][128 rows][128 B]
   unsigned char* sK = sQ + kQBytes;                        // [2 stages][2 hd halves][128 keys][128 B]
   unsigned char* sV = sK + 2 * kKVBytes;                   // [2 stages][2 hd halves][128 keys][128 B]
-  unsigned char* sP = sV + 2 * kKVBytes;                   // [2 key halves][128 rows][128 B]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + kPBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * kKVBytes);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;     // [2]
   uint64_t* k_empty = bars + 3;    // [2]
@@ -350,7 +361,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (lane == 0 && ntile > 0) {
       constexpr uint32_t idS = idesc_bf16(kRows, kKeys, 0, 0);
       constexpr uint32_t idO = idesc_bf16(kRows, kHD, 0, 1);
-      const uint32_t q_addr = su32(sQ), p_addr = su32(sP);
+      const uint32_t q_addr = su32(sQ);
       auto issue_S = [&](int t) {  // S(t) = Q K(t)^T into S buffer t % 2; frees K stage t % 2
         const int bb = t & 1;
         const uint32_t k_addr = su32(sK + bb * kKVBytes);
@@ -379,15 +390,15 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         fence_after();
         const uint32_t v_addr = su32(sV + bb * kKVBytes);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {  // O(t) = P(t) V(t) over keys
-          const uint32_t poff = (kk >> 2) * (kPBytes / 2) + (kk & 3) * 32;
-          const uint32_t voff = kk * 16 * 128;  // 16 keys = 16 rows of 128 bytes
-          umma(tO(bb), desc_sw128(p_addr + poff, 16, 1024), desc_sw128(v_addr + voff, kKVBytes / 2, 1024), idO,
-               kk > 0);
+        for (int kk = 0; kk < kKeys / 16; ++kk) {  // O(t) = P(t) V(t) over keys; P from TMEM
+          const uint32_t voff = kk * 16 * 128;     // 16 keys = 16 rows of 128 bytes
+          umma_ts(tO(bb), tS(bb) + kk * 8, desc_sw128(v_addr + voff, kKVBytes / 2, 1024), idO, kk > 0);
         }
-        umma_commit(&o_full[bb]);   // O(t) ready; the P buffer and V stage t % 2 are free
+        umma_commit(&o_full[bb]);   // O(t) ready; V stage t % 2 is free
         umma_commit(&v_empty[bb]);
         if (t + 2 < ntile) {
+          // S(t+2) overwrites P(t): PV(t) must have completed
+          if (!bar_wait(&o_full[bb], (t >> 1) & 1, abort)) break;
           if (!bar_wait(&k_full[bb], ((t + 2) >> 1) & 1, abort)) break;
           fence_after();
           issue_S(t + 2);
@@ -463,11 +474,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           if ((valid >> j) & 1u) pmax = fmaxf(pmax, v[j] * c2);
       }
       s_max[((t & 1) * 4 + pp) * kRows + r] = pmax;
+      fence_before();  // this part's S loads are done before the others overwrite S with P
       bar_arrive(&xch[q]);
       if (!bar_wait(&xch[q], t & 1, abort)) {
         live = false;
         break;
       }
+      fence_after();
       float tmax = s_max[((t & 1) * 4) * kRows + r];
 #pragma unroll
       for (int x = 1; x < 4; ++x) tmax = fmaxf(tmax, s_max[((t & 1) * 4 + x) * kRows + r]);
@@ -492,13 +505,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
       l = l * corr + rs;
       m = mn;
-      // PV(t-1) must have read the P buffer (and O(t-1) is then ready to fold)
-      if (t > 0 && !fold_O(t - 1)) {
-        live = false;
-        break;
-      }
-      corr_prev = corr;
+      // P(t) over this part's S columns: keys [32pp, 32pp+32) -> columns [16pp, 16pp+16)
+      // of the S buffer (all four parts have read their scores: the exchange above)
+      tmem_st16(tS(bb) + lane_base + pp * 16, pk);
       // V rows of keys outside the range are zeroed so that masked keys add exactly 0
+      bool zeroed = false;
       if (tid_sm < kKeys) {
         const int T = T0 + tid_sm;
         if (T < k0 || T >= k1) {
@@ -513,18 +524,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
             for (int c = 0; c < 8; ++c) rowp[c] = z;
           }
+          zeroed = true;
         }
       }
-      // P(t) for keys [32pp, 32pp+32): key half pp/2, 8-key chunks (pp%2)*4 + c4,
-      // each at 16-byte slot (chunk ^ (r & 7)) of row r (K-major, 128-byte swizzle)
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int c8 = (pp & 1) * 4 + c4;
-        *reinterpret_cast<uint4*>(sP + (pp >> 1) * (kPBytes / 2) + r * 128 + ((c8 ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
-      }
-      fence_async_smem();  // generic-proxy writes (P, zeroed V rows) -> tensor core
+      if (zeroed) fence_async_smem();  // generic-proxy writes -> tensor core
+      fence_before();                  // order the tcgen05.st before the arrival
       bar_arrive(&p_full[bb]);
+      // fold in the previous tile's O while this tile's PV runs
+      if (t > 0 && !fold_O(t - 1)) {
+        live = false;
+        break;
+      }
+      corr_prev = corr;
     }
     if (live && ntile > 0) fold_O(ntile - 1);
     // total of the four parts' sums
