@@ -28,9 +28,17 @@ e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_
                         int B, int R, int H, int max_kv_len, float sm_scale, void* O, float* lse,
                         int32_t* dev_err, void* ws, size_t ws_bytes, cudaStream_t s);
 
+// How the keys of one (request, KV head) are split across CTAs: n_pre prefix
+// segments of `chunk` keys, S partial records per row; fold = 1 when the tree
+// slots are processed by the last prefix segment (no separate tree segment).
+struct VerifySplit {
+  int n_pre, S, chunk, fold;
+};
 bool verify_tc_supported(const e3_kv_layer& kv, int H);
+// On entry *split is the workspace's split (at most split->S records per row);
+// on return, the split the partial records were written with (when not merged).
 e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* kv_len, const uint64_t* mask, int B,
-                           int R, int H, int max_kv_len, float sm_scale, int n_pre, int S, int chunk, float* ws_o,
+                           int R, int H, int max_kv_len, float sm_scale, VerifySplit* split, float* ws_o,
                            float2* ws_ml, void* O, float* lse, bool* merged, int32_t* dev_err, cudaStream_t s);
 
 e3_status launch_gemm_simt(const void* a0, const void* a1, const void* a2, int dseg, const void* W,

@@ -30,6 +30,7 @@ struct VerifyGeom {
   int B, R, H, KVH, G, hd;
   int n_pre, S, chunk, RG;
   int max_kv_len;
+  int fold;  // 1: S prefix segments, the last one also holding the tree slots
 };
 
 __device__ __forceinline__ bool kv_capacity_ok(const e3_kv_layer& kv, int P, int R, int max_kv_len) {
@@ -410,8 +411,10 @@ verify_merge_kernel(e3_kv_layer kv, const int32_t* __restrict__ kv_len, VerifyGe
   const int ih = static_cast<int>(row % (static_cast<long>(g.R) * g.H));
   const int P = kv_len[b];
   if (!kv_capacity_ok(kv, P, g.R, g.max_kv_len)) return;
-  const int n_pre_b = (P + g.chunk - 1) / g.chunk;  // prefix segments that hold keys
-  const int nseg = n_pre_b + 1;                     // + the tree segment
+  // segments that hold keys: the prefix segments up to P and the tree segment, or
+  // (tree folded into the last prefix segment) every segment
+  const int n_pre_b = g.fold ? g.S : (P + g.chunk - 1) / g.chunk;
+  const int nseg = g.fold ? g.S : n_pre_b + 1;
   const size_t stride = static_cast<size_t>(g.R) * g.H;
   const size_t base = static_cast<size_t>(b) * g.S * stride + ih;
   auto seg_id = [&](int q) { return q < n_pre_b ? q : g.n_pre; };
@@ -518,10 +521,15 @@ e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_
 
   if (mma && verify_tc_supported(kv, H)) {
     bool merged = false;
-    e3_status st = launch_verify_tc(Q, kv, kv_len, mask, B, R, H, max_kv_len, sm_scale, g.n_pre, g.S, g.chunk, ws_o,
-                                    ws_ml, O, lse, &merged, dev_err, s);
+    VerifySplit sp{g.n_pre, g.S, g.chunk, 0};
+    e3_status st = launch_verify_tc(Q, kv, kv_len, mask, B, R, H, max_kv_len, sm_scale, &sp, ws_o, ws_ml, O, lse,
+                                    &merged, dev_err, s);
     if (st != E3_OK) return st;
     if (merged) return E3_OK;  // segments merged inside the cluster
+    g.n_pre = sp.n_pre;
+    g.S = sp.S;
+    g.chunk = sp.chunk;
+    g.fold = sp.fold;
   } else if (mma) {
     dim3 grid(g.RG * g.S, kv.n_kv_heads, B);
 #define E3_MMA_CASE(HDV)                                                                           \

@@ -21,7 +21,7 @@
 //   O += O_t     accumulated in registers with the online-softmax correction.
 // Warps: 0 TMA, 1 TMEM owner + MMA issuer, 2..17 softmax/epilogue (four warps per
 // TMEM lane quarter, each owning a quarter of the keys and of the head dims).
-#include <cooperative_groups.h>
+#include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -86,6 +86,14 @@ __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t par, volatile int
     }
   }
 }
+// Wait bounded by time only (for copies that are in flight whatever the abort flag says).
+__device__ __forceinline__ bool bar_wait_timed(uint64_t* b, uint32_t par) {
+  if (bar_try(b, par)) return true;
+  const uint64_t t0 = gtimer();
+  while (gtimer() - t0 < kWaitNs)
+    if (bar_try(b, par)) return true;
+  return false;
+}
 __device__ __forceinline__ void tma2d(void* dst, const CUtensorMap* m, int x, int y, uint64_t* b) {
   asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
                    "r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(su32(b))
@@ -146,6 +154,23 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+// bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into another
+// CTA's, completing as transaction bytes on that CTA's mbarrier
+__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -227,7 +252,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint64_t* p_full = bars + 11;    // [2]
   uint64_t* o_full = bars + 13;    // [2]
   uint64_t* xch = bars + 15;       // [4] exchange among the four parts of a row, per lane quarter
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+  uint64_t* recv_bar = bars + 19;  // cluster merge: the other CTAs' partial rows have landed here
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* s_max = reinterpret_cast<float*>(tmem_slot + 4);  // [2 parities][4 parts][128 rows]
   float* s_l = s_max + 8 * kRows;                           // [4 parts][128 rows]
@@ -236,10 +262,45 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int rg = CLUSTER ? blockIdx.x / g.S : blockIdx.x % g.RG;
   const int s = CLUSTER ? blockIdx.x % g.S : blockIdx.x / g.RG;
   const int kvh = blockIdx.y, b = blockIdx.z;
+  const int nodes_per_tile = kRows / g.G;
+  const int i0 = rg * nodes_per_tile;  // first node of this row group
+  if (threadIdx.x == 0) {  // barriers and the Q load first: neither depends on the request's length
+    bar_init(q_full, 1);
+    for (int bb = 0; bb < 2; ++bb) {
+      bar_init(&k_full[bb], 1);
+      bar_init(&k_empty[bb], 1);
+      bar_init(&v_full[bb], 1);
+      bar_init(&v_empty[bb], 1);
+      bar_init(&s_full[bb], 1);
+      bar_init(&p_full[bb], kSoftmaxThreads);
+      bar_init(&o_full[bb], 1);
+    }
+    for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], kSoftmaxThreads / 4);
+    bar_init(recv_bar, 1);
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    bar_expect(q_full, kQBytes);
+    for (int h = 0; h < 2; ++h) tma3d(sQ + h * (kQBytes / 2), &tmQ, h * kHalf, kvh * g.G, b * g.R + i0, q_full);
+  }
+  // Warp 0 loads, together with the request's length, the page-table entries of
+  // this segment's first prefix blocks as they are if the prefix covers the whole
+  // segment; after the length is known they are kept where that guess holds.
+  const int spec_base = (g.fold_tree || s < g.n_pre) ? s * g.chunk : -1;
+  int spec[kRowCache / 32];
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < kRowCache / 32; ++k) {
+      const int pi = (spec_base + (lane + 32 * k) * kHalf) / g.page_size;
+      spec[k] = (spec_base >= 0 && pi < g.max_pages) ? g.page_table[static_cast<size_t>(b) * g.max_pages + pi] : -1;
+    }
+  }
   const int P = kv_len[b];
   const long need = static_cast<long>(P) + g.R;
   if (P < 0 || P > g.max_kv_len || need > static_cast<long>(g.max_pages) * g.page_size) {
-    if (threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
+    if (threadIdx.x == 0) {
+      if (blockIdx.x == 0 && kvh == 0) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
+      bar_wait_timed(q_full, 0);  // the Q load lands before the CTA leaves
+    }
     return;  // uniform across the cluster (same request)
   }
   // key ranges of this CTA: a prefix range [pk0, pk1) and, for the tree segment
@@ -265,18 +326,22 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   auto tile_T0 = [&](int t) { return t < ntA ? tA + t * kKeys : tB + (t - ntA) * kKeys; };
   auto tile_lo = [&](int t) { return t < ntA ? pk0 : P; };
   auto tile_hi = [&](int t) { return t < ntA ? pk1 : P + g.R; };
-  const int nodes_per_tile = kRows / g.G;
-  const int i0 = rg * nodes_per_tile;  // first node of this row group
 
   // rows of the first kRowCache 64-key blocks, looked up by warp 0's lanes in parallel
   int* s_rows = reinterpret_cast<int*>(s_l + 4 * kRows);  // [kRowCache], -1 = bad page
   if (warp == 0) {
-    for (int i = lane; i < 2 * ntile && i < kRowCache; i += 32) {
-      const int T = tile_T0(i >> 1) + (i & 1) * kHalf;
-      bool ok = true;
-      const int page = page_of(g, b, T, &ok);
-      const int slot = ok ? T % g.page_size : 0;
-      s_rows[i] = (ok || T >= P + g.R) ? (page * g.KVH + kvh) * g.page_size + slot : -1;
+#pragma unroll
+    for (int k = 0; k < kRowCache / 32; ++k) {
+      const int i = lane + 32 * k;
+      if (i < 2 * ntile) {
+        const int T = tile_T0(i >> 1) + (i & 1) * kHalf;
+        const int pi = T / g.page_size;
+        int p = spec[k];
+        if (T != spec_base + i * kHalf || spec_base < 0)
+          p = pi < g.max_pages ? g.page_table[static_cast<size_t>(b) * g.max_pages + pi] : -1;
+        const bool ok = pi < g.max_pages && p >= 0 && p < g.n_pages;
+        s_rows[i] = (ok || T >= P + g.R) ? ((ok ? p : 0) * g.KVH + kvh) * g.page_size + (ok ? T % g.page_size : 0) : -1;
+      }
     }
     __syncwarp();
   }
@@ -308,31 +373,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int h = 0; h < 2; ++h) tma2d(base + h * (kKVBytes / 2) + blk * kBox, map, h * kHalf, row, bar);
     }
   };
-  if (threadIdx.x == 0) {
-    bar_init(q_full, 1);
-    for (int bb = 0; bb < 2; ++bb) {
-      bar_init(&k_full[bb], 1);
-      bar_init(&k_empty[bb], 1);
-      bar_init(&v_full[bb], 1);
-      bar_init(&v_empty[bb], 1);
-      bar_init(&s_full[bb], 1);
-      bar_init(&p_full[bb], kSoftmaxThreads);
-      bar_init(&o_full[bb], 1);
+  if (threadIdx.x == 0 && ntile > 0) {  // the first two tiles' K and V, before the TMEM allocation
+    bool okp = true;
+    for (int t = 0; t < ntile && t < 2; ++t) {
+      issue_kv(t, 0, &okp);
+      issue_kv(t, 1, &okp);
     }
-    for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], kSoftmaxThreads / 4);
-    *abort = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if (ntile > 0) {  // Q and the first two tiles' K and V, before the TMEM allocation
-      bool okp = true;
-      bar_expect(q_full, kQBytes);
-      for (int h = 0; h < 2; ++h)
-        tma3d(sQ + h * (kQBytes / 2), &tmQ, h * kHalf, kvh * g.G, b * g.R + i0, q_full);
-      for (int t = 0; t < ntile && t < 2; ++t) {
-        issue_kv(t, 0, &okp);
-        issue_kv(t, 1, &okp);
-      }
-      if (!okp) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
-    }
+    if (!okp) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)), "r"(512));
@@ -553,60 +600,110 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (pp == 0) ws_ml[rec] = make_float2(m, lt);
     }
   }
+  // the Q load has landed (also where no tile was processed) before the CTA's
+  // shared memory is reused or released
+  if (threadIdx.x == 0 && !bar_wait_timed(q_full, 0)) *abort = 1;
   fence_before();
   __syncthreads();
   if (*abort && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
   if (CLUSTER) {
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
     const int S = g.S;
     const int rpc = (kRows + S - 1) / S;  // rows owned (merged and written) per CTA
-    // receive area (in the now idle KV buffers of every CTA): [S][rpc][128] floats + [S][rpc] (m, l)
-    float* recv_o = reinterpret_cast<float*>(sK);  // K and V rings: 128 KB, contiguous
-    float2* recv_ml = reinterpret_cast<float2*>(sK + static_cast<size_t>(S) * rpc * kHD * 4);
-    __syncwarp();
-    cluster.sync();  // every CTA of the cluster is past its tile loop
+    // Local staging of this CTA's normalized partial rows: o as [128 rows][128] fp32
+    // in the V ring (the 16-byte chunks of each 32-float part XOR-swizzled by row so
+    // that the row-per-lane writes do not collide in banks), (m, l) as float4 rows
+    // in the Q/K region past the receive area.  Receive area (written by the bulk
+    // copies of every CTA of the cluster, this one included): [S][rpc] o rows from
+    // the start of the Q buffer (Q and K rings are contiguous, 96 KB; at most
+    // (128 + S - 1) rows = 72 KB), then [S][rpc] (m, l) float4 rows.
+    float* stage_o = reinterpret_cast<float*>(sV);
+    float4* stage_ml = reinterpret_cast<float4*>(sQ + 76 * 1024);
+    float* recv_o = reinterpret_cast<float*>(sQ);
+    float4* recv_ml = reinterpret_cast<float4*>(sQ + static_cast<size_t>(S) * rpc * kHD * 4);
+    const int n_own = max(0, min(rpc, kRows - s * rpc));
     if (softmax) {
-      const int owner = r / rpc, li = r - owner * rpc;
       const bool ok = row_ok && !*abort;
       const float inv = (ok && lt > 0.0f) ? 1.0f / lt : 0.0f;
-      float4* dst = cluster.map_shared_rank(reinterpret_cast<float4*>(recv_o + (static_cast<size_t>(s) * rpc + li) * kHD + pp * 32), owner);
+      float4* row = reinterpret_cast<float4*>(stage_o + r * kHD) + pp * 8;
 #pragma unroll
       for (int d = 0; d < 8; ++d)
-        dst[d] = make_float4(o[4 * d] * inv, o[4 * d + 1] * inv, o[4 * d + 2] * inv, o[4 * d + 3] * inv);
-      if (pp == 0) *cluster.map_shared_rank(recv_ml + s * rpc + li, owner) = make_float2(m, ok ? lt : 0.0f);
+        row[d ^ (r & 7)] = make_float4(o[4 * d] * inv, o[4 * d + 1] * inv, o[4 * d + 2] * inv, o[4 * d + 3] * inv);
+      if (pp == 0) stage_ml[r] = make_float4(m, ok ? lt : 0.0f, 0.0f, 0.0f);
     }
-    cluster.sync();  // every partial row has landed at its owner
-    const int nwarps = blockDim.x >> 5;
-    for (int li = warp; li < rpc; li += nwarps) {
-      const int rr = s * rpc + li;
-      if (rr >= kRows) break;
-      const int grr = rg * kRows + rr;
-      if (grr >= g.G * g.R) continue;
-      const int nd = grr / g.G, hh = kvh * g.G + grr % g.G;
-      float2 ml = make_float2(-INFINITY, 0.0f);
-      if (lane < S) ml = recv_ml[lane * rpc + li];
-      float M = ml.y > 0.0f ? ml.x : -INFINITY;
-      M = warp_reduce(M, MaxF());
-      const float w = ml.y > 0.0f ? ml.y * fast_exp2(ml.x - M) : 0.0f;
-      const float den = warp_reduce(w, [](float a, float c) { return a + c; });
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int sg = 0; sg < S; ++sg) {
-        const float wj = __shfl_sync(0xFFFFFFFFu, w, sg);
-        const float4 vv = reinterpret_cast<const float4*>(recv_o + (static_cast<size_t>(sg) * rpc + li) * kHD)[lane];
-        acc.x = fmaf(wj, vv.x, acc.x);
-        acc.y = fmaf(wj, vv.y, acc.y);
-        acc.z = fmaf(wj, vv.z, acc.z);
-        acc.w = fmaf(wj, vv.w, acc.w);
+    fence_async_smem();  // staged rows -> bulk-copy engine
+    if (threadIdx.x == 0) bar_expect(recv_bar, static_cast<uint32_t>(S * n_own) * (kHD * 4 + 16));
+    __syncthreads();
+    // every CTA of the cluster is past its tile loop: receive areas are idle.  The
+    // barrier orders execution only (the tensor-core reads and TMA writes of those
+    // areas completed before the loop ended); the receive mbarrier's initialization
+    // was published by the release fence after it.
+    __syncwarp();
+    cluster_arrive_relaxed();
+    cluster_wait();
+    if (threadIdx.x == 0) {
+      const uint32_t bar_local = su32(recv_bar);
+      for (int ow = 0; ow < S; ++ow) {
+        const int n = min(rpc, kRows - ow * rpc);
+        if (n <= 0) continue;
+        const uint32_t bar = cluster_addr(bar_local, ow);
+        bulk_to_peer(cluster_addr(su32(recv_o + static_cast<size_t>(s) * rpc * kHD), ow),
+                     su32(stage_o + static_cast<size_t>(ow) * rpc * kHD), n * kHD * 4, bar);
+        bulk_to_peer(cluster_addr(su32(recv_ml + s * rpc), ow), su32(stage_ml + ow * rpc), n * 16, bar);
       }
-      const float inv = den > 0.0f ? 1.0f / den : 0.0f;
-      const size_t orow = (static_cast<size_t>(b) * g.R + nd) * g.H + hh;
-      uint2 pk;
-      pk.x = pack2_bf16(acc.x * inv, acc.y * inv);
-      pk.y = pack2_bf16(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(O + orow * kHD + lane * 4) = pk;
-      if (lane == 0) lse[orow] = (M + __log2f(den)) * 0.6931471805599453f;
     }
+    // inbound rows (time-bounded only: the copies are in flight whatever the abort flag says)
+    const bool got = bar_wait_timed(recv_bar, 0);
+    if (!got) *abort = 1;
+    // this CTA's inbound copies are complete (the matching wait before exit keeps
+    // every CTA's staging alive until all copies of the cluster have landed)
+    __syncwarp();
+    cluster_arrive_relaxed();  // control only: no data is published through this barrier
+    // merge: 16 threads per owned row, each with 8 head dims (two swizzled chunks)
+    for (int it = threadIdx.x; got && it < n_own * 16; it += kThreads) {
+      const int li = it >> 4, c = it & 15;
+      const int rr = s * rpc + li;
+      const int grr = rg * kRows + rr;
+      if (grr < g.G * g.R) {
+        const int nd = grr / g.G, hh = kvh * g.G + grr % g.G;
+        const int c0 = (c >> 2) * 8 + (((2 * c) & 7) ^ (rr & 7));  // chunk of head dims 8c..8c+3
+        const int c1 = (c >> 2) * 8 + (((2 * c + 1) & 7) ^ (rr & 7));
+        float M = -INFINITY;
+        for (int sg = 0; sg < S; ++sg) {
+          const float4 ml = recv_ml[sg * rpc + li];
+          if (ml.y > 0.0f) M = fmaxf(M, ml.x);
+        }
+        float den = 0.0f;
+        float a[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = 0.0f;
+        for (int sg = 0; sg < S; ++sg) {
+          const float4 ml = recv_ml[sg * rpc + li];
+          const float w = ml.y > 0.0f ? ml.y * fast_exp2(ml.x - M) : 0.0f;
+          den += w;
+          const float4* rowp = reinterpret_cast<const float4*>(recv_o + (static_cast<size_t>(sg) * rpc + li) * kHD);
+          const float4 v0 = rowp[c0], v1 = rowp[c1];
+          a[0] = fmaf(w, v0.x, a[0]);
+          a[1] = fmaf(w, v0.y, a[1]);
+          a[2] = fmaf(w, v0.z, a[2]);
+          a[3] = fmaf(w, v0.w, a[3]);
+          a[4] = fmaf(w, v1.x, a[4]);
+          a[5] = fmaf(w, v1.y, a[5]);
+          a[6] = fmaf(w, v1.z, a[6]);
+          a[7] = fmaf(w, v1.w, a[7]);
+        }
+        const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+        const size_t orow = (static_cast<size_t>(b) * g.R + nd) * g.H + hh;
+        uint4 pk;
+        pk.x = pack2_bf16(a[0] * inv, a[1] * inv);
+        pk.y = pack2_bf16(a[2] * inv, a[3] * inv);
+        pk.z = pack2_bf16(a[4] * inv, a[5] * inv);
+        pk.w = pack2_bf16(a[6] * inv, a[7] * inv);
+        *reinterpret_cast<uint4*>(O + orow * kHD + c * 8) = pk;
+        if (c == 0) lse[orow] = (M + __log2f(den)) * 0.6931471805599453f;
+      }
+    }
+    if (!got && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
+    cluster_wait();
   }
   if (warp == 1) {
     __syncwarp();
@@ -673,7 +770,7 @@ bool verify_tc_supported(const e3_kv_layer& kv, int H) {
 }
 
 e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* kv_len, const uint64_t* mask, int B,
-                           int R, int H, int max_kv_len, float sm_scale, int n_pre, int S, int chunk, float* ws_o,
+                           int R, int H, int max_kv_len, float sm_scale, VerifySplit* split, float* ws_o,
                            float2* ws_ml, void* O, float* lse, bool* merged, int32_t* dev_err, cudaStream_t s) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   E3_REQUIRE(enc != nullptr, E3_ERR_CUDA, "tree_verify_attn: tensor-map encoder unavailable");
@@ -706,9 +803,9 @@ e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* 
   g.H = H;
   g.KVH = kv.n_kv_heads;
   g.G = G;
-  g.n_pre = n_pre;
-  g.S = S;
-  g.chunk = chunk;
+  g.n_pre = split->n_pre;
+  g.S = split->S;
+  g.chunk = split->chunk;
   g.RG = (G * R + kRows - 1) / kRows;
   g.max_kv_len = max_kv_len;
   g.page_size = kv.page_size;
@@ -727,10 +824,18 @@ e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* 
     attr_done = true;
   }
   *merged = false;
-  const int Sc = pick_cluster_segments(g.RG * kv.n_kv_heads * B, max_kv_len);
-  if (Sc >= 1) {
+  const int groups = g.RG * kv.n_kv_heads * B;
+  const int Sc = pick_cluster_segments(groups, max_kv_len);
+  // The alternative: one wave of independent CTAs (as many segments as fit the
+  // SMs and the workspace, tree folded into the last) and the separate merge
+  // kernel.  It costs a few microseconds more in fixed latency, so it is taken
+  // only where it saves at least four 128-key tiles per CTA.
+  const int Sn = std::max(1, std::min(split->S, max_active_clusters(1) / std::max(1, groups)));
+  auto tiles = [&](int Sx) { return ((max_kv_len + Sx - 1) / Sx + kKeys - 1) / kKeys; };
+  const bool use_cluster = Sc >= 1 && (Sn <= Sc || tiles(Sc) - tiles(Sn) < 4);
+  if (use_cluster) {
     // cluster mode: Sc prefix segments, the tree folded into the last one
-    S = Sc;
+    const int S = Sc;
     g.S = Sc;
     g.n_pre = Sc;
     g.fold_tree = 1;
@@ -754,7 +859,14 @@ e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* 
     *merged = true;
     return E3_OK;
   }
-  dim3 grid(g.RG * S, kv.n_kv_heads, B);
+  if (Sn > 1 && Sn <= split->S) {  // one wave, tree folded into the last segment
+    g.S = Sn;
+    g.n_pre = Sn;
+    g.fold_tree = 1;
+    g.chunk = std::max(kHalf, ((max_kv_len + Sn - 1) / Sn + kHalf - 1) / kHalf * kHalf);
+    *split = VerifySplit{Sn, Sn, g.chunk, 1};
+  }
+  dim3 grid(g.RG * g.S, kv.n_kv_heads, B);
   verify_tc_kernel<false><<<grid, kThreads, kSmem, s>>>(mq, mk, mv, g, kv_len, mask, sm_scale, ws_o, ws_ml,
                                                    static_cast<__nv_bfloat16*>(O), lse, dev_err);
   E3_LAUNCH_CHECK("verify_tc_kernel");

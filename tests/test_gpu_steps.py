@@ -278,6 +278,8 @@ def mask_from_parent(par):
     dict(dt="bf16", lens=[100], R=256, H=4, KVH=2, hd=128, ps=64, D=16),        # maximum tree
     dict(dt="bf16", lens=[0, 128, 64, 65], R=20, H=8, KVH=2, hd=128, ps=64, D=5),  # empty / page-aligned prefixes
     dict(dt="bf16", lens=[300, 1], R=61, H=16, KVH=16, hd=128, ps=128, D=6),    # 128-token pages, MHA (G = 1)
+    dict(dt="bf16", lens=[12000], R=61, H=32, KVH=8, hd=128, ps=64, D=6),       # long prefix: one wave + merge kernel
+    dict(dt="bf16", lens=[12000, 5, 1000], R=61, H=32, KVH=8, hd=128, ps=64, D=6),  # ragged long: empty segments
 ])
 def test_verify_attention(case):
     dt, lens, R, H, KVH, hd, ps, D = (case[x] for x in ("dt", "lens", "R", "H", "KVH", "hd", "ps", "D"))
