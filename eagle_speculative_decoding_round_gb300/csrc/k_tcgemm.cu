@@ -11,8 +11,12 @@
 //
 // Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM owner + MMA issuer,
 // warps 2..5 epilogue (each reads the 32 TMEM lanes its warp may access).
+// The LM head runs persistently (one CTA per SM, tiles round-robin) with the
+// accumulator double-buffered in tensor memory, so that a tile's epilogue (the
+// logits store and the per-token best key) overlaps the next tile's K loop.
 // Every mbarrier wait is bounded (%globaltimer); on expiry the CTA sets
 // E3_DEV_ERR_TIMEOUT, stops issuing, frees its TMEM and returns.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -137,19 +141,17 @@ struct TcCfg {
   static constexpr int STAGE = A_BYTES + B_BYTES;
   static constexpr int STAGES = BN <= 64 ? 4 : (BN <= 128 ? 5 : 4);
   static constexpr int TMEM_COLS = BN < 32 ? 32 : BN;
-  static constexpr int SMEM = 1024 /*align slack*/ + STAGES * STAGE + 512 /*barriers*/ + 4 * BN * 8 /*column maxima*/;
+  static constexpr int SMEM = 1024 /*align slack*/ + STAGES * STAGE + 512 /*barriers*/;
 };
 
-enum { kModeLogits = 0, kModePartial = 1 };
+enum { kModePartial = 1 };
 
-// out (kModeLogits): logits [Mx][Nw] fp32; best[m]: packed (value, -row) maxima.
 // out (kModePartial): split-K partial [Mx][Nw] fp32 of split blockIdx.z.
 template <int BN, int MODE>
 __global__ void __launch_bounds__(192, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, int Nw, int Mx,
-               int kb_per_src, int kb_total, int kb_per_split, float* __restrict__ out,
-               unsigned long long* __restrict__ best, const float* __restrict__ temp, int32_t* dev_err) {
+               int kb_per_src, int kb_total, int kb_per_split, float* __restrict__ out, int32_t* dev_err) {
   using C = TcCfg<BN>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -158,7 +160,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint64_t* accum = empty + C::STAGES;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  unsigned long long* colbest = reinterpret_cast<unsigned long long*>(smem + C::STAGES * C::STAGE + 512);  // [4][BN]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tile_n = blockIdx.x, tile_m = blockIdx.y, split = blockIdx.z;
@@ -225,52 +226,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int row = tile_m * BM + q * 32 + lane;
     bool ok = mbar_wait(accum, 0, abort);
     tc_fence_after();
-    int bad = 0;
     if (ok && nkb > 0) {
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 32) {
         float v[32];
         tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
-        if (MODE == kModeLogits) {
+        float* o = out + static_cast<size_t>(split) * Mx * Nw;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = tile_n * BN + c0 + j;
-            if (m < Mx) {  // uniform across the warp
-              const float z = v[j];
-              bad |= !isfinite(z);
-              uint64_t key = 0;
-              if (row < Nw) {
-                out[static_cast<size_t>(m) * Nw + row] = z;
-                key = pack_best(__fmul_rn(z, inv_temp(temp[m])), static_cast<uint32_t>(row));
-              }
-              key = warp_reduce(key, MaxU64());
-              if (lane == 0) colbest[q * BN + c0 + j] = key;
-            }
-          }
-        } else {
-          float* o = out + static_cast<size_t>(split) * Mx * Nw;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = tile_n * BN + c0 + j;
-            if (m < Mx && row < Nw) o[static_cast<size_t>(m) * Nw + row] = v[j];
-          }
+        for (int j = 0; j < 32; ++j) {
+          const int m = tile_n * BN + c0 + j;
+          if (m < Mx && row < Nw) o[static_cast<size_t>(m) * Nw + row] = v[j];
         }
       }
     }
-    if (bad) dev_flag(dev_err, E3_DEV_ERR_NONFINITE);
   }
   tc_fence_before();
   __syncthreads();
-  if (MODE == kModeLogits && threadIdx.x >= 64 && nkb > 0 && !*abort) {
-    // one atomic per token column per CTA: combine the four lane quarters
-    for (int j = threadIdx.x - 64; j < BN; j += 128) {
-      const int m = tile_n * BN + j;
-      if (m >= Mx) continue;
-      uint64_t k = colbest[j];
-      for (int qq = 1; qq < 4; ++qq) k = max(k, static_cast<uint64_t>(colbest[qq * BN + j]));
-      atomicMax(&best[m], static_cast<unsigned long long>(k));
-    }
-  }
   if (*abort && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
   if (warp == 1) {
     __syncwarp();
@@ -292,36 +263,246 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits,
   }
 }
 
-// Second pass of the LM-head softmax statistics: best[m] holds the packed row
-// maximum (from the GEMM epilogue); compute Q over the row and publish
-// row_max, row_argmax and row_Q (row_Q doubles as the packed-maximum scratch).
-__global__ void __launch_bounds__(1024)
+// ---------------------------------------------------------------------------
+// LM head (persistent)
+// ---------------------------------------------------------------------------
+constexpr int kSmemCap = 227 * 1024;
+constexpr int kXposeBytes = 4 * 32 * 33 * 8;  // per epilogue warp: 32 x 33 u64 (padded transpose)
+
+template <int BN>
+struct LmCfg {
+  static_assert(BN % 32 == 0, "the epilogue reads 32 accumulator columns at a time");
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE = A_BYTES + B_BYTES;
+  static constexpr int TMEM_COLS = 2 * BN < 32 ? 32 : 2 * BN;  // two accumulators
+  static constexpr int FIXED = 1024 /*align slack*/ + 256 /*barriers*/ + kXposeBytes + 4 * BN * 8 /*warp bests*/ +
+                               BN * 4 /*inverse temperatures*/;
+  static constexpr int FIT = (kSmemCap - FIXED) / STAGE;
+  static constexpr int STAGES = FIT > 8 ? 8 : FIT;
+  static constexpr int SMEM = FIXED + STAGES * STAGE;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(bar)) : "memory");
+}
+
+// logits[m][v] = h[m] . W[v] for every (128-row vocabulary tile, BN-token tile),
+// tiles taken round-robin by a grid of at most one CTA per SM.  best[m] receives
+// (atomic max) the packed key (z[m][v] / T_m, -v) of every tile, for the
+// statistics pass that follows.
+template <int BN>
+__global__ void __launch_bounds__(192, 1)
+lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int V, int M,
+              int kb_total, int n_mt, int n_tiles, float* __restrict__ logits, unsigned long long* __restrict__ best,
+              const float* __restrict__ temp, int32_t* dev_err) {
+  using C = LmCfg<BN>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* acc_full = empty + C::STAGES;   // [2] MMAs of the buffer's tile done
+  uint64_t* acc_empty = acc_full + 2;       // [2] epilogue done reading the buffer
+  uint64_t* ep_sync = acc_empty + 2;        // [2] epilogue-internal syncs (128 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ep_sync + 2);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* xpose = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE + 256);  // [4][32][33]
+  uint64_t* wbest = xpose + 4 * 32 * 33;                                                // [4][BN]
+  float* s_it = reinterpret_cast<float*>(wbest + 4 * BN);                               // [BN]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < C::STAGES; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 128);
+      mbar_init(&ep_sync[a], 128);
+    }
+    *abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                 "r"(C::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer: the K loop of every tile through one ring
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+        const int vt = tile / n_mt, mt = tile % n_mt;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int st = it % C::STAGES;
+          if (!mbar_wait(&empty[st], ((it / C::STAGES) & 1) ^ 1, abort)) {
+            ok = false;
+            break;
+          }
+          unsigned char* a_s = smem + st * C::STAGE;
+          mbar_expect_tx(&full[st], C::STAGE);
+          tma_load_2d(a_s, &tmA, kb * BK, vt * BM, &full[st]);
+          tma_load_2d(a_s + A_BYTES, &tmB, kb * BK, mt * BN, &full[st]);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      constexpr uint32_t idesc = instr_desc(BM, BN);
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++local) {
+        const int a = local & 1;
+        if (!mbar_wait(&acc_empty[a], ((local >> 1) & 1) ^ 1, abort)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + a * BN;
+        for (int kb = 0; kb < kb_total; ++kb, ++it) {
+          const int st = it % C::STAGES;
+          if (!mbar_wait(&full[st], (it / C::STAGES) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = su32(smem + st * C::STAGE);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16_ss(d, smem_desc(a_addr + k * 32), smem_desc(a_addr + A_BYTES + k * 32), idesc, (kb | k) != 0);
+          mma_commit(&empty[st]);
+        }
+        if (ok) mma_commit(&acc_full[a]);
+      }
+    }
+  } else {
+    // epilogue warps 2..5: TMEM lane quarter q = warp % 4 (vocabulary rows 32q..32q+31 of the tile)
+    const int q = warp & 3;
+    const int et = threadIdx.x - 64;  // 0..127
+    uint64_t* xp = xpose + q * 32 * 33;
+    int bad = 0, local = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+      const int vt = tile / n_mt, mt = tile % n_mt;
+      const int a = local & 1;
+      for (int j = et; j < BN; j += 128) {
+        const int m = mt * BN + j;
+        s_it[j] = m < M ? inv_temp(temp[m]) : 1.0f;
+      }
+      mbar_arrive(&ep_sync[0]);
+      if (!mbar_wait(&ep_sync[0], local & 1, abort)) break;
+      if (!mbar_wait(&acc_full[a], (local >> 1) & 1, abort)) break;
+      tc_fence_after();
+      const int vrow = vt * BM + q * 32 + lane;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem + a * BN + (static_cast<uint32_t>(q * 32) << 16) + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int m = mt * BN + c0 + j;
+          uint64_t key = 0ull;
+          if (m < M) {
+            const float z = v[j];
+            bad |= !isfinite(z);
+            if (vrow < V) {
+              logits[static_cast<size_t>(m) * V + vrow] = z;
+              key = pack_best(__fmul_rn(z, s_it[c0 + j]), static_cast<uint32_t>(vrow));
+            }
+          }
+          xp[lane * 33 + j] = key;
+        }
+        __syncwarp();
+        uint64_t kbest = 0ull;  // column c0 + lane: best of this warp's 32 rows
+#pragma unroll 8
+        for (int r = 0; r < 32; ++r) kbest = max(kbest, static_cast<uint64_t>(xp[r * 33 + lane]));
+        if (c0 + lane < BN) wbest[q * BN + c0 + lane] = kbest;
+        __syncwarp();
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[a]);  // the accumulator buffer may take the tile after next
+      mbar_arrive(&ep_sync[1]);
+      if (!mbar_wait(&ep_sync[1], local & 1, abort)) break;
+      for (int j = et; j < BN; j += 128) {  // one atomic per token column per tile
+        const int m = mt * BN + j;
+        if (m >= M) continue;
+        uint64_t k = wbest[j];
+        for (int qq = 1; qq < 4; ++qq) k = max(k, static_cast<uint64_t>(wbest[qq * BN + j]));
+        if (k != 0ull) atomicMax(&best[m], static_cast<unsigned long long>(k));
+      }
+    }
+    if (bad) dev_flag(dev_err, E3_DEV_ERR_NONFINITE);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (*abort && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS));
+  }
+}
+
+// Second pass of the LM-head softmax statistics, one cluster of kRowQCluster CTAs
+// per row: row_Q[m] holds the packed row maximum (from the GEMM epilogue); each
+// CTA sums the fixed-point masses of its part of the row, CTA 0 adds the parts
+// and publishes row_max, row_argmax and row_Q (row_Q doubles as the packed-
+// maximum scratch; every CTA has read it before the first cluster barrier).
+constexpr int kRowQCluster = 8;
+constexpr int kRowQThreads = 256;
+
+__global__ void __launch_bounds__(kRowQThreads)
 row_q_kernel(const float* __restrict__ logits, int V, const float* __restrict__ temp, float* __restrict__ row_max,
              uint64_t* __restrict__ row_Q, int32_t* __restrict__ row_argmax) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
   __shared__ uint64_t red64[32];
-  const int m = blockIdx.x;
-  const float* z = logits + static_cast<size_t>(m) * V;
+  __shared__ int redi[32];
+  __shared__ uint64_t part_Q;
+  __shared__ int part_bad;
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int m = blockIdx.x / kRowQCluster;
+  const float4* z4 = reinterpret_cast<const float4*>(logits + static_cast<size_t>(m) * V);
   const float it = inv_temp(temp[m]);
   const uint64_t best = row_Q[m];
   const float mx = unord_f32(static_cast<uint32_t>(best >> 32));
-  __shared__ int redi[32];
+  const int nv4 = V >> 2;
+  const int per = (nv4 + kRowQCluster - 1) / kRowQCluster;
+  const int q0 = min(nv4, rank * per), q1 = min(nv4, q0 + per);
   uint64_t Q = 0;
   int bad = 0;
-  const float4* z4 = reinterpret_cast<const float4*>(z);
-#pragma unroll 8
-  for (int q = threadIdx.x; q < (V >> 2); q += blockDim.x) {
+#pragma unroll 4
+  for (int q = q0 + threadIdx.x; q < q1; q += kRowQThreads) {
     const float4 v = z4[q];
     bad |= !isfinite(v.x) | !isfinite(v.y) | !isfinite(v.z) | !isfinite(v.w);
     Q += fx_mass(__fmul_rn(v.x, it), mx) + fx_mass(__fmul_rn(v.y, it), mx) + fx_mass(__fmul_rn(v.z, it), mx) +
          fx_mass(__fmul_rn(v.w, it), mx);
   }
-  Q = block_reduce(Q, SumU64(), red64);  // contains __syncthreads: every thread has read best
+  Q = block_reduce(Q, SumU64(), red64);
   bad = block_reduce(bad, OrI(), redi);
   if (threadIdx.x == 0) {
-    row_max[m] = bad ? __int_as_float(0x7FC00000) : mx;
-    row_argmax[m] = bad ? -1 : static_cast<int32_t>(packed_id(best));
-    row_Q[m] = bad ? 0ull : Q;
+    part_Q = Q;
+    part_bad = bad;
   }
+  cluster.sync();  // every part is published; every CTA has read row_Q[m]
+  if (rank == 0 && threadIdx.x < 32) {
+    uint64_t v = 0ull;
+    int bd = 0;
+    if (threadIdx.x < kRowQCluster) {
+      v = *cluster.map_shared_rank(&part_Q, threadIdx.x);
+      bd = *cluster.map_shared_rank(&part_bad, threadIdx.x);
+    }
+    v = warp_reduce(v, SumU64());
+    bd = warp_reduce(bd, OrI());
+    if (threadIdx.x == 0) {
+      row_max[m] = bd ? __int_as_float(0x7FC00000) : mx;
+      row_argmax[m] = bd ? -1 : static_cast<int32_t>(packed_id(best));
+      row_Q[m] = bd ? 0ull : v;
+    }
+  }
+  cluster.sync();  // CTA 0 is done reading the others' shared memory
 }
 
 // ---------------------------------------------------------------------------
@@ -356,36 +537,35 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int cols, int box_ro
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int MODE>
-e3_status launch_tc(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b2,
-                    int Nw, int Mx, int kb_per_src, int kb_total, int splits, float* out, unsigned long long* best,
-                    const float* temp, int32_t* dev_err, cudaStream_t s) {
+template <int BN>
+e3_status launch_fuse_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b2,
+                         int Nw, int Mx, int kb_per_src, int kb_total, int splits, float* out, int32_t* dev_err,
+                         cudaStream_t s) {
   using C = TcCfg<BN>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, kModePartial>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return cuda_status(e, "tc_gemm_kernel smem attribute");
     attr_done = true;
   }
   const int kb_per_split = (kb_total + splits - 1) / splits;  // callers pass splits with no empty split
   dim3 grid((Mx + BN - 1) / BN, (Nw + BM - 1) / BM, splits);
-  tc_gemm_kernel<BN, MODE><<<grid, 192, C::SMEM, s>>>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, kb_per_split,
-                                                      out, best, temp, dev_err);
+  tc_gemm_kernel<BN, kModePartial><<<grid, 192, C::SMEM, s>>>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total,
+                                                             kb_per_split, out, dev_err);
   E3_LAUNCH_CHECK("tc_gemm_kernel");
   return E3_OK;
 }
 
-template <int MODE>
-e3_status dispatch_bn(int bn, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                      const CUtensorMap& b2, int Nw, int Mx, int kb_per_src, int kb_total, int splits, float* out,
-                      unsigned long long* best, const float* temp, int32_t* dev_err, cudaStream_t s) {
+e3_status dispatch_fuse(int bn, const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                        const CUtensorMap& b2, int Nw, int Mx, int kb_per_src, int kb_total, int splits, float* out,
+                        int32_t* dev_err, cudaStream_t s) {
   switch (bn) {
-    case 16: return launch_tc<16, MODE>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, splits, out, best, temp, dev_err, s);
-    case 32: return launch_tc<32, MODE>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, splits, out, best, temp, dev_err, s);
-    case 64: return launch_tc<64, MODE>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, splits, out, best, temp, dev_err, s);
-    case 128: return launch_tc<128, MODE>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, splits, out, best, temp, dev_err, s);
-    default: return launch_tc<256, MODE>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, splits, out, best, temp, dev_err, s);
+    case 16: return launch_fuse_bn<16>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, splits, out, dev_err, s);
+    case 32: return launch_fuse_bn<32>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, splits, out, dev_err, s);
+    case 64: return launch_fuse_bn<64>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, splits, out, dev_err, s);
+    case 128: return launch_fuse_bn<128>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, splits, out, dev_err, s);
+    default: return launch_fuse_bn<256>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total, splits, out, dev_err, s);
   }
 }
 
@@ -429,8 +609,7 @@ e3_status launch_fuse_tc(const void* h_low, const void* h_mid, const void* h_hig
              E3_ERR_INVALID_ARG, "eagle3_fuse: cuTensorMapEncodeTiled rejected an operand");
   const int splits = fuse_splits(M, d, d_out);
   float* part = static_cast<float*>(ws);
-  e3_status st = dispatch_bn<kModePartial>(bn, a, b0, b1, b2, d_out, M, d / BK, 3 * d / BK, splits, part, nullptr,
-                                           nullptr, dev_err, s);
+  e3_status st = dispatch_fuse(bn, a, b0, b1, b2, d_out, M, d / BK, 3 * d / BK, splits, part, dev_err, s);
   if (st != E3_OK) return st;
   const size_t n = static_cast<size_t>(M) * d_out;
   const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
@@ -439,19 +618,65 @@ e3_status launch_fuse_tc(const void* h_low, const void* h_mid, const void* h_hig
   return E3_OK;
 }
 
+template <int BN>
+e3_status launch_lmhead_bn(const CUtensorMap& a, const CUtensorMap& b, int V, int M, int kb_total, float* logits,
+                           unsigned long long* best, const float* temp, int32_t* dev_err, cudaStream_t s) {
+  using C = LmCfg<BN>;
+  static_assert(C::STAGES >= 2, "LM-head ring too small");
+  static bool attr_done = false;
+  static int n_sm = 0;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return cuda_status(e, "lmhead_kernel smem attribute");
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    if (n_sm < 1) n_sm = 1;
+    attr_done = true;
+  }
+  const int n_mt = (M + BN - 1) / BN;
+  const int n_vt = (V + BM - 1) / BM;
+  const long n_tiles = static_cast<long>(n_mt) * n_vt;
+  E3_REQUIRE(n_tiles < (1L << 31), E3_ERR_SHAPE, "lmhead_logits: %ld tiles", n_tiles);
+  const int grid = static_cast<int>(std::min<long>(n_tiles, n_sm));
+  lmhead_kernel<BN><<<grid, 192, C::SMEM, s>>>(a, b, V, M, kb_total, n_mt, static_cast<int>(n_tiles), logits, best,
+                                               temp, dev_err);
+  E3_LAUNCH_CHECK("lmhead_kernel");
+  return E3_OK;
+}
+
 e3_status launch_lmhead_tc(const void* h, const void* W_lm, int M, int d, int V, const float* temp, float* logits,
                            float* row_max, uint64_t* row_Q, int32_t* row_argmax, int32_t* dev_err, cudaStream_t s) {
-  const int bn = pick_bn(M);
+  const int bn = std::max(32, pick_bn(M));  // the epilogue reads the accumulator 32 columns at a time
   CUtensorMap a, b;
   E3_REQUIRE(make_map(&a, W_lm, V, d, BM) && make_map(&b, h, M, d, bn), E3_ERR_INVALID_ARG,
              "lmhead_logits: cuTensorMapEncodeTiled rejected an operand");
   cudaError_t e = cudaMemsetAsync(row_Q, 0, static_cast<size_t>(M) * sizeof(uint64_t), s);
   if (e != cudaSuccess) return cuda_status(e, "lmhead_logits memset");
-  e3_status st = dispatch_bn<kModeLogits>(bn, a, b, b, b, V, M, d / BK, d / BK, 1, logits,
-                                          reinterpret_cast<unsigned long long*>(row_Q), temp, dev_err, s);
+  unsigned long long* best = reinterpret_cast<unsigned long long*>(row_Q);
+  const int kb = d / BK;
+  e3_status st;
+  switch (bn) {
+    case 32: st = launch_lmhead_bn<32>(a, b, V, M, kb, logits, best, temp, dev_err, s); break;
+    case 64: st = launch_lmhead_bn<64>(a, b, V, M, kb, logits, best, temp, dev_err, s); break;
+    case 128: st = launch_lmhead_bn<128>(a, b, V, M, kb, logits, best, temp, dev_err, s); break;
+    default: st = launch_lmhead_bn<256>(a, b, V, M, kb, logits, best, temp, dev_err, s); break;
+  }
   if (st != E3_OK) return st;
-  row_q_kernel<<<M, 1024, 0, s>>>(logits, V, temp, row_max, row_Q, row_argmax);
-  E3_LAUNCH_CHECK("row_q_kernel");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(M) * kRowQCluster);
+  cfg.blockDim = dim3(kRowQThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeClusterDimension;
+  at.val.clusterDim.x = kRowQCluster;
+  at.val.clusterDim.y = 1;
+  at.val.clusterDim.z = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, row_q_kernel, static_cast<const float*>(logits), V, temp, row_max, row_Q, row_argmax);
+  if (e != cudaSuccess) return cuda_status(e, "row_q_kernel");
   return E3_OK;
 }
 
