@@ -52,10 +52,57 @@ __device__ void warp_merge_topk(uint64_t (&keys)[KMAX], int k, uint64_t* out) {
   }
 }
 
-// One cluster of CL CTAs per frontier row (CL = 16 where the device allows
-// clusters of that size, else 8).  CTA r stages chunk r of the row in shared
-// memory; the row maximum, the non-finite flag, the fixed-point mass and the
-// per-CTA top-k lists are exchanged through distributed shared memory.
+__device__ __forceinline__ uint32_t cl_addr(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+               : "=r"(r)
+               : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cl_st64(uint32_t a, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ void cl_st32(uint32_t a, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+// arrive (release at cluster scope: this thread's earlier stores to the peer are
+// visible to whoever observes the phase) on the mbarrier at cluster address a
+__device__ __forceinline__ void cl_arrive(uint32_t a) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(a) : "memory");
+}
+__device__ __forceinline__ void mb_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(b))),
+               "r"(n));
+}
+// bounded wait (acquire at cluster scope) for phase 0 of a local mbarrier
+__device__ __forceinline__ bool mb_wait0(uint64_t* b) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(b));
+  uint64_t t0 = 0;
+  for (int i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], 0;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(a)
+        : "memory");
+    if (ok) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    if (i == 0) t0 = t;
+    if (t - t0 > 1000000000ull) return false;
+  }
+}
+
+// One cluster of CL CTAs per frontier row.  CTA r stages chunk r of the row (scaled
+// by 1/T) in shared memory.  Its top-k: candidates are the elements not below the
+// smallest of the 16 warp maxima (at least 16 >= k elements qualify, typically a
+// few dozen), ranked exactly; if more than fit, the exact threshold (k-th largest
+// per-thread maximum, which admits at most k * per-thread elements) is used.
+// Exchanges go through the peers' shared memory with mbarrier arrivals: every CTA
+// sends its maximum key and non-finite flag to every CTA (each then knows the row
+// maximum m), and its mass and top-k list to CTA 0, which merges and writes the
+// k children.
 template <int KMAX>
 __global__ void __launch_bounds__(kExpandThreads)
 expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float it,
@@ -70,23 +117,35 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   const float* z = logits + static_cast<size_t>(row) * V;
   extern __shared__ float4 chunk4[];
   __shared__ uint64_t warp_lists[kExpandThreads / 32][E3_MAX_TOPK];
-  __shared__ uint64_t ltop[E3_MAX_TOPK];   // this CTA's best k keys
-  __shared__ uint64_t lbest;               // this CTA's best key
-  __shared__ uint64_t lQ;                  // this CTA's mass
-  __shared__ int lbad;
-  __shared__ uint64_t red64[32];
-  __shared__ int redi[32];
-  __shared__ uint64_t all_top[kMaxCluster * E3_MAX_TOPK];
+  __shared__ uint64_t s_wmax[kExpandThreads / 32];
+  __shared__ uint64_t ltop[E3_MAX_TOPK];              // this CTA's best k keys
   __shared__ uint64_t top[E3_MAX_TOPK];
+  __shared__ uint64_t red64[32];
   __shared__ int s_cnt;
+  // written by the peers
+  __shared__ uint64_t s_pmax[kMaxCluster];            // each CTA's maximum key
+  __shared__ uint32_t s_pbad[kMaxCluster];            // each CTA's non-finite flag
+  __shared__ uint64_t s_pQ[kMaxCluster];              // (CTA 0) each CTA's mass
+  __shared__ uint64_t s_ptop[kMaxCluster * E3_MAX_TOPK];  // (CTA 0) each CTA's top-k keys
+  __shared__ uint64_t mx_bar, fin_bar;
 
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mb_init(&mx_bar, CL);
+    mb_init(&fin_bar, CL);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   const bool vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
   const int nvec = vec ? (V >> 2) : V;
   const int per = (nvec + CL - 1) / CL;
   const int v0 = min(nvec, rank * per), v1 = min(nvec, v0 + per);
   float* chunk = reinterpret_cast<float*>(chunk4);
+  const int e0 = vec ? 4 * v0 : v0;  // token id of chunk[0]
+  const int n_local = vec ? 4 * (v1 - v0) : (v1 - v0);
 
-  // stage the chunk (scaled by 1/T) in shared memory with independent, unrolled loads
+  // stage the chunk (scaled by 1/T); per-thread maximum key and non-finite flag
+  uint64_t tmax = 0ull;
+  int bad = 0;
   if (vec) {
     const float4* z4 = reinterpret_cast<const float4*>(z);
 #pragma unroll 4
@@ -97,135 +156,161 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
       v.z = __fmul_rn(v.z, it);
       v.w = __fmul_rn(v.w, it);
       chunk4[q - v0] = v;
+      const uint32_t id = static_cast<uint32_t>(4 * q);
+      bad |= !isfinite(v.x) | !isfinite(v.y) | !isfinite(v.z) | !isfinite(v.w);
+      tmax = max(tmax, max(max(pack_best(v.x, id), pack_best(v.y, id + 1)),
+                           max(pack_best(v.z, id + 2), pack_best(v.w, id + 3))));
     }
   } else {
 #pragma unroll 4
-    for (int j = v0 + threadIdx.x; j < v1; j += blockDim.x) chunk[j - v0] = __fmul_rn(__ldg(z + j), it);
-  }
-  __syncthreads();
-  const int e0 = vec ? 4 * v0 : v0;  // token id of chunk[0]
-  const int n_local = vec ? 4 * (v1 - v0) : (v1 - v0);
-  // (1) per-thread maximum key (value desc, token id asc) and the non-finite flag
-  uint64_t tmax = 0ull;
-  int bad = 0;
-  for (int j = threadIdx.x; j < n_local; j += blockDim.x) {
-    const float sj = chunk[j];
-    bad |= !isfinite(sj);
-    const uint64_t key = pack_best(sj, static_cast<uint32_t>(e0 + j));
-    tmax = key > tmax ? key : tmax;
-  }
-  bad = block_reduce(bad, OrI(), redi);
-  // (2) thr = k-th largest per-thread maximum: every element of this CTA's top k
-  // is >= thr, and only threads whose maximum is >= thr can hold one
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  {
-    uint64_t v = tmax;
-    for (int r = 0; r < k; ++r) {
-      const uint64_t best = warp_reduce(v, MaxU64());
-      if (v == best) v = 0ull;  // keys are distinct: exactly one lane (or all-zero lanes)
-      if (lane == 0) warp_lists[warp][r] = best;
+    for (int j = v0 + threadIdx.x; j < v1; j += blockDim.x) {
+      const float v = __fmul_rn(__ldg(z + j), it);
+      chunk[j - v0] = v;
+      bad |= !isfinite(v);
+      tmax = max(tmax, pack_best(v, static_cast<uint32_t>(j)));
     }
   }
-  __syncthreads();
-  if (warp == 0) {
-    const int nw = blockDim.x >> 5;
-    uint64_t lk[KMAX];
-#pragma unroll
-    for (int i = 0; i < KMAX; ++i)
-      lk[i] = (lane < nw && i < k) ? warp_lists[lane][i] : 0ull;
-    warp_merge_topk(lk, k, top);
-  }
+  // the peers' mbarriers are initialized before anyone arrives on them
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  const uint64_t wmax = warp_reduce(tmax, MaxU64());
+  if (lane == 0) s_wmax[warp] = wmax;
   if (threadIdx.x == 0) s_cnt = 0;
-  __syncthreads();
-  const uint64_t thr = top[k - 1];
-  // (3) candidates >= thr, then their exact ranks
-  uint64_t* cand = reinterpret_cast<uint64_t*>(chunk4 + (per + 1));
-  for (int j = threadIdx.x; j < n_local; j += blockDim.x) {
-    const uint64_t key = pack_best(chunk[j], static_cast<uint32_t>(e0 + j));
-    if (key >= thr && key != 0ull) {
-      const int at = atomicAdd(&s_cnt, 1);
-      if (at < cand_cap) cand[at] = key;
+  bad = __syncthreads_or(bad);
+  // each thread visits the chunk elements it staged: float4 slots q - v0 (vec) or j - v0
+  auto for_own = [&](auto&& fn) {
+    if (vec) {
+      for (int q = threadIdx.x; q < v1 - v0; q += blockDim.x) {
+        const float4 v = chunk4[q];
+        const uint32_t id = static_cast<uint32_t>(e0 + 4 * q);
+        fn(v.x, id);
+        fn(v.y, id + 1);
+        fn(v.z, id + 2);
+        fn(v.w, id + 3);
+      }
+    } else {
+      for (int j = threadIdx.x; j < n_local; j += blockDim.x) fn(chunk[j], static_cast<uint32_t>(e0 + j));
     }
+  };
+  uint64_t* cand = reinterpret_cast<uint64_t*>(chunk4 + (per + 1));
+  uint64_t thr = ~0ull;
+  if (k <= kExpandThreads / 32) {
+    for (int w = 0; w < kExpandThreads / 32; ++w) thr = min(thr, s_wmax[w]);
+    for_own([&](float v, uint32_t id) {
+      const uint64_t key = pack_best(v, id);
+      if (key >= thr && key != 0ull) {
+        const int at = atomicAdd(&s_cnt, 1);
+        if (at < cand_cap) cand[at] = key;
+      }
+    });
   }
   __syncthreads();
+  if (k > kExpandThreads / 32 || s_cnt > cand_cap) {
+    // exact threshold: the k-th largest per-thread maximum
+    {
+      uint64_t v = tmax;
+      for (int r = 0; r < k; ++r) {
+        const uint64_t bst = warp_reduce(v, MaxU64());
+        if (v == bst) v = 0ull;  // keys are distinct: exactly one lane (or all-zero lanes)
+        if (lane == 0) warp_lists[warp][r] = bst;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const int nw = blockDim.x >> 5;
+      uint64_t lk[KMAX];
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) lk[i] = (lane < nw && i < k) ? warp_lists[lane][i] : 0ull;
+      warp_merge_topk(lk, k, top);
+    }
+    if (threadIdx.x == 0) s_cnt = 0;
+    __syncthreads();
+    thr = top[k - 1];
+    for_own([&](float v, uint32_t id) {
+      const uint64_t key = pack_best(v, id);
+      if (key >= thr && key != 0ull) {
+        const int at = atomicAdd(&s_cnt, 1);
+        if (at < cand_cap) cand[at] = key;
+      }
+    });
+    __syncthreads();
+  }
   const int ncand = min(s_cnt, cand_cap);
   if (threadIdx.x < E3_MAX_TOPK) ltop[threadIdx.x] = 0ull;
   __syncthreads();
   for (int i = threadIdx.x; i < ncand; i += blockDim.x) {
     const uint64_t key = cand[i];
-    int rank = 0;
-    for (int j = 0; j < ncand; ++j) rank += cand[j] > key;
-    if (rank < k) ltop[rank] = key;
+    int rnk = 0;
+    for (int j = 0; j < ncand; ++j) rnk += cand[j] > key;
+    if (rnk < k) ltop[rnk] = key;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    lbest = ltop[0];
-    lbad = bad;
+  // send this CTA's maximum key and flag to every CTA of the cluster
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (threadIdx.x < CL) {
+    uint64_t lbest = 0ull;
+    for (int w = 0; w < kExpandThreads / 32; ++w) lbest = max(lbest, s_wmax[w]);
+    cl_st64(cl_addr(&s_pmax[rank], threadIdx.x), lbest);
+    cl_st32(cl_addr(&s_pbad[rank], threadIdx.x), static_cast<uint32_t>(bad));
+    cl_arrive(cl_addr(&mx_bar, threadIdx.x));
   }
-  cluster.sync();  // every CTA's maximum and flag are visible
-  __shared__ uint64_t s_gbest;
-  __shared__ int s_gbad;
-  if (warp == 0) {  // lane r gathers rank r, then a warp reduction
-    uint64_t v = 0ull;
-    int bd = 0;
-    if (lane < CL) {
-      v = *cluster.map_shared_rank(&lbest, lane);
-      bd = *cluster.map_shared_rank(&lbad, lane);
-    }
-    v = warp_reduce(v, MaxU64());
-    bd = warp_reduce(bd, OrI());
-    if (lane == 0) {
-      s_gbest = v;
-      s_gbad = bd;
-    }
+  const bool got = mb_wait0(&mx_bar);
+  uint64_t gbest = 0ull;
+  uint32_t gbad = got ? 0u : 1u;
+  for (int r = 0; r < CL; ++r) {
+    gbest = max(gbest, s_pmax[r]);
+    gbad |= s_pbad[r];
   }
-  __syncthreads();
-  const uint64_t gbest = s_gbest;
-  const int gbad = s_gbad;
+  if (!got) {
+    if (threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
+    return;
+  }
   if (gbad) {
     if (rank == 0 && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_NONFINITE);
-    cluster.sync();  // nobody leaves while a peer may still read its shared memory
-    return;
+    return;  // every CTA saw the same flags; no further exchange
   }
   const float m = unord_f32(static_cast<uint32_t>(gbest >> 32));
   uint64_t Q = 0;
-  for (int j = threadIdx.x; j < n_local; j += blockDim.x) Q += fx_mass(chunk[j], m);
-  Q = block_reduce(Q, SumU64(), red64);
-  if (threadIdx.x == 0) lQ = Q;
-  cluster.sync();  // masses and top-k lists are visible
-  if (rank == 0) {
-    for (int i = threadIdx.x; i < CL * k; i += blockDim.x)
-      all_top[i] = *cluster.map_shared_rank(&ltop[i % k], i / k);
-    __shared__ uint64_t s_Qt;
-    if (warp == 0) {
-      uint64_t v = lane < CL ? static_cast<uint64_t>(*cluster.map_shared_rank(&lQ, lane)) : 0ull;
-      v = warp_reduce(v, SumU64());
-      if (lane == 0) s_Qt = v;
-    }
-    __syncthreads();
-    const uint64_t Qt = s_Qt;
-    if (warp == 0) {
-      uint64_t lk[KMAX];
-#pragma unroll
-      for (int i = 0; i < KMAX; ++i)
-        lk[i] = (static_cast<int>(threadIdx.x) < CL && i < k) ? all_top[threadIdx.x * k + i] : 0ull;
-      warp_merge_topk(lk, k, top);  // top[] is free again: thr was consumed above
-    }
-    __syncthreads();
-    if (threadIdx.x < k) {
-      const int r = threadIdx.x;
-      const float ell = fx_ell(Qt);
-      const uint32_t t = packed_id(top[r]);
-      const float sc = unord_f32(static_cast<uint32_t>(top[r] >> 32));
-      const float ps = parent_score[row];
-      const size_t ci = static_cast<size_t>(b) * c.cap + cand_offset + f * k + r;
-      c.tok[ci] = static_cast<int32_t>(t);
-      c.parent[ci] = parent_id[row];
-      c.score[ci] = __fsub_rn(__fadd_rn(ps, __fsub_rn(sc, m)), ell);
-      c.depth[ci] = depth;
-    }
+  for_own([&](float v, uint32_t) { Q += fx_mass(v, m); });
+  Q = block_reduce(Q, SumU64(), red64);  // also orders ltop[] before thread 0 reads it
+  if (threadIdx.x == 0) {  // mass and top-k list to CTA 0
+    cl_st64(cl_addr(&s_pQ[rank], 0), Q);
+    for (int i = 0; i < k; ++i) cl_st64(cl_addr(&s_ptop[rank * k + i], 0), ltop[i]);
+    cl_arrive(cl_addr(&fin_bar, 0));
   }
-  cluster.sync();  // rank 0 is done reading the peers' shared memory
+  if (rank != 0) return;  // nothing reads this CTA's shared memory any more
+  const bool fin = mb_wait0(&fin_bar);
+  if (!fin) {
+    if (threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
+    return;
+  }
+  const int nall = CL * k;
+  if (threadIdx.x < E3_MAX_TOPK) top[threadIdx.x] = 0ull;
+  __syncthreads();
+  for (int i = threadIdx.x; i < nall; i += blockDim.x) {
+    const uint64_t key = s_ptop[i];
+    if (key == 0ull) continue;
+    int rnk = 0;
+    for (int j = 0; j < nall; ++j) rnk += s_ptop[j] > key;
+    if (rnk < k) top[rnk] = key;
+  }
+  __shared__ uint64_t s_Qt;
+  if (threadIdx.x == 0) {
+    uint64_t t = 0;
+    for (int r = 0; r < CL; ++r) t += s_pQ[r];
+    s_Qt = t;
+  }
+  __syncthreads();
+  if (threadIdx.x < k) {
+    const int r = threadIdx.x;
+    const float ell = fx_ell(s_Qt);
+    const uint32_t t = packed_id(top[r]);
+    const float sc = unord_f32(static_cast<uint32_t>(top[r] >> 32));
+    const float ps = parent_score[row];
+    const size_t ci = static_cast<size_t>(b) * c.cap + cand_offset + f * k + r;
+    c.tok[ci] = static_cast<int32_t>(t);
+    c.parent[ci] = parent_id[row];
+    c.score[ci] = __fsub_rn(__fadd_rn(ps, __fsub_rn(sc, m)), ell);
+    c.depth[ci] = depth;
+  }
 }
 
 template <int KMAX>
