@@ -97,6 +97,40 @@ __device__ __forceinline__ uint64_t fx_mass(float s, float m) {
   return fx_scale40_floor(fx_exp(__fsub_rn(s, m)));
 }
 
+// Two lanes of fx_exp at once with the packed fp32x2 operations (each lane is
+// rounded exactly as the scalar operation it replaces, so the results are
+// bit-identical to fx_exp on each lane).
+__device__ __forceinline__ float2 fx_exp_x2(float2 x) {
+  const float2 kLog2e = make_float2(0x1.715476p+0f, 0x1.715476p+0f);
+  const float2 kLn2Hi = make_float2(0x1.62e4p-1f, 0x1.62e4p-1f);
+  const float2 kLn2Lo = make_float2(0x1.7f7d1cp-20f, 0x1.7f7d1cp-20f);
+  const float2 t = __fmul2_rn(x, kLog2e);
+  const float2 n = make_float2(rintf(t.x), rintf(t.y));
+  const float2 nn = make_float2(-n.x, -n.y);
+  float2 r = __ffma2_rn(nn, kLn2Hi, x);
+  r = __ffma2_rn(nn, kLn2Lo, r);
+  float2 p = make_float2(0x1.a01a02p-13f, 0x1.a01a02p-13f);
+  p = __ffma2_rn(p, r, make_float2(0x1.6c16c2p-10f, 0x1.6c16c2p-10f));
+  p = __ffma2_rn(p, r, make_float2(0x1.111112p-7f, 0x1.111112p-7f));
+  p = __ffma2_rn(p, r, make_float2(0x1.555556p-5f, 0x1.555556p-5f));
+  p = __ffma2_rn(p, r, make_float2(0x1.555556p-3f, 0x1.555556p-3f));
+  p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
+  p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+  p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
+  const float2 scale = make_float2(__int_as_float((static_cast<int>(n.x) + 127) << 23),
+                                   __int_as_float((static_cast<int>(n.y) + 127) << 23));
+  float2 e = __fmul2_rn(p, scale);
+  if (x.x < -32.0f) e.x = 0.0f;
+  if (x.y < -32.0f) e.y = 0.0f;
+  return e;
+}
+
+// fx_mass(a, m) + fx_mass(b, m)
+__device__ __forceinline__ uint64_t fx_mass_x2(float a, float b, float m) {
+  const float2 e = fx_exp_x2(make_float2(__fsub_rn(a, m), __fsub_rn(b, m)));
+  return fx_scale40_floor(e.x) + fx_scale40_floor(e.y);
+}
+
 __device__ __forceinline__ float fx_ell(uint64_t Q) {
   const float kLn2Hi = 0x1.62e4p-1f;
   const float kLn2Lo = 0x1.7f7d1cp-20f;

@@ -23,6 +23,7 @@ namespace {
 constexpr int kExpandThreads = 512;
 constexpr int kMaxCluster = 16;  // CTAs per frontier row (at most)
 constexpr int kPreferCluster = 8;  // eight-CTA clusters keep every row of a depth in one wave
+constexpr uint32_t kBulkPiece = 32768;  // bytes per bulk copy of the staged chunk
 
 template <int KMAX>
 __device__ __forceinline__ void topk_insert(uint64_t (&keys)[KMAX], uint64_t key) {
@@ -104,7 +105,7 @@ __device__ __forceinline__ bool mb_wait0(uint64_t* b) {
 // maximum m), and its mass and top-k list to CTA 0, which merges and writes the
 // k children.
 template <int KMAX>
-__global__ void __launch_bounds__(kExpandThreads)
+__global__ void __launch_bounds__(kExpandThreads, 2)
 expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float it,
                    const float* __restrict__ parent_score, const int32_t* __restrict__ parent_id,
                    int depth, int cand_offset, e3_cand c, int32_t* dev_err, int cand_cap) {
@@ -127,14 +128,9 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   __shared__ uint32_t s_pbad[kMaxCluster];            // each CTA's non-finite flag
   __shared__ uint64_t s_pQ[kMaxCluster];              // (CTA 0) each CTA's mass
   __shared__ uint64_t s_ptop[kMaxCluster * E3_MAX_TOPK];  // (CTA 0) each CTA's top-k keys
-  __shared__ uint64_t mx_bar, fin_bar;
+  __shared__ uint64_t mx_bar, fin_bar, ld_bar;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    mb_init(&mx_bar, CL);
-    mb_init(&fin_bar, CL);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
   const bool vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
   const int nvec = vec ? (V >> 2) : V;
   const int per = (nvec + CL - 1) / CL;
@@ -142,24 +138,51 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   float* chunk = reinterpret_cast<float*>(chunk4);
   const int e0 = vec ? 4 * v0 : v0;  // token id of chunk[0]
   const int n_local = vec ? 4 * (v1 - v0) : (v1 - v0);
+  if (threadIdx.x == 0) {
+    mb_init(&mx_bar, CL);
+    mb_init(&fin_bar, CL);
+    mb_init(&ld_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (vec) {  // the chunk: bulk copies of 16-byte aligned row pieces
+      const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(&ld_bar));
+      const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+      for (uint32_t off = 0; off < bytes; off += kBulkPiece) {
+        const uint32_t n = min(kBulkPiece, bytes - off);
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                static_cast<uint32_t>(__cvta_generic_to_shared(chunk4)) + off),
+            "l"(reinterpret_cast<const unsigned char*>(z + 4 * static_cast<size_t>(v0)) + off), "r"(n), "r"(bar)
+            : "memory");
+      }
+    }
+  }
+  // no thread polls a barrier before thread 0 has initialized it
+  __syncthreads();
 
-  // stage the chunk (scaled by 1/T); per-thread maximum key and non-finite flag
-  uint64_t tmax = 0ull;
+  // the chunk is staged by the bulk copies above (16-byte aligned rows), else by
+  // plain loads; then scaled by 1/T in place, with the per-thread maximum (first occurrence of the
+  // largest value, i.e. the lowest token id among ties) and the non-finite flag
+  float bv = -INFINITY;
+  uint32_t bid = 0xFFFFFFFFu;
   int bad = 0;
   if (vec) {
-    const float4* z4 = reinterpret_cast<const float4*>(z);
-#pragma unroll 4
-    for (int q = v0 + threadIdx.x; q < v1; q += blockDim.x) {
-      float4 v = __ldg(z4 + q);
-      v.x = __fmul_rn(v.x, it);
-      v.y = __fmul_rn(v.y, it);
-      v.z = __fmul_rn(v.z, it);
-      v.w = __fmul_rn(v.w, it);
-      chunk4[q - v0] = v;
-      const uint32_t id = static_cast<uint32_t>(4 * q);
+    if (!mb_wait0(&ld_bar)) bad = 1;  // (flagged as non-finite: the row is skipped)
+    for (int q = threadIdx.x; q < v1 - v0; q += blockDim.x) {
+      float4 v = chunk4[q];
+      if (it != 1.0f) {
+        v.x = __fmul_rn(v.x, it);
+        v.y = __fmul_rn(v.y, it);
+        v.z = __fmul_rn(v.z, it);
+        v.w = __fmul_rn(v.w, it);
+        chunk4[q] = v;
+      }
       bad |= !isfinite(v.x) | !isfinite(v.y) | !isfinite(v.z) | !isfinite(v.w);
-      tmax = max(tmax, max(max(pack_best(v.x, id), pack_best(v.y, id + 1)),
-                           max(pack_best(v.z, id + 2), pack_best(v.w, id + 3))));
+      const uint32_t id = static_cast<uint32_t>(e0 + 4 * q);
+      if (v.x > bv) bv = v.x, bid = id;
+      if (v.y > bv) bv = v.y, bid = id + 1;
+      if (v.z > bv) bv = v.z, bid = id + 2;
+      if (v.w > bv) bv = v.w, bid = id + 3;
     }
   } else {
 #pragma unroll 4
@@ -167,9 +190,10 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
       const float v = __fmul_rn(__ldg(z + j), it);
       chunk[j - v0] = v;
       bad |= !isfinite(v);
-      tmax = max(tmax, pack_best(v, static_cast<uint32_t>(j)));
+      if (v > bv) bv = v, bid = static_cast<uint32_t>(j);
     }
   }
+  const uint64_t tmax = bid == 0xFFFFFFFFu ? 0ull : pack_best(bv, bid);
   // the peers' mbarriers are initialized before anyone arrives on them
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const uint64_t wmax = warp_reduce(tmax, MaxU64());
@@ -269,7 +293,14 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   }
   const float m = unord_f32(static_cast<uint32_t>(gbest >> 32));
   uint64_t Q = 0;
-  for_own([&](float v, uint32_t) { Q += fx_mass(v, m); });
+  if (vec) {
+    for (int q = threadIdx.x; q < v1 - v0; q += blockDim.x) {
+      const float4 v = chunk4[q];
+      Q += fx_mass_x2(v.x, v.y, m) + fx_mass_x2(v.z, v.w, m);
+    }
+  } else {
+    for_own([&](float v, uint32_t) { Q += fx_mass(v, m); });
+  }
   Q = block_reduce(Q, SumU64(), red64);  // also orders ltop[] before thread 0 reads it
   if (threadIdx.x == 0) {  // mass and top-k list to CTA 0
     cl_st64(cl_addr(&s_pQ[rank], 0), Q);

@@ -477,8 +477,7 @@ row_q_kernel(const float* __restrict__ logits, int V, const float* __restrict__ 
   for (int q = q0 + threadIdx.x; q < q1; q += kRowQThreads) {
     const float4 v = z4[q];
     bad |= !isfinite(v.x) | !isfinite(v.y) | !isfinite(v.z) | !isfinite(v.w);
-    Q += fx_mass(__fmul_rn(v.x, it), mx) + fx_mass(__fmul_rn(v.y, it), mx) + fx_mass(__fmul_rn(v.z, it), mx) +
-         fx_mass(__fmul_rn(v.w, it), mx);
+    Q += fx_mass_x2(__fmul_rn(v.x, it), __fmul_rn(v.y, it), mx) + fx_mass_x2(__fmul_rn(v.z, it), __fmul_rn(v.w, it), mx);
   }
   Q = block_reduce(Q, SumU64(), red64);
   bad = block_reduce(bad, OrI(), redi);

@@ -133,7 +133,9 @@ def run_gpu_expansion(logits_per_depth, B, k, W, D):
 
 @pytest.mark.parametrize("V,k,W,D,B,ties", [(1024, 2, 1 << 20, 3, 1, False), (128256, 10, 10, 3, 1, False),
                                             (4096, 10, 10, 6, 3, False), (512, 4, 4, 4, 2, True),
-                                            (300, 7, 9, 3, 2, False)])
+                                            (300, 7, 9, 3, 2, False),
+                                            # 320 rows x 8 CTAs: several waves, SMs reused
+                                            (128256, 10, 10, 2, 32, False)])
 def test_expand_bitexact(V, k, W, D, B, ties):
     rng = np.random.default_rng(V + k + D)
     sizes, F = [], 1
