@@ -22,8 +22,20 @@ namespace {
 
 constexpr int kExpandThreads = 512;
 constexpr int kMaxCluster = 16;  // CTAs per frontier row (at most)
-constexpr int kPreferCluster = 8;  // eight-CTA clusters keep every row of a depth in one wave
 constexpr uint32_t kBulkPiece = 32768;  // bytes per bulk copy of the staged chunk
+
+// candidate-list capacity and dynamic shared memory of one CTA (CL CTAs per row)
+int expand_cand_cap(int V, bool vec, int k, int CL) {
+  const int nvec = vec ? V / 4 : V;
+  const int per = (nvec + CL - 1) / CL;
+  const int per_thread = ((vec ? per * 4 : per) + kExpandThreads - 1) / kExpandThreads;
+  return k * per_thread + 32;
+}
+size_t expand_smem_bytes(int V, bool vec, int k, int CL) {
+  const int nvec = vec ? V / 4 : V;
+  const int per = (nvec + CL - 1) / CL;
+  return static_cast<size_t>(per + 1) * 16 + static_cast<size_t>(expand_cand_cap(V, vec, k, CL)) * 8 + 16;
+}
 
 template <int KMAX>
 __device__ __forceinline__ void topk_insert(uint64_t (&keys)[KMAX], uint64_t key) {
@@ -194,6 +206,8 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     }
   }
   const uint64_t tmax = bid == 0xFFFFFFFFu ? 0ull : pack_best(bv, bid);
+  // the dependent frontier kernel may be scheduled (it waits for this grid to finish)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the peers' mbarriers are initialized before anyone arrives on them
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const uint64_t wmax = warp_reduce(tmax, MaxU64());
@@ -219,7 +233,10 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   uint64_t thr = ~0ull;
   if (k <= kExpandThreads / 32) {
     for (int w = 0; w < kExpandThreads / 32; ++w) thr = min(thr, s_wmax[w]);
+    // value part of the threshold: a cheap first filter (none if some warp has no element)
+    const float thr_v = thr == 0ull ? -INFINITY : unord_f32(static_cast<uint32_t>(thr >> 32));
     for_own([&](float v, uint32_t id) {
+      if (v < thr_v) return;
       const uint64_t key = pack_best(v, id);
       if (key >= thr && key != 0ull) {
         const int at = atomicAdd(&s_cnt, 1);
@@ -249,7 +266,9 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     if (threadIdx.x == 0) s_cnt = 0;
     __syncthreads();
     thr = top[k - 1];
+    const float thr_v = thr == 0ull ? -INFINITY : unord_f32(static_cast<uint32_t>(thr >> 32));
     for_own([&](float v, uint32_t id) {
+      if (v < thr_v) return;
       const uint64_t key = pack_best(v, id);
       if (key >= thr && key != 0ull) {
         const int at = atomicAdd(&s_cnt, 1);
@@ -344,18 +363,19 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   }
 }
 
+// Clusters of 16 CTAs (half the work per CTA) where every row of the call still
+// fits one wave of such clusters, else clusters of 8.
 template <int KMAX>
-int cluster_size_for() {
-  static int cl = 0;
-  if (cl == 0) {
-    cl = 8;
-    if (kPreferCluster == 8) return cl;
+int cluster_size_for(int rows, int V, bool vec, int k) {
+  static int cached_v = -1, cached_k = -1, max16 = 0;
+  if (cached_v != V || cached_k != k) {
+    max16 = 0;
     if (cudaFuncSetAttribute(expand_rows_kernel<KMAX>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
         cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(16);
       cfg.blockDim = dim3(kExpandThreads);
-      cfg.dynamicSmemBytes = 64 * 1024;
+      cfg.dynamicSmemBytes = expand_smem_bytes(V, vec, k, 16);
       cudaLaunchAttribute at;
       at.id = cudaLaunchAttributeClusterDimension;
       at.val.clusterDim.x = 16;
@@ -364,11 +384,13 @@ int cluster_size_for() {
       cfg.attrs = &at;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, expand_rows_kernel<KMAX>, &cfg) == cudaSuccess && n > 0) cl = 16;
+      if (cudaOccupancyMaxActiveClusters(&n, expand_rows_kernel<KMAX>, &cfg) == cudaSuccess) max16 = n;
     }
     cudaGetLastError();
+    cached_v = V;
+    cached_k = k;
   }
-  return cl;
+  return rows <= max16 ? 16 : 8;
 }
 
 template <int KMAX>
@@ -380,13 +402,10 @@ e3_status launch_rows(const float* logits, int rows, int F, int V, int k, float 
     cudaFuncSetAttribute(expand_rows_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     attr_done = true;
   }
-  const int CL = cluster_size_for<KMAX>();
   const bool vec = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
-  const int nvec = vec ? V / 4 : V;
-  const int per = (nvec + CL - 1) / CL;
-  const int per_thread = ((vec ? per * 4 : per) + kExpandThreads - 1) / kExpandThreads;
-  const int cand_cap = k * per_thread + 32;
-  const size_t smem = static_cast<size_t>(per + 1) * 16 + static_cast<size_t>(cand_cap) * 8 + 16;
+  const int CL = cluster_size_for<KMAX>(rows, V, vec, k);
+  const int cand_cap = expand_cand_cap(V, vec, k, CL);
+  const size_t smem = expand_smem_bytes(V, vec, k, CL);
   E3_REQUIRE(smem <= 200 * 1024, E3_ERR_SHAPE, "eagle3_expand: V=%d too large", V);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(rows * CL);
@@ -413,6 +432,8 @@ namespace {
 __global__ void __launch_bounds__(256)
 expand_frontier_kernel(int n, int Wn, int cand_offset, e3_cand c, int32_t* next_id, float* next_score,
                        const int32_t* dev_err) {
+  // launched as a programmatic dependent of the row kernel: wait for its results
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ uint64_t keys[2048];
   const int b = blockIdx.x;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
@@ -468,8 +489,21 @@ e3_status launch_expand(const float* logits, int B, int F, int V, int k, int W, 
   E3_LAUNCH_CHECK("expand_rows_kernel");
   const int n = F * k;
   const int Wn = W < n ? W : n;
-  expand_frontier_kernel<<<B, 256, 0, s>>>(n, Wn, cand_offset, c, next_id, next_score, dev_err);
-  E3_LAUNCH_CHECK("expand_frontier_kernel");
+  // programmatic dependent launch: the frontier kernel is scheduled while the row
+  // kernel drains and waits (griddepcontrol.wait) for its completion
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, expand_frontier_kernel, n, Wn, cand_offset, c, next_id, next_score,
+                                     static_cast<const int32_t*>(dev_err));
+  if (e != cudaSuccess) return cuda_status(e, "expand_frontier_kernel");
   return E3_OK;
 }
 
