@@ -44,6 +44,7 @@ constexpr int kThreads = 576;         // warp 0 TMA, warp 1 MMA, warps 2..17 sof
 constexpr int kSoftmaxThreads = 512;
 constexpr int kSmem = 1024 + kQBytes + 4 * kKVBytes + 256 + 12 * 128 * 4 + 4 * kRowCache + 64;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazy = 8.0f;  // log2 headroom before the exponent base moves
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
 __device__ __forceinline__ uint64_t gtimer() {
@@ -151,6 +152,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),
+      "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]),
+      "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31]));
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -172,6 +183,8 @@ __device__ __forceinline__ void cluster_arrive_relaxed() {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
+// TMEM address bits of the lane quarter warp w may access
+__device__ __forceinline__ uint32_t lane_base_of(int w) { return static_cast<uint32_t>((w & 3) * 32) << 16; }
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -250,7 +263,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint64_t* v_empty = bars + 7;    // [2]
   uint64_t* s_full = bars + 9;     // [2]
   uint64_t* p_full = bars + 11;    // [2]
-  uint64_t* o_full = bars + 13;    // [2]
+  uint64_t* o_done = bars + 13;    // PV(t) completed (once per tile); bars + 14 unused
   uint64_t* xch = bars + 15;       // [4] exchange among the four parts of a row, per lane quarter
   uint64_t* recv_bar = bars + 19;  // cluster merge: the other CTAs' partial rows have landed here
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
@@ -273,9 +286,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       bar_init(&v_empty[bb], 1);
       bar_init(&s_full[bb], 1);
       bar_init(&p_full[bb], kSoftmaxThreads);
-      bar_init(&o_full[bb], 1);
     }
     for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], kSoftmaxThreads / 4);
+    bar_init(o_done, 1);
     bar_init(recv_bar, 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -391,7 +404,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const uint32_t tmem = *tmem_slot;
   // TMEM: S buffers at columns [0,128) and [128,256), O buffers at [256,384), [384,512)
   auto tS = [&](int bb) { return tmem + bb * kKeys; };
-  auto tO = [&](int bb) { return tmem + 2 * kKeys + bb * kHD; };
+  const uint32_t tO = tmem + 2 * kKeys;  // the O accumulator
 
   if (warp == 0) {
     // lane 0 streams K, lane 1 streams V: a slow V release never delays the next K
@@ -437,15 +450,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         fence_after();
         const uint32_t v_addr = su32(sV + bb * kKVBytes);
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {  // O(t) = P(t) V(t) over keys; P from TMEM
+        for (int kk = 0; kk < kKeys / 16; ++kk) {  // O (+)= P(t) V(t) over keys; P from TMEM
           const uint32_t voff = kk * 16 * 128;     // 16 keys = 16 rows of 128 bytes
-          umma_ts(tO(bb), tS(bb) + kk * 8, desc_sw128(v_addr + voff, kKVBytes / 2, 1024), idO, kk > 0);
+          umma_ts(tO, tS(bb) + kk * 8, desc_sw128(v_addr + voff, kKVBytes / 2, 1024), idO,
+                  (t > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&o_full[bb]);   // O(t) ready; V stage t % 2 is free
+        umma_commit(o_done);  // O holds tiles 0..t; V stage t % 2 is free
         umma_commit(&v_empty[bb]);
         if (t + 2 < ntile) {
           // S(t+2) overwrites P(t): PV(t) must have completed
-          if (!bar_wait(&o_full[bb], (t >> 1) & 1, abort)) break;
+          if (!bar_wait(o_done, t & 1, abort)) break;
           if (!bar_wait(&k_full[bb], ((t + 2) >> 1) & 1, abort)) break;
           fence_after();
           issue_S(t + 2);
@@ -465,10 +479,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const bool row_ok = softmax && gr < g.G * g.R;
   const int node = row_ok ? gr / g.G : 0;
   const int head = kvh * g.G + (row_ok ? gr % g.G : 0);
-  float o[32];
-#pragma unroll
-  for (int d = 0; d < 32; ++d) o[d] = 0.0f;
-  float m = -INFINITY, lt = 0.0f;
+  float m = -INFINITY, lt = 0.0f;  // exponent base (moved lazily) and the row's total sum
+  bool live = true;
   if (softmax) {
     const int words = (g.R + 63) >> 6;
     const uint64_t* mrow = mask + (static_cast<size_t>(b) * g.R + node) * words;
@@ -476,18 +488,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const int tid_sm = threadIdx.x - 64;  // 0..511
     float l = 0.0f;
-    float corr_prev = 1.0f;  // correction of the previous tile, applied when its O is folded in
-    auto fold_O = [&](int t) {  // wait PV(t); o = o * corr(t) + O(t)
-      const int bb = t & 1;
-      if (!bar_wait(&o_full[bb], (t >> 1) & 1, abort)) return false;
-      fence_after();
-      float v[32];
-      tmem_ld32(tO(bb) + lane_base + pp * 32, v);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = fmaf(o[j], corr_prev, v[j]);
-      return true;
-    };
-    bool live = true;
     for (int t = 0; t < ntile; ++t) {
       const int T0 = tile_T0(t);
       const int k0 = tile_lo(t), k1 = tile_hi(t);
@@ -531,9 +531,32 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       float tmax = s_max[((t & 1) * 4) * kRows + r];
 #pragma unroll
       for (int x = 1; x < 4; ++x) tmax = fmaxf(tmax, s_max[((t & 1) * 4 + x) * kRows + r]);
-      const float mn = fmaxf(m, tmax);
-      const float corr = (mn == -INFINITY) ? 1.0f : fast_exp2(m - mn);
-      const float nsub = (mn == -INFINITY) ? 0.0f : -mn;
+      // The base moves only when the tile's maximum exceeds it by more than 2^8; then
+      // O (tiles 0..t-1, which needs PV(t-1) completed) is rescaled in TMEM, warp-
+      // wide (lanes whose base stays multiply by 1).  Each thread waits every phase
+      // of o_done in order: PV(t-1) here or before posting P(t).
+      const bool move = tmax > m + kLazy;  // (also the first tile with a valid key)
+      float corr = 1.0f;
+      if (move) {
+        corr = m == -INFINITY ? 0.0f : fast_exp2(m - tmax);
+        l *= corr;
+        m = tmax;
+      }
+      bool waited_prev = false;
+      if (t > 0 && __any_sync(0xFFFFFFFFu, move)) {
+        if (!bar_wait(o_done, (t - 1) & 1, abort)) {
+          live = false;
+          break;
+        }
+        waited_prev = true;
+        fence_after();
+        float ov[32];
+        tmem_ld32(tO + lane_base + pp * 32, ov);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ov[j] *= corr;
+        tmem_st32(tO + lane_base + pp * 32, ov);
+      }
+      const float nsub = (m == -INFINITY) ? 0.0f : -m;
       // probabilities of this part's 32 keys, packed to bf16 pairs
       uint32_t pk[16];
       float rs = 0.0f;
@@ -550,8 +573,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         rs += e0 + e1;
         pk[j >> 1] = pack2_bf16(e0, e1);
       }
-      l = l * corr + rs;
-      m = mn;
+      l += rs;
+      if (t > 0 && !waited_prev && !bar_wait(o_done, (t - 1) & 1, abort)) {
+        live = false;
+        break;
+      }
       // P(t) over this part's S columns: keys [32pp, 32pp+32) -> columns [16pp, 16pp+16)
       // of the S buffer (all four parts have read their scores: the exchange above)
       tmem_st16(tS(bb) + lane_base + pp * 16, pk);
@@ -577,28 +603,38 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (zeroed) fence_async_smem();  // generic-proxy writes -> tensor core
       fence_before();                  // order the tcgen05.st before the arrival
       bar_arrive(&p_full[bb]);
-      // fold in the previous tile's O while this tile's PV runs
-      if (t > 0 && !fold_O(t - 1)) {
-        live = false;
-        break;
-      }
-      corr_prev = corr;
     }
-    if (live && ntile > 0) fold_O(ntile - 1);
     // total of the four parts' sums
     s_l[pp * kRows + r] = l;
     bar_arrive(&xch[q]);
     bar_wait(&xch[q], ntile & 1, abort);
     lt = s_l[r] + s_l[kRows + r] + s_l[2 * kRows + r] + s_l[3 * kRows + r];
-    if (!CLUSTER && row_ok && !*abort) {
-      const size_t rec = ((static_cast<size_t>(b) * g.S + s) * g.R + node) * g.H + head;
-      const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
-      float4* dst = reinterpret_cast<float4*>(ws_o + rec * kHD + pp * 32);
-#pragma unroll
-      for (int d = 0; d < 8; ++d)
-        dst[d] = make_float4(o[4 * d] * inv, o[4 * d + 1] * inv, o[4 * d + 2] * inv, o[4 * d + 3] * inv);
-      if (pp == 0) ws_ml[rec] = make_float2(m, lt);
+  }
+  // this part's 32 columns of O, from TMEM once the last PV has completed (zero
+  // where no tile was processed); warp-uniform, as the TMEM loads are warp-wide
+  float o[32];
+  {
+    bool o_ready = false;
+    if (softmax && live && ntile > 0) {
+      o_ready = bar_wait(o_done, (ntile - 1) & 1, abort);
+      fence_after();
     }
+    o_ready = __all_sync(0xFFFFFFFFu, o_ready);
+    if (o_ready) {
+      tmem_ld32(tO + lane_base_of(warp) + pp * 32, o);
+    } else {
+#pragma unroll
+      for (int d = 0; d < 32; ++d) o[d] = 0.0f;
+    }
+  }
+  if (!CLUSTER && row_ok && !*abort) {
+    const size_t rec = ((static_cast<size_t>(b) * g.S + s) * g.R + node) * g.H + head;
+    const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+    float4* dst = reinterpret_cast<float4*>(ws_o + rec * kHD + pp * 32);
+#pragma unroll
+    for (int d = 0; d < 8; ++d)
+      dst[d] = make_float4(o[4 * d] * inv, o[4 * d + 1] * inv, o[4 * d + 2] * inv, o[4 * d + 3] * inv);
+    if (pp == 0) ws_ml[rec] = make_float2(m, lt);
   }
   // the Q load has landed (also where no tile was processed) before the CTA's
   // shared memory is reused or released

@@ -282,6 +282,7 @@ def mask_from_parent(par):
     dict(dt="bf16", lens=[300, 1], R=61, H=16, KVH=16, hd=128, ps=128, D=6),    # 128-token pages, MHA (G = 1)
     dict(dt="bf16", lens=[12000], R=61, H=32, KVH=8, hd=128, ps=64, D=6),       # long prefix: one wave + merge kernel
     dict(dt="bf16", lens=[12000, 5, 1000], R=61, H=32, KVH=8, hd=128, ps=64, D=6),  # ragged long: empty segments
+    dict(dt="bf16", lens=[30000], R=61, H=16, KVH=4, hd=128, ps=64, D=6),       # long: one wave without clusters
 ])
 def test_verify_attention(case):
     dt, lens, R, H, KVH, hd, ps, D = (case[x] for x in ("dt", "lens", "R", "H", "KVH", "hd", "ps", "D"))
