@@ -8,9 +8,12 @@
 // candidates.
 //
 // One CTA per request: bitonic sort of the candidate keys (score desc, index
-// asc) in shared memory; the first N are kept.  Flat indices are assigned
-// depth by depth with a parallel rank count on (parent's flat index, candidate
-// index); each mask row is the OR of the bits on its ancestor walk.
+// asc), one key per thread in registers (shuffles within a warp, shared memory
+// across warps); the first N are kept.  Flat indices are assigned depth by
+// depth with a parallel rank count on (parent's flat index, candidate index);
+// each mask row is the OR of the bits on its ancestor walk.
+#include <algorithm>
+
 #include "e3_common.cuh"
 #include "e3_kernels.h"
 
@@ -18,47 +21,79 @@ namespace e3 {
 
 namespace {
 
-constexpr int kTreeThreads = 256;
+constexpr int kTreeThreads = 256;  // at least E3_MAX_NODES + 1 (one thread per flat row)
 
-__global__ void __launch_bounds__(kTreeThreads)
+// Descending bitonic sort of n = blockDim.x keys (a power of two, <= 1024), one
+// key per thread: partners within a warp exchange through shuffles, the others
+// through two alternating shared-memory buffers (one barrier per such step).
+__device__ __forceinline__ uint64_t bitonic_desc_thread(uint64_t v, uint64_t* buf /* [2][n] */) {
+  const int n = blockDim.x, tid = threadIdx.x;
+  int flip = 0;
+  for (int kk = 2; kk <= n; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      uint64_t o;
+      if (j >= 32) {
+        uint64_t* b = buf + flip * n;
+        b[tid] = v;
+        __syncthreads();
+        o = b[tid ^ j];
+        flip ^= 1;
+      } else {
+        o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+      }
+      const bool lower = (tid & j) == 0;  // the lower index of the pair keeps the larger key...
+      const bool desc = (tid & kk) == 0;  // ...in the descending halves of the merge
+      v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
+    }
+  }
+  return v;
+}
+
+__global__ void __launch_bounds__(1024)
 tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root_tok,
                   const int32_t* __restrict__ kv_len, int32_t* tok, int32_t* parent, int32_t* depth,
                   int32_t* pos, uint64_t* mask) {
   extern __shared__ uint64_t sh[];
-  uint64_t* keys = sh;                                       // [np]
+  uint64_t* keys = sh;  // [2 * max(np, blockDim.x)]: the two exchange buffers, or the in-place sort
   const int b = blockIdx.x;
   int np = 1;
   while (np < n_cand) np <<= 1;
-  int16_t* flat_of = reinterpret_cast<int16_t*>(keys + np);  // [n_cand]
-  __shared__ int kc[E3_MAX_NODES], kd[E3_MAX_NODES], pfl[E3_MAX_NODES];
+  const bool per_thread = np <= static_cast<int>(blockDim.x);  // then blockDim.x == np
+  int16_t* flat_of = reinterpret_cast<int16_t*>(keys + 2 * max(np, static_cast<int>(blockDim.x)));  // [n_cand]
+  __shared__ int kkey[E3_MAX_NODES];  // per level: (parent flat index, candidate index) of its nodes
   __shared__ int pflat[E3_MAX_NODES + 1];
   __shared__ int cnt[E3_MAX_DEPTH + 2], base[E3_MAX_DEPTH + 2];
 
   const size_t cb = static_cast<size_t>(b) * c.cap;
-  for (int i = threadIdx.x; i < np; i += blockDim.x)
-    keys[i] = i < n_cand ? pack_best(c.score[cb + i], static_cast<uint32_t>(i)) : 0ull;
-  for (int i = threadIdx.x; i < n_cand; i += blockDim.x) flat_of[i] = -1;
-  if (threadIdx.x < E3_MAX_DEPTH + 2) cnt[threadIdx.x] = 0;
-  __syncthreads();
-  block_bitonic_desc(keys, np);
-
-  const int R = N + 1;
-  const int P = kv_len[b];
   const int i = threadIdx.x;
-  int my_c = -1, my_d = 0, my_p = -1;
+  for (int q = i; q < n_cand; q += blockDim.x) flat_of[q] = -1;
+  if (i < E3_MAX_DEPTH + 2) cnt[i] = 0;
+  const int P = kv_len[b];
+  uint64_t top;  // (thread i < N) the i-th best candidate key
+  if (per_thread) {
+    const uint64_t v = i < n_cand ? pack_best(c.score[cb + i], static_cast<uint32_t>(i)) : 0ull;
+    top = bitonic_desc_thread(v, keys);
+  } else {
+    for (int q = i; q < np; q += blockDim.x)
+      keys[q] = q < n_cand ? pack_best(c.score[cb + q], static_cast<uint32_t>(q)) : 0ull;
+    __syncthreads();
+    block_bitonic_desc(keys, np);
+    top = i < np ? keys[i] : 0ull;
+  }
+  // the kept nodes' candidate data, loaded once
+  int my_c = -1, my_d = 0, my_p = -1, my_tok = 0;
   if (i < N) {
-    my_c = static_cast<int>(packed_id(keys[i]));
+    my_c = static_cast<int>(packed_id(top));
     my_d = c.depth[cb + my_c];
     my_p = c.parent[cb + my_c];
+    my_tok = c.tok[cb + my_c];
     if (my_p >= n_cand) my_p = -1;  // malformed parent: hang the node off the root
     if (my_d < 1) my_d = 1;
     if (my_d > E3_MAX_DEPTH) my_d = E3_MAX_DEPTH;
-    kc[i] = my_c;
-    kd[i] = my_d;
     atomicAdd(&cnt[my_d], 1);
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (i == 0) {
     int acc = 1;
     for (int d = 1; d <= E3_MAX_DEPTH; ++d) {
       base[d] = acc;
@@ -67,34 +102,41 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
     pflat[0] = -1;
   }
   __syncthreads();
+  // flat indices depth by depth: rank among the level's nodes by (parent's flat
+  // index, candidate index), packed into one integer key (both below 2^12)
+  int my_fl = 0, my_pf = 0;
   for (int d = 1; d <= E3_MAX_DEPTH; ++d) {
     if (cnt[d] == 0) continue;  // uniform across the block
-    if (i < N && my_d == d) {
-      int pf = my_p < 0 ? 0 : flat_of[my_p];
-      if (pf < 0) pf = 0;  // parent not kept: cannot happen for expansion scores
-      pfl[i] = pf;
+    if (i < N) {
+      int key = 0x7FFFFFFF;
+      if (my_d == d) {
+        int pf = my_p < 0 ? 0 : flat_of[my_p];
+        if (pf < 0) pf = 0;  // parent not kept: cannot happen for expansion scores
+        my_pf = pf;
+        key = (pf << 12) | my_c;
+      }
+      kkey[i] = key;
     }
     __syncthreads();
     if (i < N && my_d == d) {
-      const int pf = pfl[i];
+      const int mine = (my_pf << 12) | my_c;
       int rank = 0;
-      for (int j = 0; j < N; ++j) {
-        if (kd[j] != d) continue;
-        const int pj = pfl[j];
-        rank += (pj < pf) || (pj == pf && kc[j] < my_c);
-      }
-      const int fl = base[d] + rank;
-      flat_of[my_c] = static_cast<int16_t>(fl);
-      pflat[fl] = pf;
-      const size_t o = static_cast<size_t>(b) * R + fl;
-      tok[o] = c.tok[cb + my_c];
-      parent[o] = pf;
-      depth[o] = d;
-      pos[o] = P + d;
+      for (int j = 0; j < N; ++j) rank += kkey[j] < mine;
+      my_fl = base[d] + rank;
+      flat_of[my_c] = static_cast<int16_t>(my_fl);
+      pflat[my_fl] = my_pf;
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
+  const int R = N + 1;
+  if (i < N) {
+    const size_t o = static_cast<size_t>(b) * R + my_fl;
+    tok[o] = my_tok;
+    parent[o] = my_pf;
+    depth[o] = my_d;
+    pos[o] = P + my_d;
+  }
+  if (i == 0) {
     const size_t o = static_cast<size_t>(b) * R;
     tok[o] = root_tok[b];
     parent[o] = -1;
@@ -122,14 +164,16 @@ e3_status launch_tree_build(const e3_cand& c, int B, int n_cand, int N, const in
                             int32_t* pos, uint64_t* mask, cudaStream_t s) {
   int np = 1;
   while (np < n_cand) np <<= 1;
-  const size_t smem = static_cast<size_t>(np) * 8 + static_cast<size_t>(n_cand) * 2 + 16;
+  // one thread per sort key up to 1024 keys (sorted in registers and shuffles),
+  // else 1024 threads over a shared-memory sort
+  const int threads = std::max(kTreeThreads, std::min(np, 1024));
+  const size_t smem = static_cast<size_t>(std::max(np, threads)) * 16 + static_cast<size_t>(n_cand) * 2 + 16;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_status(e, "tree_build_kernel smem attribute");
   }
-  tree_build_kernel<<<B, kTreeThreads, smem, s>>>(c, n_cand, N, root_tok, kv_len, tok, parent, depth,
-                                                  pos, mask);
+  tree_build_kernel<<<B, threads, smem, s>>>(c, n_cand, N, root_tok, kv_len, tok, parent, depth, pos, mask);
   E3_LAUNCH_CHECK("tree_build_kernel");
   return E3_OK;
 }
