@@ -44,6 +44,7 @@ constexpr int kThreads = 576;         // warp 0 TMA, warp 1 MMA, warps 2..17 sof
 constexpr int kSoftmaxThreads = 512;
 constexpr int kSmem = 1024 + kQBytes + 4 * kKVBytes + 256 + 12 * 128 * 4 + 4 * kRowCache + 64;
 constexpr float kLog2e = 1.4426950408889634f;
+static_assert(kQBytes == kKVBytes, "Q and K halves share the slice offsets");
 constexpr float kLazy = 8.0f;  // log2 headroom before the exponent base moves
 constexpr unsigned long long kWaitNs = 1000000000ull;
 
@@ -285,9 +286,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       bar_init(&v_full[bb], 1);
       bar_init(&v_empty[bb], 1);
       bar_init(&s_full[bb], 1);
-      bar_init(&p_full[bb], kSoftmaxThreads);
+      bar_init(&p_full[bb], kSoftmaxThreads / 32);  // one arrival per softmax warp
     }
-    for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], kSoftmaxThreads / 4);
+    for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], 4);  // one arrival per part (warp) of a lane quarter
     bar_init(o_done, 1);
     bar_init(recv_bar, 1);
     *abort = 0;
@@ -421,15 +422,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     if (lane == 0 && ntile > 0) {
       constexpr uint32_t idS = idesc_bf16(kRows, kKeys, 0, 0);
       constexpr uint32_t idO = idesc_bf16(kRows, kHD, 0, 1);
-      const uint32_t q_addr = su32(sQ);
+      // Descriptors are built once; a K slice or a stage only adds its byte offset / 16
+      // to the start-address field (all addresses stay below 256 KB, so the 14-bit
+      // field never carries into the others).  Issuing is then a few instructions per
+      // MMA, so the tensor core, not the issuing thread, sets the pace.
+      const uint64_t q_desc = desc_sw128(su32(sQ), 16, 1024);
+      const uint64_t k_desc = desc_sw128(su32(sK), 16, 1024);
+      const uint64_t v_desc = desc_sw128(su32(sV), kKVBytes / 2, 1024);
       auto issue_S = [&](int t) {  // S(t) = Q K(t)^T into S buffer t % 2; frees K stage t % 2
         const int bb = t & 1;
-        const uint32_t k_addr = su32(sK + bb * kKVBytes);
+        const uint64_t kd = k_desc + static_cast<uint64_t>((bb * kKVBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kKVBytes / 2) + (kk & 3) * 32;
-          const uint32_t qoff = (kk >> 2) * (kQBytes / 2) + (kk & 3) * 32;
-          umma(tS(bb), desc_sw128(q_addr + qoff, 16, 1024), desc_sw128(k_addr + off, 16, 1024), idS, kk > 0);
+          constexpr int kHalfBytes = kKVBytes / 2;  // == kQBytes / 2
+          const uint64_t off = static_cast<uint64_t>(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
+          umma(tS(bb), q_desc + off, kd + off, idS, kk > 0 ? 1u : 0u);
         }
         umma_commit(&s_full[bb]);
         umma_commit(&k_empty[bb]);
@@ -448,13 +455,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (!bar_wait(&p_full[bb], (t >> 1) & 1, abort)) break;
         if (!bar_wait(&v_full[bb], (t >> 1) & 1, abort)) break;
         fence_after();
-        const uint32_t v_addr = su32(sV + bb * kKVBytes);
+        const uint64_t vd = v_desc + static_cast<uint64_t>((bb * kKVBytes) >> 4);
+        const uint32_t acc0 = t > 0 ? 1u : 0u;
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {  // O (+)= P(t) V(t) over keys; P from TMEM
-          const uint32_t voff = kk * 16 * 128;     // 16 keys = 16 rows of 128 bytes
-          umma_ts(tO, tS(bb) + kk * 8, desc_sw128(v_addr + voff, kKVBytes / 2, 1024), idO,
-                  (t > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kKeys / 16; ++kk)  // O (+)= P(t) V(t) over keys; P from TMEM; 16 keys = 16 rows of 128 B
+          umma_ts(tO, tS(bb) + kk * 8, vd + static_cast<uint64_t>((kk * 16 * 128) >> 4), idO, kk > 0 ? 1u : acc0);
         umma_commit(o_done);  // O holds tiles 0..t; V stage t % 2 is free
         umma_commit(&v_empty[bb]);
         if (t + 2 < ntile) {
@@ -522,7 +527,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
       s_max[((t & 1) * 4 + pp) * kRows + r] = pmax;
       fence_before();  // this part's S loads are done before the others overwrite S with P
-      bar_arrive(&xch[q]);
+      __syncwarp();    // the warp's s_max writes, then one arrival for the warp
+      if (lane == 0) bar_arrive(&xch[q]);
       if (!bar_wait(&xch[q], t & 1, abort)) {
         live = false;
         break;
@@ -602,11 +608,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
       if (zeroed) fence_async_smem();  // generic-proxy writes -> tensor core
       fence_before();                  // order the tcgen05.st before the arrival
-      bar_arrive(&p_full[bb]);
+      __syncwarp();
+      if (lane == 0) bar_arrive(&p_full[bb]);
     }
     // total of the four parts' sums
     s_l[pp * kRows + r] = l;
-    bar_arrive(&xch[q]);
+    __syncwarp();
+    if (lane == 0) bar_arrive(&xch[q]);
     bar_wait(&xch[q], ntile & 1, abort);
     lt = s_l[r] + s_l[kRows + r] + s_l[2 * kRows + r] + s_l[3 * kRows + r];
   }

@@ -241,20 +241,47 @@ def tree_verify_attn(Q, Kc, Vc, page_table, kv_len, parent, sm_scale):
         Kb = gather_tokens(Kc, page_table[b], 0, P + R)
         Vb = gather_tokens(Vc, page_table[b], 0, P + R)
         for i in range(R):
-            anc = []
-            j = i
-            while j >= 0:
-                anc.append(j)
-                j = int(parent[b][j])
-            keys = list(range(P)) + [P + j for j in sorted(anc)]
+            keys = _node_keys(P, parent[b], i)
             for h in range(H):
-                kh = h // grp
-                s = (Kb[keys, kh, :] @ Q[b, i, h]) * sm_scale
-                mx = s.max()
-                w = np.exp(s - mx)
-                den = w.sum()
-                O[b, i, h] = (w @ Vb[keys, kh, :]) / den
-                lse[b, i, h] = mx + np.log(den)
+                O[b, i, h], lse[b, i, h] = _attend(Kb, Vb, keys, Q[b, i, h], h // grp, sm_scale)
+    return O, lse
+
+
+def _node_keys(P, parent_row, i):
+    """Key slots node i attends to: the prefix [0, P) and P + j for the nodes j on
+    its ancestor path (itself included)."""
+    anc = []
+    j = i
+    while j >= 0:
+        anc.append(j)
+        j = int(parent_row[j])
+    return list(range(P)) + [P + j for j in sorted(anc)]
+
+
+def _attend(Kb, Vb, keys, q, kh, sm_scale):
+    """One query row over its key list: softmax(q . K / sqrt) V and the lse (fp64)."""
+    s = (Kb[keys, kh, :] @ np.asarray(q, np.float64)) * sm_scale
+    mx = s.max()
+    w = np.exp(s - mx)
+    den = w.sum()
+    return (w @ Vb[keys, kh, :]) / den, mx + np.log(den)
+
+
+def tree_verify_attn_rows(Q, Kc, Vc, page_table, kv_len, parent, sm_scale, rows):
+    """tree_verify_attn for the listed (b, i, h) query rows only (the same key lists
+    and the same per-row arithmetic); returns O [n, hd] and lse [n] in fp64."""
+    Q = np.asarray(Q, np.float64)
+    B, R, H, hd = Q.shape
+    grp = H // Kc.shape[1]
+    O = np.zeros((len(rows), hd))
+    lse = np.zeros(len(rows))
+    cache = {}
+    for n, (b, i, h) in enumerate(rows):
+        if b not in cache:
+            P = int(kv_len[b])
+            cache[b] = (P, gather_tokens(Kc, page_table[b], 0, P + R), gather_tokens(Vc, page_table[b], 0, P + R))
+        P, Kb, Vb = cache[b]
+        O[n], lse[n] = _attend(Kb, Vb, _node_keys(P, parent[b], i), Q[b, i, h], h // grp, sm_scale)
     return O, lse
 
 

@@ -1,0 +1,128 @@
+"""Every benchmarked configuration, one whole round on the GPU in the benchmark's
+own launch configuration (its workload, buffers and round function), checked
+against the oracle:
+
+  fusion        sampled output features, within the dtype tolerance
+  expansion     every candidate of every request and depth, bit-exact
+  tree          tokens, parents, depths, positions and mask rows, bit-exact
+  verify        sampled (request, node, head) rows of the first and last layer,
+                within the dtype tolerance (the oracle runs those rows only)
+  LM head       sampled rows on sampled vocabulary columns within tolerance; the
+                softmax statistics of every row bit-exact from the GPU logits
+  accept        accepted length, path and emitted tokens, bit-exact
+  compaction    slots P + j of sampled layers hold what slot P + path[j] held
+"""
+import math
+import os
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close
+
+ROOT = os.path.abspath(os.path.join(os.path.dirname(__file__), ".."))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def host(t):
+    return t.cpu().numpy()
+
+
+def f32(t):
+    return t.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b", "batched", "long", "70b"])
+def test_round_matches_oracle(name):
+    w = bench.Workload(name, seed=11)
+    b, c = w.bufs, w.cfg
+    B, R, L = c.B, c.R, c.L
+    rng = np.random.default_rng(7)
+    tol = 2e-2 if c.dtype == "bf16" else 1e-5
+
+    # what the round reads, before it runs
+    hs = [f32(t) for t in b.h]
+    drafts = [host(x) for x in b.draft_logits]
+    P = host(w.kv_len0)
+    layers = sorted({0, L - 1})
+    Kpre = {l: f32(b.K[l]) for l in layers}
+    Vpre = {l: f32(b.Vc[l]) for l in layers}
+    Qs = {l: f32(b.Q[l]) for l in layers}
+
+    w.round()
+    torch.cuda.synchronize()
+    assert int(b.dev_err.item()) == 0
+
+    # fusion: 64 sampled output features of every token row
+    cols = rng.choice(c.d, 64, replace=False)
+    Wf_rows = f32(b.W_f[torch.from_numpy(cols).cuda()])
+    assert_close(f32(b.g)[:, cols], oracle.fuse(hs[0], hs[1], hs[2], Wf_rows), tol, "fusion")
+
+    # expansion and tree, per request
+    sizes, n_cand = c.frontier_sizes()
+    ctok, cpar, cdep, csc = host(b.c_tok), host(b.c_parent), host(b.c_depth), host(b.c_score)
+    roots = host(b.root_tok)
+    tok, par, dep, pos, mask = host(b.tok), host(b.parent), host(b.depth), host(b.pos), host(b.mask)
+    for bb in range(B):
+        cands = oracle.new_cands(n_cand)
+        fid, fsc = np.array([-1], np.int32), np.zeros(1, np.float32)
+        for di, (F, off) in enumerate(sizes):
+            fid, fsc = oracle.expand(drafts[di][bb][:F], c.k, c.W, fsc, fid, di + 1, off, cands)
+        assert np.array_equal(ctok[bb], cands["tok"]), (name, bb)
+        assert np.array_equal(cpar[bb], cands["parent"]), (name, bb)
+        assert np.array_equal(cdep[bb], cands["depth"]), (name, bb)
+        assert np.array_equal(csc[bb].view(np.uint32), cands["score"].view(np.uint32)), (name, bb)
+        tree = oracle.build_tree(cands, n_cand, c.N, int(roots[bb]), int(P[bb]))
+        for key, got in (("tok", tok), ("parent", par), ("depth", dep), ("pos", pos)):
+            assert np.array_equal(got[bb], tree[key]), (name, key, bb)
+        assert np.array_equal(mask[bb].view(np.uint64), tree["mask"]), (name, bb)
+
+    # verify: sampled rows of the first and the last layer
+    sm = 1.0 / math.sqrt(c.hd)
+    for l in layers:
+        rows = [(int(rng.integers(B)), int(rng.integers(R)), int(rng.integers(c.H))) for _ in range(12)]
+        Oref, lref = oracle.tree_verify_attn_rows(Qs[l], Kpre[l], Vpre[l], w.pt, P, par, sm, rows)
+        Og, lg = f32(b.O[l]), host(b.lse[l])
+        assert_close(np.stack([Og[bb, i, h] for bb, i, h in rows]), Oref, tol, f"O layer {l}")
+        assert_close(np.array([lg[bb, i, h] for bb, i, h in rows]), lref, tol, f"lse layer {l}")
+
+    # LM head: sampled rows x sampled vocabulary columns; statistics of every row
+    z = host(b.logits)
+    hrow = f32(b.O[L - 1]).reshape(B * R, c.H * c.hd)
+    sel = rng.choice(B * R, min(4, B * R), replace=False)
+    vcols = rng.choice(c.V, min(2048, c.V), replace=False)
+    Wl = f32(b.W_lm[torch.from_numpy(vcols).cuda()])
+    assert_close(z[sel][:, vcols], oracle.lmhead_logits(hrow[sel], Wl), tol, "logits")
+    m, Q, am, bad = oracle.row_stats(z, host(b.temp_rows))
+    assert not bad.any()
+    assert np.array_equal(host(b.row_max).view(np.uint32), m.view(np.uint32))
+    assert np.array_equal(host(b.row_Q).view(np.uint64), Q)
+    assert np.array_equal(host(b.row_argmax), am)
+
+    # accept, per request
+    temps, ua, ub = host(b.temp), host(b.u_acc).view(np.uint32), host(b.u_bonus).view(np.uint32)
+    acc, path, out = host(b.acc_len), host(b.path), host(b.out_tok)
+    for bb in range(B):
+        a, p, o = oracle.accept({"tok": tok[bb], "parent": par[bb]}, z[bb * R:(bb + 1) * R], temps[bb], ua[bb],
+                                ub[bb], c.D)
+        assert acc[bb] == a and np.array_equal(path[bb], p) and np.array_equal(out[bb], o), (name, bb)
+    assert np.array_equal(host(b.kv_len), P + 1 + acc)
+
+    # compaction: logical slot P + j now holds what P + path[j] held (K and V)
+    for l in layers:
+        for pre, cache in ((Kpre[l], b.K[l]), (Vpre[l], b.Vc[l])):
+            post = f32(cache)
+            for bb in range(B):
+                a = int(acc[bb])
+                before = oracle.gather_tokens(pre, w.pt[bb], int(P[bb]), int(P[bb]) + R)
+                after = oracle.gather_tokens(post, w.pt[bb], int(P[bb]), int(P[bb]) + a + 1)
+                assert np.array_equal(after, before[path[bb][:a + 1]]), (name, l, bb)
+
+    del w, b
+    torch.cuda.empty_cache()

@@ -181,3 +181,26 @@ def test_lse_merge_of_prefix_and_tree_segments():
             om = math.exp(l1 - lm) * o1 + math.exp(l2 - lm) * o2
             assert abs(lse[0, i, h] - lm) < 1e-12
             assert np.abs(O[0, i, h] - om).max() < 1e-12
+
+
+def test_verify_rows_equal_full_oracle():
+    """The sampled-row form runs the same per-row step as the full form."""
+    rng = np.random.default_rng(5)
+    B, R, H, KVH, hd, ps = 2, 7, 4, 2, 16, 4
+    lens = [9, 3]
+    npages = sum((p + R + ps - 1) // ps for p in lens)
+    pt = np.full((B, 8), -1, np.int32)
+    nxt = 0
+    for b, p in enumerate(lens):
+        for j in range((p + R + ps - 1) // ps):
+            pt[b, j] = nxt
+            nxt += 1
+    K = rng.standard_normal((npages, KVH, ps, hd))
+    V = rng.standard_normal((npages, KVH, ps, hd))
+    Q = rng.standard_normal((B, R, H, hd))
+    par = np.array([[-1, 0, 0, 1, 1, 2, 5], [-1, 0, 1, 2, 3, 4, 5]])
+    O, lse = oracle.tree_verify_attn(Q, K, V, pt, np.array(lens), par, 0.25)
+    rows = [(0, 6, 3), (1, 0, 0), (1, 5, 2), (0, 3, 1)]
+    Or, lr = oracle.tree_verify_attn_rows(Q, K, V, pt, np.array(lens), par, 0.25, rows)
+    for n, (b, i, h) in enumerate(rows):
+        assert np.array_equal(Or[n], O[b, i, h]) and lr[n] == lse[b, i, h]
