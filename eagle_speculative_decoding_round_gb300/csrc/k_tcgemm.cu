@@ -205,17 +205,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = instr_desc(BM, BN);
+      const uint64_t desc0 = smem_desc(su32(smem));  // stage / K-slice offsets add to its address field
       for (int it = 0; it < nkb; ++it) {
         const int s = it % C::STAGES;
         const uint32_t ph = (it / C::STAGES) & 1;
         if (!mbar_wait(&full[s], ph, abort)) break;
         tc_fence_after();
-        const uint32_t a_addr = su32(smem + s * C::STAGE);
-        const uint32_t b_addr = a_addr + A_BYTES;
+        const uint64_t da = desc0 + static_cast<uint64_t>((s * C::STAGE) >> 4);
+        const uint64_t db = da + static_cast<uint64_t>(A_BYTES >> 4);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          mma_bf16_ss(tmem, smem_desc(a_addr + k * 32), smem_desc(b_addr + k * 32), idesc, (it | k) != 0);
-        }
+        for (int k = 0; k < BK / 16; ++k)
+          mma_bf16_ss(tmem, da + 2 * k, db + 2 * k, idesc, (it | k) != 0);  // +32 bytes per K slice
         mma_commit(&empty[s]);  // frees the stage once these MMAs have read it
       }
       mma_commit(accum);  // accumulator complete (or nothing issued)
@@ -355,6 +355,9 @@ lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   } else if (warp == 1) {
     if (lane == 0) {  // MMA issuer
       constexpr uint32_t idesc = instr_desc(BM, BN);
+      // descriptors built once: a stage or a K slice only adds its byte offset / 16 to
+      // the start-address field (shared addresses stay below 256 KB: no carry)
+      const uint64_t desc0 = smem_desc(su32(smem));
       int it = 0, local = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++local) {
@@ -369,10 +372,11 @@ lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = su32(smem + st * C::STAGE);
+          const uint64_t da = desc0 + static_cast<uint64_t>((st * C::STAGE) >> 4);
+          const uint64_t db = da + static_cast<uint64_t>(A_BYTES >> 4);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16_ss(d, smem_desc(a_addr + k * 32), smem_desc(a_addr + A_BYTES + k * 32), idesc, (kb | k) != 0);
+            mma_bf16_ss(d, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);  // +32 bytes per K slice
           mma_commit(&empty[st]);
         }
         if (ok) mma_commit(&acc_full[a]);
