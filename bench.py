@@ -49,6 +49,11 @@ CONFIGS = {
                          "prefix 4096, fusion 24576->8192, 60-node depth-6 tree, temp 1, 80 layers"),
 }
 METRIC = "tree-verify rounds/s & nodes/s (8B-shape, 60-node tree); % HBM/tensor roofline"
+# dram__bytes_read.sum + dram__bytes_write.sum per launch, from one ncu capture of the
+# kernel on this workload (None until the current kernel has been captured)
+TRAFFIC = {
+    "8b": {"verify": 9217024, "lmhead": 1082355200},
+}
 TAB_ROWS = 4096  # token-keyed Q/K/V tables of the synthetic target (token id modulo this)
 
 
@@ -406,15 +411,18 @@ def main():
     from eagle_speculative_decoding_round_gb300 import eagle3 as e3
     from eagle_speculative_decoding_round_gb300.round import run_round
     graph = torch.cuda.CUDAGraph()
+    counts = []  # library launch counter at each phase boundary of the first captured round
+    n0 = e3.launch_count()
     with torch.cuda.graph(graph, stream=s):
         for k in range(K):
             w.bufs.kv_len.copy_(w.kv_len0)
-            run_round_phased(w, ev[k], e3)
+            run_round_phased(w, ev[k], e3, counts if k == 0 else None)
+    launches_timed = e3.launch_count() - n0  # libeagle3 kernels in the K captured rounds
+    phase_launches = {p: counts[i + 1] - counts[i] for i, p in enumerate(phases)}
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         graph.replay()  # one untimed replay of the captured work
     torch.cuda.synchronize()
-    launches_per_step = count_launches(cfg)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -451,20 +459,32 @@ def main():
     peaks = load_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
     tflops = peaks.get("bf16_tflops_sustained", 1700.0)
+    src = "of measured" if "hbm_gbs" in peaks else "of fallback"
+    traffic = TRAFFIC.get(args.config, {})
+    # dominant kernel: verify_tc_kernel, one launch per layer on the single-wave workloads
+    # (a second, merge launch per layer where the split spans several waves)
+    ver_launches = phase_launches["verify"]
+    ver_ms = phase_ms["verify"] / cfg.L  # per layer: its verify_tc launch (+ merge launch, if any)
+    ver_gbs = wm["verify_bytes"] / (ver_ms * 1e-3) / 1e9
+    roofline = {"kernel": "verify_tc_kernel (tree_verify_attn, one layer)", "bound": "hbm",
+                "achieved": round(ver_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(ver_gbs / hbm, 4),
+                "traffic": traffic.get("verify"), "algorithmic_bytes": int(wm["verify_bytes"]),
+                "launches_per_layer": ver_launches / cfg.L, "us_per_layer": round(ver_ms * 1e3, 2),
+                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({src})"}
     lm_ms = phase_ms["lmhead"]
     lm_gbs = wm["lm_bytes"] / (lm_ms * 1e-3) / 1e9
     lm_tf = wm["lm_flops"] / (lm_ms * 1e-3) / 1e12
-    ver_ms = phase_ms["verify"] / cfg.L
-    ver_gbs = wm["verify_bytes"] / (ver_ms * 1e-3) / 1e9
     lm_bound = "hbm" if wm["lm_flops"] / wm["lm_bytes"] < tflops * 1e12 / (hbm * 1e9) else "tensor"
+    lm = {"kernel": "lmhead_kernel + row_q_kernel (lmhead_logits)", "bound": lm_bound,
+          "traffic": traffic.get("lmhead"), "algorithmic_bytes": int(wm["lm_bytes"]),
+          "algorithmic_flops": int(wm["lm_flops"]), "us": round(lm_ms * 1e3, 2)}
     if lm_bound == "hbm":
-        roofline = {"kernel": "lmhead_logits (GEMM + row statistics)", "bound": "hbm", "achieved": round(lm_gbs, 1),
-                    "peak": hbm, "unit": "GB/s", "frac": round(lm_gbs / hbm, 4), "traffic": None,
-                    "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if "hbm_gbs" in peaks else "fallback"}
+        lm.update(achieved=round(lm_gbs, 1), peak=hbm, unit="GB/s", frac=round(lm_gbs / hbm, 4),
+                  peak_source=f"MEASURED_PEAKS.json hbm_gbs ({src})")
     else:
-        roofline = {"kernel": "lmhead_logits (GEMM + row statistics)", "bound": "tensor", "achieved": round(lm_tf, 1),
-                    "peak": tflops, "unit": "TFLOP/s", "frac": round(lm_tf / tflops, 4), "traffic": None,
-                    "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (of measured)"}
+        lm.update(achieved=round(lm_tf, 1), peak=tflops, unit="TFLOP/s", frac=round(lm_tf / tflops, 4),
+                  peak_source="MEASURED_PEAKS.json bf16_tflops_sustained (of measured)")
+    lm["tensor_frac"] = round(lm_tf / tflops, 4)
     e2e = None if args.no_e2e else e2e_leg(w, s, K, args.warmup)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -488,9 +508,9 @@ def main():
             "accepted_mean": float(np.mean(accepted)),
             "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
             "roofline": roofline,
-            "roofline_verify": {"bound": "hbm", "achieved": round(ver_gbs, 1), "peak": hbm, "unit": "GB/s",
-                                "frac": round(ver_gbs / hbm, 4), "per_layer_us": round(ver_ms * 1e3, 2)},
-            "gpu_launches": launches_per_step * K,
+            "roofline_lmhead": lm,
+            "gpu_launches": launches_timed,
+            "launches_per_round": phase_launches,
             "clocks": clk,
             "e2e": e2e,
             "cpu_baseline": cpu,
@@ -513,12 +533,24 @@ def summarize(P):
     return P if len(P) <= 4 else {"n": len(P), "min": min(P), "max": max(P), "mean": float(np.mean(P))}
 
 
-def run_round_phased(w, evs, e3):
-    """One round with a timing event at each phase boundary (same calls as run_round)."""
+def run_round_phased(w, evs, e3, counts=None):
+    """One round with a timing event at each phase boundary (same calls as run_round).
+    With ``counts`` (a list), also append the library's launch counter there."""
     import torch
     b, c = w.bufs, w.cfg
     s = torch.cuda.current_stream()
     R = c.R
+
+    class _Ev:  # records the event and, when asked, the launch counter
+        def __init__(self, e):
+            self.e = e
+
+        def record(self, st):
+            self.e.record(st)
+            if counts is not None:
+                counts.append(e3.launch_count())
+
+    evs = [_Ev(e) for e in evs]
     evs[0].record(s)
     e3.eagle3_fuse(b.h[0], b.h[1], b.h[2], b.W_f, None, b.g, c.M, c.d, c.d, c.dt, b.fuse_ws, b.fuse_ws_bytes, b.dev_err)
     evs[1].record(s)
@@ -541,12 +573,6 @@ def run_round_phased(w, evs, e3):
     evs[6].record(s)
     e3.kv_compact(b.kv, c.B, b.path, b.acc_len, c.D, b.kv_len, b.dev_err)
     evs[7].record(s)
-
-
-def count_launches(cfg):
-    """Kernels of libeagle3 per round: fuse 1, expand 2 per depth, tree 1, verify 2
-    per layer, LM head 2, accept 1, compact 2."""
-    return 1 + 2 * cfg.D + 1 + 2 * cfg.L + 2 + 1 + 2
 
 
 def e2e_leg(w, s, K, warmup):

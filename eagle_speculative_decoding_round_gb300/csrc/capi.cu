@@ -1,8 +1,11 @@
 // capi.cu -- the extern "C" entry points of libeagle3 (declared in include/eagle3.h).
 // Host-side validation happens here, before any launch; kernels live in k_*.cu.
 #include <stdarg.h>
+#include <stdint.h>
 #include <stdio.h>
 #include <string.h>
+
+#include <atomic>
 
 #include "e3_common.cuh"
 #include "e3_kernels.h"
@@ -10,6 +13,12 @@
 namespace e3 {
 
 static thread_local char g_err[512] = {0};
+
+// Kernels this library has launched in this process (every launch site calls
+// note_launch() once the launch call has succeeded).
+static std::atomic<unsigned long long> g_launches{0};
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 void set_error(const char* fmt, ...) {
   va_list ap;
@@ -48,6 +57,8 @@ extern "C" {
 E3_API const char* eagle3_last_error(void) { return g_err; }
 
 E3_API int eagle3_abi_version(void) { return 1; }
+
+E3_API uint64_t eagle3_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 static bool fuse_uses_tc(int d, int d_out, e3_dtype dt) { return dt == E3_BF16 && d % 64 == 0 && d_out >= 1; }
 

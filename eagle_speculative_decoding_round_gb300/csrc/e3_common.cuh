@@ -22,10 +22,15 @@ e3_status cuda_status(cudaError_t e, const char* what);
     }                                 \
   } while (0)
 
+// Host-side count of the library's kernel launches (eagle3_launch_count).
+void note_launch();
+
+// After one kernel launch: report a launch error, else count the launch.
 #define E3_LAUNCH_CHECK(what)                                   \
   do {                                                          \
     cudaError_t _e = cudaGetLastError();                        \
     if (_e != cudaSuccess) return ::e3::cuda_status(_e, what);  \
+    ::e3::note_launch();                                        \
   } while (0)
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

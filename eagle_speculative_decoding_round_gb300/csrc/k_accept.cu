@@ -289,6 +289,7 @@ e3_status launch_accept(const int32_t* tok, const int32_t* parent, int B, int R,
   cudaError_t e = cudaLaunchKernelEx(&cfg, accept_kernel, tok, parent, R, D, logits, row_max, row_Q, row_argmax, V,
                                      temp, u_acc, u_bonus, acc_len, path, out_tok, status);
   if (e != cudaSuccess) return cuda_status(e, "accept_kernel");
+  note_launch();
   return E3_OK;
 }
 

@@ -422,6 +422,7 @@ e3_status launch_rows(const float* logits, int rows, int F, int V, int k, float 
   cudaError_t e = cudaLaunchKernelEx(&cfg, expand_rows_kernel<KMAX>, logits, F, V, k, inv_temp, parent_score,
                                      parent_id, depth, cand_offset, c, dev_err, cand_cap);
   if (e != cudaSuccess) return cuda_status(e, "expand_rows_kernel");
+  note_launch();
   return E3_OK;
 }
 
@@ -486,7 +487,6 @@ e3_status launch_expand(const float* logits, int B, int F, int V, int k, int W, 
   else
     st = launch_rows<32>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
   if (st != E3_OK) return st;
-  E3_LAUNCH_CHECK("expand_rows_kernel");
   const int n = F * k;
   const int Wn = W < n ? W : n;
   // programmatic dependent launch: the frontier kernel is scheduled while the row
@@ -504,6 +504,7 @@ e3_status launch_expand(const float* logits, int B, int F, int V, int k, int W, 
   cudaError_t e = cudaLaunchKernelEx(&cfg, expand_frontier_kernel, n, Wn, cand_offset, c, next_id, next_score,
                                      static_cast<const int32_t*>(dev_err));
   if (e != cudaSuccess) return cuda_status(e, "expand_frontier_kernel");
+  note_launch();
   return E3_OK;
 }
 

@@ -680,6 +680,7 @@ e3_status launch_lmhead_tc(const void* h, const void* W_lm, int M, int d, int V,
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, row_q_kernel, static_cast<const float*>(logits), V, temp, row_max, row_Q, row_argmax);
   if (e != cudaSuccess) return cuda_status(e, "row_q_kernel");
+  note_launch();
   return E3_OK;
 }
 

@@ -548,6 +548,7 @@ e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_
     else
       E3_MMA_CASE(64);
 #undef E3_MMA_CASE
+    E3_LAUNCH_CHECK("tree_verify_attn segment kernel");
   } else {
     dim3 grid(g.S, kv.n_kv_heads, B);
 #define E3_SIMT_CASE(TT, HDV)                                                                  \
@@ -575,8 +576,8 @@ e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_
       }
     }
 #undef E3_SIMT_CASE
+    E3_LAUNCH_CHECK("tree_verify_attn segment kernel");
   }
-  E3_LAUNCH_CHECK("tree_verify_attn segment kernel");
   const long nrows = static_cast<long>(B) * R * H;
   const int blocks = static_cast<int>((nrows + 7) / 8);
 #define E3_MERGE_CASE(TT, HDV) \

@@ -900,6 +900,7 @@ e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* 
     cudaError_t e = cudaLaunchKernelEx(&cfg, verify_tc_kernel<true>, mq, mk, mv, g, kv_len, mask, sm_scale, ws_o,
                                        ws_ml, static_cast<__nv_bfloat16*>(O), lse, dev_err);
     if (e != cudaSuccess) return cuda_status(e, "verify_tc_kernel (cluster)");
+    note_launch();
     *merged = true;
     return E3_OK;
   }

@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "E3_OK", 1: "E3_ERR_INVALID_ARG", 2: "E3_ERR_SHAPE", 3: "E3_E
 SYMBOLS = ["eagle3_fuse", "eagle3_fuse_workspace_bytes", "eagle3_fuse_noalloc",
            "eagle3_fuse_noalloc_max_scratch_bytes", "eagle3_expand", "tree_build_mask",
            "tree_verify_attn", "eagle3_verify_workspace_bytes", "lmhead_logits", "spec_accept",
-           "kv_compact", "eagle3_last_error", "eagle3_abi_version"]
+           "kv_compact", "eagle3_last_error", "eagle3_abi_version", "eagle3_launch_count"]
 
 
 class E3Error(RuntimeError):
@@ -62,6 +62,7 @@ def _load() -> ctypes.CDLL:
         "kv_compact": (I, [ctypes.POINTER(e3_kv_layer), I, I, P, P, I, P, P, P]),
         "eagle3_last_error": (ctypes.c_char_p, []),
         "eagle3_abi_version": (I, []),
+        "eagle3_launch_count": (ctypes.c_uint64, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -110,6 +111,11 @@ def make_kv_layer(k, v, page_table, n_pages, page_size, max_pages, n_kv_heads, h
 
 def abi_version() -> int:
     return _lib.eagle3_abi_version()
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(_lib.eagle3_launch_count())
 
 
 def eagle3_fuse_workspace_bytes(M, d, d_out, dt) -> int:

@@ -273,6 +273,13 @@ E3_API const char* eagle3_last_error(void);
 /* ABI version: 1. */
 E3_API int eagle3_abi_version(void);
 
+/* Diagnostic with no counterpart in the method: the number of kernels this
+ * library has launched in the calling process since it was loaded (summed over
+ * threads; a launch counts once its launch call has succeeded, whether or not
+ * the kernel has run yet).  Read it before and after a sequence of calls to
+ * learn how many kernels the sequence enqueued.  Never fails. */
+E3_API uint64_t eagle3_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif
