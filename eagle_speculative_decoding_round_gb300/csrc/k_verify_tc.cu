@@ -4,23 +4,30 @@
 // Same segment decomposition as the mma.sync kernel in k_verify.cu ("EAGLE-3 投机
 // 解码与 USP 长序列训练优化", USP 核心设计：三步走: the prefix is the main segment,
 // split across CTAs, the tree is the branch segment; all are merged by their
-// log-sum-exp), and the same partial (o, m, l) records, merged by
-// verify_merge_kernel.  The mask is the ancestor-only tree mask of "EAGLE 系列与
-// DFlash", §二 关键新增步骤②.
+// log-sum-exp).  The mask is the ancestor-only tree mask of "EAGLE 系列与 DFlash",
+// §二 关键新增步骤②.
 //
 // One CTA = (segment, 128-query-row group) of one KV head of one request.  The
 // 128 rows are the G query heads of 128/G consecutive tree nodes (a 3-D TMA box
 // over Q[B*R][H][hd]).  Keys stream in tiles of 128 (two 64-token page boxes per
 // operand):
-//   S = Q K^T    tcgen05.mma, M = 128 rows, N = 128 keys, K = head_dim (K-major)
+//   S = Q K^T    tcgen05.mma, M = 128 rows, N = 128 keys, K = head_dim (K-major),
+//                into one of two S buffers in TMEM
 //   softmax      the threads of a query row read its TMEM lane; running max and
 //                sum in registers; P (bf16) is written back over S in TMEM
-//   O_t = P V    tcgen05.mma with A (P) from TMEM, N = head_dim, K = keys; V is
-//                used in place as an MN-major operand (rows of 64 head-dim values
-//                per key)
-//   O += O_t     accumulated in registers with the online-softmax correction.
+//   O += P V     tcgen05.mma with A (P) from TMEM, N = head_dim, K = keys; V is
+//                used in place as an MN-major operand.  O stays in TMEM for the
+//                whole key range: its exponent base moves only when a tile's
+//                maximum exceeds it by more than 2^8, and then the softmax warps
+//                rescale it in place.
 // Warps: 0 TMA, 1 TMEM owner + MMA issuer, 2..17 softmax/epilogue (four warps per
 // TMEM lane quarter, each owning a quarter of the keys and of the head dims).
+//
+// Segments are combined in one of two ways.  CLUSTER: the S segments of one row
+// group form a thread-block cluster and merge their partial (o, m, l) rows through
+// distributed shared memory (bulk copies), writing O and lse directly.  Otherwise
+// (prefixes long enough to fill the GPU with independent CTAs) the partial records
+// go to a workspace and verify_merge_kernel combines them.
 #include <algorithm>
 #include <cuda.h>
 #include <cudaTypedefs.h>
