@@ -20,8 +20,9 @@
 //                whole key range: its exponent base moves only when a tile's
 //                maximum exceeds it by more than 2^8, and then the softmax warps
 //                rescale it in place.
-// Warps: 0 TMA, 1 TMEM owner + MMA issuer, 2..17 softmax/epilogue (four warps per
-// TMEM lane quarter, each owning a quarter of the keys and of the head dims).
+// Warps: 0 K loads (TMA), 1 TMEM owner + MMA issuer, 2..17 softmax/epilogue (four
+// warps per TMEM lane quarter, each owning a quarter of the keys and of the head
+// dims), 18 V loads (TMA).
 //
 // Segments are combined in one of two ways.  CLUSTER: the S segments of one row
 // group form a thread-block cluster and merge their partial (o, m, l) rows through
@@ -47,7 +48,8 @@ constexpr int kBox = kHalf * kHalf * 2;        // 64 x 64 bf16 = 8 KB
 constexpr int kQBytes = kRows * kHD * 2;       // 32 KB (two 16 KB halves)
 constexpr int kKVBytes = kKeys * kHD * 2;      // 32 KB per operand per tile
 constexpr int kRowCache = 128;       // KV block rows looked up ahead
-constexpr int kThreads = 576;         // warp 0 TMA, warp 1 MMA, warps 2..17 softmax
+constexpr int kThreads = 608;         // warp 0 K loads, warp 1 MMA, warps 2..17 softmax, warp 18 V loads
+constexpr int kVWarp = 18;
 constexpr int kSoftmaxThreads = 512;
 constexpr int kSmem = 1024 + kQBytes + 4 * kKVBytes + 256 + 12 * 128 * 4 + 4 * kRowCache + 64;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -160,6 +162,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 16 consecutive 32-bit TMEM columns of this thread's lane, as floats (load / store)
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
+      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]));
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
@@ -193,6 +214,11 @@ __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.w
 
 // TMEM address bits of the lane quarter warp w may access
 __device__ __forceinline__ uint32_t lane_base_of(int w) { return static_cast<uint32_t>((w & 3) * 32) << 16; }
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -414,14 +440,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   auto tS = [&](int bb) { return tmem + bb * kKeys; };
   const uint32_t tO = tmem + 2 * kKeys;  // the O accumulator
 
-  if (warp == 0) {
-    // lane 0 streams K, lane 1 streams V: a slow V release never delays the next K
-    if (lane < 2 && ntile > 2) {
+  if (warp == 0 || warp == kVWarp) {
+    // warp 0 streams K, warp kVWarp streams V: each producer waits on its own
+    // stage releases in a warp of its own, so neither wait delays the other's loads
+    const int which = warp == 0 ? 0 : 1;
+    if (lane == 0 && ntile > 2) {
       bool okp = true;
       for (int t = 2; t < ntile; ++t) {
-        uint64_t* empty = lane == 0 ? &k_empty[t & 1] : &v_empty[t & 1];
+        uint64_t* empty = which == 0 ? &k_empty[t & 1] : &v_empty[t & 1];
         if (!bar_wait(empty, ((t >> 1) & 1) ^ 1, abort)) break;
-        issue_kv(t, lane, &okp);
+        issue_kv(t, which, &okp);
       }
       if (!okp) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
     }
@@ -483,7 +511,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   // 32q..32q+31) and owns part pp of the row: keys [32pp, 32pp+32) of S and
   // head dims [32pp, 32pp+32) of O.  The four parts of a row exchange maxima and
   // sums through shared memory, ordered by a per-quarter mbarrier (bounded wait).
-  const bool softmax = warp >= 2;
+  const bool softmax = warp >= 2 && warp < kVWarp;
   const int q = warp & 3;
   const int pp = softmax ? (warp - 2) >> 2 : 0;
   const int r = q * 32 + lane;
@@ -518,15 +546,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const bool full = valid == 0xFFFFFFFFu;  // interior chunk: no per-element tests
       float pmax = -INFINITY;
       if (full) {
-        float a0 = fmaxf(v[0], v[1]), a1 = fmaxf(v[2], v[3]), a2 = fmaxf(v[4], v[5]), a3 = fmaxf(v[6], v[7]);
+        float a0 = fmax3f(v[0], v[1], v[2]), a1 = fmax3f(v[3], v[4], v[5]);
+        float a2 = fmax3f(v[6], v[7], v[8]), a3 = fmax3f(v[9], v[10], v[11]);
 #pragma unroll
-        for (int j = 8; j < 32; j += 8) {
-          a0 = fmaxf(a0, fmaxf(v[j], v[j + 1]));
-          a1 = fmaxf(a1, fmaxf(v[j + 2], v[j + 3]));
-          a2 = fmaxf(a2, fmaxf(v[j + 4], v[j + 5]));
-          a3 = fmaxf(a3, fmaxf(v[j + 6], v[j + 7]));
+        for (int j = 12; j < 28; j += 8) {
+          a0 = fmax3f(a0, v[j], v[j + 1]);
+          a1 = fmax3f(a1, v[j + 2], v[j + 3]);
+          a2 = fmax3f(a2, v[j + 4], v[j + 5]);
+          a3 = fmax3f(a3, v[j + 6], v[j + 7]);
         }
-        pmax = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c2;
+        a0 = fmax3f(a0, v[28], v[29]);
+        a1 = fmax3f(a1, v[30], v[31]);
+        pmax = fmax3f(a0, a1, fmaxf(a2, a3)) * c2;
       } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -536,14 +567,46 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       fence_before();  // this part's S loads are done before the others overwrite S with P
       __syncwarp();    // the warp's s_max writes, then one arrival for the warp
       if (lane == 0) bar_arrive(&xch[q]);
+      // probabilities of this part's 32 keys against base -nsub, packed to bf16 pairs
+      uint32_t pk[16];
+      float rs = 0.0f;
+      auto probs = [&](float nsub) {
+        const float2 c2v = make_float2(c2, c2), nv = make_float2(nsub, nsub);
+        float2 acc = make_float2(0.0f, 0.0f);
+        if (full) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 a = __ffma2_rn(make_float2(v[j], v[j + 1]), c2v, nv);
+            const float e0 = fast_exp2(a.x), e1 = fast_exp2(a.y);
+            acc = __fadd2_rn(acc, make_float2(e0, e1));
+            pk[j >> 1] = pack2_bf16(e0, e1);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float2 a = __ffma2_rn(make_float2(v[j], v[j + 1]), c2v, nv);
+            const float e0 = ((valid >> j) & 1u) ? fast_exp2(a.x) : 0.0f;
+            const float e1 = ((valid >> (j + 1)) & 1u) ? fast_exp2(a.y) : 0.0f;
+            acc = __fadd2_rn(acc, make_float2(e0, e1));
+            pk[j >> 1] = pack2_bf16(e0, e1);
+          }
+        }
+        rs = acc.x + acc.y;
+      };
+      // While the other parts' maxima arrive, the probabilities are computed against
+      // the current base.  They are final unless some part of the row exceeds the base
+      // by more than 2^kLazy (the first tile always does); then the tile is redone
+      // below against the moved base.
+      const bool spec = __all_sync(0xFFFFFFFFu, m != -INFINITY);
+      if (spec) probs(-m);
       if (!bar_wait(&xch[q], t & 1, abort)) {
         live = false;
         break;
       }
       fence_after();
-      float tmax = s_max[((t & 1) * 4) * kRows + r];
-#pragma unroll
-      for (int x = 1; x < 4; ++x) tmax = fmaxf(tmax, s_max[((t & 1) * 4 + x) * kRows + r]);
+      const float tmax = fmaxf(fmax3f(s_max[((t & 1) * 4) * kRows + r], s_max[((t & 1) * 4 + 1) * kRows + r],
+                                      s_max[((t & 1) * 4 + 2) * kRows + r]),
+                               s_max[((t & 1) * 4 + 3) * kRows + r]);
       // The base moves only when the tile's maximum exceeds it by more than 2^8; then
       // O (tiles 0..t-1, which needs PV(t-1) completed) is rescaled in TMEM, warp-
       // wide (lanes whose base stays multiply by 1).  Each thread waits every phase
@@ -555,37 +618,25 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         l *= corr;
         m = tmax;
       }
+      const bool any_move = __any_sync(0xFFFFFFFFu, move);
       bool waited_prev = false;
-      if (t > 0 && __any_sync(0xFFFFFFFFu, move)) {
+      if (t > 0 && any_move) {
         if (!bar_wait(o_done, (t - 1) & 1, abort)) {
           live = false;
           break;
         }
         waited_prev = true;
         fence_after();
-        float ov[32];
-        tmem_ld32(tO + lane_base + pp * 32, ov);
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {  // in two halves, to keep register pressure low
+          float ov[16];
+          tmem_ld16f(tO + lane_base + pp * 32 + h * 16, ov);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ov[j] *= corr;
-        tmem_st32(tO + lane_base + pp * 32, ov);
-      }
-      const float nsub = (m == -INFINITY) ? 0.0f : -m;
-      // probabilities of this part's 32 keys, packed to bf16 pairs
-      uint32_t pk[16];
-      float rs = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        float e0, e1;
-        if (full) {
-          e0 = fast_exp2(fmaf(v[j], c2, nsub));
-          e1 = fast_exp2(fmaf(v[j + 1], c2, nsub));
-        } else {
-          e0 = ((valid >> j) & 1u) ? fast_exp2(fmaf(v[j], c2, nsub)) : 0.0f;
-          e1 = ((valid >> (j + 1)) & 1u) ? fast_exp2(fmaf(v[j + 1], c2, nsub)) : 0.0f;
+          for (int j = 0; j < 16; ++j) ov[j] *= corr;
+          tmem_st16f(tO + lane_base + pp * 32 + h * 16, ov);
         }
-        rs += e0 + e1;
-        pk[j >> 1] = pack2_bf16(e0, e1);
       }
+      if (!spec || any_move) probs((m == -INFINITY) ? 0.0f : -m);
       l += rs;
       if (t > 0 && !waited_prev && !bar_wait(o_done, (t - 1) & 1, abort)) {
         live = false;
