@@ -51,7 +51,11 @@ constexpr int kRowCache = 128;       // KV block rows looked up ahead
 constexpr int kThreads = 608;         // warp 0 K loads, warp 1 MMA, warps 2..17 softmax, warp 18 V loads
 constexpr int kVWarp = 18;
 constexpr int kSoftmaxThreads = 512;
-constexpr int kSmem = 1024 + kQBytes + 4 * kKVBytes + 256 + 12 * 128 * 4 + 4 * kRowCache + 64;
+// Cluster merge receive area: (128 + 15) rows (the most a CTA owns times 16 segments)
+// of bf16 partial o and float2 (m, l), written by every CTA of the cluster.
+constexpr int kRecvRows = kRows + 15;
+constexpr int kRecvBytes = kRecvRows * (kHD * 2 + 8);
+constexpr int kSmem = 1024 + kQBytes + 4 * kKVBytes + 256 + 12 * 128 * 4 + 4 * kRowCache + 64 + kRecvBytes + 16;
 constexpr float kLog2e = 1.4426950408889634f;
 static_assert(kQBytes == kKVBytes, "Q and K halves share the slice offsets");
 constexpr float kLazy = 8.0f;  // log2 headroom before the exponent base moves
@@ -181,16 +185,6 @@ __device__ __forceinline__ void tmem_st16f(uint32_t taddr, const float (&v)[16])
       "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]));
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
-      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]), "f"(v[9]),
-      "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]),
-      "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]),
-      "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31]));
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -200,15 +194,15 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t a, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
   return r;
 }
-// bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into another
-// CTA's, completing as transaction bytes on that CTA's mbarrier
-__device__ __forceinline__ void bulk_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "r"(src), "r"(bytes), "r"(bar)
-               : "memory");
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+// 16 bytes / 8 bytes into (possibly another CTA's) shared memory at a shared::cluster address
+__device__ __forceinline__ void st_cluster_v4(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ void st_cluster_v2f(uint32_t a, float x, float y) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
@@ -297,9 +291,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint64_t* v_empty = bars + 7;    // [2]
   uint64_t* s_full = bars + 9;     // [2]
   uint64_t* p_full = bars + 11;    // [2]
-  uint64_t* o_done = bars + 13;    // PV(t) completed (once per tile); bars + 14 unused
+  uint64_t* o_done = bars + 13;    // PV(t) completed (once per tile); bars + 14, 19 unused
   uint64_t* xch = bars + 15;       // [4] exchange among the four parts of a row, per lane quarter
-  uint64_t* recv_bar = bars + 19;  // cluster merge: the other CTAs' partial rows have landed here
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* s_max = reinterpret_cast<float*>(tmem_slot + 4);  // [2 parities][4 parts][128 rows]
@@ -323,7 +316,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
     for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], 4);  // one arrival per part (warp) of a lane quarter
     bar_init(o_done, 1);
-    bar_init(recv_bar, 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     bar_expect(q_full, kQBytes);
@@ -702,6 +694,32 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       dst[d] = make_float4(o[4 * d] * inv, o[4 * d + 1] * inv, o[4 * d + 2] * inv, o[4 * d + 3] * inv);
     if (pp == 0) ws_ml[rec] = make_float2(m, lt);
   }
+  // Cluster merge.  Row r of the group is owned (merged and written) by CTA r / rpc
+  // of the cluster.  Every CTA stores its normalized partial rows (bf16) and their
+  // (m, l) straight into the owners' receive areas -- a region of its own in each
+  // CTA's shared memory, so no CTA has to wait for another's tile loop before the
+  // stores -- then one cluster barrier publishes them and each CTA merges its rows.
+  const int rpc = CLUSTER ? (kRows + g.S - 1) / g.S : kRows;  // rows owned per CTA
+  unsigned char* recv = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(s_rows + kRowCache) + 15) & ~static_cast<uintptr_t>(15));
+  __nv_bfloat16* recv_o = reinterpret_cast<__nv_bfloat16*>(recv);         // [S][rpc][128]
+  float2* recv_ml = reinterpret_cast<float2*>(recv + kRecvRows * kHD * 2);  // [S][rpc]
+  if (CLUSTER && softmax) {
+    const bool ok = row_ok && !*abort;
+    const float inv = (ok && lt > 0.0f) ? 1.0f / lt : 0.0f;
+    const int ow = r / rpc, li = r - ow * rpc;
+    // this part's 32 head dims = 16-byte chunks 4pp..4pp+3 of the row, XOR-swizzled by
+    // the owner-local row so that the 32 lanes' stores spread over the banks
+    const uint32_t row = cluster_addr(su32(recv_o + static_cast<size_t>(s * rpc + li) * kHD), ow);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int slot = (4 * pp + k) ^ (li & 7);
+      st_cluster_v4(row + slot * 16, pack2_bf16(o[8 * k] * inv, o[8 * k + 1] * inv),
+                    pack2_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv), pack2_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
+                    pack2_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
+    }
+    if (pp == 0) st_cluster_v2f(cluster_addr(su32(recv_ml + s * rpc + li), ow), m, ok ? lt : 0.0f);
+  }
   // the Q load has landed (also where no tile was processed) before the CTA's
   // shared memory is reused or released
   if (threadIdx.x == 0 && !bar_wait_timed(q_full, 0)) *abort = 1;
@@ -710,68 +728,21 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   if (*abort && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
   if (CLUSTER) {
     const int S = g.S;
-    const int rpc = (kRows + S - 1) / S;  // rows owned (merged and written) per CTA
-    // Local staging of this CTA's normalized partial rows: o as [128 rows][128] fp32
-    // in the V ring (the 16-byte chunks of each 32-float part XOR-swizzled by row so
-    // that the row-per-lane writes do not collide in banks), (m, l) as float4 rows
-    // in the Q/K region past the receive area.  Receive area (written by the bulk
-    // copies of every CTA of the cluster, this one included): [S][rpc] o rows from
-    // the start of the Q buffer (Q and K rings are contiguous, 96 KB; at most
-    // (128 + S - 1) rows = 72 KB), then [S][rpc] (m, l) float4 rows.
-    float* stage_o = reinterpret_cast<float*>(sV);
-    float4* stage_ml = reinterpret_cast<float4*>(sQ + 76 * 1024);
-    float* recv_o = reinterpret_cast<float*>(sQ);
-    float4* recv_ml = reinterpret_cast<float4*>(sQ + static_cast<size_t>(S) * rpc * kHD * 4);
     const int n_own = max(0, min(rpc, kRows - s * rpc));
-    if (softmax) {
-      const bool ok = row_ok && !*abort;
-      const float inv = (ok && lt > 0.0f) ? 1.0f / lt : 0.0f;
-      float4* row = reinterpret_cast<float4*>(stage_o + r * kHD) + pp * 8;
-#pragma unroll
-      for (int d = 0; d < 8; ++d)
-        row[d ^ (r & 7)] = make_float4(o[4 * d] * inv, o[4 * d + 1] * inv, o[4 * d + 2] * inv, o[4 * d + 3] * inv);
-      if (pp == 0) stage_ml[r] = make_float4(m, ok ? lt : 0.0f, 0.0f, 0.0f);
-    }
-    fence_async_smem();  // staged rows -> bulk-copy engine
-    if (threadIdx.x == 0) bar_expect(recv_bar, static_cast<uint32_t>(S * n_own) * (kHD * 4 + 16));
-    __syncthreads();
-    // every CTA of the cluster is past its tile loop: receive areas are idle.  The
-    // barrier orders execution only (the tensor-core reads and TMA writes of those
-    // areas completed before the loop ended); the receive mbarrier's initialization
-    // was published by the release fence after it.
     __syncwarp();
-    cluster_arrive_relaxed();
+    cluster_arrive_release();  // publishes the stores above to the owners
     cluster_wait();
-    if (threadIdx.x == 0) {
-      const uint32_t bar_local = su32(recv_bar);
-      for (int ow = 0; ow < S; ++ow) {
-        const int n = min(rpc, kRows - ow * rpc);
-        if (n <= 0) continue;
-        const uint32_t bar = cluster_addr(bar_local, ow);
-        bulk_to_peer(cluster_addr(su32(recv_o + static_cast<size_t>(s) * rpc * kHD), ow),
-                     su32(stage_o + static_cast<size_t>(ow) * rpc * kHD), n * kHD * 4, bar);
-        bulk_to_peer(cluster_addr(su32(recv_ml + s * rpc), ow), su32(stage_ml + ow * rpc), n * 16, bar);
-      }
-    }
-    // inbound rows (time-bounded only: the copies are in flight whatever the abort flag says)
-    const bool got = bar_wait_timed(recv_bar, 0);
-    if (!got) *abort = 1;
-    // this CTA's inbound copies are complete (the matching wait before exit keeps
-    // every CTA's staging alive until all copies of the cluster have landed)
-    __syncwarp();
-    cluster_arrive_relaxed();  // control only: no data is published through this barrier
-    // merge: 16 threads per owned row, each with 8 head dims (two swizzled chunks)
-    for (int it = threadIdx.x; got && it < n_own * 16; it += kThreads) {
+    // merge: 16 threads per owned row, each with 8 head dims (one swizzled chunk)
+    for (int it = threadIdx.x; it < n_own * 16; it += kThreads) {
       const int li = it >> 4, c = it & 15;
       const int rr = s * rpc + li;
       const int grr = rg * kRows + rr;
       if (grr < g.G * g.R) {
         const int nd = grr / g.G, hh = kvh * g.G + grr % g.G;
-        const int c0 = (c >> 2) * 8 + (((2 * c) & 7) ^ (rr & 7));  // chunk of head dims 8c..8c+3
-        const int c1 = (c >> 2) * 8 + (((2 * c + 1) & 7) ^ (rr & 7));
+        const int slot = c ^ (li & 7);
         float M = -INFINITY;
         for (int sg = 0; sg < S; ++sg) {
-          const float4 ml = recv_ml[sg * rpc + li];
+          const float2 ml = recv_ml[sg * rpc + li];
           if (ml.y > 0.0f) M = fmaxf(M, ml.x);
         }
         float den = 0.0f;
@@ -779,19 +750,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 #pragma unroll
         for (int j = 0; j < 8; ++j) a[j] = 0.0f;
         for (int sg = 0; sg < S; ++sg) {
-          const float4 ml = recv_ml[sg * rpc + li];
+          const float2 ml = recv_ml[sg * rpc + li];
           const float w = ml.y > 0.0f ? ml.y * fast_exp2(ml.x - M) : 0.0f;
           den += w;
-          const float4* rowp = reinterpret_cast<const float4*>(recv_o + (static_cast<size_t>(sg) * rpc + li) * kHD);
-          const float4 v0 = rowp[c0], v1 = rowp[c1];
-          a[0] = fmaf(w, v0.x, a[0]);
-          a[1] = fmaf(w, v0.y, a[1]);
-          a[2] = fmaf(w, v0.z, a[2]);
-          a[3] = fmaf(w, v0.w, a[3]);
-          a[4] = fmaf(w, v1.x, a[4]);
-          a[5] = fmaf(w, v1.y, a[5]);
-          a[6] = fmaf(w, v1.z, a[6]);
-          a[7] = fmaf(w, v1.w, a[7]);
+          const uint4 raw = reinterpret_cast<const uint4*>(recv_o + static_cast<size_t>(sg * rpc + li) * kHD)[slot];
+          const uint32_t wd[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            a[2 * j] = fmaf(w, __uint_as_float(wd[j] << 16), a[2 * j]);
+            a[2 * j + 1] = fmaf(w, __uint_as_float(wd[j] & 0xFFFF0000u), a[2 * j + 1]);
+          }
         }
         const float inv = den > 0.0f ? 1.0f / den : 0.0f;
         const size_t orow = (static_cast<size_t>(b) * g.R + nd) * g.H + hh;
@@ -804,8 +772,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         if (c == 0) lse[orow] = (M + __log2f(den)) * 0.6931471805599453f;
       }
     }
-    if (!got && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
-    cluster_wait();
   }
   if (warp == 1) {
     __syncwarp();
