@@ -72,7 +72,12 @@ __device__ __forceinline__ float fx_exp(float x) {
   const float kLn2Hi = 0x1.62e4p-1f;
   const float kLn2Lo = 0x1.7f7d1cp-20f;
   float t = __fmul_rn(x, kLog2e);
-  float n = rintf(t);
+  // n = rint(t) (ties to even) and its integer value, from t + 1.5 * 2^23: the sum
+  // rounds t to an integer exactly as rint does for |t| < 2^22, and its low
+  // mantissa bits are that integer (for larger |t| the result is zeroed below)
+  const float tm = __fadd_rn(t, 0x1.8p23f);
+  const float n = __fsub_rn(tm, 0x1.8p23f);
+  const int ni = static_cast<int>(__float_as_uint(tm) - 0x4B400000u);
   float r = __fmaf_rn(-n, kLn2Hi, x);
   r = __fmaf_rn(-n, kLn2Lo, r);
   float p = 0x1.a01a02p-13f;
@@ -83,7 +88,7 @@ __device__ __forceinline__ float fx_exp(float x) {
   p = __fmaf_rn(p, r, 0.5f);
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
-  float scale = __int_as_float((static_cast<int>(n) + 127) << 23);
+  float scale = __uint_as_float(static_cast<uint32_t>(ni + 127) << 23);
   return __fmul_rn(p, scale);
 }
 
@@ -110,8 +115,12 @@ __device__ __forceinline__ float2 fx_exp_x2(float2 x) {
   const float2 kLn2Hi = make_float2(0x1.62e4p-1f, 0x1.62e4p-1f);
   const float2 kLn2Lo = make_float2(0x1.7f7d1cp-20f, 0x1.7f7d1cp-20f);
   const float2 t = __fmul2_rn(x, kLog2e);
-  const float2 n = make_float2(rintf(t.x), rintf(t.y));
-  const float2 nn = make_float2(-n.x, -n.y);
+  // rint(t) and its integer value per lane, as in fx_exp (scalar adds: a paired
+  // add may be contracted with the paired multiply above into one fused operation)
+  const float2 tm = make_float2(__fadd_rn(t.x, 0x1.8p23f), __fadd_rn(t.y, 0x1.8p23f));
+  const float2 nn = make_float2(__fsub_rn(0x1.8p23f, tm.x), __fsub_rn(0x1.8p23f, tm.y));  // -n
+  const int nix = static_cast<int>(__float_as_uint(tm.x) - 0x4B400000u);
+  const int niy = static_cast<int>(__float_as_uint(tm.y) - 0x4B400000u);
   float2 r = __ffma2_rn(nn, kLn2Hi, x);
   r = __ffma2_rn(nn, kLn2Lo, r);
   float2 p = make_float2(0x1.a01a02p-13f, 0x1.a01a02p-13f);
@@ -122,8 +131,8 @@ __device__ __forceinline__ float2 fx_exp_x2(float2 x) {
   p = __ffma2_rn(p, r, make_float2(0.5f, 0.5f));
   p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
   p = __ffma2_rn(p, r, make_float2(1.0f, 1.0f));
-  const float2 scale = make_float2(__int_as_float((static_cast<int>(n.x) + 127) << 23),
-                                   __int_as_float((static_cast<int>(n.y) + 127) << 23));
+  const float2 scale = make_float2(__uint_as_float(static_cast<uint32_t>(nix + 127) << 23),
+                                   __uint_as_float(static_cast<uint32_t>(niy + 127) << 23));
   float2 e = __fmul2_rn(p, scale);
   if (x.x < -32.0f) e.x = 0.0f;
   if (x.y < -32.0f) e.y = 0.0f;

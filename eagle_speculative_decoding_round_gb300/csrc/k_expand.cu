@@ -171,6 +171,9 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   }
   // no thread polls a barrier before thread 0 has initialized it
   __syncthreads();
+  // the peers' mbarriers are initialized before anyone arrives on them (waited
+  // for just before the first exchange)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   // the chunk is staged by the bulk copies above (16-byte aligned rows), else by
   // plain loads; then scaled by 1/T in place, with the per-thread maximum (first occurrence of the
@@ -208,12 +211,20 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   const uint64_t tmax = bid == 0xFFFFFFFFu ? 0ull : pack_best(bv, bid);
   // the dependent frontier kernel may be scheduled (it waits for this grid to finish)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // the peers' mbarriers are initialized before anyone arrives on them
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   const uint64_t wmax = warp_reduce(tmax, MaxU64());
   if (lane == 0) s_wmax[warp] = wmax;
   if (threadIdx.x == 0) s_cnt = 0;
   bad = __syncthreads_or(bad);
+  // send this CTA's maximum key and flag to every CTA of the cluster now; the
+  // candidate selection below runs while they travel
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (threadIdx.x < CL) {
+    uint64_t lbest = 0ull;
+    for (int w = 0; w < kExpandThreads / 32; ++w) lbest = max(lbest, s_wmax[w]);
+    cl_st64(cl_addr(&s_pmax[rank], threadIdx.x), lbest);
+    cl_st32(cl_addr(&s_pbad[rank], threadIdx.x), static_cast<uint32_t>(bad));
+    cl_arrive(cl_addr(&mx_bar, threadIdx.x));
+  }
   // each thread visits the chunk elements it staged: float4 slots q - v0 (vec) or j - v0
   auto for_own = [&](auto&& fn) {
     if (vec) {
@@ -286,15 +297,6 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     for (int j = 0; j < ncand; ++j) rnk += cand[j] > key;
     if (rnk < k) ltop[rnk] = key;
   }
-  // send this CTA's maximum key and flag to every CTA of the cluster
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  if (threadIdx.x < CL) {
-    uint64_t lbest = 0ull;
-    for (int w = 0; w < kExpandThreads / 32; ++w) lbest = max(lbest, s_wmax[w]);
-    cl_st64(cl_addr(&s_pmax[rank], threadIdx.x), lbest);
-    cl_st32(cl_addr(&s_pbad[rank], threadIdx.x), static_cast<uint32_t>(bad));
-    cl_arrive(cl_addr(&mx_bar, threadIdx.x));
-  }
   const bool got = mb_wait0(&mx_bar);
   uint64_t gbest = 0ull;
   uint32_t gbad = got ? 0u : 1u;
@@ -332,15 +334,13 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     if (threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
     return;
   }
-  const int nall = CL * k;
-  if (threadIdx.x < E3_MAX_TOPK) top[threadIdx.x] = 0ull;
-  __syncthreads();
-  for (int i = threadIdx.x; i < nall; i += blockDim.x) {
-    const uint64_t key = s_ptop[i];
-    if (key == 0ull) continue;
-    int rnk = 0;
-    for (int j = 0; j < nall; ++j) rnk += s_ptop[j] > key;
-    if (rnk < k) top[rnk] = key;
+  // every CTA's list is sorted (best first, zero-padded): warp 0 merges them, one
+  // list per lane
+  if (warp == 0) {
+    uint64_t lk[KMAX];
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) lk[i] = (lane < CL && i < k) ? s_ptop[lane * k + i] : 0ull;
+    warp_merge_topk(lk, k, top);
   }
   __shared__ uint64_t s_Qt;
   if (threadIdx.x == 0) {
