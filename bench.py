@@ -57,8 +57,10 @@ TRAFFIC = {
 TAB_ROWS = 4096  # token-keyed Q/K/V tables of the synthetic target (token id modulo this)
 
 
-def cfg_values(name, seed):
+def cfg_values(name, seed, layers=None):
     c = dict(CONFIGS[name])
+    if layers:
+        c["L"] = int(layers)
     rng = np.random.default_rng(seed)
     if isinstance(c["P"], str):
         lo, hi = (int(x) for x in c["P"].split(":")[1:])
@@ -73,7 +75,7 @@ def cfg_values(name, seed):
 # ---------------------------------------------------------------------------
 
 class Workload:
-    def __init__(self, name, seed=0, device="cuda"):
+    def __init__(self, name, seed=0, device="cuda", layers=None):
         import torch
 
         from eagle_speculative_decoding_round_gb300 import eagle3 as e3
@@ -81,7 +83,7 @@ class Workload:
         from eagle_speculative_decoding_round_gb300.round import RoundBuffers, RoundConfig
 
         self.torch, self.e3, self.synth = torch, e3, synth
-        c = cfg_values(name, seed)
+        c = cfg_values(name, seed, layers)
         self.name, self.c, self.seed = name, c, seed
         R = c["N"] + 1
         self.cfg = RoundConfig(B=c["B"], N=c["N"], D=c["D"], k=c["k"], W=c["W"], H=c["H"], KVH=c["KVH"],
@@ -380,6 +382,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="profiling only: fewer target layers than the configuration (small ncu captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -394,7 +398,7 @@ def main():
     if args.impl == "reference":
         return reference_arm(args, rank, world)
     torch.cuda.set_device(local)
-    w = Workload(args.config, seed=args.seed + 1000 * rank)
+    w = Workload(args.config, seed=args.seed + 1000 * rank, layers=args.layers)
     cfg = w.cfg
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
