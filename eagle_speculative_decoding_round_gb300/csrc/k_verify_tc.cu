@@ -152,6 +152,41 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 __device__ __forceinline__ void umma_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b)) : "memory");
 }
+// 32 consecutive 32-bit TMEM columns of this thread's lane as 16 register pairs
+// (columns 2i, 2i+1 in v[2i], v[2i+1]), so that paired fp32 operations take them
+// without register moves
+__device__ __forceinline__ void tmem_ld32p(uint32_t taddr, float (&v)[32]) {
+  unsigned long long q[16];
+  asm volatile(
+      "{\n .reg .b32 t<32>;\n"
+      " tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%16];\n"
+      " tcgen05.wait::ld.sync.aligned;\n"
+      " mov.b64 %0, {t0, t1};\n"
+      " mov.b64 %1, {t2, t3};\n"
+      " mov.b64 %2, {t4, t5};\n"
+      " mov.b64 %3, {t6, t7};\n"
+      " mov.b64 %4, {t8, t9};\n"
+      " mov.b64 %5, {t10, t11};\n"
+      " mov.b64 %6, {t12, t13};\n"
+      " mov.b64 %7, {t14, t15};\n"
+      " mov.b64 %8, {t16, t17};\n"
+      " mov.b64 %9, {t18, t19};\n"
+      " mov.b64 %10, {t20, t21};\n"
+      " mov.b64 %11, {t22, t23};\n"
+      " mov.b64 %12, {t24, t25};\n"
+      " mov.b64 %13, {t26, t27};\n"
+      " mov.b64 %14, {t28, t29};\n"
+      " mov.b64 %15, {t30, t31};\n"
+      "}\n"
+      : "=l"(q[0]), "=l"(q[1]), "=l"(q[2]), "=l"(q[3]), "=l"(q[4]), "=l"(q[5]), "=l"(q[6]), "=l"(q[7]), "=l"(q[8]), "=l"(q[9]), "=l"(q[10]), "=l"(q[11]), "=l"(q[12]), "=l"(q[13]), "=l"(q[14]), "=l"(q[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[2 * i] = __uint_as_float(static_cast<uint32_t>(q[i]));
+    v[2 * i + 1] = __uint_as_float(static_cast<uint32_t>(q[i] >> 32));
+  }
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -531,7 +566,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
       fence_after();
       float v[32];
-      tmem_ld32(tS(bb) + lane_base + pp * 32, v);  // this part's 32 scores
+      tmem_ld32p(tS(bb) + lane_base + pp * 32, v);  // this part's 32 scores
       const int Tc = T0 + pp * 32;
       uint32_t valid = range_bits32(Tc, k0, k1);
       if (tree) valid &= mask_bits32(mrow, words, Tc - P);
