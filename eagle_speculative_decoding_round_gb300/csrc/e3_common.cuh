@@ -2,6 +2,8 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <utility>
 #include <stdint.h>
 
 #include "../../include/eagle3.h"
@@ -26,6 +28,44 @@ e3_status cuda_status(cudaError_t e, const char* what);
 void note_launch();
 
 // After one kernel launch: report a launch error, else count the launch.
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialization and calls pdl_wait() before its first access
+// to global memory, which returns once the preceding kernel has completed and its
+// writes are visible; so only the launch itself (and setup in shared or tensor
+// memory) overlaps the predecessor, never work on its results.  pdl_trigger()
+// lets the next kernel be scheduled early (it waits the same way).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// cudaLaunchKernelEx with programmatic stream serialization and, for cluster_x > 1,
+// clusters of cluster_x CTAs along x.  Counts the launch when it succeeds.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  int n = 0;
+  at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    at[n].id = cudaLaunchAttributeClusterDimension;
+    at[n].val.clusterDim.x = cluster_x;
+    at[n].val.clusterDim.y = 1;
+    at[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = n;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+  if (e == cudaSuccess) note_launch();
+  return e;
+}
+
 #define E3_LAUNCH_CHECK(what)                                   \
   do {                                                          \
     cudaError_t _e = cudaGetLastError();                        \

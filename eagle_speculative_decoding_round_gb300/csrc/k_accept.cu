@@ -54,6 +54,8 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
   __shared__ unsigned long long s_x, s_sum;
   __shared__ unsigned long long s_wsum[kAcceptThreads / 32];
 
+  pdl_wait();
+  pdl_trigger();
   const size_t rb = static_cast<size_t>(b) * R;
   const float T = temp[b];
   const float it = inv_temp(T);
@@ -274,22 +276,10 @@ e3_status launch_accept(const int32_t* tok, const int32_t* parent, int B, int R,
   const size_t smem = static_cast<size_t>((V + CL - 1) / CL) * sizeof(unsigned long long) + 16;
   E3_REQUIRE(smem <= 200 * 1024, E3_ERR_SHAPE, "spec_accept: V=%d too large", V);
   E3_REQUIRE(static_cast<long>(B) * CL < (1L << 31), E3_ERR_SHAPE, "spec_accept: B=%d too large", B);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(B * CL);
-  cfg.blockDim = dim3(kAcceptThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute at;
-  at.id = cudaLaunchAttributeClusterDimension;
-  at.val.clusterDim.x = CL;
-  at.val.clusterDim.y = 1;
-  at.val.clusterDim.z = 1;
-  cfg.attrs = &at;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, accept_kernel, tok, parent, R, D, logits, row_max, row_Q, row_argmax, V,
-                                     temp, u_acc, u_bonus, acc_len, path, out_tok, status);
+  cudaError_t e = launch_pdl(accept_kernel, dim3(B * CL), dim3(kAcceptThreads), smem, s, static_cast<unsigned>(CL), tok,
+                             parent, R, D, logits, row_max, row_Q, row_argmax, V, temp, u_acc, u_bonus, acc_len, path,
+                             out_tok, status);
   if (e != cudaSuccess) return cuda_status(e, "accept_kernel");
-  note_launch();
   return E3_OK;
 }
 

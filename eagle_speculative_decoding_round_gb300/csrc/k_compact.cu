@@ -34,6 +34,8 @@ __global__ void __launch_bounds__(128)
 compact_kernel(CompactLayers layers, e3_kv_layer geo, int D, const int32_t* __restrict__ path,
                const int32_t* __restrict__ acc_len, const int32_t* __restrict__ kv_len, int32_t* dev_err) {
   __shared__ __align__(16) uint4 buf[2 * E3_MAX_DEPTH * 64];  // up to 2 x 16 rows x 1 KiB
+  pdl_wait();
+  pdl_trigger();
   const int l = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int a = acc_len[b];
   if (a <= 0) return;
@@ -75,6 +77,8 @@ compact_kernel(CompactLayers layers, e3_kv_layer geo, int D, const int32_t* __re
 }
 
 __global__ void kv_len_update_kernel(int B, const int32_t* __restrict__ acc_len, int32_t* kv_len) {
+  pdl_wait();  // compact_kernel has read kv_len
+  pdl_trigger();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < B) kv_len[b] += 1 + acc_len[b];
 }
@@ -83,11 +87,11 @@ __global__ void kv_len_update_kernel(int B, const int32_t* __restrict__ acc_len,
 
 e3_status launch_compact(const CompactLayers& layers, const e3_kv_layer& geo, int L, int B, const int32_t* path,
                          const int32_t* acc_len, int D, int32_t* kv_len, int32_t* dev_err, cudaStream_t s) {
-  dim3 grid(L, geo.n_kv_heads, B);
-  compact_kernel<<<grid, 128, 0, s>>>(layers, geo, D, path, acc_len, kv_len, dev_err);
-  E3_LAUNCH_CHECK("compact_kernel");
-  kv_len_update_kernel<<<(B + 255) / 256, 256, 0, s>>>(B, acc_len, kv_len);
-  E3_LAUNCH_CHECK("kv_len_update_kernel");
+  cudaError_t e = launch_pdl(compact_kernel, dim3(L, geo.n_kv_heads, B), dim3(128), 0, s, 1, layers, geo, D, path,
+                             acc_len, static_cast<const int32_t*>(kv_len), dev_err);
+  if (e != cudaSuccess) return cuda_status(e, "compact_kernel");
+  e = launch_pdl(kv_len_update_kernel, dim3((B + 255) / 256), dim3(256), 0, s, 1, B, acc_len, kv_len);
+  if (e != cudaSuccess) return cuda_status(e, "kv_len_update_kernel");
   return E3_OK;
 }
 

@@ -150,6 +150,7 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   float* chunk = reinterpret_cast<float*>(chunk4);
   const int e0 = vec ? 4 * v0 : v0;  // token id of chunk[0]
   const int n_local = vec ? 4 * (v1 - v0) : (v1 - v0);
+  pdl_wait();  // the previous depth's frontier (parent ids and scores) is complete
   if (threadIdx.x == 0) {
     mb_init(&mx_bar, CL);
     mb_init(&fin_bar, CL);
@@ -210,7 +211,7 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   }
   const uint64_t tmax = bid == 0xFFFFFFFFu ? 0ull : pack_best(bv, bid);
   // the dependent frontier kernel may be scheduled (it waits for this grid to finish)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  pdl_trigger();
   const uint64_t wmax = warp_reduce(tmax, MaxU64());
   if (lane == 0) s_wmax[warp] = wmax;
   if (threadIdx.x == 0) s_cnt = 0;
@@ -407,22 +408,10 @@ e3_status launch_rows(const float* logits, int rows, int F, int V, int k, float 
   const int cand_cap = expand_cand_cap(V, vec, k, CL);
   const size_t smem = expand_smem_bytes(V, vec, k, CL);
   E3_REQUIRE(smem <= 200 * 1024, E3_ERR_SHAPE, "eagle3_expand: V=%d too large", V);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(rows * CL);
-  cfg.blockDim = dim3(kExpandThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute at;
-  at.id = cudaLaunchAttributeClusterDimension;
-  at.val.clusterDim.x = CL;
-  at.val.clusterDim.y = 1;
-  at.val.clusterDim.z = 1;
-  cfg.attrs = &at;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, expand_rows_kernel<KMAX>, logits, F, V, k, inv_temp, parent_score,
-                                     parent_id, depth, cand_offset, c, dev_err, cand_cap);
+  const cudaError_t e = launch_pdl(expand_rows_kernel<KMAX>, dim3(rows * CL), dim3(kExpandThreads), smem, s,
+                                   static_cast<unsigned>(CL), logits, F, V, k, inv_temp, parent_score, parent_id, depth,
+                                   cand_offset, c, dev_err, cand_cap);
   if (e != cudaSuccess) return cuda_status(e, "expand_rows_kernel");
-  note_launch();
   return E3_OK;
 }
 
@@ -434,7 +423,8 @@ __global__ void __launch_bounds__(256)
 expand_frontier_kernel(int n, int Wn, int cand_offset, e3_cand c, int32_t* next_id, float* next_score,
                        const int32_t* dev_err) {
   // launched as a programmatic dependent of the row kernel: wait for its results
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint64_t keys[2048];
   const int b = blockIdx.x;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {

@@ -153,6 +153,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2, int Nw, int Mx,
                int kb_per_src, int kb_total, int kb_per_split, float* __restrict__ out, int32_t* dev_err) {
   using C = TcCfg<BN>;
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
@@ -253,6 +255,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // g[m][o] = bf16(sum_z part[z][m][o] + bias[o])
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, int splits, int Mx, int Nw,
                                      const float* __restrict__ bias, __nv_bfloat16* __restrict__ g) {
+  pdl_wait();
+  pdl_trigger();
   const size_t n = static_cast<size_t>(Mx) * Nw;
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
@@ -296,6 +300,8 @@ lmhead_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
               int kb_total, int n_mt, int n_tiles, float* __restrict__ logits, unsigned long long* __restrict__ best,
               const float* __restrict__ temp, int32_t* dev_err) {
   using C = LmCfg<BN>;
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
@@ -468,6 +474,8 @@ row_q_kernel(const float* __restrict__ logits, int V, const float* __restrict__ 
   __shared__ int part_bad;
   const int rank = static_cast<int>(cluster.block_rank());
   const int m = blockIdx.x / kRowQCluster;
+  pdl_wait();
+  pdl_trigger();
   const float4* z4 = reinterpret_cast<const float4*>(logits + static_cast<size_t>(m) * V);
   const float it = inv_temp(temp[m]);
   const uint64_t best = row_Q[m];
@@ -554,9 +562,9 @@ e3_status launch_fuse_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUte
   }
   const int kb_per_split = (kb_total + splits - 1) / splits;  // callers pass splits with no empty split
   dim3 grid((Mx + BN - 1) / BN, (Nw + BM - 1) / BM, splits);
-  tc_gemm_kernel<BN, kModePartial><<<grid, 192, C::SMEM, s>>>(a, b0, b1, b2, Nw, Mx, kb_per_src, kb_total,
-                                                             kb_per_split, out, dev_err);
-  E3_LAUNCH_CHECK("tc_gemm_kernel");
+  const cudaError_t e = launch_pdl(tc_gemm_kernel<BN, kModePartial>, grid, dim3(192), C::SMEM, s, 1, a, b0, b1, b2, Nw,
+                                   Mx, kb_per_src, kb_total, kb_per_split, out, dev_err);
+  if (e != cudaSuccess) return cuda_status(e, "tc_gemm_kernel");
   return E3_OK;
 }
 
@@ -616,8 +624,10 @@ e3_status launch_fuse_tc(const void* h_low, const void* h_mid, const void* h_hig
   if (st != E3_OK) return st;
   const size_t n = static_cast<size_t>(M) * d_out;
   const int blocks = static_cast<int>(std::min<size_t>((n + 255) / 256, 4096));
-  splitk_reduce_kernel<<<blocks, 256, 0, s>>>(part, splits, M, d_out, bias, static_cast<__nv_bfloat16*>(g));
-  E3_LAUNCH_CHECK("splitk_reduce_kernel");
+  const cudaError_t e = launch_pdl(splitk_reduce_kernel, dim3(blocks), dim3(256), 0, s, 1,
+                                   static_cast<const float*>(part), splits, M, d_out, bias,
+                                   static_cast<__nv_bfloat16*>(g));
+  if (e != cudaSuccess) return cuda_status(e, "splitk_reduce_kernel");
   return E3_OK;
 }
 
@@ -642,9 +652,9 @@ e3_status launch_lmhead_bn(const CUtensorMap& a, const CUtensorMap& b, int V, in
   const long n_tiles = static_cast<long>(n_mt) * n_vt;
   E3_REQUIRE(n_tiles < (1L << 31), E3_ERR_SHAPE, "lmhead_logits: %ld tiles", n_tiles);
   const int grid = static_cast<int>(std::min<long>(n_tiles, n_sm));
-  lmhead_kernel<BN><<<grid, 192, C::SMEM, s>>>(a, b, V, M, kb_total, n_mt, static_cast<int>(n_tiles), logits, best,
-                                               temp, dev_err);
-  E3_LAUNCH_CHECK("lmhead_kernel");
+  const cudaError_t e = launch_pdl(lmhead_kernel<BN>, dim3(grid), dim3(192), C::SMEM, s, 1, a, b, V, M, kb_total, n_mt,
+                                   static_cast<int>(n_tiles), logits, best, temp, dev_err);
+  if (e != cudaSuccess) return cuda_status(e, "lmhead_kernel");
   return E3_OK;
 }
 
@@ -666,21 +676,10 @@ e3_status launch_lmhead_tc(const void* h, const void* W_lm, int M, int d, int V,
     default: st = launch_lmhead_bn<256>(a, b, V, M, kb, logits, best, temp, dev_err, s); break;
   }
   if (st != E3_OK) return st;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(M) * kRowQCluster);
-  cfg.blockDim = dim3(kRowQThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute at;
-  at.id = cudaLaunchAttributeClusterDimension;
-  at.val.clusterDim.x = kRowQCluster;
-  at.val.clusterDim.y = 1;
-  at.val.clusterDim.z = 1;
-  cfg.attrs = &at;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, row_q_kernel, static_cast<const float*>(logits), V, temp, row_max, row_Q, row_argmax);
+  e = launch_pdl(row_q_kernel, dim3(static_cast<unsigned>(M) * kRowQCluster), dim3(kRowQThreads), 0, s,
+                 static_cast<unsigned>(kRowQCluster), static_cast<const float*>(logits), V, temp, row_max, row_Q,
+                 row_argmax);
   if (e != cudaSuccess) return cuda_status(e, "row_q_kernel");
-  note_launch();
   return E3_OK;
 }
 

@@ -55,6 +55,8 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
                   int32_t* pos, uint64_t* mask) {
   extern __shared__ uint64_t sh[];
   uint64_t* keys = sh;  // [2 * max(np, blockDim.x)]: the two exchange buffers, or the in-place sort
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   int np = 1;
   while (np < n_cand) np <<= 1;
@@ -173,8 +175,9 @@ e3_status launch_tree_build(const e3_cand& c, int B, int n_cand, int N, const in
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_status(e, "tree_build_kernel smem attribute");
   }
-  tree_build_kernel<<<B, threads, smem, s>>>(c, n_cand, N, root_tok, kv_len, tok, parent, depth, pos, mask);
-  E3_LAUNCH_CHECK("tree_build_kernel");
+  const cudaError_t e = launch_pdl(tree_build_kernel, dim3(B), dim3(threads), smem, s, 1, c, n_cand, N, root_tok, kv_len,
+                                   tok, parent, depth, pos, mask);
+  if (e != cudaSuccess) return cuda_status(e, "tree_build_kernel");
   return E3_OK;
 }
 

@@ -403,6 +403,8 @@ verify_merge_kernel(e3_kv_layer kv, const int32_t* __restrict__ kv_len, VerifyGe
                     const float* __restrict__ ws_o, const float2* __restrict__ ws_ml, T* __restrict__ O,
                     float* __restrict__ lse) {
   constexpr int PER = HD / 32;
+  pdl_wait();  // the segment kernel's partial records are complete
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long row = static_cast<long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const long nrows = static_cast<long>(g.B) * g.R * g.H;
@@ -580,8 +582,10 @@ e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_
   }
   const long nrows = static_cast<long>(B) * R * H;
   const int blocks = static_cast<int>((nrows + 7) / 8);
-#define E3_MERGE_CASE(TT, HDV) \
-  verify_merge_kernel<TT, HDV><<<blocks, 256, 0, s>>>(kv, kv_len, g, ws_o, ws_ml, static_cast<TT*>(O), lse)
+  cudaError_t me = cudaSuccess;
+#define E3_MERGE_CASE(TT, HDV)                                                                               \
+  me = launch_pdl(verify_merge_kernel<TT, HDV>, dim3(blocks), dim3(256), 0, s, 1, kv, kv_len, g,                    \
+                  static_cast<const float*>(ws_o), static_cast<const float2*>(ws_ml), static_cast<TT*>(O), lse)
   if (kv.dt == E3_F32) {
     switch (hd) {
       case 32: E3_MERGE_CASE(float, 32); break;
@@ -606,7 +610,7 @@ e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_
     }
   }
 #undef E3_MERGE_CASE
-  E3_LAUNCH_CHECK("tree_verify_attn merge kernel");
+  if (me != cudaSuccess) return cuda_status(me, "tree_verify_attn merge kernel");
   return E3_OK;
 }
 

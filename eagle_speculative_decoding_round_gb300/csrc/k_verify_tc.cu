@@ -339,7 +339,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int nodes_per_tile = kRows / g.G;
   const int i0 = rg * nodes_per_tile;  // first node of this row group
-  if (threadIdx.x == 0) {  // barriers and the Q load first: neither depends on the request's length
+  if (threadIdx.x == 0) {  // barriers first: they depend on nothing in global memory
     bar_init(q_full, 1);
     for (int bb = 0; bb < 2; ++bb) {
       bar_init(&k_full[bb], 1);
@@ -353,6 +353,16 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     bar_init(o_done, 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)), "r"(512));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  // Launched as a programmatic dependent: everything above touches only this CTA's
+  // shared and tensor memory; nothing in global memory is read or written before
+  // the preceding kernel has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) {
     bar_expect(q_full, kQBytes);
     for (int h = 0; h < 2; ++h) tma3d(sQ + h * (kQBytes / 2), &tmQ, h * kHalf, kvh * g.G, b * g.R + i0, q_full);
   }
@@ -375,6 +385,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       if (blockIdx.x == 0 && kvh == 0) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
       bar_wait_timed(q_full, 0);  // the Q load lands before the CTA leaves
     }
+    // the tensor memory allocated above is released (uniform across the CTA: same request)
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(*tmem_slot), "r"(512));
     return;  // uniform across the cluster (same request)
   }
   // key ranges of this CTA: a prefix range [pk0, pk1) and, for the tree segment
@@ -454,10 +469,6 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       issue_kv(t, 1, &okp);
     }
     if (!okp) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)), "r"(512));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   fence_before();
   __syncthreads();
@@ -755,6 +766,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
     if (pp == 0) st_cluster_v2f(cluster_addr(su32(recv_ml + s * rpc + li), ow), m, ok ? lt : 0.0f);
   }
+  // the next kernel may be scheduled (it waits for this grid's completion before
+  // touching global memory)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // the Q load has landed (also where no tile was processed) before the CTA's
   // shared memory is reused or released
   if (threadIdx.x == 0 && !bar_wait_timed(q_full, 0)) *abort = 1;
@@ -949,13 +963,15 @@ e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* 
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmem;
     cfg.stream = s;
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeClusterDimension;
-    at.val.clusterDim.x = S;
-    at.val.clusterDim.y = 1;
-    at.val.clusterDim.z = 1;
-    cfg.attrs = &at;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = S;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // programmatic dependent launch
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelEx(&cfg, verify_tc_kernel<true>, mq, mk, mv, g, kv_len, mask, sm_scale, ws_o,
                                        ws_ml, static_cast<__nv_bfloat16*>(O), lse, dev_err);
     if (e != cudaSuccess) return cuda_status(e, "verify_tc_kernel (cluster)");
@@ -970,10 +986,20 @@ e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* 
     g.chunk = std::max(kHalf, ((max_kv_len + Sn - 1) / Sn + kHalf - 1) / kHalf * kHalf);
     *split = VerifySplit{Sn, Sn, g.chunk, 1};
   }
-  dim3 grid(g.RG * g.S, kv.n_kv_heads, B);
-  verify_tc_kernel<false><<<grid, kThreads, kSmem, s>>>(mq, mk, mv, g, kv_len, mask, sm_scale, ws_o, ws_ml,
-                                                   static_cast<__nv_bfloat16*>(O), lse, dev_err);
-  E3_LAUNCH_CHECK("verify_tc_kernel");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g.RG * g.S, kv.n_kv_heads, B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at;
+  at.id = cudaLaunchAttributeProgrammaticStreamSerialization;  // programmatic dependent launch
+  at.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, verify_tc_kernel<false>, mq, mk, mv, g, kv_len, mask, sm_scale, ws_o, ws_ml,
+                                     static_cast<__nv_bfloat16*>(O), lse, dev_err);
+  if (e != cudaSuccess) return cuda_status(e, "verify_tc_kernel");
+  note_launch();
   return E3_OK;
 }
 
