@@ -15,6 +15,44 @@ namespace {
 
 constexpr int BM = 64, BN = 64, BK = 16;
 
+// Few rows (M <= kSkinnyRows): one warp per output column n, the lanes striding
+// over k (coalesced rows of W and of A), one accumulator per row, then a warp
+// reduction.  Same definition as gemm_simt_kernel below.
+constexpr int kSkinnyRows = 16;
+template <typename T, typename TO>
+__global__ void __launch_bounds__(256)
+gemm_skinny_kernel(const T* __restrict__ a0, const T* __restrict__ a1, const T* __restrict__ a2, int dseg,
+                   const T* __restrict__ W, const float* __restrict__ bias, TO* __restrict__ out, int M, int N,
+                   int K) {
+  const int lane = threadIdx.x & 31;
+  const int n = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (n >= N) return;
+  float acc[kSkinnyRows];
+#pragma unroll
+  for (int m = 0; m < kSkinnyRows; ++m) acc[m] = 0.0f;
+  const T* wrow = W + static_cast<size_t>(n) * K;
+  for (int seg = 0; seg * dseg < K; ++seg) {
+    const T* src = seg == 0 ? a0 : (seg == 1 ? a1 : a2);
+    const int klen = min(dseg, K - seg * dseg);
+    for (int kin = lane; kin < klen; kin += 32) {
+      const float w = ld_elem(wrow, static_cast<size_t>(seg) * dseg + kin);
+#pragma unroll
+      for (int m = 0; m < kSkinnyRows; ++m)
+        if (m < M) acc[m] = fmaf(ld_elem(src, static_cast<size_t>(m) * dseg + kin), w, acc[m]);
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kSkinnyRows; ++m) {
+    float v = acc[m];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if (lane == 0 && m < M) {
+      if (bias) v += bias[n];
+      st_elem(out, static_cast<size_t>(m) * N + n, v);
+    }
+  }
+}
+
 // out[m][n] = sum_k A(m, k) * W[n][k]  (+ bias[n]); A(m, k) reads segment k / dseg.
 template <typename T, typename TO>
 __global__ void __launch_bounds__(256)
@@ -143,6 +181,27 @@ row_stats_kernel(const float* __restrict__ logits, int V, const float* __restric
 e3_status launch_gemm_simt(const void* a0, const void* a1, const void* a2, int dseg, const void* W,
                            const float* bias, void* out, bool out_f32, int M, int N, int K, e3_dtype dt,
                            cudaStream_t s) {
+  if (M <= kSkinnyRows) {
+    const dim3 sg((N + 7) / 8);
+    if (dt == E3_F32) {
+      if (!out_f32) return E3_ERR_UNSUPPORTED;
+      gemm_skinny_kernel<float, float><<<sg, 256, 0, s>>>(
+          static_cast<const float*>(a0), static_cast<const float*>(a1), static_cast<const float*>(a2), dseg,
+          static_cast<const float*>(W), bias, static_cast<float*>(out), M, N, K);
+    } else {
+      using B16 = __nv_bfloat16;
+      if (out_f32)
+        gemm_skinny_kernel<B16, float><<<sg, 256, 0, s>>>(
+            static_cast<const B16*>(a0), static_cast<const B16*>(a1), static_cast<const B16*>(a2), dseg,
+            static_cast<const B16*>(W), bias, static_cast<float*>(out), M, N, K);
+      else
+        gemm_skinny_kernel<B16, B16><<<sg, 256, 0, s>>>(
+            static_cast<const B16*>(a0), static_cast<const B16*>(a1), static_cast<const B16*>(a2), dseg,
+            static_cast<const B16*>(W), bias, static_cast<B16*>(out), M, N, K);
+    }
+    E3_LAUNCH_CHECK("gemm_skinny_kernel");
+    return E3_OK;
+  }
   dim3 grid((N + BN - 1) / BN, (M + BM - 1) / BM);
   if (dt == E3_F32) {
     if (out_f32)

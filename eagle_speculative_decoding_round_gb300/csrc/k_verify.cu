@@ -89,30 +89,57 @@ verify_simt_kernel(const T* __restrict__ Q, e3_kv_layer kv, const int32_t* __res
     }
     float m = -INFINITY, l = 0.0f;
     const uint64_t* mrow = mask + (static_cast<size_t>(b) * g.R + i) * words;
-    for (int kk = k0; kk < k1; ++kk) {
-      int t = kk;
-      if (tree) {
-        if (!((mrow[kk >> 6] >> (kk & 63)) & 1ull)) continue;
-        t = P + kk;
-      }
-      const T* kr = kv_row(Kb, kv, b, kvh, t);
-      const T* vr = kv_row(Vb, kv, b, kvh, t);
-      if (!kr || !vr) {
-        if (lane == 0) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
-        continue;
-      }
-      float d = 0.0f;
+    // keys in groups of kGrp: the group's K and V rows are loaded before any of its
+    // dot products is reduced, so that the loads overlap; the online-softmax updates
+    // then run in key order
+    constexpr int kGrp = 8;
+    for (int kb = k0; kb < k1; kb += kGrp) {
+      float kvals[kGrp][PER], vvals[kGrp][PER];
+      bool use[kGrp];
 #pragma unroll
-      for (int u = 0; u < PER; ++u) d = fmaf(qv[u], ld_elem(kr, lane + 32 * u), d);
-      d = warp_reduce(d, [](float a, float bb) { return a + bb; });
-      const float sc = d * c2;
-      const float mn = fmaxf(m, sc);
-      const float corr = exp2f(m - mn);  // m = -inf -> 0
-      const float p = exp2f(sc - mn);
-      l = l * corr + p;
+      for (int j = 0; j < kGrp; ++j) {
+        const int kk = kb + j;
+        use[j] = kk < k1;
+        int t = kk;
+        if (use[j] && tree) {
+          use[j] = (mrow[kk >> 6] >> (kk & 63)) & 1ull;
+          t = P + kk;
+        }
+        const T* kr = use[j] ? kv_row(Kb, kv, b, kvh, t) : nullptr;
+        const T* vr = use[j] ? kv_row(Vb, kv, b, kvh, t) : nullptr;
+        if (use[j] && (!kr || !vr)) {
+          if (lane == 0) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
+          use[j] = false;
+        }
 #pragma unroll
-      for (int u = 0; u < PER; ++u) acc[u] = fmaf(p, ld_elem(vr, lane + 32 * u), acc[u] * corr);
-      m = mn;
+        for (int u = 0; u < PER; ++u) {
+          kvals[j][u] = use[j] ? ld_elem(kr, lane + 32 * u) : 0.0f;
+          vvals[j][u] = use[j] ? ld_elem(vr, lane + 32 * u) : 0.0f;
+        }
+      }
+      float d[kGrp];
+#pragma unroll
+      for (int j = 0; j < kGrp; ++j) {
+        d[j] = 0.0f;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) d[j] = fmaf(qv[u], kvals[j][u], d[j]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < kGrp; ++j) d[j] += __shfl_xor_sync(0xFFFFFFFFu, d[j], o);
+#pragma unroll
+      for (int j = 0; j < kGrp; ++j) {
+        if (!use[j]) continue;
+        const float sc = d[j] * c2;
+        const float mn = fmaxf(m, sc);
+        const float corr = exp2f(m - mn);  // m = -inf -> 0
+        const float p = exp2f(sc - mn);
+        l = l * corr + p;
+#pragma unroll
+        for (int u = 0; u < PER; ++u) acc[u] = fmaf(p, vvals[j][u], acc[u] * corr);
+        m = mn;
+      }
     }
     const size_t rec = ((static_cast<size_t>(b) * g.S + s) * g.R + i) * g.H + h;
     const float inv = l > 0.0f ? 1.0f / l : 0.0f;
