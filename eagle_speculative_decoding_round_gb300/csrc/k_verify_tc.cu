@@ -48,9 +48,12 @@ constexpr int kBox = kHalf * kHalf * 2;        // 64 x 64 bf16 = 8 KB
 constexpr int kQBytes = kRows * kHD * 2;       // 32 KB (two 16 KB halves)
 constexpr int kKVBytes = kKeys * kHD * 2;      // 32 KB per operand per tile
 constexpr int kRowCache = 128;       // KV block rows looked up ahead
-constexpr int kThreads = 608;         // warp 0 K loads, warp 1 MMA, warps 2..17 softmax, warp 18 V loads
-constexpr int kVWarp = 18;
-constexpr int kSoftmaxThreads = 512;
+constexpr int kParts = 2;             // parts of a query row (warps per TMEM lane quarter)
+constexpr int kPK = kKeys / kParts;   // keys of a part per tile
+constexpr int kPD = kHD / kParts;     // head dims of a part
+constexpr int kSoftmaxThreads = 128 * kParts;
+constexpr int kVWarp = 2 + 4 * kParts;  // warp 0 K loads, warp 1 MMA, softmax warps, then the V-load warp
+constexpr int kThreads = 32 * (kVWarp + 1);
 // Cluster merge receive area: (128 + 15) rows (the most a CTA owns times 16 segments)
 // of bf16 partial o and float2 (m, l), written by every CTA of the cluster.
 constexpr int kRecvRows = kRows + 15;
@@ -349,7 +352,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       bar_init(&s_full[bb], 1);
       bar_init(&p_full[bb], kSoftmaxThreads / 32);  // one arrival per softmax warp
     }
-    for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], 4);  // one arrival per part (warp) of a lane quarter
+    for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], kParts);  // one arrival per part (warp) of a lane quarter
     bar_init(o_done, 1);
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -545,10 +548,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       }
     }
   }
-  // softmax warps 2..17: warp w reads TMEM lane quarter q = w % 4 (query rows
-  // 32q..32q+31) and owns part pp of the row: keys [32pp, 32pp+32) of S and
-  // head dims [32pp, 32pp+32) of O.  The four parts of a row exchange maxima and
-  // sums through shared memory, ordered by a per-quarter mbarrier (bounded wait).
+  // softmax warps 2..(2 + 4 kParts - 1): warp w reads TMEM lane quarter q = w % 4
+  // (query rows 32q..32q+31) and owns part pp of the row: keys [kPK pp, kPK (pp+1))
+  // of S and head dims [kPD pp, kPD (pp+1)) of O.  The parts of a row exchange maxima
+  // and sums through shared memory, ordered by a per-quarter mbarrier (bounded wait).
   const bool softmax = warp >= 2 && warp < kVWarp;
   const int q = warp & 3;
   const int pp = softmax ? (warp - 2) >> 2 : 0;
@@ -557,14 +560,14 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const bool row_ok = softmax && gr < g.G * g.R;
   const int node = row_ok ? gr / g.G : 0;
   const int head = kvh * g.G + (row_ok ? gr % g.G : 0);
+  const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
   float m = -INFINITY, lt = 0.0f;  // exponent base (moved lazily) and the row's total sum
   bool live = true;
   if (softmax) {
     const int words = (g.R + 63) >> 6;
     const uint64_t* mrow = mask + (static_cast<size_t>(b) * g.R + node) * words;
     const float c2 = sm_scale * kLog2e;
-    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-    const int tid_sm = threadIdx.x - 64;  // 0..511
+    const int tid_sm = threadIdx.x - 64;  // 0 .. kSoftmaxThreads - 1
     float l = 0.0f;
     for (int t = 0; t < ntile; ++t) {
       const int T0 = tile_T0(t);
@@ -576,44 +579,51 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         break;
       }
       fence_after();
-      float v[32];
-      tmem_ld32p(tS(bb) + lane_base + pp * 32, v);  // this part's 32 scores
-      const int Tc = T0 + pp * 32;
-      uint32_t valid = range_bits32(Tc, k0, k1);
-      if (tree) valid &= mask_bits32(mrow, words, Tc - P);
-      const bool full = valid == 0xFFFFFFFFu;  // interior chunk: no per-element tests
+      float v[kPK];
+#pragma unroll
+      for (int c = 0; c < kPK / 32; ++c)  // this part's scores, 32 columns at a time
+        tmem_ld32p(tS(bb) + lane_base + pp * kPK + 32 * c, *reinterpret_cast<float(*)[32]>(&v[32 * c]));
+      uint32_t valid[kPK / 32];
+      bool full = true;
+#pragma unroll
+      for (int c = 0; c < kPK / 32; ++c) {
+        const int Tc = T0 + pp * kPK + 32 * c;
+        valid[c] = range_bits32(Tc, k0, k1);
+        if (tree) valid[c] &= mask_bits32(mrow, words, Tc - P);
+        full = full && valid[c] == 0xFFFFFFFFu;  // interior chunk: no per-element tests
+      }
       float pmax = -INFINITY;
       if (full) {
         float a0 = fmax3f(v[0], v[1], v[2]), a1 = fmax3f(v[3], v[4], v[5]);
         float a2 = fmax3f(v[6], v[7], v[8]), a3 = fmax3f(v[9], v[10], v[11]);
 #pragma unroll
-        for (int j = 12; j < 28; j += 8) {
+        for (int j = 12; j + 8 <= kPK - 4; j += 8) {
           a0 = fmax3f(a0, v[j], v[j + 1]);
           a1 = fmax3f(a1, v[j + 2], v[j + 3]);
           a2 = fmax3f(a2, v[j + 4], v[j + 5]);
           a3 = fmax3f(a3, v[j + 6], v[j + 7]);
         }
-        a0 = fmax3f(a0, v[28], v[29]);
-        a1 = fmax3f(a1, v[30], v[31]);
+        a0 = fmax3f(a0, v[kPK - 4], v[kPK - 3]);
+        a1 = fmax3f(a1, v[kPK - 2], v[kPK - 1]);
         pmax = fmax3f(a0, a1, fmaxf(a2, a3)) * c2;
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if ((valid >> j) & 1u) pmax = fmaxf(pmax, v[j] * c2);
+        for (int j = 0; j < kPK; ++j)
+          if ((valid[j >> 5] >> (j & 31)) & 1u) pmax = fmaxf(pmax, v[j] * c2);
       }
-      s_max[((t & 1) * 4 + pp) * kRows + r] = pmax;
+      s_max[((t & 1) * kParts + pp) * kRows + r] = pmax;
       fence_before();  // this part's S loads are done before the others overwrite S with P
       __syncwarp();    // the warp's s_max writes, then one arrival for the warp
       if (lane == 0) bar_arrive(&xch[q]);
-      // probabilities of this part's 32 keys against base -nsub, packed to bf16 pairs
-      uint32_t pk[16];
+      // probabilities of this part's keys against base -nsub, packed to bf16 pairs
+      uint32_t pk[kPK / 2];
       float rs = 0.0f;
       auto probs = [&](float nsub) {
         const float2 c2v = make_float2(c2, c2), nv = make_float2(nsub, nsub);
         float2 acc = make_float2(0.0f, 0.0f);
         if (full) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
+          for (int j = 0; j < kPK; j += 2) {
             const float2 a = __ffma2_rn(make_float2(v[j], v[j + 1]), c2v, nv);
             const float e0 = fast_exp2(a.x), e1 = fast_exp2(a.y);
             acc = __fadd2_rn(acc, make_float2(e0, e1));
@@ -621,10 +631,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
           }
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
+          for (int j = 0; j < kPK; j += 2) {
+            const uint32_t vb = valid[j >> 5];
             const float2 a = __ffma2_rn(make_float2(v[j], v[j + 1]), c2v, nv);
-            const float e0 = ((valid >> j) & 1u) ? fast_exp2(a.x) : 0.0f;
-            const float e1 = ((valid >> (j + 1)) & 1u) ? fast_exp2(a.y) : 0.0f;
+            const float e0 = ((vb >> (j & 31)) & 1u) ? fast_exp2(a.x) : 0.0f;
+            const float e1 = ((vb >> ((j + 1) & 31)) & 1u) ? fast_exp2(a.y) : 0.0f;
             acc = __fadd2_rn(acc, make_float2(e0, e1));
             pk[j >> 1] = pack2_bf16(e0, e1);
           }
@@ -642,9 +653,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         break;
       }
       fence_after();
-      const float tmax = fmaxf(fmax3f(s_max[((t & 1) * 4) * kRows + r], s_max[((t & 1) * 4 + 1) * kRows + r],
-                                      s_max[((t & 1) * 4 + 2) * kRows + r]),
-                               s_max[((t & 1) * 4 + 3) * kRows + r]);
+      float tmax = s_max[((t & 1) * kParts) * kRows + r];
+#pragma unroll
+      for (int x = 1; x < kParts; ++x) tmax = fmaxf(tmax, s_max[((t & 1) * kParts + x) * kRows + r]);
       // The base moves only when the tile's maximum exceeds it by more than 2^8; then
       // O (tiles 0..t-1, which needs PV(t-1) completed) is rescaled in TMEM, warp-
       // wide (lanes whose base stays multiply by 1).  Each thread waits every phase
@@ -666,12 +677,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         waited_prev = true;
         fence_after();
 #pragma unroll 1
-        for (int h = 0; h < 2; ++h) {  // in two halves, to keep register pressure low
+        for (int h = 0; h < kPD / 16; ++h) {  // in 16-column steps, to keep register pressure low
           float ov[16];
-          tmem_ld16f(tO + lane_base + pp * 32 + h * 16, ov);
+          tmem_ld16f(tO + lane_base + pp * kPD + h * 16, ov);
 #pragma unroll
           for (int j = 0; j < 16; ++j) ov[j] *= corr;
-          tmem_st16f(tO + lane_base + pp * 32 + h * 16, ov);
+          tmem_st16f(tO + lane_base + pp * kPD + h * 16, ov);
         }
       }
       if (!spec || any_move) probs((m == -INFINITY) ? 0.0f : -m);
@@ -680,9 +691,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         live = false;
         break;
       }
-      // P(t) over this part's S columns: keys [32pp, 32pp+32) -> columns [16pp, 16pp+16)
-      // of the S buffer (all four parts have read their scores: the exchange above)
-      tmem_st16(tS(bb) + lane_base + pp * 16, pk);
+      // P(t) over this part's S columns: keys [kPK pp, kPK (pp+1)) -> columns
+      // [kPK/2 pp, kPK/2 (pp+1)) of the S buffer (all parts have read their scores:
+      // the exchange above)
+#pragma unroll
+      for (int c = 0; c < kPK / 32; ++c)
+        tmem_st16(tS(bb) + lane_base + pp * (kPK / 2) + 16 * c, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16 * c]));
       // V rows of keys outside the range are zeroed so that masked keys add exactly 0
       bool zeroed = false;
       if (tid_sm < kKeys) {
@@ -707,16 +721,18 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       __syncwarp();
       if (lane == 0) bar_arrive(&p_full[bb]);
     }
-    // total of the four parts' sums
+    // total of the parts' sums
     s_l[pp * kRows + r] = l;
     __syncwarp();
     if (lane == 0) bar_arrive(&xch[q]);
     bar_wait(&xch[q], ntile & 1, abort);
-    lt = s_l[r] + s_l[kRows + r] + s_l[2 * kRows + r] + s_l[3 * kRows + r];
+    lt = 0.0f;
+#pragma unroll
+    for (int x = 0; x < kParts; ++x) lt += s_l[x * kRows + r];
   }
-  // this part's 32 columns of O, from TMEM once the last PV has completed (zero
+  // this part's kPD columns of O, from TMEM once the last PV has completed (zero
   // where no tile was processed); warp-uniform, as the TMEM loads are warp-wide
-  float o[32];
+  float o[kPD];
   {
     bool o_ready = false;
     if (softmax && live && ntile > 0) {
@@ -724,19 +740,22 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       fence_after();
     }
     o_ready = __all_sync(0xFFFFFFFFu, o_ready);
-    if (o_ready) {
-      tmem_ld32(tO + lane_base_of(warp) + pp * 32, o);
-    } else {
 #pragma unroll
-      for (int d = 0; d < 32; ++d) o[d] = 0.0f;
+    for (int c = 0; c < kPD / 32; ++c) {
+      if (o_ready) {
+        tmem_ld32(tO + lane_base + pp * kPD + 32 * c, *reinterpret_cast<float(*)[32]>(&o[32 * c]));
+      } else {
+#pragma unroll
+        for (int d = 0; d < 32; ++d) o[32 * c + d] = 0.0f;
+      }
     }
   }
   if (!CLUSTER && row_ok && !*abort) {
     const size_t rec = ((static_cast<size_t>(b) * g.S + s) * g.R + node) * g.H + head;
     const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
-    float4* dst = reinterpret_cast<float4*>(ws_o + rec * kHD + pp * 32);
+    float4* dst = reinterpret_cast<float4*>(ws_o + rec * kHD + pp * kPD);
 #pragma unroll
-    for (int d = 0; d < 8; ++d)
+    for (int d = 0; d < kPD / 4; ++d)
       dst[d] = make_float4(o[4 * d] * inv, o[4 * d + 1] * inv, o[4 * d + 2] * inv, o[4 * d + 3] * inv);
     if (pp == 0) ws_ml[rec] = make_float2(m, lt);
   }
@@ -754,12 +773,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     const bool ok = row_ok && !*abort;
     const float inv = (ok && lt > 0.0f) ? 1.0f / lt : 0.0f;
     const int ow = r / rpc, li = r - ow * rpc;
-    // this part's 32 head dims = 16-byte chunks 4pp..4pp+3 of the row, XOR-swizzled by
-    // the owner-local row so that the 32 lanes' stores spread over the banks
+    // this part's kPD head dims = 16-byte chunks of the row (8 bf16 each), XOR-swizzled
+    // by the owner-local row so that the 32 lanes' stores spread over the banks
     const uint32_t row = cluster_addr(su32(recv_o + static_cast<size_t>(s * rpc + li) * kHD), ow);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int slot = (4 * pp + k) ^ (li & 7);
+    for (int k = 0; k < kPD / 8; ++k) {
+      const int slot = ((kPD / 8) * pp + k) ^ (li & 7);
       st_cluster_v4(row + slot * 16, pack2_bf16(o[8 * k] * inv, o[8 * k + 1] * inv),
                     pack2_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv), pack2_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
                     pack2_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
