@@ -190,6 +190,56 @@ __device__ __forceinline__ void tmem_ld32p(uint32_t taddr, float (&v)[32]) {
     v[2 * i + 1] = __uint_as_float(static_cast<uint32_t>(q[i] >> 32));
   }
 }
+// 64 consecutive 32-bit TMEM columns of this thread's lane as 32 register pairs,
+// one load instruction and one wait
+__device__ __forceinline__ void tmem_ld64p(uint32_t taddr, float (&v)[64]) {
+  unsigned long long q[32];
+  asm volatile(
+      "{\n .reg .b32 t<64>;\n"
+      " tcgen05.ld.sync.aligned.32x32b.x64.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31,t32,t33,t34,t35,t36,t37,t38,t39,t40,t41,t42,t43,t44,t45,t46,t47,t48,t49,t50,t51,t52,t53,t54,t55,t56,t57,t58,t59,t60,t61,t62,t63}, [%32];\n"
+      " tcgen05.wait::ld.sync.aligned;\n"
+      " mov.b64 %0, {t0, t1};\n"
+      " mov.b64 %1, {t2, t3};\n"
+      " mov.b64 %2, {t4, t5};\n"
+      " mov.b64 %3, {t6, t7};\n"
+      " mov.b64 %4, {t8, t9};\n"
+      " mov.b64 %5, {t10, t11};\n"
+      " mov.b64 %6, {t12, t13};\n"
+      " mov.b64 %7, {t14, t15};\n"
+      " mov.b64 %8, {t16, t17};\n"
+      " mov.b64 %9, {t18, t19};\n"
+      " mov.b64 %10, {t20, t21};\n"
+      " mov.b64 %11, {t22, t23};\n"
+      " mov.b64 %12, {t24, t25};\n"
+      " mov.b64 %13, {t26, t27};\n"
+      " mov.b64 %14, {t28, t29};\n"
+      " mov.b64 %15, {t30, t31};\n"
+      " mov.b64 %16, {t32, t33};\n"
+      " mov.b64 %17, {t34, t35};\n"
+      " mov.b64 %18, {t36, t37};\n"
+      " mov.b64 %19, {t38, t39};\n"
+      " mov.b64 %20, {t40, t41};\n"
+      " mov.b64 %21, {t42, t43};\n"
+      " mov.b64 %22, {t44, t45};\n"
+      " mov.b64 %23, {t46, t47};\n"
+      " mov.b64 %24, {t48, t49};\n"
+      " mov.b64 %25, {t50, t51};\n"
+      " mov.b64 %26, {t52, t53};\n"
+      " mov.b64 %27, {t54, t55};\n"
+      " mov.b64 %28, {t56, t57};\n"
+      " mov.b64 %29, {t58, t59};\n"
+      " mov.b64 %30, {t60, t61};\n"
+      " mov.b64 %31, {t62, t63};\n"
+      "}\n"
+      : "=l"(q[0]), "=l"(q[1]), "=l"(q[2]), "=l"(q[3]), "=l"(q[4]), "=l"(q[5]), "=l"(q[6]), "=l"(q[7]), "=l"(q[8]), "=l"(q[9]), "=l"(q[10]), "=l"(q[11]), "=l"(q[12]), "=l"(q[13]), "=l"(q[14]), "=l"(q[15]), "=l"(q[16]), "=l"(q[17]), "=l"(q[18]), "=l"(q[19]), "=l"(q[20]), "=l"(q[21]), "=l"(q[22]), "=l"(q[23]), "=l"(q[24]), "=l"(q[25]), "=l"(q[26]), "=l"(q[27]), "=l"(q[28]), "=l"(q[29]), "=l"(q[30]), "=l"(q[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[2 * i] = __uint_as_float(static_cast<uint32_t>(q[i]));
+    v[2 * i + 1] = __uint_as_float(static_cast<uint32_t>(q[i] >> 32));
+  }
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -579,10 +629,9 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         break;
       }
       fence_after();
+      static_assert(kPK == 64, "one 64-column load per part");
       float v[kPK];
-#pragma unroll
-      for (int c = 0; c < kPK / 32; ++c)  // this part's scores, 32 columns at a time
-        tmem_ld32p(tS(bb) + lane_base + pp * kPK + 32 * c, *reinterpret_cast<float(*)[32]>(&v[32 * c]));
+      tmem_ld64p(tS(bb) + lane_base + pp * kPK, v);  // this part's scores
       uint32_t valid[kPK / 32];
       bool full = true;
 #pragma unroll
@@ -620,13 +669,14 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       float rs = 0.0f;
       auto probs = [&](float nsub) {
         const float2 c2v = make_float2(c2, c2), nv = make_float2(nsub, nsub);
-        float2 acc = make_float2(0.0f, 0.0f);
+        float2 acc[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                         make_float2(0.0f, 0.0f)};  // four independent sum chains
         if (full) {
 #pragma unroll
           for (int j = 0; j < kPK; j += 2) {
             const float2 a = __ffma2_rn(make_float2(v[j], v[j + 1]), c2v, nv);
             const float e0 = fast_exp2(a.x), e1 = fast_exp2(a.y);
-            acc = __fadd2_rn(acc, make_float2(e0, e1));
+            acc[(j >> 1) & 3] = __fadd2_rn(acc[(j >> 1) & 3], make_float2(e0, e1));
             pk[j >> 1] = pack2_bf16(e0, e1);
           }
         } else {
@@ -636,11 +686,13 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
             const float2 a = __ffma2_rn(make_float2(v[j], v[j + 1]), c2v, nv);
             const float e0 = ((vb >> (j & 31)) & 1u) ? fast_exp2(a.x) : 0.0f;
             const float e1 = ((vb >> ((j + 1) & 31)) & 1u) ? fast_exp2(a.y) : 0.0f;
-            acc = __fadd2_rn(acc, make_float2(e0, e1));
+            acc[(j >> 1) & 3] = __fadd2_rn(acc[(j >> 1) & 3], make_float2(e0, e1));
             pk[j >> 1] = pack2_bf16(e0, e1);
           }
         }
-        rs = acc.x + acc.y;
+        const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
+        const float2 st = __fadd2_rn(s01, s23);
+        rs = st.x + st.y;
       };
       // While the other parts' maxima arrive, the probabilities are computed against
       // the current base.  They are final unless some part of the row exceeds the base
