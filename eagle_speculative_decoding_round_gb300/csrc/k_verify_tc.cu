@@ -389,7 +389,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rg = CLUSTER ? blockIdx.x / g.S : blockIdx.x % g.RG;
   const int s = CLUSTER ? blockIdx.x % g.S : blockIdx.x / g.RG;
-  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int kvh = blockIdx.y;
   const int nodes_per_tile = kRows / g.G;
   const int i0 = rg * nodes_per_tile;  // first node of this row group
   if (threadIdx.x == 0) {  // barriers first: they depend on nothing in global memory
@@ -415,6 +415,25 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   // shared and tensor memory; nothing in global memory is read or written before
   // the preceding kernel has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Requests are taken in order of decreasing length (ties: lower index first): the
+  // CTAs of blockIdx.z = j serve the request of rank j, so that the longest requests
+  // are launched first and the short ones fill the last wave.
+  int b = blockIdx.z;
+  if (gridDim.z > 1) {
+    __shared__ int s_req;
+    const int nb = static_cast<int>(gridDim.z);
+    for (int c = threadIdx.x; c < nb; c += blockDim.x) {
+      const int Pc = kv_len[c];
+      int rank = 0;
+      for (int o = 0; o < nb; ++o) {
+        const int Po = kv_len[o];
+        rank += (Po > Pc) || (Po == Pc && o < c);
+      }
+      if (rank == static_cast<int>(blockIdx.z)) s_req = c;
+    }
+    __syncthreads();
+    b = s_req;
+  }
   if (threadIdx.x == 0) {
     bar_expect(q_full, kQBytes);
     for (int h = 0; h < 2; ++h) tma3d(sQ + h * (kQBytes / 2), &tmQ, h * kHalf, kvh * g.G, b * g.R + i0, q_full);
