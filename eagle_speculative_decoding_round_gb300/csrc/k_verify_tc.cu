@@ -840,7 +840,20 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       (reinterpret_cast<uintptr_t>(s_rows + kRowCache) + 15) & ~static_cast<uintptr_t>(15));
   __nv_bfloat16* recv_o = reinterpret_cast<__nv_bfloat16*>(recv);         // [S][rpc][128]
   float2* recv_ml = reinterpret_cast<float2*>(recv + kRecvRows * kHD * 2);  // [S][rpc]
-  if (CLUSTER && softmax) {
+  if (CLUSTER && softmax && g.S == 1) {
+    // the row group is not split: this part of the row is final
+    if (row_ok && !*abort) {
+      const float inv = lt > 0.0f ? 1.0f / lt : 0.0f;
+      const size_t orow = (static_cast<size_t>(b) * g.R + node) * g.H + head;
+      uint4* dst = reinterpret_cast<uint4*>(O + orow * kHD + pp * kPD);
+#pragma unroll
+      for (int k = 0; k < kPD / 8; ++k)
+        dst[k] = make_uint4(pack2_bf16(o[8 * k] * inv, o[8 * k + 1] * inv), pack2_bf16(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
+                            pack2_bf16(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
+                            pack2_bf16(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
+      if (pp == 0) lse[orow] = (m + __log2f(lt)) * 0.6931471805599453f;
+    }
+  } else if (CLUSTER && softmax) {
     const bool ok = row_ok && !*abort;
     const float inv = (ok && lt > 0.0f) ? 1.0f / lt : 0.0f;
     const int ow = r / rpc, li = r - ow * rpc;
@@ -865,7 +878,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   fence_before();
   __syncthreads();
   if (*abort && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
-  if (CLUSTER) {
+  if (CLUSTER && g.S > 1) {
     const int S = g.S;
     const int n_own = max(0, min(rpc, kRows - s * rpc));
     __syncwarp();
