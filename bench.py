@@ -449,14 +449,12 @@ def main():
         extra += 1
     torch.cuda.synchronize()
     clk = clocks.stop()
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    check_dev_err(w, "timed rounds")
+    ms = ranks_max(ms, world)
     ms_step = ms / K
     phase_ms = {p: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
                 for i, p in enumerate(phases)}
-    rounds_s = world * 1000.0 / ms_step
+    rounds_s = job_rounds_per_s(ms_step, world)
     nodes_s = rounds_s * cfg.B * cfg.N
 
     wm = work_model(w)
@@ -489,7 +487,7 @@ def main():
         lm.update(achieved=round(lm_tf, 1), peak=tflops, unit="TFLOP/s", frac=round(lm_tf / tflops, 4),
                   peak_source="MEASURED_PEAKS.json bf16_tflops_sustained (of measured)")
     lm["tensor_frac"] = round(lm_tf / tflops, 4)
-    e2e = None if args.no_e2e else e2e_leg(w, s, K, args.warmup)
+    e2e = None if args.no_e2e else e2e_leg(w, s, K, args.warmup, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         o = oracle_sample(w)
@@ -579,16 +577,16 @@ def run_round_phased(w, evs, e3, counts=None):
     evs[7].record(s)
 
 
-def e2e_leg(w, s, K, warmup):
+def e2e_leg(w, s, K, warmup, world=1):
     """Same rounds through the C ABI, from pinned HOST buffers: each step copies the
     round's inputs host->device (fusion inputs, draft logits, per-layer Q, uniforms,
-    temperatures, root tokens), runs the round, and copies the result (emitted
-    tokens, path, accepted length) back."""
+    temperatures, root tokens, request lengths), runs the round, and copies the
+    result (emitted tokens, path, accepted length) back."""
     import torch
     b = w.bufs
-    ins = [*b.h, *b.draft_logits, *b.Q, b.u_acc, b.u_bonus, b.temp, b.temp_rows, b.root_tok]
+    ins = [*b.h, *b.draft_logits, *b.Q, b.u_acc, b.u_bonus, b.temp, b.temp_rows, b.root_tok, b.kv_len]
     outs = [b.out_tok, b.path, b.acc_len]
-    h_in = [t.detach().cpu().pin_memory() for t in ins]
+    h_in = [t.detach().cpu().pin_memory() for t in ins[:-1]] + [w.kv_len0.detach().cpu().pin_memory()]
     h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
     bi = sum(t.numel() * t.element_size() for t in ins)
     bo = sum(t.numel() * t.element_size() for t in outs)
@@ -615,9 +613,37 @@ def e2e_leg(w, s, K, warmup):
         step()
     z.record(s)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(z) / K
-    return {"value": round(1000.0 / ms, 3), "unit": "rounds/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "ms_per_step": round(ms, 4)}
+    check_dev_err(w, "e2e")
+    ms = ranks_max(a.elapsed_time(z) / K, world)
+    return {"value": round(job_rounds_per_s(ms, world), 3), "unit": "rounds/s", "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 4)}
+
+
+def check_dev_err(w, where):
+    """A round that flagged a device error (capacity, non-finite, timeout) took an
+    early-exit path: its timing is not a measurement of the round."""
+    err = int(w.bufs.dev_err.item())
+    if err != 0:
+        raise RuntimeError(f"{where}: device error flags {err:#x} set during the timed rounds")
+
+
+def job_rounds_per_s(ms_per_step, world):
+    """Whole-job throughput: each of the `world` replicas completes one round per
+    step, and a step lasts as long as the slowest rank's (ms_per_step is that max)."""
+    return world * 1000.0 / ms_per_step
+
+
+def ranks_max(x, world):
+    """Largest value of x over the ranks (x itself for one process).  NCCL reduces
+    GPU tensors, gloo CPU tensors."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def load_peaks():
