@@ -408,21 +408,28 @@ def main():
     s.synchronize()
     accepted = w.bufs.acc_len.cpu().numpy().copy()
 
-    # the timed region: one graph of K rounds, with events at the phase boundaries
+    # The timed region: one graph of K rounds (nothing but the rounds: each round first
+    # resets kv_len).  A second graph of the same rounds with events at the phase
+    # boundaries gives the phase split; it is replayed separately, because an event
+    # between two kernels also cuts the programmatic launch edge between them.
     K = args.steps
     phases = ["fuse", "expand", "tree", "verify", "lmhead", "accept", "compact"]
     ev = [[graph_event() for _ in range(len(phases) + 1)] for _ in range(K)]
     from eagle_speculative_decoding_round_gb300 import eagle3 as e3
-    from eagle_speculative_decoding_round_gb300.round import run_round
     graph = torch.cuda.CUDAGraph()
     counts = []  # library launch counter at each phase boundary of the first captured round
     n0 = e3.launch_count()
     with torch.cuda.graph(graph, stream=s):
         for k in range(K):
             w.bufs.kv_len.copy_(w.kv_len0)
-            run_round_phased(w, ev[k], e3, counts if k == 0 else None)
+            run_round_phased(w, None, e3, counts if k == 0 else None)
     launches_timed = e3.launch_count() - n0  # libeagle3 kernels in the K captured rounds
     phase_launches = {p: counts[i + 1] - counts[i] for i, p in enumerate(phases)}
+    graph_phased = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_phased, stream=s):
+        for k in range(K):
+            w.bufs.kv_len.copy_(w.kv_len0)
+            run_round_phased(w, ev[k], e3)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         graph.replay()  # one untimed replay of the captured work
@@ -449,6 +456,9 @@ def main():
         extra += 1
     torch.cuda.synchronize()
     clk = clocks.stop()
+    with torch.cuda.stream(s):
+        graph_phased.replay()  # the phase split (not timed as a whole)
+    torch.cuda.synchronize()
     check_dev_err(w, "timed rounds")
     ms = ranks_max(ms, world)
     ms_step = ms / K
@@ -536,8 +546,9 @@ def summarize(P):
 
 
 def run_round_phased(w, evs, e3, counts=None):
-    """One round with a timing event at each phase boundary (same calls as run_round).
-    With ``counts`` (a list), also append the library's launch counter there."""
+    """One round with a timing event at each phase boundary (same calls as run_round;
+    no events when ``evs`` is None).  With ``counts`` (a list), also append the
+    library's launch counter there."""
     import torch
     b, c = w.bufs, w.cfg
     s = torch.cuda.current_stream()
@@ -548,11 +559,12 @@ def run_round_phased(w, evs, e3, counts=None):
             self.e = e
 
         def record(self, st):
-            self.e.record(st)
+            if self.e is not None:
+                self.e.record(st)
             if counts is not None:
                 counts.append(e3.launch_count())
 
-    evs = [_Ev(e) for e in evs]
+    evs = [_Ev(e) for e in (evs if evs is not None else [None] * 8)]
     evs[0].record(s)
     e3.eagle3_fuse(b.h[0], b.h[1], b.h[2], b.W_f, None, b.g, c.M, c.d, c.d, c.dt, b.fuse_ws, b.fuse_ws_bytes, b.dev_err)
     evs[1].record(s)
