@@ -35,6 +35,11 @@ CONFIGS = {
                temps=[1.0], noise=1.0,
                workload="Llama-3.1-8B-shaped verify round, bf16: d=4096, 32/8 heads x 128, vocab 128256, batch 1, "
                         "prefix 2048, 60-node depth-6 tree, top-k 10, 32 layers, fusion 12288->4096, temp 1"),
+    "8b_d8": dict(B=1, P=[2048], N=60, D=8, k=10, W=10, H=32, KVH=8, hd=128, d=4096, V=128256, L=32, dtype="bf16",
+                  temps=[1.0], noise=1.0,
+                  workload="Llama-3.1-8B-shaped verify round with an EAGLE-3 depth-8 tree at the same node count: "
+                           "d=4096, 32/8 heads x 128, vocab 128256, batch 1, prefix 2048, 60-node depth-8 tree, "
+                           "top-k 10, 32 layers, fusion 12288->4096, temp 1"),
     "batched": dict(B=32, P="uniform:512:8192", N=60, D=6, k=10, W=10, H=32, KVH=8, hd=128, d=4096, V=128256,
                     L=32, dtype="bf16", temps="mixed", noise=1.0,
                     workload="batched serving, 8B shape, bf16: 32 requests, prefix U[512,8192], 60-node depth-6 "
@@ -405,6 +410,7 @@ def main():
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
         for _ in range(args.warmup):
+            w.bufs.kv_len.copy_(w.kv_len0)  # every round starts from the same request lengths
             w.round()
     s.synchronize()
     accepted = w.bufs.acc_len.cpu().numpy().copy()
@@ -519,6 +525,7 @@ def main():
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "nodes_per_s": round(nodes_s, 1),
             "accepted_mean": float(np.mean(accepted)),
+            "accepted_hist": np.bincount(accepted.astype(np.int64), minlength=cfg.D + 1).tolist(),
             "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
             "roofline": roofline,
             "roofline_lmhead": lm,
