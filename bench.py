@@ -40,6 +40,11 @@ CONFIGS = {
                   workload="Llama-3.1-8B-shaped verify round with an EAGLE-3 depth-8 tree at the same node count: "
                            "d=4096, 32/8 heads x 128, vocab 128256, batch 1, prefix 2048, 60-node depth-8 tree, "
                            "top-k 10, 32 layers, fusion 12288->4096, temp 1"),
+    "8b_chain3": dict(B=1, P=[2048], N=3, D=3, k=1, W=1, H=32, KVH=8, hd=128, d=4096, V=128256, L=32, dtype="bf16",
+                      temps=[1.0], noise=1.0,
+                      workload="Llama-3.1-8B-shaped verify round with a chain draft (top-1, three tokens): d=4096, "
+                               "32/8 heads x 128, vocab 128256, batch 1, prefix 2048, 32 layers, "
+                               "fusion 12288->4096, temp 1"),
     "batched": dict(B=32, P="uniform:512:8192", N=60, D=6, k=10, W=10, H=32, KVH=8, hd=128, d=4096, V=128256,
                     L=32, dtype="bf16", temps="mixed", noise=1.0,
                     workload="batched serving, 8B shape, bf16: 32 requests, prefix U[512,8192], 60-node depth-6 "

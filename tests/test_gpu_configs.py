@@ -38,7 +38,7 @@ def f32(t):
     return t.float().cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["tiny", "8b", "8b_d8", "batched", "long", "70b"])
+@pytest.mark.parametrize("name", ["tiny", "8b", "8b_d8", "8b_chain3", "batched", "long", "70b"])
 def test_round_matches_oracle(name):
     w = bench.Workload(name, seed=11)
     b, c = w.bufs, w.cfg
