@@ -13,20 +13,23 @@
 // operand):
 //   S = Q K^T    tcgen05.mma, M = 128 rows, N = 128 keys, K = head_dim (K-major),
 //                into one of two S buffers in TMEM
-//   softmax      the threads of a query row read its TMEM lane; running max and
-//                sum in registers; P (bf16) is written back over S in TMEM
+//   softmax      the kParts threads of a query row read its TMEM lane (kPK keys
+//                each); running max and sum in registers; P (bf16) is written
+//                back over S in TMEM
 //   O += P V     tcgen05.mma with A (P) from TMEM, N = head_dim, K = keys; V is
 //                used in place as an MN-major operand.  O stays in TMEM for the
 //                whole key range: its exponent base moves only when a tile's
 //                maximum exceeds it by more than 2^8, and then the softmax warps
 //                rescale it in place.
-// Warps: 0 K loads (TMA), 1 TMEM owner + MMA issuer, 2..17 softmax/epilogue (four
-// warps per TMEM lane quarter, each owning a quarter of the keys and of the head
-// dims), 18 V loads (TMA).
+// Warps: 0 K loads (TMA), 1 TMEM owner + MMA issuer, 2 .. kVWarp-1 softmax and
+// epilogue (kParts warps per TMEM lane quarter, each owning kPK keys of a tile and
+// kPD head dims of O), kVWarp V loads (TMA).
 //
-// Segments are combined in one of two ways.  CLUSTER: the S segments of one row
-// group form a thread-block cluster and merge their partial (o, m, l) rows through
-// distributed shared memory (bulk copies), writing O and lse directly.  Otherwise
+// Segments are combined in one of three ways.  A row group that is not split (S =
+// 1) writes O and lse directly.  CLUSTER with S > 1: the S segments of one row
+// group form a thread-block cluster; every CTA stores its partial (o, m, l) rows
+// into the owning CTA's receive area with distributed-shared-memory stores, and
+// after one cluster barrier each CTA merges and writes its rows.  Otherwise
 // (prefixes long enough to fill the GPU with independent CTAs) the partial records
 // go to a workspace and verify_merge_kernel combines them.
 #include <algorithm>
@@ -54,6 +57,7 @@ constexpr int kPD = kHD / kParts;     // head dims of a part
 constexpr int kSoftmaxThreads = 128 * kParts;
 constexpr int kVWarp = 2 + 4 * kParts;  // warp 0 K loads, warp 1 MMA, softmax warps, then the V-load warp
 constexpr int kThreads = 32 * (kVWarp + 1);
+static_assert(kParts >= 1 && kParts <= 4 && kKeys % (32 * kParts) == 0, "parts of 32-key multiples, at most four");
 // Cluster merge receive area: (128 + 15) rows (the most a CTA owns times 16 segments)
 // of bf16 partial o and float2 (m, l), written by every CTA of the cluster.
 constexpr int kRecvRows = kRows + 15;
@@ -380,11 +384,11 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint64_t* s_full = bars + 9;     // [2]
   uint64_t* p_full = bars + 11;    // [2]
   uint64_t* o_done = bars + 13;    // PV(t) completed (once per tile); bars + 14, 19 unused
-  uint64_t* xch = bars + 15;       // [4] exchange among the four parts of a row, per lane quarter
+  uint64_t* xch = bars + 15;       // [4] exchange among the parts of a row, per lane quarter
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* s_max = reinterpret_cast<float*>(tmem_slot + 4);  // [2 parities][4 parts][128 rows]
-  float* s_l = s_max + 8 * kRows;                           // [4 parts][128 rows]
+  float* s_max = reinterpret_cast<float*>(tmem_slot + 4);  // [2 parities][kParts <= 4][128 rows]
+  float* s_l = s_max + 8 * kRows;                           // [kParts <= 4][128 rows]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rg = CLUSTER ? blockIdx.x / g.S : blockIdx.x % g.RG;
@@ -534,7 +538,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int h = 0; h < 2; ++h) tma2d(base + h * (kKVBytes / 2) + blk * kBox, map, h * kHalf, row, bar);
     }
   };
-  if (threadIdx.x == 0 && ntile > 0) {  // the first two tiles' K and V, before the TMEM allocation
+  if (threadIdx.x == 0 && ntile > 0) {  // the first two tiles' K and V
     bool okp = true;
     for (int t = 0; t < ntile && t < 2; ++t) {
       issue_kv(t, 0, &okp);
