@@ -24,11 +24,14 @@ constexpr int kExpandThreads = 512;
 constexpr int kMaxCluster = 16;  // CTAs per frontier row (at most)
 constexpr uint32_t kBulkPiece = 32768;  // bytes per bulk copy of the staged chunk
 
-// candidate-list capacity and dynamic shared memory of one CTA (CL CTAs per row)
+// candidate-list capacity and dynamic shared memory of one CTA (CL CTAs per row).
+// The exact threshold admits only elements of the k threads whose maximum reaches
+// it, so k times the elements one thread holds (a float4 slot is 4 of them) bounds
+// the list.
 int expand_cand_cap(int V, bool vec, int k, int CL) {
   const int nvec = vec ? V / 4 : V;
   const int per = (nvec + CL - 1) / CL;
-  const int per_thread = ((vec ? per * 4 : per) + kExpandThreads - 1) / kExpandThreads;
+  const int per_thread = (vec ? 4 : 1) * ((per + kExpandThreads - 1) / kExpandThreads);
   return k * per_thread + 32;
 }
 size_t expand_smem_bytes(int V, bool vec, int k, int CL) {
@@ -289,6 +292,8 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     });
     __syncthreads();
   }
+  // (the bound above makes this unreachable; a dropped key would be a wrong child)
+  if (threadIdx.x == 0 && s_cnt > cand_cap) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
   const int ncand = min(s_cnt, cand_cap);
   if (threadIdx.x < E3_MAX_TOPK) ltop[threadIdx.x] = 0ull;
   __syncthreads();

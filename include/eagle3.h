@@ -74,7 +74,9 @@ typedef enum { E3_F32 = 0, E3_BF16 = 1 } e3_dtype;
 
 /* bits of the device error word */
 #define E3_DEV_ERR_NONFINITE 1 /* a logit was NaN or +-Inf */
-#define E3_DEV_ERR_CAPACITY 2  /* kv_len + R exceeds the request's pages */
+#define E3_DEV_ERR_CAPACITY 2  /* kv_len + R exceeds the request's pages (verify,
+                                  compaction); an internal candidate list of
+                                  eagle3_expand overflowed (not expected) */
 #define E3_DEV_ERR_TIMEOUT 4   /* a bounded on-device wait ran out; outputs invalid */
 
 /* Limits of this build. */
@@ -158,7 +160,9 @@ E3_API size_t eagle3_fuse_noalloc_max_scratch_bytes(void);
  * Next frontier: the first Wn = min(W, F*k) of these children in the order
  *   (score descending, candidate index ascending) -> next_id [B][Wn] (candidate
  *   index) and next_score [B][Wn].
- * Non-finite logits set E3_DEV_ERR_NONFINITE.
+ * Non-finite logits set E3_DEV_ERR_NONFINITE; E3_DEV_ERR_CAPACITY marks a row
+ * whose children may be wrong (an internal list overflowed; its size bound makes
+ * this unreachable).
  * Limits: 1 <= k <= E3_MAX_TOPK, k <= V, 1 <= W <= E3_MAX_FRONTIER or W >= F*k,
  *   F*k <= 2048, cand_offset + F*k <= cands->cap <= E3_MAX_CAND.
  * ------------------------------------------------------------------------- */

@@ -27,7 +27,9 @@ def i32(n, fill=0):
 
 @pytest.mark.parametrize("M,d,dout,dt", [(3, 256, 256, "f32"), (1, 256, 256, "f32"), (7, 4096, 4096, "bf16"),
                                          (13, 256, 384, "bf16"), (130, 512, 256, "bf16"), (1, 64, 128, "bf16"),
-                                         (300, 128, 200, "bf16"), (5, 96, 256, "bf16")])
+                                         (300, 128, 200, "bf16"), (5, 96, 256, "bf16"),
+                                         # fp32 with more than 16 rows: the tiled SIMT GEMM
+                                         (20, 128, 192, "f32"), (70, 96, 130, "f32")])
 def test_fuse(M, d, dout, dt):
     hs = [synth.normal(M * d + dout, f"h{i}", (M, d), 0.02) for i in range(3)]
     W = synth.normal(M * d + dout, "Wf", (dout, 3 * d), 0.02)
@@ -59,7 +61,9 @@ def test_fuse(M, d, dout, dt):
 
 @pytest.mark.parametrize("M,d,V,dt", [(15, 256, 1024, "f32"), (61, 4096, 128256, "bf16"), (3, 128, 1000, "bf16"),
                                       (200, 256, 4096, "bf16"), (300, 192, 2048, "bf16"), (1, 64, 256, "bf16"),
-                                      (20, 256, 1000, "bf16"), (40, 100, 512, "bf16")])
+                                      (20, 256, 1000, "bf16"), (40, 100, 512, "bf16"),
+                                      # fp32 with more than 16 rows: the tiled SIMT GEMM
+                                      (20, 256, 1000, "f32"), (67, 100, 515, "f32")])
 def test_lmhead_logits_and_stats(M, d, V, dt):
     h = synth.normal(V + M, "h", (M, d), 1.0)
     W = synth.normal(V + M, "Wlm", (V, d), 4.0 / math.sqrt(d))
@@ -135,7 +139,10 @@ def run_gpu_expansion(logits_per_depth, B, k, W, D):
                                             (4096, 10, 10, 6, 3, False), (512, 4, 4, 4, 2, True),
                                             (300, 7, 9, 3, 2, False),
                                             # 320 rows x 8 CTAs: several waves, SMs reused
-                                            (128256, 10, 10, 2, 32, False)])
+                                            (128256, 10, 10, 2, 32, False),
+                                            # k above 16: the 32-wide per-thread lists
+                                            (4096, 20, 20, 3, 2, False), (1000, 32, 64, 3, 1, True),
+                                            (999, 24, 40, 3, 2, True)])
 def test_expand_bitexact(V, k, W, D, B, ties):
     rng = np.random.default_rng(V + k + D)
     sizes, F = [], 1
@@ -174,7 +181,9 @@ def test_expand_flags_nonfinite():
 # ---------------------------------------------------------------- tree build ----
 
 @pytest.mark.parametrize("V,k,W,D,N,B", [(1024, 2, 1 << 20, 3, 14, 1), (4096, 10, 10, 6, 60, 3),
-                                         (2048, 4, 4, 7, 32, 2), (512, 8, 16, 8, 255, 1), (512, 3, 3, 2, 1, 2)])
+                                         (2048, 4, 4, 7, 32, 2), (512, 8, 16, 8, 255, 1), (512, 3, 3, 2, 1, 2),
+                                         # 1296 candidates: the shared-memory sort over 1024 threads
+                                         (4096, 16, 16, 6, 60, 2)])
 def test_tree_build_bitexact(V, k, W, D, N, B):
     rng = np.random.default_rng(N + D)
     sizes, F = [], 1
