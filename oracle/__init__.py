@@ -81,6 +81,20 @@ def _load():
             lib.e3o_accept.argtypes = [P, P, i32, i32, P, i32, f32, P, P, P, P, P]
             lib.e3o_accept_many.restype = None
             lib.e3o_accept_many.argtypes = [i32, P, P, i32, i32, P, i32, f32, P, P, P, P, P]
+            lib.e3o_splitmix64_at.restype = u64
+            lib.e3o_splitmix64_at.argtypes = [u64, u64]
+            lib.e3o_exp_variate.restype = f32
+            lib.e3o_exp_variate.argtypes = [u64, i32, i32, i32, i32]
+            lib.e3o_expand_sampled.restype = i32
+            lib.e3o_expand_sampled.argtypes = [P, i32, i32, i32, i32, f32, P, P, i32, i32, u64, i32, P, P, P,
+                                               P, P, P, P, P]
+            lib.e3o_build_tree_cand.restype = i32
+            lib.e3o_build_tree_cand.argtypes = [i32, P, P, P, P, i32, i32, i32, P, P, P, P, P, i32, P]
+            lib.e3o_accept_sampled.restype = i32
+            lib.e3o_accept_sampled.argtypes = [P, P, i32, i32, P, i32, f32, P, f32, P, P, P, P, P]
+            lib.e3o_sampled_trials.restype = i32
+            lib.e3o_sampled_trials.argtypes = [i32, i32, i32, i32, i32, P, i32, f32, P, f32, u64, P, P, i32,
+                                               P, P]
             _lib = lib
     return _lib
 
@@ -169,6 +183,45 @@ def expand(logits, k, W, parent_score, parent_id, depth, cand_offset, cands, inv
     return nid, nsc
 
 
+def splitmix64_at(seed: int, i: int) -> int:
+    """Output number i >= 1 of the SplitMix64 stream started at ``seed``."""
+    return int(_load().e3o_splitmix64_at(seed & (2 ** 64 - 1), i & (2 ** 64 - 1)))
+
+
+def exp_variate(seed: int, b: int, depth: int, f: int, j: int) -> float:
+    """E = -ln U of the draw for token j of frontier row f at ``depth`` of request b (fp32)."""
+    return float(_load().e3o_exp_variate(seed & (2 ** 64 - 1), b, depth, f, j))
+
+
+def expand_sampled(logits, k, W, parent_score, parent_id, depth, cand_offset, cands, seed, b, inv_T=1.0):
+    """One depth of expansion with sampled children, one request (request index b
+    keys the draws).  Each row's k children are drawn without replacement from
+    the draft distribution (exponential race on E_j / e_j), in draw order; scores
+    and the next frontier are as in ``expand``.  Returns (next_id, next_score,
+    row_m, row_Q): the next frontier and each row's draft statistics.
+
+    "EAGLE 系列与 DFlash", §四 DFlash: drafts proposed by the drafter and checked
+    with min(1, p_target / p_draft); drawing them from the draft distribution is
+    what makes that rule exact.
+    """
+    z = np.ascontiguousarray(logits, dtype=np.float32)
+    F, V = z.shape
+    ps = np.ascontiguousarray(parent_score, np.float32)
+    pid = np.ascontiguousarray(parent_id, np.int32)
+    nf_cap = min(W, F * k)
+    nid = np.zeros(nf_cap, np.int32)
+    nsc = np.zeros(nf_cap, np.float32)
+    rm = np.zeros(F, np.float32)
+    rq = np.zeros(F, np.uint64)
+    rc = _load().e3o_expand_sampled(_p(z), F, V, k, W, float(np.float32(inv_T)), _p(ps), _p(pid), depth,
+                                    cand_offset, seed & (2 ** 64 - 1), b, _p(cands["tok"]),
+                                    _p(cands["parent"]), _p(cands["score"]), _p(cands["depth"]), _p(nid),
+                                    _p(nsc), _p(rm), _p(rq))
+    if rc < 0:
+        raise FloatingPointError("non-finite draft logit")
+    return nid, nsc, rm, rq
+
+
 def new_cands(C: int) -> dict:
     return {"tok": np.full(C, -1, np.int32), "parent": np.full(C, -1, np.int32),
             "score": np.zeros(C, np.float32), "depth": np.zeros(C, np.int32)}
@@ -183,13 +236,14 @@ def build_tree(cands: dict, n_cand: int, N: int, root_tok: int, kv_len: int):
     depth = np.zeros(R, np.int32)
     pos = np.zeros(R, np.int32)
     mask = np.zeros((R, words), np.uint64)
+    node_cand = np.zeros(R, np.int32)
     c = {k: np.ascontiguousarray(v[:n_cand]) for k, v in cands.items()}
-    rc = _load().e3o_build_tree(n_cand, _p(c["tok"]), _p(c["parent"]), _p(c["score"]), _p(c["depth"]),
-                                N, int(root_tok), int(kv_len), _p(tok), _p(parent), _p(depth), _p(pos),
-                                _p(mask), words)
+    rc = _load().e3o_build_tree_cand(n_cand, _p(c["tok"]), _p(c["parent"]), _p(c["score"]), _p(c["depth"]),
+                                     N, int(root_tok), int(kv_len), _p(tok), _p(parent), _p(depth), _p(pos),
+                                     _p(mask), words, _p(node_cand))
     if rc != 0:
         raise AssertionError("kept candidate set is not closed under parents")
-    return {"tok": tok, "parent": parent, "depth": depth, "pos": pos, "mask": mask}
+    return {"tok": tok, "parent": parent, "depth": depth, "pos": pos, "mask": mask, "node_cand": node_cand}
 
 
 def mask_to_dense(mask: np.ndarray, R: int) -> np.ndarray:
@@ -356,6 +410,57 @@ def accept_many(tok, parent, D, logits, T, u_acc, u_bonus):
                             _p(np.ascontiguousarray(parent, np.int32)), R, D, _p(z), V,
                             float(np.float32(T)), _p(ua), _p(ub), _p(acc), _p(path), _p(out))
     return acc, path, out
+
+
+def accept_sampled(tree: dict, logits, T, qlogits, inv_Tq, u_acc, u_bonus, D):
+    """Accept/reject for children drawn from the draft distribution.
+
+    logits: [R, V] fp32 target logits of the flattened nodes; qlogits: [R, V]
+    fp32, row u = the draft row from which node u's children were drawn (any
+    values for nodes without children), at inverse temperature ``inv_Tq``.
+    Child c is accepted with probability min(1, p_res(c) / q_res(c)); a
+    rejection replaces p_res by norm(max(0, p_res - q_res)) and removes c from
+    q_res ("EAGLE 系列与 DFlash", §四 DFlash; "SpecForge…", 先看 checkpoint 最终要参与
+    什么计算: correct at the rejection point).  Integer recipe: see
+    ``e3o_accept_sampled`` in eagle3_oracle.c.
+    """
+    z = np.ascontiguousarray(logits, dtype=np.float32)
+    zq = np.ascontiguousarray(qlogits, dtype=np.float32)
+    R, V = z.shape
+    assert zq.shape == (R, V)
+    ua = np.ascontiguousarray(u_acc, np.uint32)
+    ub = np.ascontiguousarray(u_bonus, np.uint32)
+    acc = np.zeros(1, np.int32)
+    path = np.zeros(D + 1, np.int32)
+    out = np.zeros(D + 1, np.int32)
+    rc = _load().e3o_accept_sampled(_p(np.ascontiguousarray(tree["tok"], np.int32)),
+                                    _p(np.ascontiguousarray(tree["parent"], np.int32)), R, D, _p(z), V,
+                                    float(np.float32(T)), _p(zq), float(np.float32(inv_Tq)), _p(ua), _p(ub),
+                                    _p(acc), _p(path), _p(out))
+    if rc != 0:
+        raise FloatingPointError("non-finite logit")
+    return int(acc[0]), path, out
+
+
+def sampled_trials(n, k, W, D, qtab, inv_Tq, ptab, T, seed0, u_acc, u_bonus):
+    """n rounds of a small synthetic model with sampled drafts (see
+    ``e3o_sampled_trials``): qtab [D, Fmax, V] draft logits per (depth, frontier
+    row), ptab [V + 1, V] target logits (row 0 the root, row 1 + t after token t).
+    u_acc / u_bonus: [n, Rcap] uint32.  Returns (acc_len [n], out_tok [n, D+1])."""
+    qt = np.ascontiguousarray(qtab, np.float32)
+    pt = np.ascontiguousarray(ptab, np.float32)
+    Dq, Fmax, V = qt.shape
+    assert Dq >= D and pt.shape == (V + 1, V)
+    ua = np.ascontiguousarray(u_acc, np.uint32)
+    ub = np.ascontiguousarray(u_bonus, np.uint32)
+    acc = np.zeros(n, np.int32)
+    out = np.zeros((n, D + 1), np.int32)
+    R = _load().e3o_sampled_trials(n, V, k, W, D, _p(qt), Fmax, float(np.float32(inv_Tq)), _p(pt),
+                                   float(np.float32(T)), seed0 & (2 ** 64 - 1), _p(ua), _p(ub), ua.shape[1],
+                                   _p(acc), _p(out))
+    if R < 0:
+        raise ValueError("tree larger than the uniform arrays")
+    return acc, out
 
 
 # ---------------------------------------------------------------------------
