@@ -56,7 +56,7 @@ extern "C" {
 
 E3_API const char* eagle3_last_error(void) { return g_err; }
 
-E3_API int eagle3_abi_version(void) { return 1; }
+E3_API int eagle3_abi_version(void) { return 2; }
 
 E3_API uint64_t eagle3_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -85,33 +85,59 @@ E3_API e3_status eagle3_fuse(const void* h_low, const void* h_mid, const void* h
   return launch_gemm_simt(h_low, h_mid, h_high, d, W_f, bias, g, dt == E3_F32, M, d_out, 3 * d, dt, s);
 }
 
+static e3_status check_expand(const char* fn, const float* draft_logits, int B, int F, int V, int k, int W,
+                              float inv_temp, const float* parent_score, const int32_t* parent_id, int depth,
+                              int cand_offset, const e3_cand* cands, int32_t* next_id, float* next_score) {
+  E3_REQUIRE(draft_logits && parent_score && parent_id && cands && next_id && next_score, E3_ERR_INVALID_ARG,
+             "%s: null pointer", fn);
+  E3_REQUIRE(cands->tok && cands->parent && cands->score && cands->depth, E3_ERR_INVALID_ARG,
+             "%s: null candidate array", fn);
+  E3_REQUIRE(B >= 1 && F >= 1 && V >= 1, E3_ERR_SHAPE, "%s: B, F, V must be positive", fn);
+  E3_REQUIRE(k >= 1 && k <= E3_MAX_TOPK && k <= V, E3_ERR_SHAPE, "%s: k=%d out of [1, min(%d, V)]", fn, k,
+             E3_MAX_TOPK);
+  E3_REQUIRE(F * k <= 2048, E3_ERR_SHAPE, "%s: F*k=%d > 2048", fn, F * k);
+  E3_REQUIRE(W >= 1 && (W <= E3_MAX_FRONTIER || W >= F * k), E3_ERR_SHAPE, "%s: W=%d", fn, W);
+  E3_REQUIRE(depth >= 1 && depth <= E3_MAX_DEPTH, E3_ERR_SHAPE, "%s: depth=%d", fn, depth);
+  E3_REQUIRE(cands->cap >= 1 && cands->cap <= E3_MAX_CAND, E3_ERR_SHAPE, "%s: cap=%d", fn, cands->cap);
+  E3_REQUIRE(cand_offset >= 0 && cand_offset + F * k <= cands->cap, E3_ERR_CAPACITY,
+             "%s: cand_offset %d + F*k %d exceeds cap %d", fn, cand_offset, F * k, cands->cap);
+  E3_REQUIRE(static_cast<long>(B) * F <= 2147483647L / 1, E3_ERR_SHAPE, "%s: too many rows", fn);
+  E3_REQUIRE(inv_temp > 0.0f && inv_temp < 1e30f, E3_ERR_INVALID_ARG, "%s: inv_temp must be > 0", fn);
+  return E3_OK;
+}
+
 E3_API e3_status eagle3_expand(const float* draft_logits, int B, int F, int V, int k, int W, float inv_temp,
                         const float* parent_score, const int32_t* parent_id, int depth, int cand_offset,
                         const e3_cand* cands, int32_t* next_id, float* next_score, int32_t* dev_err,
                         e3_stream_t stream) {
   g_err[0] = 0;
-  E3_REQUIRE(draft_logits && parent_score && parent_id && cands && next_id && next_score, E3_ERR_INVALID_ARG,
-             "eagle3_expand: null pointer");
-  E3_REQUIRE(cands->tok && cands->parent && cands->score && cands->depth, E3_ERR_INVALID_ARG,
-             "eagle3_expand: null candidate array");
-  E3_REQUIRE(B >= 1 && F >= 1 && V >= 1, E3_ERR_SHAPE, "eagle3_expand: B, F, V must be positive");
-  E3_REQUIRE(k >= 1 && k <= E3_MAX_TOPK && k <= V, E3_ERR_SHAPE, "eagle3_expand: k=%d out of [1, min(%d, V)]", k,
-             E3_MAX_TOPK);
-  E3_REQUIRE(F * k <= 2048, E3_ERR_SHAPE, "eagle3_expand: F*k=%d > 2048", F * k);
-  E3_REQUIRE(W >= 1 && (W <= E3_MAX_FRONTIER || W >= F * k), E3_ERR_SHAPE, "eagle3_expand: W=%d", W);
-  E3_REQUIRE(depth >= 1 && depth <= E3_MAX_DEPTH, E3_ERR_SHAPE, "eagle3_expand: depth=%d", depth);
-  E3_REQUIRE(cands->cap >= 1 && cands->cap <= E3_MAX_CAND, E3_ERR_SHAPE, "eagle3_expand: cap=%d", cands->cap);
-  E3_REQUIRE(cand_offset >= 0 && cand_offset + F * k <= cands->cap, E3_ERR_CAPACITY,
-             "eagle3_expand: cand_offset %d + F*k %d exceeds cap %d", cand_offset, F * k, cands->cap);
-  E3_REQUIRE(static_cast<long>(B) * F <= 2147483647L / 1, E3_ERR_SHAPE, "eagle3_expand: too many rows");
-  E3_REQUIRE(inv_temp > 0.0f && inv_temp < 1e30f, E3_ERR_INVALID_ARG, "eagle3_expand: inv_temp must be > 0");
+  const e3_status st = check_expand("eagle3_expand", draft_logits, B, F, V, k, W, inv_temp, parent_score, parent_id,
+                                    depth, cand_offset, cands, next_id, next_score);
+  if (st != E3_OK) return st;
   return launch_expand(draft_logits, B, F, V, k, W, inv_temp, parent_score, parent_id, depth, cand_offset,
-                       *cands, next_id, next_score, dev_err, reinterpret_cast<cudaStream_t>(stream));
+                       *cands, next_id, next_score, false, 0ull, nullptr, dev_err,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+E3_API e3_status eagle3_expand_sampled(const float* draft_logits, int B, int F, int V, int k, int W, float inv_temp,
+                                       const float* parent_score, const int32_t* parent_id, int depth,
+                                       int cand_offset, const e3_cand* cands, int32_t* next_id, float* next_score,
+                                       uint64_t seed, e3_qstat* q_stats, int32_t* dev_err, e3_stream_t stream) {
+  g_err[0] = 0;
+  const e3_status st = check_expand("eagle3_expand_sampled", draft_logits, B, F, V, k, W, inv_temp, parent_score,
+                                    parent_id, depth, cand_offset, cands, next_id, next_score);
+  if (st != E3_OK) return st;
+  E3_REQUIRE(q_stats, E3_ERR_INVALID_ARG, "eagle3_expand_sampled: null q_stats");
+  E3_REQUIRE(V < (1 << 24) && F < 4096 && B < (1 << 20), E3_ERR_SHAPE,
+             "eagle3_expand_sampled: V=%d F=%d B=%d beyond the draw counter's fields", V, F, B);
+  return launch_expand(draft_logits, B, F, V, k, W, inv_temp, parent_score, parent_id, depth, cand_offset,
+                       *cands, next_id, next_score, true, seed, q_stats, dev_err,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 E3_API e3_status tree_build_mask(const e3_cand* cands, int B, int n_cand, int N, const int32_t* root_tok,
                           const int32_t* kv_len, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* pos,
-                          uint64_t* mask, e3_stream_t stream) {
+                          uint64_t* mask, int32_t* node_cand, e3_stream_t stream) {
   g_err[0] = 0;
   E3_REQUIRE(cands && root_tok && kv_len && tok && parent && depth && pos && mask, E3_ERR_INVALID_ARG,
              "tree_build_mask: null pointer");
@@ -122,7 +148,7 @@ E3_API e3_status tree_build_mask(const e3_cand* cands, int B, int n_cand, int N,
              "tree_build_mask: n_cand=%d cap=%d", n_cand, cands->cap);
   E3_REQUIRE(N >= 1 && N <= n_cand && N <= E3_MAX_NODES, E3_ERR_SHAPE, "tree_build_mask: N=%d (n_cand=%d, max %d)",
              N, n_cand, E3_MAX_NODES);
-  return launch_tree_build(*cands, B, n_cand, N, root_tok, kv_len, tok, parent, depth, pos, mask,
+  return launch_tree_build(*cands, B, n_cand, N, root_tok, kv_len, tok, parent, depth, pos, mask, node_cand,
                            reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -181,12 +207,32 @@ E3_API e3_status spec_accept(const int32_t* tok, const int32_t* parent, int B, i
   E3_REQUIRE(tok && parent && logits && row_max && row_Q && row_argmax && temp && u_acc && u_bonus && acc_len &&
                  path && out_tok && status,
              E3_ERR_INVALID_ARG, "spec_accept: null pointer");
+  E3_REQUIRE(mode != E3_ACCEPT_SAMPLED, E3_ERR_UNSUPPORTED,
+             "spec_accept: E3_ACCEPT_SAMPLED needs the draft statistics: call spec_accept_sampled");
   E3_REQUIRE(mode == E3_ACCEPT_TREE_DET, E3_ERR_UNSUPPORTED, "spec_accept: mode %d not supported", mode);
   E3_REQUIRE(B >= 1 && R >= 1 && R <= E3_MAX_NODES + 1, E3_ERR_SHAPE, "spec_accept: B=%d R=%d", B, R);
   E3_REQUIRE(D >= 0 && D <= E3_MAX_DEPTH, E3_ERR_SHAPE, "spec_accept: D=%d", D);
   E3_REQUIRE(V >= 1, E3_ERR_SHAPE, "spec_accept: V=%d", V);
   return launch_accept(tok, parent, B, R, D, logits, row_max, row_Q, row_argmax, V, temp, u_acc, u_bonus, acc_len,
                        path, out_tok, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+E3_API e3_status spec_accept_sampled(const int32_t* tok, const int32_t* parent, const int32_t* node_cand, int B, int R,
+                                     int D, const float* logits, const float* row_max, const uint64_t* row_Q,
+                                     const int32_t* row_argmax, int V, const float* temp, const e3_qstat* q_stats,
+                                     int q_cap, const uint32_t* u_acc, const uint32_t* u_bonus, int32_t* acc_len,
+                                     int32_t* path, int32_t* out_tok, int32_t* status, e3_stream_t stream) {
+  g_err[0] = 0;
+  E3_REQUIRE(tok && parent && node_cand && logits && row_max && row_Q && row_argmax && temp && q_stats && u_acc &&
+                 u_bonus && acc_len && path && out_tok && status,
+             E3_ERR_INVALID_ARG, "spec_accept_sampled: null pointer");
+  E3_REQUIRE(B >= 1 && R >= 1 && R <= E3_MAX_NODES + 1, E3_ERR_SHAPE, "spec_accept_sampled: B=%d R=%d", B, R);
+  E3_REQUIRE(D >= 0 && D <= E3_MAX_DEPTH, E3_ERR_SHAPE, "spec_accept_sampled: D=%d", D);
+  E3_REQUIRE(V >= 1 && V < (1 << 24), E3_ERR_SHAPE, "spec_accept_sampled: V=%d", V);
+  E3_REQUIRE(q_cap >= 1 && q_cap <= E3_MAX_CAND + 1, E3_ERR_SHAPE, "spec_accept_sampled: q_cap=%d", q_cap);
+  return launch_accept_sampled(tok, parent, node_cand, B, R, D, logits, row_max, row_Q, row_argmax, V, temp, q_stats,
+                               q_cap, u_acc, u_bonus, acc_len, path, out_tok, status,
+                               reinterpret_cast<cudaStream_t>(stream));
 }
 
 E3_API e3_status kv_compact(const e3_kv_layer* layers, int L, int B, const int32_t* path, const int32_t* acc_len, int D,

@@ -221,6 +221,21 @@ __device__ __forceinline__ uint64_t mulhi32(uint32_t u, uint64_t R) {
   return (hi << 32) | (lo >> 32);
 }
 
+// floor(a * b / c) for c > 0 and a * b < 2^128.
+__device__ __forceinline__ uint64_t muldiv_u64(uint64_t a, uint64_t b, uint64_t c) {
+  const unsigned __int128 p = static_cast<unsigned __int128>(a) * b;
+  return static_cast<uint64_t>(p / c);
+}
+
+// SplitMix64 (Steele, Lea & Flood, OOPSLA 2014): output number i >= 1 of the
+// stream started at `seed` is mix(seed + i * 0x9E3779B97F4A7C15).
+__device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t i) {
+  uint64_t z = seed + i * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
 // Order-preserving map of a finite float to uint32 (-0 folded onto +0).
 __device__ __forceinline__ uint32_t ord_f32(float f) {
   f = __fadd_rn(f, 0.0f);

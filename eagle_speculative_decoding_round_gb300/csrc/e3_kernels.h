@@ -15,12 +15,12 @@ struct CompactLayers {
 
 e3_status launch_expand(const float* logits, int B, int F, int V, int k, int W, float inv_temp,
                         const float* parent_score, const int32_t* parent_id, int depth, int cand_offset,
-                        const e3_cand& c, int32_t* next_id, float* next_score, int32_t* dev_err,
-                        cudaStream_t s);
+                        const e3_cand& c, int32_t* next_id, float* next_score, bool sampled, uint64_t seed,
+                        e3_qstat* q_stats, int32_t* dev_err, cudaStream_t s);
 
 e3_status launch_tree_build(const e3_cand& c, int B, int n_cand, int N, const int32_t* root_tok,
                             const int32_t* kv_len, int32_t* tok, int32_t* parent, int32_t* depth, int32_t* pos,
-                            uint64_t* mask, cudaStream_t s);
+                            uint64_t* mask, int32_t* node_cand, cudaStream_t s);
 
 size_t verify_workspace_bytes(int B, int R, int H, int KVH, int hd, int max_kv_len, bool mma);
 bool verify_uses_mma(e3_dtype dt, int hd);
@@ -59,6 +59,12 @@ e3_status launch_accept(const int32_t* tok, const int32_t* parent, int B, int R,
                         const float* row_max, const uint64_t* row_Q, const int32_t* row_argmax, int V,
                         const float* temp, const uint32_t* u_acc, const uint32_t* u_bonus, int32_t* acc_len,
                         int32_t* path, int32_t* out_tok, int32_t* status, cudaStream_t s);
+
+e3_status launch_accept_sampled(const int32_t* tok, const int32_t* parent, const int32_t* node_cand, int B, int R,
+                                int D, const float* logits, const float* row_max, const uint64_t* row_Q,
+                                const int32_t* row_argmax, int V, const float* temp, const e3_qstat* q_stats,
+                                int q_cap, const uint32_t* u_acc, const uint32_t* u_bonus, int32_t* acc_len,
+                                int32_t* path, int32_t* out_tok, int32_t* status, cudaStream_t s);
 
 e3_status launch_compact(const CompactLayers& layers, const e3_kv_layer& geo, int L, int B, const int32_t* path,
                          const int32_t* acc_len, int D, int32_t* kv_len, int32_t* dev_err, cudaStream_t s);

@@ -33,6 +33,70 @@ namespace {
 constexpr int kAcceptThreads = 512;
 constexpr int kMaxR = E3_MAX_NODES + 1;
 
+namespace cg = cooperative_groups;
+
+// Inverse-CDF draw over residual masses spread across the cluster: CTA r holds
+// the masses of tokens [j0_r, j0_r + n_r) in qbuf[0, n_r) (chunks in rank order).
+// Finds the smallest token whose cumulative mass exceeds x: the chunk sums are
+// exchanged through distributed shared memory, the CTA whose chunk holds x
+// locates the warp, and that warp scans 32 tokens at a time.  Sets *s_bonus in
+// that CTA (untouched if the total is <= x) and returns its rank (0 if none).
+// Every thread of every CTA calls it; qbuf is complete and visible on entry.
+__device__ int cluster_inverse_cdf(cg::cluster_group& cluster, const unsigned long long* qbuf, int n, int j0,
+                                   uint64_t x, unsigned long long* s_wsum, unsigned long long* s_sum,
+                                   int* s_bonus) {
+  const int CL = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  // per-warp sums of contiguous sub-segments
+  const int wseg = (n + nw - 1) / nw;
+  const int a0 = min(n, w * wseg), a1 = min(n, a0 + wseg);
+  uint64_t local = 0;
+  for (int j = a0 + lane; j < a1; j += 32) local += qbuf[j];
+  local = warp_reduce(local, SumU64());
+  if (lane == 0) s_wsum[w] = local;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint64_t tot = 0;
+    for (int i = 0; i < nw; ++i) tot += s_wsum[i];
+    *s_sum = tot;
+  }
+  cluster.sync();  // chunk sums visible
+  uint64_t excl = 0;
+  int found = -1;
+  for (int r = 0; r < CL; ++r) {  // the chunk sums partition [0, total)
+    const uint64_t sr = *cluster.map_shared_rank(s_sum, r);
+    if (found < 0 && x >= excl && x < excl + sr) found = r;
+    excl += sr;
+  }
+  if (found == rank) {
+    uint64_t wex = 0;
+    for (int r = 0; r < rank; ++r) wex += *cluster.map_shared_rank(s_sum, r);
+    for (int i = 0; i < w; ++i) wex += s_wsum[i];
+    if (x >= wex && x < wex + s_wsum[w]) {  // uniform within the warp
+      uint64_t base = wex;
+      for (int c0 = a0; c0 < a1; c0 += 32) {
+        const int j = c0 + lane;
+        const uint64_t q = j < a1 ? qbuf[j] : 0ull;
+        uint64_t incl = q;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, base + incl > x);
+        if (hit) {
+          if (lane == __ffs(hit) - 1) *s_bonus = j0 + j;
+          break;
+        }
+        base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
+    }
+  }
+  __syncthreads();
+  return found < 0 ? 0 : found;
+}
+
 __global__ void __launch_bounds__(kAcceptThreads)
 accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ parent, int R, int D,
               const float* __restrict__ logits, const float* __restrict__ row_max,
@@ -40,7 +104,6 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
               const float* __restrict__ temp, const uint32_t* __restrict__ u_acc,
               const uint32_t* __restrict__ u_bonus, int32_t* acc_len, int32_t* path, int32_t* out_tok,
               int32_t* status) {
-  namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
@@ -169,54 +232,7 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
       }
     }
     __syncthreads();
-    // per-warp sums of contiguous sub-segments
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    const int wseg = (n + nw - 1) / nw;
-    const int a0 = min(n, w * wseg), a1 = min(n, a0 + wseg);
-    uint64_t local = 0;
-    for (int j = a0 + lane; j < a1; j += 32) local += qbuf[j];
-    local = warp_reduce(local, SumU64());
-    if (lane == 0) s_wsum[w] = local;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      uint64_t tot = 0;
-      for (int i = 0; i < nw; ++i) tot += s_wsum[i];
-      s_sum = tot;
-    }
-    cluster.sync();  // chunk sums visible
-    uint64_t excl = 0;
-    int found = -1;
-    for (int r = 0; r < CL; ++r) {  // the chunk sums partition [0, Rmass)
-      const uint64_t sr = *cluster.map_shared_rank(&s_sum, r);
-      if (found < 0 && x >= excl && x < excl + sr) found = r;
-      excl += sr;
-    }
-    writer = found < 0 ? 0 : found;
-    if (found == rank) {
-      uint64_t wex = 0;
-      for (int r = 0; r < rank; ++r) wex += *cluster.map_shared_rank(&s_sum, r);
-      for (int i = 0; i < w; ++i) wex += s_wsum[i];
-      if (x >= wex && x < wex + s_wsum[w]) {  // uniform within the warp
-        uint64_t base = wex;
-        for (int c0 = a0; c0 < a1; c0 += 32) {
-          const int j = c0 + lane;
-          const uint64_t q = j < a1 ? qbuf[j] : 0ull;
-          uint64_t incl = q;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += y;
-          }
-          const unsigned hit = __ballot_sync(0xFFFFFFFFu, base + incl > x);
-          if (hit) {
-            if (lane == __ffs(hit) - 1) s_bonus = j0 + j;
-            break;
-          }
-          base += __shfl_sync(0xFFFFFFFFu, incl, 31);
-        }
-      }
-    }
-    __syncthreads();
+    writer = cluster_inverse_cdf(cluster, qbuf, n, j0, x, s_wsum, &s_sum, &s_bonus);
   }
   if (rank == writer && threadIdx.x == 0) {
     const int a = err ? 0 : s_acc;
@@ -235,6 +251,240 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
     status[b] = err;
   }
   cluster.sync();  // peers may still read this CTA's chunk sum
+}
+
+// Children drawn from the draft distribution q (eagle3_expand_sampled): accept
+// with min(1, p_res / q_res), residual max(0, p_res - q_res) on each rejection.
+// One cluster of CL CTAs per request walks the tree in lockstep: every CTA's
+// thread 0 takes the same decisions from the same integers.  CTA r keeps the
+// target residual masses R_j of its vocabulary chunk in qbuf once a rejection
+// at the current node has made them differ from the row's plain masses
+// (`fresh` until then), and a bit per token of the chunk for the draft tokens
+// already rejected at this node.  A rejection costs one pass over the chunk
+// (new R_j and their sum) and two cluster barriers; an acceptance test reads
+// R_t from the owning CTA's shared memory.
+__global__ void __launch_bounds__(kAcceptThreads)
+accept_sampled_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ parent,
+                      const int32_t* __restrict__ node_cand, int R, int D, const float* __restrict__ logits,
+                      const float* __restrict__ row_max, const uint64_t* __restrict__ row_Q,
+                      const int32_t* __restrict__ row_argmax, int V, const float* __restrict__ temp,
+                      const e3_qstat* __restrict__ qs, int q_cap, const uint32_t* __restrict__ u_acc,
+                      const uint32_t* __restrict__ u_bonus, int32_t* acc_len, int32_t* path, int32_t* out_tok,
+                      int32_t* status) {
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int b = blockIdx.x / CL;
+  const int per = (V + CL - 1) / CL;
+  const int j0 = min(V, rank * per), j1 = min(V, j0 + per);
+  const int n = j1 - j0;
+  const int nwords = (per + 31) >> 5;
+  extern __shared__ unsigned long long qbuf[];                     // [per] R_j of this CTA's tokens
+  uint32_t* rbits = reinterpret_cast<uint32_t*>(qbuf + per);      // [nwords] rejected draft tokens
+  __shared__ int s_tok[kMaxR], s_par[kMaxR], s_nch[kMaxR], s_first[kMaxR + 1], s_child[kMaxR];
+  __shared__ int s_removed[kMaxR];
+  __shared__ int s_path[E3_MAX_DEPTH + 1];
+  __shared__ int s_nrem, s_u, s_a, s_err, s_bonus, s_fresh, s_dec, s_t, s_am;
+  __shared__ unsigned long long s_SR, s_SD, s_Dt, s_part, s_sum;
+  __shared__ unsigned long long s_wsum[kAcceptThreads / 32];
+  __shared__ uint64_t s_red[32];
+  __shared__ float s_mp, s_mq, s_itq;
+  __shared__ const float* s_zq;
+
+  pdl_wait();
+  pdl_trigger();
+  const size_t rb = static_cast<size_t>(b) * R;
+  const float T = temp[b];
+  const float it = inv_temp(T);
+  for (int i = threadIdx.x; i < R; i += blockDim.x) {
+    s_tok[i] = tok[rb + i];
+    s_par[i] = parent[rb + i];
+  }
+  for (int w = threadIdx.x; w < nwords; w += blockDim.x) rbits[w] = 0u;
+  __syncthreads();
+  // children lists in CSR form, children in ascending flat order (= draw order)
+  for (int u = threadIdx.x; u < R; u += blockDim.x) {
+    int cnt = 0;
+    for (int c = u + 1; c < R; ++c) cnt += (s_par[c] == u);
+    s_nch[u] = cnt;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int u = 0; u < R; ++u) {
+      s_first[u] = acc;
+      acc += s_nch[u];
+    }
+    s_first[R] = acc;
+    s_err = 0;
+    s_bonus = -1;
+    s_path[0] = 0;
+    s_u = 0;
+    s_a = 0;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < R; c += blockDim.x) {
+    const int p = s_par[c];
+    if (c == 0 || p < 0 || p >= c) continue;
+    int rk = 0;
+    for (int c2 = p + 1; c2 < c; ++c2) rk += (s_par[c2] == p);
+    s_child[s_first[p] + rk] = c;
+  }
+  __syncthreads();
+
+  for (;;) {  // one iteration per visited node, uniform across the cluster
+    if (threadIdx.x == 0) {
+      const int u = s_u;
+      const size_t row = rb + u;
+      s_mp = row_max[row];
+      s_am = row_argmax[row];
+      s_SR = row_Q[row];
+      s_fresh = 1;
+      s_nrem = 0;
+      s_SD = 0ull;
+      s_zq = nullptr;
+      if (s_am < 0 || !isfinite(s_mp)) s_err = E3_DEV_ERR_NONFINITE;
+      if (!s_err && T > 0.0f && s_nch[u] > 0) {
+        const int nc = node_cand[row];
+        const e3_qstat* q = (nc >= -1 && nc + 1 < q_cap) ? qs + static_cast<size_t>(b) * q_cap + (nc + 1) : nullptr;
+        if (q == nullptr || q->row == nullptr || !isfinite(q->m) || q->Q == 0ull) {
+          s_err = E3_DEV_ERR_NONFINITE;
+        } else {
+          s_zq = q->row;
+          s_SD = q->Q;
+          s_mq = q->m;
+          s_itq = q->inv_temp;
+        }
+      }
+    }
+    __syncthreads();
+    if (s_err) break;
+    const int u = s_u;
+    const size_t row = rb + u;
+    const float* z = logits + row * V;
+    int accepted = -1;
+    for (int e = s_first[u]; e < s_first[u] + s_nch[u]; ++e) {
+      const int c = s_child[e];
+      if (threadIdx.x == 0) {
+        const int t = s_tok[c];
+        int dec = 2;  // 0 reject, 1 accept, 2 skip (not a draw)
+        if (T <= 0.0f) {
+          dec = (t == s_am) ? 1 : 2;
+        } else if (t >= 0 && t < V) {
+          bool rem = false;
+          for (int i = 0; i < s_nrem; ++i) rem |= (s_removed[i] == t);
+          const uint64_t Dt = rem ? 0ull : fx_mass(__fmul_rn(s_zq[t], s_itq), s_mq);
+          if (Dt != 0ull) {
+            uint64_t Rt;
+            if (s_fresh) {
+              Rt = fx_mass(__fmul_rn(z[t], it), s_mp);
+            } else {
+              const int owner = t / per;
+              Rt = cluster.map_shared_rank(qbuf, owner)[t - owner * per];
+            }
+            const uint64_t qt = muldiv_u64(Dt, s_SR, s_SD);
+            const unsigned __int128 lhs = static_cast<unsigned __int128>(u_acc[rb + c]) * qt;
+            dec = lhs < (static_cast<unsigned __int128>(Rt) << 32) ? 1 : 0;
+            s_Dt = Dt;
+            s_t = t;
+          }
+        }
+        s_dec = dec;
+      }
+      __syncthreads();
+      const int dec = s_dec;
+      __syncthreads();  // everyone has read s_dec before thread 0 may write it again
+      if (dec == 1) {
+        accepted = c;
+        break;
+      }
+      if (dec == 2) continue;
+      // rejection: the residual pass over this CTA's tokens
+      cluster.sync();  // no CTA still reads a peer's qbuf for the decision above
+      const bool fresh = s_fresh != 0;
+      const uint64_t SR = s_SR, SD = s_SD;
+      const float mq = s_mq, itq = s_itq, mp = s_mp;
+      const float* zq = s_zq;
+      uint64_t local = 0;
+      for (int j = threadIdx.x; j < n; j += blockDim.x) {
+        const int tj = j0 + j;
+        const bool rem = (rbits[j >> 5] >> (j & 31)) & 1u;
+        const uint64_t Dj = rem ? 0ull : fx_mass(__fmul_rn(zq[tj], itq), mq);
+        uint64_t Rj = fresh ? fx_mass(__fmul_rn(z[tj], it), mp) : qbuf[j];
+        const uint64_t qj = Dj ? muldiv_u64(Dj, SR, SD) : 0ull;
+        Rj = Rj > qj ? Rj - qj : 0ull;
+        qbuf[j] = Rj;
+        local += Rj;
+      }
+      local = block_reduce(local, SumU64(), s_red);
+      if (threadIdx.x == 0) {
+        s_part = local;
+        const int t = s_t;
+        if (t >= j0 && t < j1) rbits[(t - j0) >> 5] |= 1u << ((t - j0) & 31);
+      }
+      cluster.sync();  // partial sums and residuals visible
+      if (threadIdx.x == 0) {
+        uint64_t tot = 0;
+        for (int r = 0; r < CL; ++r) tot += *cluster.map_shared_rank(&s_part, r);
+        s_SR = tot;
+        s_SD -= s_Dt;
+        s_removed[s_nrem++] = s_t;
+        s_fresh = 0;
+      }
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      if (accepted >= 0 && s_a < D) {
+        s_a += 1;
+        s_path[s_a] = accepted;
+        s_u = accepted;
+        s_dec = 3;
+      } else {
+        s_dec = 4;
+      }
+    }
+    __syncthreads();
+    const bool stop = s_dec == 4;
+    for (int w = threadIdx.x; w < nwords; w += blockDim.x) rbits[w] = 0u;  // the next node starts afresh
+    __syncthreads();
+    if (stop) break;
+  }
+
+  const int err = s_err;
+  int writer = 0;
+  if (!err && T > 0.0f) {
+    const int u = s_u;
+    const uint64_t x = mulhi32(u_bonus[rb + u], s_SR);
+    const float* z = logits + (rb + u) * V;
+    const float mp = s_mp;
+    const bool fresh = s_fresh != 0;
+    cluster.sync();  // no CTA still reads a peer's qbuf
+    if (fresh) {
+#pragma unroll 4
+      for (int j = threadIdx.x; j < n; j += blockDim.x) qbuf[j] = fx_mass(__fmul_rn(z[j0 + j], it), mp);
+    }
+    __syncthreads();
+    writer = cluster_inverse_cdf(cluster, qbuf, n, j0, x, s_wsum, &s_sum, &s_bonus);
+  } else if (!err && threadIdx.x == 0) {
+    s_bonus = s_am;
+  }
+  if (rank == writer && threadIdx.x == 0) {
+    const int a = err ? 0 : s_a;
+    const size_t o = static_cast<size_t>(b) * (D + 1);
+    for (int j = 0; j <= D; ++j) {
+      path[o + j] = (!err && j <= a) ? s_path[j] : -1;
+      out_tok[o + j] = -1;
+    }
+    if (err) {
+      path[o] = 0;
+    } else {
+      for (int j = 1; j <= a; ++j) out_tok[o + j - 1] = s_tok[s_path[j]];
+      out_tok[o + a] = s_bonus;
+    }
+    acc_len[b] = a;
+    status[b] = err;
+  }
+  cluster.sync();  // peers may still read this CTA's shared memory
 }
 
 int accept_cluster_size() {
@@ -261,7 +511,57 @@ int accept_cluster_size() {
   return cl;
 }
 
+// 16-CTA clusters of accept_sampled_kernel where the GPU allows them, else 8.
+int accept_sampled_cluster_size(int V) {
+  static int cached_v = -1, cl = 8;
+  if (cached_v != V) {
+    cl = 8;
+    cached_v = V;
+    if (cudaFuncSetAttribute(accept_sampled_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16);
+      cfg.blockDim = dim3(kAcceptThreads);
+      const int per = (V + 15) / 16;
+      cfg.dynamicSmemBytes = static_cast<size_t>(per) * 8 + static_cast<size_t>((per + 31) / 32) * 4 + 16;
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = 16;
+      at.val.clusterDim.y = 1;
+      at.val.clusterDim.z = 1;
+      cfg.attrs = &at;
+      cfg.numAttrs = 1;
+      int nclu = 0;
+      if (cudaOccupancyMaxActiveClusters(&nclu, accept_sampled_kernel, &cfg) == cudaSuccess && nclu > 0) cl = 16;
+    }
+    cudaGetLastError();
+  }
+  return cl;
+}
+
 }  // namespace
+
+e3_status launch_accept_sampled(const int32_t* tok, const int32_t* parent, const int32_t* node_cand, int B, int R,
+                                int D, const float* logits, const float* row_max, const uint64_t* row_Q,
+                                const int32_t* row_argmax, int V, const float* temp, const e3_qstat* q_stats,
+                                int q_cap, const uint32_t* u_acc, const uint32_t* u_bonus, int32_t* acc_len,
+                                int32_t* path, int32_t* out_tok, int32_t* status, cudaStream_t s) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaFuncSetAttribute(accept_sampled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr_done = true;
+  }
+  const int CL = accept_sampled_cluster_size(V);
+  const int per = (V + CL - 1) / CL;
+  const size_t smem = static_cast<size_t>(per) * 8 + static_cast<size_t>((per + 31) / 32) * 4 + 16;
+  E3_REQUIRE(smem <= 200 * 1024, E3_ERR_SHAPE, "spec_accept_sampled: V=%d too large", V);
+  E3_REQUIRE(static_cast<long>(B) * CL < (1L << 31), E3_ERR_SHAPE, "spec_accept_sampled: B=%d too large", B);
+  cudaError_t e = launch_pdl(accept_sampled_kernel, dim3(B * CL), dim3(kAcceptThreads), smem, s,
+                             static_cast<unsigned>(CL), tok, parent, node_cand, R, D, logits, row_max, row_Q,
+                             row_argmax, V, temp, q_stats, q_cap, u_acc, u_bonus, acc_len, path, out_tok, status);
+  if (e != cudaSuccess) return cuda_status(e, "accept_sampled_kernel");
+  return E3_OK;
+}
 
 e3_status launch_accept(const int32_t* tok, const int32_t* parent, int B, int R, int D, const float* logits,
                         const float* row_max, const uint64_t* row_Q, const int32_t* row_argmax, int V,

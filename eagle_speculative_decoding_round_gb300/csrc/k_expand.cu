@@ -119,11 +119,20 @@ __device__ __forceinline__ bool mb_wait0(uint64_t* b) {
 // sends its maximum key and non-finite flag to every CTA (each then knows the row
 // maximum m), and its mass and top-k list to CTA 0, which merges and writes the
 // k children.
-template <int KMAX>
+//
+// SAMPLED: the children are drawn from the row's draft distribution instead of
+// taken as its top k.  Once the row maximum m is known, each CTA makes one pass
+// over its staged values that computes the fixed-point masses and overwrites
+// each s_j with minus the token's arrival time E_j / e_j (e_j = E(s_j - m),
+// E_j = -ln U_j from the counter-based stream), so that the same top-k machinery
+// picks the k earliest arrivals; CTA 0 re-reads s of the chosen tokens for the
+// scores and records the row's draft statistics.
+template <int KMAX, bool SAMPLED>
 __global__ void __launch_bounds__(kExpandThreads, 2)
 expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float it,
                    const float* __restrict__ parent_score, const int32_t* __restrict__ parent_id,
-                   int depth, int cand_offset, e3_cand c, int32_t* dev_err, int cand_cap) {
+                   int depth, int cand_offset, e3_cand c, int32_t* dev_err, int cand_cap, uint64_t seed,
+                   e3_qstat* qs) {
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = static_cast<int>(cluster.num_blocks());
@@ -245,64 +254,69 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     }
   };
   uint64_t* cand = reinterpret_cast<uint64_t*>(chunk4 + (per + 1));
-  uint64_t thr = ~0ull;
-  if (k <= kExpandThreads / 32) {
-    for (int w = 0; w < kExpandThreads / 32; ++w) thr = min(thr, s_wmax[w]);
-    // value part of the threshold: a cheap first filter (none if some warp has no element)
-    const float thr_v = thr == 0ull ? -INFINITY : unord_f32(static_cast<uint32_t>(thr >> 32));
-    for_own([&](float v, uint32_t id) {
-      if (v < thr_v) return;
-      const uint64_t key = pack_best(v, id);
-      if (key >= thr && key != 0ull) {
-        const int at = atomicAdd(&s_cnt, 1);
-        if (at < cand_cap) cand[at] = key;
-      }
-    });
-  }
-  __syncthreads();
-  if (k > kExpandThreads / 32 || s_cnt > cand_cap) {
-    // exact threshold: the k-th largest per-thread maximum
-    {
-      uint64_t v = tmax;
-      for (int r = 0; r < k; ++r) {
-        const uint64_t bst = warp_reduce(v, MaxU64());
-        if (v == bst) v = 0ull;  // keys are distinct: exactly one lane (or all-zero lanes)
-        if (lane == 0) warp_lists[warp][r] = bst;
-      }
+  // this CTA's best k keys of the staged values -> ltop[] (s_wmax holds the warp
+  // maxima of the per-thread best keys tkey, s_cnt is 0; both visible)
+  auto local_topk = [&](uint64_t tkey) {
+    uint64_t thr = ~0ull;
+    if (k <= kExpandThreads / 32) {
+      for (int w = 0; w < kExpandThreads / 32; ++w) thr = min(thr, s_wmax[w]);
+      // value part of the threshold: a cheap first filter (none if some warp has no element)
+      const float thr_v = thr == 0ull ? -INFINITY : unord_f32(static_cast<uint32_t>(thr >> 32));
+      for_own([&](float v, uint32_t id) {
+        if (v < thr_v) return;
+        const uint64_t key = pack_best(v, id);
+        if (key >= thr && key != 0ull) {
+          const int at = atomicAdd(&s_cnt, 1);
+          if (at < cand_cap) cand[at] = key;
+        }
+      });
     }
     __syncthreads();
-    if (warp == 0) {
-      const int nw = blockDim.x >> 5;
-      uint64_t lk[KMAX];
+    if (k > kExpandThreads / 32 || s_cnt > cand_cap) {
+      // exact threshold: the k-th largest per-thread maximum
+      {
+        uint64_t v = tkey;
+        for (int r = 0; r < k; ++r) {
+          const uint64_t bst = warp_reduce(v, MaxU64());
+          if (v == bst) v = 0ull;  // keys are distinct: exactly one lane (or all-zero lanes)
+          if (lane == 0) warp_lists[warp][r] = bst;
+        }
+      }
+      __syncthreads();
+      if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        uint64_t lk[KMAX];
 #pragma unroll
-      for (int i = 0; i < KMAX; ++i) lk[i] = (lane < nw && i < k) ? warp_lists[lane][i] : 0ull;
-      warp_merge_topk(lk, k, top);
-    }
-    if (threadIdx.x == 0) s_cnt = 0;
-    __syncthreads();
-    thr = top[k - 1];
-    const float thr_v = thr == 0ull ? -INFINITY : unord_f32(static_cast<uint32_t>(thr >> 32));
-    for_own([&](float v, uint32_t id) {
-      if (v < thr_v) return;
-      const uint64_t key = pack_best(v, id);
-      if (key >= thr && key != 0ull) {
-        const int at = atomicAdd(&s_cnt, 1);
-        if (at < cand_cap) cand[at] = key;
+        for (int i = 0; i < KMAX; ++i) lk[i] = (lane < nw && i < k) ? warp_lists[lane][i] : 0ull;
+        warp_merge_topk(lk, k, top);
       }
-    });
+      if (threadIdx.x == 0) s_cnt = 0;
+      __syncthreads();
+      thr = top[k - 1];
+      const float thr_v = thr == 0ull ? -INFINITY : unord_f32(static_cast<uint32_t>(thr >> 32));
+      for_own([&](float v, uint32_t id) {
+        if (v < thr_v) return;
+        const uint64_t key = pack_best(v, id);
+        if (key >= thr && key != 0ull) {
+          const int at = atomicAdd(&s_cnt, 1);
+          if (at < cand_cap) cand[at] = key;
+        }
+      });
+      __syncthreads();
+    }
+    // (the bound above makes this unreachable; a dropped key would be a wrong child)
+    if (threadIdx.x == 0 && s_cnt > cand_cap) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
+    const int ncand = min(s_cnt, cand_cap);
+    if (threadIdx.x < E3_MAX_TOPK) ltop[threadIdx.x] = 0ull;
     __syncthreads();
-  }
-  // (the bound above makes this unreachable; a dropped key would be a wrong child)
-  if (threadIdx.x == 0 && s_cnt > cand_cap) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
-  const int ncand = min(s_cnt, cand_cap);
-  if (threadIdx.x < E3_MAX_TOPK) ltop[threadIdx.x] = 0ull;
-  __syncthreads();
-  for (int i = threadIdx.x; i < ncand; i += blockDim.x) {
-    const uint64_t key = cand[i];
-    int rnk = 0;
-    for (int j = 0; j < ncand; ++j) rnk += cand[j] > key;
-    if (rnk < k) ltop[rnk] = key;
-  }
+    for (int i = threadIdx.x; i < ncand; i += blockDim.x) {
+      const uint64_t key = cand[i];
+      int rnk = 0;
+      for (int j = 0; j < ncand; ++j) rnk += cand[j] > key;
+      if (rnk < k) ltop[rnk] = key;
+    }
+  };
+  if constexpr (!SAMPLED) local_topk(tmax);
   const bool got = mb_wait0(&mx_bar);
   uint64_t gbest = 0ull;
   uint32_t gbad = got ? 0u : 1u;
@@ -320,7 +334,44 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   }
   const float m = unord_f32(static_cast<uint32_t>(gbest >> 32));
   uint64_t Q = 0;
-  if (vec) {
+  if constexpr (SAMPLED) {
+    // masses, and minus the arrival time of every token, in place
+    const uint64_t ctr = (static_cast<uint64_t>(b) << 44) | (static_cast<uint64_t>(depth) << 36) |
+                         (static_cast<uint64_t>(f) << 24);
+    uint64_t tbest = 0ull;
+    auto draw = [&](float sv, uint32_t id) -> float {
+      const float e = fx_exp(__fsub_rn(sv, m));
+      const uint64_t q = fx_scale40_floor(e);
+      Q += q;
+      float v = -INFINITY;  // a token of zero mass never arrives
+      if (q != 0ull) {
+        const uint64_t u24 = splitmix64_at(seed, ctr + id + 1) >> 40;
+        const float E = __fsub_rn(0.0f, fx_ell((u24 + 1ull) << 16));
+        v = __fsub_rn(0.0f, __fdiv_rn(E, e));
+      }
+      tbest = max(tbest, pack_best(v, id));
+      return v;
+    };
+    __syncthreads();  // every read of s_wmax for the max exchange is done
+    if (vec) {
+      for (int q = threadIdx.x; q < v1 - v0; q += blockDim.x) {
+        float4 v = chunk4[q];
+        const uint32_t id = static_cast<uint32_t>(e0 + 4 * q);
+        v.x = draw(v.x, id);
+        v.y = draw(v.y, id + 1);
+        v.z = draw(v.z, id + 2);
+        v.w = draw(v.w, id + 3);
+        chunk4[q] = v;
+      }
+    } else {
+      for (int j = threadIdx.x; j < n_local; j += blockDim.x) chunk[j] = draw(chunk[j], static_cast<uint32_t>(e0 + j));
+    }
+    const uint64_t wbest = warp_reduce(tbest, MaxU64());
+    if (lane == 0) s_wmax[warp] = wbest;
+    if (threadIdx.x == 0) s_cnt = 0;
+    __syncthreads();
+    local_topk(tbest);
+  } else if (vec) {
     for (int q = threadIdx.x; q < v1 - v0; q += blockDim.x) {
       const float4 v = chunk4[q];
       Q += fx_mass_x2(v.x, v.y, m) + fx_mass_x2(v.z, v.w, m);
@@ -355,11 +406,23 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     s_Qt = t;
   }
   __syncthreads();
+  if (SAMPLED && threadIdx.x == 0) {
+    const int pid = parent_id[row];
+    if (pid >= -1 && pid < c.cap) {
+      e3_qstat st;
+      st.row = z;
+      st.Q = s_Qt;
+      st.m = m;
+      st.inv_temp = it;
+      qs[static_cast<size_t>(b) * (c.cap + 1) + (pid + 1)] = st;
+    }
+  }
   if (threadIdx.x < k) {
     const int r = threadIdx.x;
     const float ell = fx_ell(s_Qt);
     const uint32_t t = packed_id(top[r]);
-    const float sc = unord_f32(static_cast<uint32_t>(top[r] >> 32));
+    const float sc = SAMPLED ? (t < static_cast<uint32_t>(V) ? __fmul_rn(__ldg(z + t), it) : -INFINITY)
+                             : unord_f32(static_cast<uint32_t>(top[r] >> 32));
     const float ps = parent_score[row];
     const size_t ci = static_cast<size_t>(b) * c.cap + cand_offset + f * k + r;
     c.tok[ci] = static_cast<int32_t>(t);
@@ -371,12 +434,12 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
 
 // Clusters of 16 CTAs (half the work per CTA) where every row of the call still
 // fits one wave of such clusters, else clusters of 8.
-template <int KMAX>
+template <int KMAX, bool SAMPLED>
 int cluster_size_for(int rows, int V, bool vec, int k) {
   static int cached_v = -1, cached_k = -1, max16 = 0;
   if (cached_v != V || cached_k != k) {
     max16 = 0;
-    if (cudaFuncSetAttribute(expand_rows_kernel<KMAX>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+    if (cudaFuncSetAttribute(expand_rows_kernel<KMAX, SAMPLED>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
         cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(16);
@@ -390,7 +453,7 @@ int cluster_size_for(int rows, int V, bool vec, int k) {
       cfg.attrs = &at;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, expand_rows_kernel<KMAX>, &cfg) == cudaSuccess) max16 = n;
+      if (cudaOccupancyMaxActiveClusters(&n, expand_rows_kernel<KMAX, SAMPLED>, &cfg) == cudaSuccess) max16 = n;
     }
     cudaGetLastError();
     cached_v = V;
@@ -399,23 +462,23 @@ int cluster_size_for(int rows, int V, bool vec, int k) {
   return rows <= max16 ? 16 : 8;
 }
 
-template <int KMAX>
+template <int KMAX, bool SAMPLED>
 e3_status launch_rows(const float* logits, int rows, int F, int V, int k, float inv_temp, const float* parent_score,
-                      const int32_t* parent_id, int depth, int cand_offset, const e3_cand& c, int32_t* dev_err,
-                      cudaStream_t s) {
+                      const int32_t* parent_id, int depth, int cand_offset, const e3_cand& c, uint64_t seed,
+                      e3_qstat* qs, int32_t* dev_err, cudaStream_t s) {
   static bool attr_done = false;
   if (!attr_done) {
-    cudaFuncSetAttribute(expand_rows_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaFuncSetAttribute(expand_rows_kernel<KMAX, SAMPLED>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     attr_done = true;
   }
   const bool vec = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
-  const int CL = cluster_size_for<KMAX>(rows, V, vec, k);
+  const int CL = cluster_size_for<KMAX, SAMPLED>(rows, V, vec, k);
   const int cand_cap = expand_cand_cap(V, vec, k, CL);
   const size_t smem = expand_smem_bytes(V, vec, k, CL);
   E3_REQUIRE(smem <= 200 * 1024, E3_ERR_SHAPE, "eagle3_expand: V=%d too large", V);
-  const cudaError_t e = launch_pdl(expand_rows_kernel<KMAX>, dim3(rows * CL), dim3(kExpandThreads), smem, s,
-                                   static_cast<unsigned>(CL), logits, F, V, k, inv_temp, parent_score, parent_id, depth,
-                                   cand_offset, c, dev_err, cand_cap);
+  const cudaError_t e = launch_pdl(expand_rows_kernel<KMAX, SAMPLED>, dim3(rows * CL), dim3(kExpandThreads), smem,
+                                   s, static_cast<unsigned>(CL), logits, F, V, k, inv_temp, parent_score, parent_id,
+                                   depth, cand_offset, c, dev_err, cand_cap, seed, qs);
   if (e != cudaSuccess) return cuda_status(e, "expand_rows_kernel");
   return E3_OK;
 }
@@ -463,24 +526,38 @@ expand_frontier_kernel(int n, int Wn, int cand_offset, e3_cand c, int32_t* next_
   }
 }
 
+template <bool SAMPLED>
+e3_status launch_rows_k(const float* logits, int rows, int F, int V, int k, float inv_temp, const float* parent_score,
+                        const int32_t* parent_id, int depth, int cand_offset, const e3_cand& c, uint64_t seed,
+                        e3_qstat* qs, int32_t* dev_err, cudaStream_t s) {
+  if (k <= 2)
+    return launch_rows<2, SAMPLED>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c,
+                                   seed, qs, dev_err, s);
+  if (k <= 4)
+    return launch_rows<4, SAMPLED>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c,
+                                   seed, qs, dev_err, s);
+  if (k <= 8)
+    return launch_rows<8, SAMPLED>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c,
+                                   seed, qs, dev_err, s);
+  if (k <= 16)
+    return launch_rows<16, SAMPLED>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c,
+                                    seed, qs, dev_err, s);
+  return launch_rows<32, SAMPLED>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c,
+                                  seed, qs, dev_err, s);
+}
+
 }  // namespace
 
 e3_status launch_expand(const float* logits, int B, int F, int V, int k, int W, float inv_temp,
                         const float* parent_score, const int32_t* parent_id, int depth,
-                        int cand_offset, const e3_cand& c, int32_t* next_id, float* next_score,
-                        int32_t* dev_err, cudaStream_t s) {
+                        int cand_offset, const e3_cand& c, int32_t* next_id, float* next_score, bool sampled,
+                        uint64_t seed, e3_qstat* q_stats, int32_t* dev_err, cudaStream_t s) {
   const int rows = B * F;
-  e3_status st;
-  if (k <= 2)
-    st = launch_rows<2>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
-  else if (k <= 4)
-    st = launch_rows<4>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
-  else if (k <= 8)
-    st = launch_rows<8>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
-  else if (k <= 16)
-    st = launch_rows<16>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
-  else
-    st = launch_rows<32>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c, dev_err, s);
+  const e3_status st =
+      sampled ? launch_rows_k<true>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c,
+                                    seed, q_stats, dev_err, s)
+              : launch_rows_k<false>(logits, rows, F, V, k, inv_temp, parent_score, parent_id, depth, cand_offset, c,
+                                     0ull, nullptr, dev_err, s);
   if (st != E3_OK) return st;
   const int n = F * k;
   const int Wn = W < n ? W : n;

@@ -52,7 +52,7 @@ __device__ __forceinline__ uint64_t bitonic_desc_thread(uint64_t v, uint64_t* bu
 __global__ void __launch_bounds__(1024)
 tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root_tok,
                   const int32_t* __restrict__ kv_len, int32_t* tok, int32_t* parent, int32_t* depth,
-                  int32_t* pos, uint64_t* mask) {
+                  int32_t* pos, uint64_t* mask, int32_t* node_cand) {
   extern __shared__ uint64_t sh[];
   uint64_t* keys = sh;  // [2 * max(np, blockDim.x)]: the two exchange buffers, or the in-place sort
   pdl_wait();
@@ -137,6 +137,7 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
     parent[o] = my_pf;
     depth[o] = my_d;
     pos[o] = P + my_d;
+    if (node_cand) node_cand[o] = my_c;
   }
   if (i == 0) {
     const size_t o = static_cast<size_t>(b) * R;
@@ -144,6 +145,7 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
     parent[o] = -1;
     depth[o] = 0;
     pos[o] = P;
+    if (node_cand) node_cand[o] = -1;
   }
   // ancestor-or-self bit rows
   const int words = (R + 63) >> 6;
@@ -163,7 +165,7 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
 
 e3_status launch_tree_build(const e3_cand& c, int B, int n_cand, int N, const int32_t* root_tok,
                             const int32_t* kv_len, int32_t* tok, int32_t* parent, int32_t* depth,
-                            int32_t* pos, uint64_t* mask, cudaStream_t s) {
+                            int32_t* pos, uint64_t* mask, int32_t* node_cand, cudaStream_t s) {
   int np = 1;
   while (np < n_cand) np <<= 1;
   // one thread per sort key up to 1024 keys (sorted in registers and shuffles),
@@ -176,7 +178,7 @@ e3_status launch_tree_build(const e3_cand& c, int B, int n_cand, int N, const in
     if (e != cudaSuccess) return cuda_status(e, "tree_build_kernel smem attribute");
   }
   const cudaError_t e = launch_pdl(tree_build_kernel, dim3(B), dim3(threads), smem, s, 1, c, n_cand, N, root_tok, kv_len,
-                                   tok, parent, depth, pos, mask);
+                                   tok, parent, depth, pos, mask, node_cand);
   if (e != cudaSuccess) return cuda_status(e, "tree_build_kernel");
   return E3_OK;
 }

@@ -16,13 +16,13 @@ LIB_PATH = os.path.join(_HERE, "_build", "libeagle3.so")
 E3_OK = 0
 E3_F32, E3_BF16 = 0, 1
 E3_DEV_ERR_NONFINITE, E3_DEV_ERR_CAPACITY, E3_DEV_ERR_TIMEOUT = 1, 2, 4
-E3_ACCEPT_TREE_DET = 0
+E3_ACCEPT_TREE_DET, E3_ACCEPT_SAMPLED = 0, 1
 STATUS_NAMES = {0: "E3_OK", 1: "E3_ERR_INVALID_ARG", 2: "E3_ERR_SHAPE", 3: "E3_ERR_UNSUPPORTED",
                 4: "E3_ERR_CAPACITY", 5: "E3_ERR_NONFINITE", 6: "E3_ERR_CUDA", 7: "E3_ERR_TIMEOUT"}
 SYMBOLS = ["eagle3_fuse", "eagle3_fuse_workspace_bytes", "eagle3_fuse_noalloc",
-           "eagle3_fuse_noalloc_max_scratch_bytes", "eagle3_expand", "tree_build_mask",
+           "eagle3_fuse_noalloc_max_scratch_bytes", "eagle3_expand", "eagle3_expand_sampled", "tree_build_mask",
            "tree_verify_attn", "eagle3_verify_workspace_bytes", "lmhead_logits", "spec_accept",
-           "kv_compact", "eagle3_last_error", "eagle3_abi_version", "eagle3_launch_count"]
+           "spec_accept_sampled", "kv_compact", "eagle3_last_error", "eagle3_abi_version", "eagle3_launch_count"]
 
 
 class E3Error(RuntimeError):
@@ -34,6 +34,14 @@ class E3Error(RuntimeError):
 class e3_cand(ctypes.Structure):
     _fields_ = [("tok", ctypes.c_void_p), ("parent", ctypes.c_void_p), ("score", ctypes.c_void_p),
                 ("depth", ctypes.c_void_p), ("cap", ctypes.c_int)]
+
+
+class e3_qstat(ctypes.Structure):
+    _fields_ = [("row", ctypes.c_void_p), ("Q", ctypes.c_uint64), ("m", ctypes.c_float),
+                ("inv_temp", ctypes.c_float)]
+
+
+QSTAT_BYTES = ctypes.sizeof(e3_qstat)  # bytes of one e3_qstat (24)
 
 
 class e3_kv_layer(ctypes.Structure):
@@ -54,11 +62,14 @@ def _load() -> ctypes.CDLL:
         "eagle3_fuse_noalloc": (I, [P, P, P, P, P, P, I, I, I, I, P, P]),
         "eagle3_fuse_noalloc_max_scratch_bytes": (S, []),
         "eagle3_expand": (I, [P, I, I, I, I, I, F, P, P, I, I, ctypes.POINTER(e3_cand), P, P, P, P]),
-        "tree_build_mask": (I, [ctypes.POINTER(e3_cand), I, I, I, P, P, P, P, P, P, P, P]),
+        "eagle3_expand_sampled": (I, [P, I, I, I, I, I, F, P, P, I, I, ctypes.POINTER(e3_cand), P, P,
+                                      ctypes.c_uint64, P, P, P]),
+        "tree_build_mask": (I, [ctypes.POINTER(e3_cand), I, I, I, P, P, P, P, P, P, P, P, P]),
         "tree_verify_attn": (I, [P, ctypes.POINTER(e3_kv_layer), P, P, I, I, I, I, F, P, P, P, P, S, P]),
         "eagle3_verify_workspace_bytes": (S, [I, I, I, I, I, I, I]),
         "lmhead_logits": (I, [P, P, I, I, I, P, P, P, P, P, P, I, P]),
         "spec_accept": (I, [P, P, I, I, I, P, P, P, P, I, P, P, P, I, P, P, P, P, P]),
+        "spec_accept_sampled": (I, [P, P, P, I, I, I, P, P, P, P, I, P, P, I, P, P, P, P, P, P, P]),
         "kv_compact": (I, [ctypes.POINTER(e3_kv_layer), I, I, P, P, I, P, P, P]),
         "eagle3_last_error": (ctypes.c_char_p, []),
         "eagle3_abi_version": (I, []),
@@ -145,10 +156,20 @@ def eagle3_expand(draft_logits, B, F, V, k, W, inv_temp, parent_score, parent_id
                                                ptr(next_id), ptr(next_score), ptr(dev_err), _stream(stream)))
 
 
-def tree_build_mask(cands: e3_cand, B, n_cand, N, root_tok, kv_len, tok, parent, depth, pos, mask, stream=None):
+def eagle3_expand_sampled(draft_logits, B, F, V, k, W, inv_temp, parent_score, parent_id, depth, cand_offset,
+                          cands: e3_cand, next_id, next_score, seed, q_stats, dev_err=None, stream=None):
+    """q_stats: device buffer of B * (1 + cands.cap) * QSTAT_BYTES bytes."""
+    _check("eagle3_expand_sampled",
+           _lib.eagle3_expand_sampled(ptr(draft_logits), B, F, V, k, W, inv_temp, ptr(parent_score), ptr(parent_id),
+                                      depth, cand_offset, ctypes.byref(cands), ptr(next_id), ptr(next_score),
+                                      int(seed) & (2 ** 64 - 1), ptr(q_stats), ptr(dev_err), _stream(stream)))
+
+
+def tree_build_mask(cands: e3_cand, B, n_cand, N, root_tok, kv_len, tok, parent, depth, pos, mask, node_cand=None,
+                    stream=None):
     _check("tree_build_mask", _lib.tree_build_mask(ctypes.byref(cands), B, n_cand, N, ptr(root_tok), ptr(kv_len),
                                                    ptr(tok), ptr(parent), ptr(depth), ptr(pos), ptr(mask),
-                                                   _stream(stream)))
+                                                   ptr(node_cand), _stream(stream)))
 
 
 def eagle3_verify_workspace_bytes(B, R, n_q_heads, n_kv_heads, head_dim, max_kv_len, dt) -> int:
@@ -173,6 +194,15 @@ def spec_accept(tok, parent, B, R, D, logits, row_max, row_Q, row_argmax, V, tem
     _check("spec_accept", _lib.spec_accept(ptr(tok), ptr(parent), B, R, D, ptr(logits), ptr(row_max), ptr(row_Q),
                                            ptr(row_argmax), V, ptr(temp), ptr(u_acc), ptr(u_bonus), mode,
                                            ptr(acc_len), ptr(path), ptr(out_tok), ptr(status), _stream(stream)))
+
+
+def spec_accept_sampled(tok, parent, node_cand, B, R, D, logits, row_max, row_Q, row_argmax, V, temp, q_stats, q_cap,
+                        u_acc, u_bonus, acc_len, path, out_tok, status, stream=None):
+    _check("spec_accept_sampled",
+           _lib.spec_accept_sampled(ptr(tok), ptr(parent), ptr(node_cand), B, R, D, ptr(logits), ptr(row_max),
+                                    ptr(row_Q), ptr(row_argmax), V, ptr(temp), ptr(q_stats), q_cap, ptr(u_acc),
+                                    ptr(u_bonus), ptr(acc_len), ptr(path), ptr(out_tok), ptr(status),
+                                    _stream(stream)))
 
 
 def kv_compact(layers, B, path, acc_len, D, kv_len, dev_err=None, stream=None):

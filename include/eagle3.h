@@ -97,6 +97,16 @@ typedef struct {
   int cap;         /* candidates per request */
 } e3_cand;
 
+/* Draft statistics of one frontier row, written by eagle3_expand_sampled for
+ * the node the row expanded and read by spec_accept_sampled (device array
+ * [B][1 + cands->cap]: slot 0 = the root, slot 1 + c = candidate c). */
+typedef struct {
+  const float* row; /* the row's draft logits [V] fp32 (device) */
+  uint64_t Q;       /* sum_j floor(2^40 E(z_j * inv_temp - m)) */
+  float m;          /* max_j z_j * inv_temp */
+  float inv_temp;   /* the draft inverse temperature of the expansion */
+} e3_qstat;
+
 /* One layer's paged KV cache.  k and v: [n_pages][n_kv_heads][page_size][head_dim]
  * of dtype dt (device).  Logical token t of request b is slot t % page_size of
  * page page_table[b*max_pages + t / page_size]. */
@@ -174,6 +184,29 @@ E3_API e3_status eagle3_expand(const float* draft_logits, int B, int F, int V, i
                         e3_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * eagle3_expand_sampled: as eagle3_expand, but the k children of a row are
+ * DRAWN from the draft distribution q_j = Q_j / Q (Q_j = floor(2^40 E(s_j - m)))
+ * without replacement, in draw order ("EAGLE 系列与 DFlash", §四 DFlash: drafts
+ * proposed by the drafter and checked with min(1, p_target / p_draft)):
+ *   token j of row f (request b) gets the arrival time E_j / e_j, e_j = E(s_j - m),
+ *   E_j = 0 - ell(((x >> 40) + 1) << 16) = -ln U_j, x = output number n + 1 of
+ *   the SplitMix64 stream started at `seed`, n = b 2^44 + depth 2^36 + f 2^24 + j;
+ *   tokens with Q_j = 0 never arrive; the children are the k earliest arrivals
+ *   (equal times: lower token id first), child r the r-th.
+ * Child scores, candidate layout and the next frontier are exactly those of
+ * eagle3_expand.  q_stats [B][1 + cands->cap] (device): the entry of the node
+ * each row expanded (slot 1 + parent_id, or 0 for the root) receives the row's
+ * address, Q, m and inv_temp, for spec_accept_sampled.
+ * Limits: those of eagle3_expand; V < 2^24, F < 4096, depth < 256, B < 2^20.
+ * ------------------------------------------------------------------------- */
+E3_API e3_status eagle3_expand_sampled(const float* draft_logits, int B, int F, int V, int k,
+                                       int W, float inv_temp, const float* parent_score,
+                                       const int32_t* parent_id, int depth, int cand_offset,
+                                       const e3_cand* cands /* host struct, device arrays */,
+                                       int32_t* next_id, float* next_score, uint64_t seed,
+                                       e3_qstat* q_stats, int32_t* dev_err, e3_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * tree_build_mask: per request, keep the N best of the first n_cand candidates
  * in the order (score descending, candidate index ascending) -- closed under
  * parents because a child's score never exceeds its parent's -- and flatten
@@ -182,12 +215,15 @@ E3_API e3_status eagle3_expand(const float* draft_logits, int B, int F, int V, i
  * Outputs ([B][R] int32 each): tok (root = root_tok[b]), parent (root -1),
  * depth (root 0), pos = kv_len[b] + depth; mask [B][R][W64] uint64 with
  * W64 = ceil(R/64): bit j of row i set iff node j is node i or an ancestor.
+ * node_cand [B][R] int32 (nullable): candidate index of each node (root -1).
  * Limits: 1 <= N <= min(n_cand, E3_MAX_NODES), n_cand <= cands->cap.
+ * With sampled children (eagle3_expand_sampled) pass N = n_cand: dropping a
+ * drawn child by its own score would bias the accepted tokens.
  * ------------------------------------------------------------------------- */
 E3_API e3_status tree_build_mask(const e3_cand* cands, int B, int n_cand, int N,
                           const int32_t* root_tok, const int32_t* kv_len, int32_t* tok,
                           int32_t* parent, int32_t* depth, int32_t* pos, uint64_t* mask,
-                          e3_stream_t stream);
+                          int32_t* node_cand, e3_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * tree_verify_attn: one attention layer of the verify pass.
@@ -249,12 +285,44 @@ E3_API e3_status lmhead_logits(const void* h, const void* W_lm, int M, int d, in
  * Limits: R <= 256, D <= E3_MAX_DEPTH, depth of every node <= D.
  * ------------------------------------------------------------------------- */
 #define E3_ACCEPT_TREE_DET 0
+#define E3_ACCEPT_SAMPLED 1 /* children drawn from q: spec_accept_sampled (it needs q) */
 E3_API e3_status spec_accept(const int32_t* tok, const int32_t* parent, int B, int R, int D,
                       const float* logits, const float* row_max, const uint64_t* row_Q,
                       const int32_t* row_argmax, int V, const float* temp,
                       const uint32_t* u_acc, const uint32_t* u_bonus, int mode,
                       int32_t* acc_len, int32_t* path, int32_t* out_tok, int32_t* status,
                       e3_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * spec_accept_sampled: accept/reject for trees whose children were drawn from
+ * the draft distribution (eagle3_expand_sampled; every candidate kept):
+ * "EAGLE 系列与 DFlash", §四 DFlash, acceptance min(1, p_target / p_draft), the
+ * dice rolled in order; "SpecForge…", 接受连续前缀，拒绝处进行校正.
+ * At node u (T = temp[b] > 0) the target residual is held as integer masses
+ * R_j = floor(2^40 E(s_j - m_u)) (total SR = row_Q[u]) and the draft residual
+ * as D_j = floor(2^40 E(zq_j inv_temp - m_q)) (total SD = Q) from the q_stats
+ * entry of u (slot 1 + node_cand[u]; root slot 0).  Children in flattened
+ * (= draw) order, token t:
+ *   D_t = 0: not a draw (the row had fewer than k tokens of positive mass), skipped;
+ *   accept iff u_acc[c] * floor(D_t SR / SD) < R_t 2^32
+ *     (probability min(1, p_res(t) / q_res(t)));
+ *   on reject, for every j: R_j -= min(R_j, floor(D_j SR / SD)) (the residual
+ *     max(0, p_res - q_res)), SR = sum R_j; then SD -= D_t, D_t = 0.
+ * An accepted child becomes u (the residuals restart from its rows).  With no
+ * child accepted, or at a leaf, the bonus token is the smallest token id whose
+ * cumulative R exceeds (u_bonus[u] * SR) >> 32.  T <= 0: exactly spec_accept's
+ * greedy rule.  Other arguments and outputs as spec_accept; node_cand from
+ * tree_build_mask; q_cap = 1 + cands->cap (entries per request of q_stats).
+ * Non-finite target or draft statistics set E3_DEV_ERR_NONFINITE in status[b].
+ * ------------------------------------------------------------------------- */
+E3_API e3_status spec_accept_sampled(const int32_t* tok, const int32_t* parent,
+                                     const int32_t* node_cand, int B, int R, int D,
+                                     const float* logits, const float* row_max,
+                                     const uint64_t* row_Q, const int32_t* row_argmax, int V,
+                                     const float* temp, const e3_qstat* q_stats, int q_cap,
+                                     const uint32_t* u_acc, const uint32_t* u_bonus,
+                                     int32_t* acc_len, int32_t* path, int32_t* out_tok,
+                                     int32_t* status, e3_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * kv_compact: for every layer l < L, request b (P = kv_len[b]) and accepted
@@ -274,7 +342,7 @@ E3_API e3_status kv_compact(const e3_kv_layer* layers, int L, int B, const int32
 /* Last error message of the calling thread ("" if none). */
 E3_API const char* eagle3_last_error(void);
 
-/* ABI version: 1. */
+/* ABI version: 2 (1 had no sampled-draft calls and no node_cand output). */
 E3_API int eagle3_abi_version(void);
 
 /* Diagnostic with no counterpart in the method: the number of kernels this

@@ -38,7 +38,8 @@ def test_library_exports_every_declared_symbol(e3):
         assert n in exported, n
         assert hasattr(e3.lib(), n)
     assert set(e3.SYMBOLS) == set(declared_functions())
-    assert e3.abi_version() == 1
+    assert e3.abi_version() == 2
+    assert e3.QSTAT_BYTES == 24
 
 
 def test_host_validation_rejects_bad_arguments(e3):
@@ -70,6 +71,20 @@ def test_host_validation_rejects_bad_arguments(e3):
     with pytest.raises(e3.E3Error) as ei:  # unknown accept mode
         e3.spec_accept(*([16] * 2), 1, 15, 3, *([16] * 4), 1000, *([16] * 3), 7, *([16] * 4), stream=0)
     assert ei.value.status == 3
+    with pytest.raises(e3.E3Error) as ei:  # sampled mode goes through spec_accept_sampled
+        e3.spec_accept(*([16] * 2), 1, 15, 3, *([16] * 4), 1000, *([16] * 3), e3.E3_ACCEPT_SAMPLED, *([16] * 4),
+                       stream=0)
+    assert ei.value.status == 3 and "spec_accept_sampled" in e3.lib().eagle3_last_error().decode()
+    with pytest.raises(e3.E3Error) as ei:  # null q_stats
+        e3.eagle3_expand_sampled(16, 1, 1, 1000, 4, 4, 1.0, 16, 16, 1, 0, cand, 16, 16, 5, None, None, stream=0)
+    assert ei.value.status == 1
+    with pytest.raises(e3.E3Error) as ei:  # vocabulary beyond the draw counter's 24-bit field
+        e3.eagle3_expand_sampled(16, 1, 1, 1 << 24, 4, 4, 1.0, 16, 16, 1, 0, cand, 16, 16, 5, 16, None, stream=0)
+    assert ei.value.status == 2
+    with pytest.raises(e3.E3Error) as ei:  # q_cap out of range
+        e3.spec_accept_sampled(16, 16, 16, 1, 15, 3, 16, 16, 16, 16, 1000, 16, 16, 0, 16, 16, 16, 16, 16, 16,
+                               stream=0)
+    assert ei.value.status == 2
     with pytest.raises(e3.E3Error) as ei:  # too many layers
         e3.kv_compact([kv] * 200, 1, 16, 16, 6, 16, None, stream=0)
     assert ei.value.status == 2

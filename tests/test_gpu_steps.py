@@ -199,15 +199,15 @@ def test_tree_build_bitexact(V, k, W, D, N, B):
     R = N + 1
     kvl = rng.integers(0, 5000, B).astype(np.int32)
     root = rng.integers(0, V, B).astype(np.int32)
-    out = {x: i32((B, R), -9) for x in ("tok", "parent", "depth", "pos")}
+    out = {x: i32((B, R), -9) for x in ("tok", "parent", "depth", "pos", "node_cand")}
     mask = torch.zeros((B, R, (R + 63) // 64), dtype=torch.int64, device="cuda")
     e3.tree_build_mask(cand, B, C, N, to_dev(root), to_dev(kvl), out["tok"], out["parent"], out["depth"],
-                       out["pos"], mask)
+                       out["pos"], mask, node_cand=out["node_cand"])
     torch.cuda.synchronize()
     for b in range(B):
         cb = {x: np.ascontiguousarray(cands[x][b]) for x in ("tok", "parent", "score", "depth")}
         ref = oracle.build_tree(cb, C, N, int(root[b]), int(kvl[b]))
-        for x in ("tok", "parent", "depth", "pos"):
+        for x in ("tok", "parent", "depth", "pos", "node_cand"):
             assert np.array_equal(host(out[x])[b], ref[x]), (x, b)
         assert np.array_equal(host(mask)[b].view(np.uint64), ref["mask"]), ("mask", b)
 
