@@ -45,6 +45,18 @@ CONFIGS = {
                       workload="Llama-3.1-8B-shaped verify round with a chain draft (top-1, three tokens): d=4096, "
                                "32/8 heads x 128, vocab 128256, batch 1, prefix 2048, 32 layers, "
                                "fusion 12288->4096, temp 1"),
+    "8b_sampled": dict(B=1, P=[2048], N=52, D=4, k=4, W=4, H=32, KVH=8, hd=128, d=4096, V=128256, L=32,
+                       dtype="bf16", temps=[1.0], noise=1.0, sampled=True,
+                       workload="Llama-3.1-8B-shaped verify round with drafts sampled from the draft distribution "
+                                "and accepted with min(1, p/q): d=4096, 32/8 heads x 128, vocab 128256, batch 1, "
+                                "prefix 2048, 4 draws per node, frontier 4, depth 4 (52 nodes), 32 layers, "
+                                "fusion 12288->4096, temp 1"),
+    "8b_chain3_sampled": dict(B=1, P=[2048], N=3, D=3, k=1, W=1, H=32, KVH=8, hd=128, d=4096, V=128256, L=32,
+                              dtype="bf16", temps=[1.0], noise=1.0, sampled=True,
+                              workload="Llama-3.1-8B-shaped verify round with a sampled chain draft (three tokens "
+                                       "drawn from the draft distribution, accepted with min(1, p/q)): d=4096, "
+                                       "32/8 heads x 128, vocab 128256, batch 1, prefix 2048, 32 layers, "
+                                       "fusion 12288->4096, temp 1"),
     "batched": dict(B=32, P="uniform:512:8192", N=60, D=6, k=10, W=10, H=32, KVH=8, hd=128, d=4096, V=128256,
                     L=32, dtype="bf16", temps="mixed", noise=1.0,
                     workload="batched serving, 8B shape, bf16: 32 requests, prefix U[512,8192], 60-node depth-6 "
@@ -98,7 +110,8 @@ class Workload:
         self.name, self.c, self.seed = name, c, seed
         R = c["N"] + 1
         self.cfg = RoundConfig(B=c["B"], N=c["N"], D=c["D"], k=c["k"], W=c["W"], H=c["H"], KVH=c["KVH"],
-                               hd=c["hd"], d=c["d"], V=c["V"], L=c["L"], max_kv_len=max(c["P"]), dtype=c["dtype"])
+                               hd=c["hd"], d=c["d"], V=c["V"], L=c["L"], max_kv_len=max(c["P"]), dtype=c["dtype"],
+                               sampled=bool(c.get("sampled", False)), draw_seed=seed * 7919 + 17)
         pt, npages = synth.page_table(seed, [p + R for p in c["P"]], self.cfg.page_size)
         self.pt = pt
         self.bufs = b = RoundBuffers(self.cfg, torch.from_numpy(pt), npages, device)
@@ -180,6 +193,7 @@ class Workload:
         """Draft stand-in: at each depth the frontier nodes' target logits (verify +
         LM head on the frontier's own mini-tree) plus N(0, noise^2) are the draft
         logits.  W_lm is first scaled so that target logits have std ~ 4."""
+        from eagle_speculative_decoding_round_gb300.round import build_tree, expand_depth
         torch, e3, b, c = self.torch, self.e3, self.bufs, self.cfg
         B = c.B
         roots = b.root_tok.cpu().numpy()
@@ -220,14 +234,13 @@ class Workload:
             zt = self.target_logits_of(tok, par, rows).view(B, F, c.V)
             noise = torch.randn(zt.shape, generator=self.gen, device="cuda") * self.c["noise"]
             b.draft_logits[di].copy_(zt + noise)
-            e3.eagle3_expand(b.draft_logits[di], B, F, c.V, c.k, c.W, 1.0, b.f_score[di], b.f_id[di], di + 1, off,
-                             b.cand, b.f_id[di + 1], b.f_score[di + 1], b.dev_err)
+            expand_depth(b, di)
             ct, cp = b.c_tok.cpu().numpy(), b.c_parent.cpu().numpy()
             for bb in range(B):
                 for i in range(off, off + F * c.k):
                     paths[bb][i] = paths[bb][int(cp[bb, i])] + [int(ct[bb, i])]
         # the final tree (same every step) and its Q/K/V in every layer
-        e3.tree_build_mask(b.cand, B, n_cand, c.N, b.root_tok, b.kv_len, b.tok, b.parent, b.depth, b.pos, b.mask)
+        build_tree(b)
         self.write_nodes(b.tok.long(), range(c.L), c.R)
         torch.cuda.synchronize()
         assert int(b.dev_err.item()) == 0, "device error during setup"
@@ -347,13 +360,21 @@ def oracle_sample(w, budget_s=20.0):
     sizes, n_cand = cfg.frontier_sizes()
     drafts = [f(x) for x in b.draft_logits]
     t = time.perf_counter()
-    trees = []
+    trees, qrows = [], []
     for bb in range(B if B <= 2 else 1):
         c = oracle.new_cands(n_cand)
         fid, fsc = np.array([-1], np.int32), np.zeros(1, np.float32)
+        rows = {}  # candidate (root -1) -> the draft row it was expanded with
         for di, (F, off) in enumerate(sizes):
-            fid, fsc = oracle.expand(drafts[di][bb], cfg.k, cfg.W, fsc, fid, di + 1, off, c)
+            if cfg.sampled:
+                for fr in range(F):
+                    rows[int(fid[fr])] = drafts[di][bb][fr]
+                fid, fsc, _, _ = oracle.expand_sampled(drafts[di][bb], cfg.k, cfg.W, fsc, fid, di + 1, off, c,
+                                                       cfg.draw_seed, bb)
+            else:
+                fid, fsc = oracle.expand(drafts[di][bb], cfg.k, cfg.W, fsc, fid, di + 1, off, c)
         trees.append(oracle.build_tree(c, n_cand, cfg.N, int(b.root_tok[bb]), int(w.kv_len0[bb])))
+        qrows.append(rows)
     times["expand_build"] = (time.perf_counter() - t) * (B / len(trees))
     p0 = int(w.c["P"][0])
     scale_b = sum(p + R for p in w.c["P"]) / (p0 + R)
@@ -379,8 +400,16 @@ def oracle_sample(w, budget_s=20.0):
     zl = f(b.logits)
     t = time.perf_counter()
     tt = {"tok": b.tok.cpu().numpy()[0], "parent": b.parent.cpu().numpy()[0]}
-    oracle.accept(tt, zl[:R], float(w.c["temps"][0]), b.u_acc.cpu().numpy()[0].view(np.uint32),
-                  b.u_bonus.cpu().numpy()[0].view(np.uint32), cfg.D)
+    ua, ub = b.u_acc.cpu().numpy()[0].view(np.uint32), b.u_bonus.cpu().numpy()[0].view(np.uint32)
+    if cfg.sampled:
+        qlog = np.zeros((R, V), np.float32)
+        for u in range(R):
+            key = -1 if u == 0 else int(trees[0]["node_cand"][u])
+            if key in qrows[0]:
+                qlog[u] = qrows[0][key]
+        oracle.accept_sampled(tt, zl[:R], float(w.c["temps"][0]), qlog, 1.0, ua, ub, cfg.D)
+    else:
+        oracle.accept(tt, zl[:R], float(w.c["temps"][0]), ua, ub, cfg.D)
     times["accept"] = (time.perf_counter() - t) * B
     total = sum(times.values())
     wall = time.perf_counter() - t0
@@ -565,47 +594,21 @@ def summarize(P):
 
 
 def run_round_phased(w, evs, e3, counts=None):
-    """One round with a timing event at each phase boundary (same calls as run_round;
-    no events when ``evs`` is None).  With ``counts`` (a list), also append the
-    library's launch counter there."""
+    """One round (the same calls as Workload.round, through run_round) with a timing
+    event recorded at each of its 8 phase boundaries (none when ``evs`` is None).
+    With ``counts`` (a list), also append the library's launch counter there."""
     import torch
-    b, c = w.bufs, w.cfg
+
+    from eagle_speculative_decoding_round_gb300.round import run_round
     s = torch.cuda.current_stream()
-    R = c.R
 
-    class _Ev:  # records the event and, when asked, the launch counter
-        def __init__(self, e):
-            self.e = e
+    def mark(i):
+        if evs is not None:
+            evs[i].record(s)
+        if counts is not None:
+            counts.append(e3.launch_count())
 
-        def record(self, st):
-            if self.e is not None:
-                self.e.record(st)
-            if counts is not None:
-                counts.append(e3.launch_count())
-
-    evs = [_Ev(e) for e in (evs if evs is not None else [None] * 8)]
-    evs[0].record(s)
-    e3.eagle3_fuse(b.h[0], b.h[1], b.h[2], b.W_f, None, b.g, c.M, c.d, c.d, c.dt, b.fuse_ws, b.fuse_ws_bytes, b.dev_err)
-    evs[1].record(s)
-    sizes, n_cand = c.frontier_sizes()
-    for di, (F, off) in enumerate(sizes):
-        e3.eagle3_expand(b.draft_logits[di], c.B, F, c.V, c.k, c.W, 1.0, b.f_score[di], b.f_id[di], di + 1, off,
-                         b.cand, b.f_id[di + 1], b.f_score[di + 1], b.dev_err)
-    evs[2].record(s)
-    e3.tree_build_mask(b.cand, c.B, n_cand, c.N, b.root_tok, b.kv_len, b.tok, b.parent, b.depth, b.pos, b.mask)
-    evs[3].record(s)
-    for l in range(c.L):
-        e3.tree_verify_attn(b.Q[l], b.kv[l], b.kv_len, b.mask, c.B, R, c.H, c.max_kv_len, 1.0 / math.sqrt(c.hd),
-                            b.O[l], b.lse[l], b.dev_err, b.ws, b.ws_bytes)
-    evs[4].record(s)
-    e3.lmhead_logits(b.O[c.L - 1], b.W_lm, c.B * R, c.H * c.hd, c.V, b.temp_rows, b.logits, b.row_max, b.row_Q,
-                     b.row_argmax, b.dev_err, c.dt)
-    evs[5].record(s)
-    e3.spec_accept(b.tok, b.parent, c.B, R, c.D, b.logits, b.row_max, b.row_Q, b.row_argmax, c.V, b.temp, b.u_acc,
-                   b.u_bonus, e3.E3_ACCEPT_TREE_DET, b.acc_len, b.path, b.out_tok, b.status)
-    evs[6].record(s)
-    e3.kv_compact(b.kv, c.B, b.path, b.acc_len, c.D, b.kv_len, b.dev_err)
-    evs[7].record(s)
+    run_round(w.bufs, stream=s, mark=mark)
 
 
 def e2e_leg(w, s, K, warmup, world=1):

@@ -227,6 +227,31 @@ __device__ __forceinline__ uint64_t muldiv_u64(uint64_t a, uint64_t b, uint64_t 
   return static_cast<uint64_t>(p / c);
 }
 
+// floor(a * b / c) for many a < 2^63 with b and c > 0 fixed, without a division
+// per a: b / c = I + bm / c (I = floor(b / c), bm = b mod c) and
+// rf = floor(bm 2^64 / c), so that t = floor(a rf / 2^64) is floor(a bm / c) or
+// one less (a rf / 2^64 > a bm / c - a / 2^64 > a bm / c - 1); one exact
+// comparison of (t + 1) c with a bm, as 128-bit (high, low) word pairs, settles
+// it.  Exact whenever the result fits 64 bits.
+struct FracMul {
+  uint64_t I, bm, rf, c;
+};
+__device__ __forceinline__ FracMul frac_mul_prep(uint64_t b, uint64_t c) {
+  FracMul f;
+  f.c = c;
+  f.I = b / c;
+  f.bm = b - f.I * c;
+  f.rf = static_cast<uint64_t>((static_cast<unsigned __int128>(f.bm) << 64) / c);
+  return f;
+}
+__device__ __forceinline__ uint64_t frac_mul(const FracMul& f, uint64_t a) {
+  const uint64_t t = __umul64hi(a, f.rf), t1 = t + 1;
+  const uint64_t n_hi = __umul64hi(a, f.bm), n_lo = a * f.bm;
+  const uint64_t m_hi = __umul64hi(t1, f.c), m_lo = t1 * f.c;
+  const bool up = (m_hi < n_hi) || (m_hi == n_hi && m_lo <= n_lo);
+  return a * f.I + (up ? t1 : t);
+}
+
 // SplitMix64 (Steele, Lea & Flood, OOPSLA 2014): output number i >= 1 of the
 // stream started at `seed` is mix(seed + i * 0x9E3779B97F4A7C15).
 __device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t i) {

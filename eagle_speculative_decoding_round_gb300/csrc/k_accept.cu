@@ -35,15 +35,19 @@ constexpr int kMaxR = E3_MAX_NODES + 1;
 
 namespace cg = cooperative_groups;
 
+constexpr int kMaxCluster = 16;
+
 // Inverse-CDF draw over residual masses spread across the cluster: CTA r holds
 // the masses of tokens [j0_r, j0_r + n_r) in qbuf[0, n_r) (chunks in rank order).
-// Finds the smallest token whose cumulative mass exceeds x: the chunk sums are
-// exchanged through distributed shared memory, the CTA whose chunk holds x
-// locates the warp, and that warp scans 32 tokens at a time.  Sets *s_bonus in
-// that CTA (untouched if the total is <= x) and returns its rank (0 if none).
-// Every thread of every CTA calls it; qbuf is complete and visible on entry.
+// Finds the smallest token whose cumulative mass exceeds x: every CTA pushes its
+// chunk sum into s_sums[rank] of every CTA (remote stores, no round trips), so
+// that after one cluster barrier each CTA reads all sums locally; the CTA whose
+// chunk holds x locates the warp, and that warp scans 32 tokens at a time.  Sets
+// *s_bonus in that CTA (untouched if the total is <= x) and returns its rank (0
+// if none).  Every thread of every CTA calls it; qbuf is complete and visible on
+// entry; s_sums ([kMaxCluster], the same variable in every CTA) is not in use.
 __device__ int cluster_inverse_cdf(cg::cluster_group& cluster, const unsigned long long* qbuf, int n, int j0,
-                                   uint64_t x, unsigned long long* s_wsum, unsigned long long* s_sum,
+                                   uint64_t x, unsigned long long* s_wsum, unsigned long long* s_sums,
                                    int* s_bonus) {
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
@@ -56,40 +60,46 @@ __device__ int cluster_inverse_cdf(cg::cluster_group& cluster, const unsigned lo
   local = warp_reduce(local, SumU64());
   if (lane == 0) s_wsum[w] = local;
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (w == 0) {
     uint64_t tot = 0;
     for (int i = 0; i < nw; ++i) tot += s_wsum[i];
-    *s_sum = tot;
+    if (lane < CL) *cluster.map_shared_rank(&s_sums[rank], lane) = tot;
   }
-  cluster.sync();  // chunk sums visible
+  cluster.sync();  // every CTA holds every chunk sum
   uint64_t excl = 0;
   int found = -1;
   for (int r = 0; r < CL; ++r) {  // the chunk sums partition [0, total)
-    const uint64_t sr = *cluster.map_shared_rank(s_sum, r);
+    const uint64_t sr = s_sums[r];
     if (found < 0 && x >= excl && x < excl + sr) found = r;
     excl += sr;
   }
   if (found == rank) {
     uint64_t wex = 0;
-    for (int r = 0; r < rank; ++r) wex += *cluster.map_shared_rank(s_sum, r);
+    for (int r = 0; r < rank; ++r) wex += s_sums[r];
     for (int i = 0; i < w; ++i) wex += s_wsum[i];
     if (x >= wex && x < wex + s_wsum[w]) {  // uniform within the warp
-      uint64_t base = wex;
-      for (int c0 = a0; c0 < a1; c0 += 32) {
-        const int j = c0 + lane;
-        const uint64_t q = j < a1 ? qbuf[j] : 0ull;
-        uint64_t incl = q;
+      // each lane sums a contiguous piece of the warp's segment; one warp scan
+      // finds the lane whose piece holds x, and that lane walks its piece
+      const int sub = (a1 - a0 + 31) >> 5;
+      const int b0 = min(a1, a0 + lane * sub), b1 = min(a1, b0 + sub);
+      uint64_t part = 0;
+      for (int j = b0; j < b1; ++j) part += qbuf[j];
+      uint64_t incl = part;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += y;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, wex + incl > x);
+      if (hit && lane == __ffs(hit) - 1) {
+        uint64_t cum = wex + incl - part;
+        for (int j = b0; j < b1; ++j) {
+          cum += qbuf[j];
+          if (cum > x) {
+            *s_bonus = j0 + j;
+            break;
+          }
         }
-        const unsigned hit = __ballot_sync(0xFFFFFFFFu, base + incl > x);
-        if (hit) {
-          if (lane == __ffs(hit) - 1) *s_bonus = j0 + j;
-          break;
-        }
-        base += __shfl_sync(0xFFFFFFFFu, incl, 31);
       }
     }
   }
@@ -114,7 +124,7 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
   __shared__ int s_removed[kMaxR];
   __shared__ int s_path[E3_MAX_DEPTH + 1];
   __shared__ int s_nrem, s_u, s_acc, s_err, s_bonus;
-  __shared__ unsigned long long s_x, s_sum;
+  __shared__ unsigned long long s_x, s_sums[kMaxCluster];
   __shared__ unsigned long long s_wsum[kAcceptThreads / 32];
 
   pdl_wait();
@@ -232,7 +242,7 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
       }
     }
     __syncthreads();
-    writer = cluster_inverse_cdf(cluster, qbuf, n, j0, x, s_wsum, &s_sum, &s_bonus);
+    writer = cluster_inverse_cdf(cluster, qbuf, n, j0, x, s_wsum, s_sums, &s_bonus);
   }
   if (rank == writer && threadIdx.x == 0) {
     const int a = err ? 0 : s_acc;
@@ -285,20 +295,48 @@ accept_sampled_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict
   __shared__ int s_removed[kMaxR];
   __shared__ int s_path[E3_MAX_DEPTH + 1];
   __shared__ int s_nrem, s_u, s_a, s_err, s_bonus, s_fresh, s_dec, s_t, s_am;
-  __shared__ unsigned long long s_SR, s_SD, s_Dt, s_part, s_sum;
+  __shared__ unsigned long long s_SR, s_SD, s_Dt, s_parts[kMaxCluster], s_sums[kMaxCluster];
   __shared__ unsigned long long s_wsum[kAcceptThreads / 32];
   __shared__ uint64_t s_red[32];
   __shared__ float s_mp, s_mq, s_itq;
   __shared__ const float* s_zq;
+  __shared__ FracMul s_fm;  // floor(D SR / SD) for the current residual totals
+  __shared__ uint32_t s_uacc[kMaxR];
+  // per node: target statistics and the draft statistics of its children's row;
+  // per child: its token's draft and target masses under its parent's rows
+  __shared__ float s_nmax[kMaxR], s_nqm[kMaxR], s_nqit[kMaxR];
+  __shared__ int s_nam[kMaxR];
+  __shared__ unsigned long long s_nQ[kMaxR], s_nqQ[kMaxR], s_Dc[kMaxR], s_Rc[kMaxR];
+  __shared__ const float* s_nqrow[kMaxR];
 
   pdl_wait();
   pdl_trigger();
   const size_t rb = static_cast<size_t>(b) * R;
   const float T = temp[b];
   const float it = inv_temp(T);
-  for (int i = threadIdx.x; i < R; i += blockDim.x) {
-    s_tok[i] = tok[rb + i];
-    s_par[i] = parent[rb + i];
+  // the tree, and every node's statistics, loaded in parallel (the walk then reads
+  // shared memory only); a node's draft entry is read whether or not it has
+  // children, and used only if it has
+  for (int u = threadIdx.x; u < R; u += blockDim.x) {
+    const size_t row = rb + u;
+    s_tok[u] = tok[row];
+    s_par[u] = parent[row];
+    s_uacc[u] = u_acc[row];
+    s_nmax[u] = row_max[row];
+    s_nam[u] = row_argmax[row];
+    s_nQ[u] = row_Q[row];
+    s_nqrow[u] = nullptr;
+    s_nqQ[u] = 0ull;
+    s_nqm[u] = 0.0f;
+    s_nqit[u] = 0.0f;
+    const int nc = node_cand[row];
+    if (T > 0.0f && nc >= -1 && nc + 1 < q_cap) {
+      const e3_qstat q = qs[static_cast<size_t>(b) * q_cap + (nc + 1)];
+      s_nqrow[u] = q.row;
+      s_nqQ[u] = q.Q;
+      s_nqm[u] = q.m;
+      s_nqit[u] = q.inv_temp;
+    }
   }
   for (int w = threadIdx.x; w < nwords; w += blockDim.x) rbits[w] = 0u;
   __syncthreads();
@@ -330,30 +368,40 @@ accept_sampled_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict
     for (int c2 = p + 1; c2 < c; ++c2) rk += (s_par[c2] == p);
     s_child[s_first[p] + rk] = c;
   }
+  for (int c = threadIdx.x; c < R; c += blockDim.x) {
+    s_Dc[c] = 0ull;
+    s_Rc[c] = 0ull;
+    const int p = s_par[c];
+    const int t = s_tok[c];
+    if (T <= 0.0f || c == 0 || p < 0 || p >= c || t < 0 || t >= V) continue;
+    const float* zq = s_nqrow[p];
+    if (zq != nullptr && isfinite(s_nqm[p]) && isfinite(s_nmax[p])) {
+      s_Dc[c] = fx_mass(__fmul_rn(zq[t], s_nqit[p]), s_nqm[p]);
+      s_Rc[c] = fx_mass(__fmul_rn(logits[(rb + p) * V + t], it), s_nmax[p]);
+    }
+  }
   __syncthreads();
 
   for (;;) {  // one iteration per visited node, uniform across the cluster
     if (threadIdx.x == 0) {
       const int u = s_u;
-      const size_t row = rb + u;
-      s_mp = row_max[row];
-      s_am = row_argmax[row];
-      s_SR = row_Q[row];
+      s_mp = s_nmax[u];
+      s_am = s_nam[u];
+      s_SR = s_nQ[u];
       s_fresh = 1;
       s_nrem = 0;
       s_SD = 0ull;
       s_zq = nullptr;
       if (s_am < 0 || !isfinite(s_mp)) s_err = E3_DEV_ERR_NONFINITE;
       if (!s_err && T > 0.0f && s_nch[u] > 0) {
-        const int nc = node_cand[row];
-        const e3_qstat* q = (nc >= -1 && nc + 1 < q_cap) ? qs + static_cast<size_t>(b) * q_cap + (nc + 1) : nullptr;
-        if (q == nullptr || q->row == nullptr || !isfinite(q->m) || q->Q == 0ull) {
+        if (s_nqrow[u] == nullptr || !isfinite(s_nqm[u]) || s_nqQ[u] == 0ull) {
           s_err = E3_DEV_ERR_NONFINITE;
         } else {
-          s_zq = q->row;
-          s_SD = q->Q;
-          s_mq = q->m;
-          s_itq = q->inv_temp;
+          s_zq = s_nqrow[u];
+          s_SD = s_nqQ[u];
+          s_mq = s_nqm[u];
+          s_itq = s_nqit[u];
+          s_fm = frac_mul_prep(s_SR, s_SD);
         }
       }
     }
@@ -373,18 +421,21 @@ accept_sampled_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict
         } else if (t >= 0 && t < V) {
           bool rem = false;
           for (int i = 0; i < s_nrem; ++i) rem |= (s_removed[i] == t);
-          const uint64_t Dt = rem ? 0ull : fx_mass(__fmul_rn(s_zq[t], s_itq), s_mq);
+          const uint64_t Dt = rem ? 0ull : s_Dc[c];
           if (Dt != 0ull) {
             uint64_t Rt;
             if (s_fresh) {
-              Rt = fx_mass(__fmul_rn(z[t], it), s_mp);
+              Rt = s_Rc[c];
             } else {
               const int owner = t / per;
               Rt = cluster.map_shared_rank(qbuf, owner)[t - owner * per];
             }
-            const uint64_t qt = muldiv_u64(Dt, s_SR, s_SD);
-            const unsigned __int128 lhs = static_cast<unsigned __int128>(u_acc[rb + c]) * qt;
-            dec = lhs < (static_cast<unsigned __int128>(Rt) << 32) ? 1 : 0;
+            // accept iff u * qt < Rt 2^32, compared as (high, low) words
+            const uint64_t qt = frac_mul(s_fm, Dt);
+            const uint64_t u = s_uacc[c];
+            const uint64_t l_hi = __umul64hi(u, qt), l_lo = u * qt;
+            const uint64_t r_hi = Rt >> 32, r_lo = Rt << 32;
+            dec = (l_hi < r_hi || (l_hi == r_hi && l_lo < r_lo)) ? 1 : 0;
             s_Dt = Dt;
             s_t = t;
           }
@@ -402,34 +453,63 @@ accept_sampled_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict
       // rejection: the residual pass over this CTA's tokens
       cluster.sync();  // no CTA still reads a peer's qbuf for the decision above
       const bool fresh = s_fresh != 0;
-      const uint64_t SR = s_SR, SD = s_SD;
       const float mq = s_mq, itq = s_itq, mp = s_mp;
       const float* zq = s_zq;
+      const FracMul fm = s_fm;  // floor(D_j SR / SD) for every j
       uint64_t local = 0;
-      for (int j = threadIdx.x; j < n; j += blockDim.x) {
-        const int tj = j0 + j;
-        const bool rem = (rbits[j >> 5] >> (j & 31)) & 1u;
-        const uint64_t Dj = rem ? 0ull : fx_mass(__fmul_rn(zq[tj], itq), mq);
-        uint64_t Rj = fresh ? fx_mass(__fmul_rn(z[tj], it), mp) : qbuf[j];
-        const uint64_t qj = Dj ? muldiv_u64(Dj, SR, SD) : 0ull;
-        Rj = Rj > qj ? Rj - qj : 0ull;
-        qbuf[j] = Rj;
-        local += Rj;
+      constexpr int kBatch = 8;  // tokens per thread in flight: their loads are issued together
+      for (int j = threadIdx.x; j < n; j += kBatch * blockDim.x) {
+        float qv[kBatch], zv[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int jj = j + i * blockDim.x;
+          qv[i] = jj < n ? zq[j0 + jj] : 0.0f;
+          zv[i] = (fresh && jj < n) ? z[j0 + jj] : 0.0f;
+        }
+        // the recipe's exponentials two lanes at a time: (draft, target) of one
+        // token while the target masses are the row's own, else the drafts of two
+        float ed[kBatch], er[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; i += 2) {
+          const float d0 = __fsub_rn(__fmul_rn(qv[i], itq), mq), d1 = __fsub_rn(__fmul_rn(qv[i + 1], itq), mq);
+          if (fresh) {
+            const float2 a = fx_exp_x2(make_float2(d0, __fsub_rn(__fmul_rn(zv[i], it), mp)));
+            const float2 c = fx_exp_x2(make_float2(d1, __fsub_rn(__fmul_rn(zv[i + 1], it), mp)));
+            ed[i] = a.x, er[i] = a.y, ed[i + 1] = c.x, er[i + 1] = c.y;
+          } else {
+            const float2 a = fx_exp_x2(make_float2(d0, d1));
+            ed[i] = a.x, ed[i + 1] = a.y, er[i] = er[i + 1] = 0.0f;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int jj = j + i * blockDim.x;
+          if (jj < n) {
+            const bool rem = (rbits[jj >> 5] >> (jj & 31)) & 1u;
+            const uint64_t Dj = rem ? 0ull : fx_scale40_floor(ed[i]);
+            uint64_t Rj = fresh ? fx_scale40_floor(er[i]) : qbuf[jj];
+            const uint64_t qj = Dj ? frac_mul(fm, Dj) : 0ull;
+            Rj = Rj > qj ? Rj - qj : 0ull;
+            qbuf[jj] = Rj;
+            local += Rj;
+          }
+        }
       }
       local = block_reduce(local, SumU64(), s_red);
+      if (threadIdx.x < CL) *cluster.map_shared_rank(&s_parts[rank], threadIdx.x) = local;  // to every CTA
       if (threadIdx.x == 0) {
-        s_part = local;
         const int t = s_t;
         if (t >= j0 && t < j1) rbits[(t - j0) >> 5] |= 1u << ((t - j0) & 31);
       }
       cluster.sync();  // partial sums and residuals visible
       if (threadIdx.x == 0) {
         uint64_t tot = 0;
-        for (int r = 0; r < CL; ++r) tot += *cluster.map_shared_rank(&s_part, r);
+        for (int r = 0; r < CL; ++r) tot += s_parts[r];
         s_SR = tot;
         s_SD -= s_Dt;
         s_removed[s_nrem++] = s_t;
         s_fresh = 0;
+        if (s_SD != 0ull) s_fm = frac_mul_prep(s_SR, s_SD);
       }
       __syncthreads();
     }
@@ -464,7 +544,7 @@ accept_sampled_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict
       for (int j = threadIdx.x; j < n; j += blockDim.x) qbuf[j] = fx_mass(__fmul_rn(z[j0 + j], it), mp);
     }
     __syncthreads();
-    writer = cluster_inverse_cdf(cluster, qbuf, n, j0, x, s_wsum, &s_sum, &s_bonus);
+    writer = cluster_inverse_cdf(cluster, qbuf, n, j0, x, s_wsum, s_sums, &s_bonus);
   } else if (!err && threadIdx.x == 0) {
     s_bonus = s_am;
   }

@@ -9,6 +9,11 @@ the allocator); ``run_round`` enqueues the seven steps on one stream:
 Nothing here computes: every step is a library kernel.  The draft model that
 turns the fused feature into draft logits needs trained weights and is not
 part of the round; its logits (one [B, F_d, V] block per depth) are inputs.
+
+With ``RoundConfig.sampled`` the children are drawn from the draft
+distribution (eagle3_expand_sampled, keyed by ``draw_seed``), every candidate
+is kept (N = number of candidates) and the accept step is spec_accept_sampled:
+"EAGLE 系列与 DFlash", §四 DFlash, acceptance min(1, p_target / p_draft).
 """
 from __future__ import annotations
 
@@ -37,6 +42,8 @@ class RoundConfig:
     dtype: str = "bf16"
     page_size: int = 64
     M_fuse: int = 0   # rows fused per round (0 -> B * (D + 1))
+    sampled: bool = False  # children drawn from the draft distribution
+    draw_seed: int = 0     # stream of those draws
 
     @property
     def R(self) -> int:
@@ -99,6 +106,10 @@ class RoundBuffers:
         self.c_score = torch.empty((c.B, n_cand), dtype=torch.float32, device=dev)
         self.c_depth = torch.empty((c.B, n_cand), **i32)
         self.cand = e3.make_cand(self.c_tok, self.c_parent, self.c_score, self.c_depth, n_cand)
+        if c.sampled and c.N != n_cand:
+            raise ValueError(f"sampled drafts keep every candidate: N must be {n_cand}, not {c.N}")
+        self.q_stats = torch.zeros((c.B * (n_cand + 1) * e3.QSTAT_BYTES if c.sampled else 16,), dtype=torch.uint8,
+                                   device=dev)
         Fmax = max(F for F, _ in sizes)
         self.f_id = [torch.empty((c.B, max(F, 1)), **i32) for F, _ in sizes] + [torch.empty((c.B, c.W if c.W < 1 << 20 else Fmax * c.k), **i32)]
         self.f_score = [torch.empty((c.B, max(F, 1)), dtype=torch.float32, device=dev) for F, _ in sizes] + [torch.empty((c.B, c.W if c.W < 1 << 20 else Fmax * c.k), dtype=torch.float32, device=dev)]
@@ -112,6 +123,7 @@ class RoundBuffers:
         self.depth = torch.empty((c.B, R), **i32)
         self.pos = torch.empty((c.B, R), **i32)
         self.mask = torch.empty((c.B, R, (R + 63) // 64), dtype=torch.int64, device=dev)
+        self.node_cand = torch.empty((c.B, R), **i32)
         # verify
         self.Q = [torch.empty((c.B, R, c.H, c.hd), dtype=td, device=dev) for _ in range(c.L)]
         self.O = [torch.empty((c.B, R, c.H, c.hd), dtype=td, device=dev) for _ in range(c.L)]
@@ -141,30 +153,63 @@ class RoundBuffers:
         self.temp_rows.copy_(self.temp.repeat_interleave(self.cfg.R))
 
 
-def run_round(bufs: RoundBuffers, stream=None, write_tree_qkv=None, sm_scale=None):
+def expand_depth(bufs: RoundBuffers, di: int, stream=None):
+    """Depth di + 1 of the draft tree: expand the frontier rows of bufs.draft_logits[di]."""
+    c = bufs.cfg
+    F, off = c.frontier_sizes()[0][di]
+    if c.sampled:
+        e3.eagle3_expand_sampled(bufs.draft_logits[di], c.B, F, c.V, c.k, c.W, 1.0, bufs.f_score[di], bufs.f_id[di],
+                                 di + 1, off, bufs.cand, bufs.f_id[di + 1], bufs.f_score[di + 1], c.draw_seed,
+                                 bufs.q_stats, bufs.dev_err, stream=stream)
+    else:
+        e3.eagle3_expand(bufs.draft_logits[di], c.B, F, c.V, c.k, c.W, 1.0, bufs.f_score[di], bufs.f_id[di],
+                         di + 1, off, bufs.cand, bufs.f_id[di + 1], bufs.f_score[di + 1], bufs.dev_err, stream=stream)
+
+
+def build_tree(bufs: RoundBuffers, stream=None):
+    c = bufs.cfg
+    e3.tree_build_mask(bufs.cand, c.B, c.n_cand, c.N, bufs.root_tok, bufs.kv_len, bufs.tok, bufs.parent,
+                       bufs.depth, bufs.pos, bufs.mask, node_cand=bufs.node_cand if c.sampled else None,
+                       stream=stream)
+
+
+def run_round(bufs: RoundBuffers, stream=None, write_tree_qkv=None, sm_scale=None, mark=None):
     """Enqueue one round.  ``write_tree_qkv(bufs)`` (optional) is called after
     tree_build_mask to write the tree nodes' Q (all layers) and K/V (slots
-    kv_len .. kv_len+R-1); without it the caller has written them beforehand."""
+    kv_len .. kv_len+R-1); without it the caller has written them beforehand.
+    ``mark(i)`` (optional) is called at the phase boundaries i = 0..7 (before
+    fusion, after fusion, expansion, tree, verify, LM head, accept, compaction)."""
     c = bufs.cfg
     R = c.R
     s = stream
+    mark = mark or (lambda i: None)
     sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(c.hd)
+    mark(0)
     e3.eagle3_fuse(bufs.h[0], bufs.h[1], bufs.h[2], bufs.W_f, None, bufs.g, c.M, c.d, c.d, c.dt,
                    bufs.fuse_ws, bufs.fuse_ws_bytes, bufs.dev_err, stream=s)
-    sizes, n_cand = c.frontier_sizes()
-    for di, (F, off) in enumerate(sizes):
-        e3.eagle3_expand(bufs.draft_logits[di], c.B, F, c.V, c.k, c.W, 1.0, bufs.f_score[di], bufs.f_id[di],
-                         di + 1, off, bufs.cand, bufs.f_id[di + 1], bufs.f_score[di + 1], bufs.dev_err, stream=s)
-    e3.tree_build_mask(bufs.cand, c.B, n_cand, c.N, bufs.root_tok, bufs.kv_len, bufs.tok, bufs.parent,
-                       bufs.depth, bufs.pos, bufs.mask, stream=s)
+    mark(1)
+    for di in range(c.D):
+        expand_depth(bufs, di, stream=s)
+    mark(2)
+    build_tree(bufs, stream=s)
+    mark(3)
     if write_tree_qkv is not None:
         write_tree_qkv(bufs)
     for l in range(c.L):
         e3.tree_verify_attn(bufs.Q[l], bufs.kv[l], bufs.kv_len, bufs.mask, c.B, R, c.H, c.max_kv_len, sm_scale,
                             bufs.O[l], bufs.lse[l], bufs.dev_err, bufs.ws, bufs.ws_bytes, stream=s)
+    mark(4)
     e3.lmhead_logits(bufs.O[c.L - 1], bufs.W_lm, c.B * R, c.H * c.hd, c.V, bufs.temp_rows, bufs.logits,
                      bufs.row_max, bufs.row_Q, bufs.row_argmax, bufs.dev_err, c.dt, stream=s)
-    e3.spec_accept(bufs.tok, bufs.parent, c.B, R, c.D, bufs.logits, bufs.row_max, bufs.row_Q, bufs.row_argmax,
-                   c.V, bufs.temp, bufs.u_acc, bufs.u_bonus, e3.E3_ACCEPT_TREE_DET, bufs.acc_len, bufs.path,
-                   bufs.out_tok, bufs.status, stream=s)
+    mark(5)
+    if c.sampled:
+        e3.spec_accept_sampled(bufs.tok, bufs.parent, bufs.node_cand, c.B, R, c.D, bufs.logits, bufs.row_max,
+                               bufs.row_Q, bufs.row_argmax, c.V, bufs.temp, bufs.q_stats, bufs.cap + 1, bufs.u_acc,
+                               bufs.u_bonus, bufs.acc_len, bufs.path, bufs.out_tok, bufs.status, stream=s)
+    else:
+        e3.spec_accept(bufs.tok, bufs.parent, c.B, R, c.D, bufs.logits, bufs.row_max, bufs.row_Q, bufs.row_argmax,
+                       c.V, bufs.temp, bufs.u_acc, bufs.u_bonus, e3.E3_ACCEPT_TREE_DET, bufs.acc_len, bufs.path,
+                       bufs.out_tok, bufs.status, stream=s)
+    mark(6)
     e3.kv_compact(bufs.kv, c.B, bufs.path, bufs.acc_len, c.D, bufs.kv_len, bufs.dev_err, stream=s)
+    mark(7)

@@ -3,13 +3,15 @@ own launch configuration (its workload, buffers and round function), checked
 against the oracle:
 
   fusion        sampled output features, within the dtype tolerance
-  expansion     every candidate of every request and depth, bit-exact
+  expansion     every candidate of every request and depth, bit-exact (drawn
+                children for the sampled configurations)
   tree          tokens, parents, depths, positions and mask rows, bit-exact
   verify        sampled (request, node, head) rows of the first and last layer,
                 within the dtype tolerance (the oracle runs those rows only)
   LM head       sampled rows on sampled vocabulary columns within tolerance; the
                 softmax statistics of every row bit-exact from the GPU logits
-  accept        accepted length, path and emitted tokens, bit-exact
+  accept        accepted length, path and emitted tokens, bit-exact (the
+                min(1, p/q) rule for the sampled configurations)
   compaction    slots P + j of sampled layers hold what slot P + path[j] held
 """
 import math
@@ -38,7 +40,8 @@ def f32(t):
     return t.float().cpu().numpy()
 
 
-@pytest.mark.parametrize("name", ["tiny", "8b", "8b_d8", "8b_chain3", "batched", "long", "70b"])
+@pytest.mark.parametrize("name", ["tiny", "8b", "8b_d8", "8b_chain3", "8b_sampled", "8b_chain3_sampled", "batched",
+                                  "long", "70b"])
 def test_round_matches_oracle(name):
     w = bench.Workload(name, seed=11)
     b, c = w.bufs, w.cfg
@@ -69,11 +72,20 @@ def test_round_matches_oracle(name):
     ctok, cpar, cdep, csc = host(b.c_tok), host(b.c_parent), host(b.c_depth), host(b.c_score)
     roots = host(b.root_tok)
     tok, par, dep, pos, mask = host(b.tok), host(b.parent), host(b.depth), host(b.pos), host(b.mask)
+    qrows = []  # sampled drafts: candidate (root -1) -> the draft row it was expanded with
     for bb in range(B):
         cands = oracle.new_cands(n_cand)
         fid, fsc = np.array([-1], np.int32), np.zeros(1, np.float32)
+        rows = {}
         for di, (F, off) in enumerate(sizes):
-            fid, fsc = oracle.expand(drafts[di][bb][:F], c.k, c.W, fsc, fid, di + 1, off, cands)
+            if c.sampled:
+                for f in range(F):
+                    rows[int(fid[f])] = drafts[di][bb][f]
+                fid, fsc, _, _ = oracle.expand_sampled(drafts[di][bb][:F], c.k, c.W, fsc, fid, di + 1, off, cands,
+                                                       c.draw_seed, bb)
+            else:
+                fid, fsc = oracle.expand(drafts[di][bb][:F], c.k, c.W, fsc, fid, di + 1, off, cands)
+        qrows.append(rows)
         assert np.array_equal(ctok[bb], cands["tok"]), (name, bb)
         assert np.array_equal(cpar[bb], cands["parent"]), (name, bb)
         assert np.array_equal(cdep[bb], cands["depth"]), (name, bb)
@@ -81,6 +93,8 @@ def test_round_matches_oracle(name):
         tree = oracle.build_tree(cands, n_cand, c.N, int(roots[bb]), int(P[bb]))
         for key, got in (("tok", tok), ("parent", par), ("depth", dep), ("pos", pos)):
             assert np.array_equal(got[bb], tree[key]), (name, key, bb)
+        if c.sampled:
+            assert np.array_equal(host(b.node_cand)[bb], tree["node_cand"]), (name, bb)
         assert np.array_equal(mask[bb].view(np.uint64), tree["mask"]), (name, bb)
 
     # verify: sampled rows of the first and the last layer
@@ -108,9 +122,18 @@ def test_round_matches_oracle(name):
     # accept, per request
     temps, ua, ub = host(b.temp), host(b.u_acc).view(np.uint32), host(b.u_bonus).view(np.uint32)
     acc, path, out = host(b.acc_len), host(b.path), host(b.out_tok)
+    nc = host(b.node_cand)
     for bb in range(B):
-        a, p, o = oracle.accept({"tok": tok[bb], "parent": par[bb]}, z[bb * R:(bb + 1) * R], temps[bb], ua[bb],
-                                ub[bb], c.D)
+        tree_b = {"tok": tok[bb], "parent": par[bb]}
+        if c.sampled:
+            qlog = np.zeros((R, c.V), np.float32)
+            for u in range(R):
+                key = -1 if u == 0 else int(nc[bb, u])
+                if key in qrows[bb]:
+                    qlog[u] = qrows[bb][key]
+            a, p, o = oracle.accept_sampled(tree_b, z[bb * R:(bb + 1) * R], temps[bb], qlog, 1.0, ua[bb], ub[bb], c.D)
+        else:
+            a, p, o = oracle.accept(tree_b, z[bb * R:(bb + 1) * R], temps[bb], ua[bb], ub[bb], c.D)
         assert acc[bb] == a and np.array_equal(path[bb], p) and np.array_equal(out[bb], o), (name, bb)
     assert np.array_equal(host(b.kv_len), P + 1 + acc)
 
