@@ -221,12 +221,6 @@ __device__ __forceinline__ uint64_t mulhi32(uint32_t u, uint64_t R) {
   return (hi << 32) | (lo >> 32);
 }
 
-// floor(a * b / c) for c > 0 and a * b < 2^128.
-__device__ __forceinline__ uint64_t muldiv_u64(uint64_t a, uint64_t b, uint64_t c) {
-  const unsigned __int128 p = static_cast<unsigned __int128>(a) * b;
-  return static_cast<uint64_t>(p / c);
-}
-
 // floor(a * b / c) for many a < 2^63 with b and c > 0 fixed, without a division
 // per a: b / c = I + bm / c (I = floor(b / c), bm = b mod c) and
 // rf = floor(bm 2^64 / c), so that t = floor(a rf / 2^64) is floor(a bm / c) or

@@ -17,10 +17,16 @@
 // builds the children lists and each child's fixed-point mass in parallel and
 // then walks the tree (integer work only).  For the bonus draw, CTA r owns a
 // contiguous chunk of the vocabulary: it computes the residual masses of its
-// chunk into shared memory; the chunk sums are exchanged through distributed
+// chunk into shared memory; every CTA pushes its chunk sum into all CTAs'
 // shared memory; the CTA whose chunk holds the target finds the token (warp
-// sums, then a warp scan of one 32-token group) and writes the request's
+// sums, then one warp scan over per-lane pieces) and writes the request's
 // outputs.
+//
+// accept_sampled_kernel (spec_accept_sampled) serves children that were drawn
+// from the draft distribution: the acceptance probability is the page's
+// min(1, p_res / q_res) and a rejection replaces the residual by
+// max(0, p_res - q_res), computed over the whole vocabulary in integer masses
+// (see the kernel's own comment).
 #include <cooperative_groups.h>
 
 #include "e3_common.cuh"

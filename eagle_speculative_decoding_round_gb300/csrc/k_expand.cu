@@ -11,6 +11,13 @@
 // shared memory; CTA 0 writes the k children.
 // Kernel 2 (one CTA per request): sort the F*k children by (score desc,
 // candidate index asc) in shared memory and emit the next frontier.
+//
+// eagle3_expand_sampled runs kernel 1's sampled variant: the k children are
+// draws without replacement from the row's draft distribution ("EAGLE 系列与
+// DFlash", §四 DFlash: drafts proposed by the drafter, checked with
+// min(1, p_target / p_draft)), picked as the k earliest arrivals of the
+// exponential race E_j / e_j with E_j = -ln U_j from a counter-based SplitMix64
+// stream; kernel 2 is unchanged.
 #include <cooperative_groups.h>
 
 #include "e3_common.cuh"

@@ -11,7 +11,9 @@
 // asc), one key per thread in registers (shuffles within a warp, shared memory
 // across warps); the first N are kept.  Flat indices are assigned depth by
 // depth with a parallel rank count on (parent's flat index, candidate index);
-// each mask row is the OR of the bits on its ancestor walk.
+// each mask row is the OR of the bits on its ancestor walk.  Optionally the
+// candidate index of every flat node is written (node_cand), which is how the
+// sampled accept finds the draft row a node's children were drawn from.
 #include <algorithm>
 
 #include "e3_common.cuh"
