@@ -132,6 +132,9 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
   __shared__ int s_nrem, s_u, s_acc, s_err, s_bonus;
   __shared__ unsigned long long s_x, s_sums[kMaxCluster];
   __shared__ unsigned long long s_wsum[kAcceptThreads / 32];
+  __shared__ float s_nmax[kMaxR];  // every node's row statistics, loaded in parallel
+  __shared__ int s_nam[kMaxR];
+  __shared__ unsigned long long s_nQ[kMaxR];
 
   pdl_wait();
   pdl_trigger();
@@ -141,6 +144,9 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
   for (int i = threadIdx.x; i < R; i += blockDim.x) {
     s_tok[i] = tok[rb + i];
     s_par[i] = parent[rb + i];
+    s_nmax[i] = row_max[rb + i];
+    s_nam[i] = row_argmax[rb + i];
+    s_nQ[i] = row_Q[rb + i];
   }
   __syncthreads();
   // children lists in CSR form (children in ascending flat order) and child masses
@@ -172,7 +178,7 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
     const int t = s_tok[c];
     if (T > 0.0f && t >= 0 && t < V) {
       const size_t prow = rb + p;
-      s_qc[c] = fx_mass(__fmul_rn(logits[prow * V + t], it), row_max[prow]);
+      s_qc[c] = fx_mass(__fmul_rn(logits[prow * V + t], it), s_nmax[p]);
     }
   }
   __syncthreads();
@@ -181,14 +187,13 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
     int u = 0, a = 0, nrem = 0;
     uint64_t Rm = 0;
     for (;;) {
-      const size_t row = rb + u;
-      const float m = row_max[row];
-      const int am = row_argmax[row];
+      const float m = s_nmax[u];
+      const int am = s_nam[u];
       if (am < 0 || !isfinite(m)) {
         s_err = E3_DEV_ERR_NONFINITE;
         break;
       }
-      Rm = row_Q[row];
+      Rm = s_nQ[u];
       nrem = 0;
       int accepted = -1;
       for (int e = s_first[u]; e < s_first[u] + s_nch[u]; ++e) {
@@ -232,7 +237,7 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
     const int u = s_u;
     const uint64_t x = s_x;
     const size_t row = rb + u;
-    const float m = row_max[row];
+    const float m = s_nmax[u];
     const float* z = logits + row * V;
     const int per = (V + CL - 1) / CL;
     const int j0 = min(V, rank * per), j1 = min(V, j0 + per);
