@@ -314,6 +314,11 @@ E3_API e3_status spec_accept(const int32_t* tok, const int32_t* parent, int B, i
  * greedy rule.  Other arguments and outputs as spec_accept; node_cand from
  * tree_build_mask; q_cap = 1 + cands->cap (entries per request of q_stats).
  * Non-finite target or draft statistics set E3_DEV_ERR_NONFINITE in status[b].
+ * Lifetime: q_stats entries point INTO the draft logit buffers given to
+ * eagle3_expand_sampled; those rows must stay allocated and unchanged until this
+ * call has run, and the entries of every node with children must come from the
+ * expansions that produced this tree (a NULL row is reported, a stale one is not
+ * detectable).
  * ------------------------------------------------------------------------- */
 E3_API e3_status spec_accept_sampled(const int32_t* tok, const int32_t* parent,
                                      const int32_t* node_cand, int B, int R, int D,
