@@ -29,6 +29,8 @@
 // (see the kernel's own comment).
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "e3_common.cuh"
 #include "e3_kernels.h"
 
@@ -579,9 +581,8 @@ accept_sampled_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict
 }
 
 int accept_cluster_size() {
-  static int cl = 0;
-  if (cl == 0) {
-    cl = 8;
+  static const int cl_once = [] {  // computed once, thread-safely
+    int cl = 8;
     if (cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(16);
@@ -598,12 +599,15 @@ int accept_cluster_size() {
       if (cudaOccupancyMaxActiveClusters(&n, accept_kernel, &cfg) == cudaSuccess && n > 0) cl = 16;
     }
     cudaGetLastError();
-  }
-  return cl;
+    return cl;
+  }();
+  return cl_once;
 }
 
 // 16-CTA clusters of accept_sampled_kernel where the GPU allows them, else 8.
 int accept_sampled_cluster_size(int V) {
+  static std::mutex mu;  // the cache below is read and refreshed as a unit
+  const std::lock_guard<std::mutex> lock(mu);
   static int cached_v = -1, cl = 8;
   if (cached_v != V) {
     cl = 8;
@@ -637,11 +641,10 @@ e3_status launch_accept_sampled(const int32_t* tok, const int32_t* parent, const
                                 const int32_t* row_argmax, int V, const float* temp, const e3_qstat* q_stats,
                                 int q_cap, const uint32_t* u_acc, const uint32_t* u_bonus, int32_t* acc_len,
                                 int32_t* path, int32_t* out_tok, int32_t* status, cudaStream_t s) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(accept_sampled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_done = true;
-  }
+  // one-time setup (a function-local static is initialised once, thread-safely)
+  static const bool attr_done =
+      (cudaFuncSetAttribute(accept_sampled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024), true);
+  (void)attr_done;
   const int CL = accept_sampled_cluster_size(V);
   const int per = (V + CL - 1) / CL;
   const size_t smem = static_cast<size_t>(per) * 8 + static_cast<size_t>((per + 31) / 32) * 4 + 16;
@@ -658,11 +661,10 @@ e3_status launch_accept(const int32_t* tok, const int32_t* parent, int B, int R,
                         const float* row_max, const uint64_t* row_Q, const int32_t* row_argmax, int V,
                         const float* temp, const uint32_t* u_acc, const uint32_t* u_bonus, int32_t* acc_len,
                         int32_t* path, int32_t* out_tok, int32_t* status, cudaStream_t s) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_done = true;
-  }
+  // one-time setup (a function-local static is initialised once, thread-safely)
+  static const bool attr_done =
+      (cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024), true);
+  (void)attr_done;
   const int CL = accept_cluster_size();
   const size_t smem = static_cast<size_t>((V + CL - 1) / CL) * sizeof(unsigned long long) + 16;
   E3_REQUIRE(smem <= 200 * 1024, E3_ERR_SHAPE, "spec_accept: V=%d too large", V);

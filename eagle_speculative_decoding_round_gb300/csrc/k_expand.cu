@@ -20,6 +20,8 @@
 // stream; kernel 2 is unchanged.
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "e3_common.cuh"
 #include "e3_kernels.h"
 
@@ -443,6 +445,8 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
 // fits one wave of such clusters, else clusters of 8.
 template <int KMAX, bool SAMPLED>
 int cluster_size_for(int rows, int V, bool vec, int k) {
+  static std::mutex mu;  // the cache below is read and refreshed as a unit
+  const std::lock_guard<std::mutex> lock(mu);
   static int cached_v = -1, cached_k = -1, max16 = 0;
   if (cached_v != V || cached_k != k) {
     max16 = 0;
@@ -473,11 +477,11 @@ template <int KMAX, bool SAMPLED>
 e3_status launch_rows(const float* logits, int rows, int F, int V, int k, float inv_temp, const float* parent_score,
                       const int32_t* parent_id, int depth, int cand_offset, const e3_cand& c, uint64_t seed,
                       e3_qstat* qs, int32_t* dev_err, cudaStream_t s) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaFuncSetAttribute(expand_rows_kernel<KMAX, SAMPLED>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_done = true;
-  }
+  // one-time setup (a function-local static is initialised once, thread-safely)
+  static const bool attr_done = (cudaFuncSetAttribute(expand_rows_kernel<KMAX, SAMPLED>,
+                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024),
+                                 true);
+  (void)attr_done;
   const bool vec = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
   const int CL = cluster_size_for<KMAX, SAMPLED>(rows, V, vec, k);
   const int cand_cap = expand_cand_cap(V, vec, k, CL);

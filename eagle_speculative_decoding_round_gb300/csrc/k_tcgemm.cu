@@ -21,6 +21,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "e3_common.cuh"
 #include "e3_kernels.h"
@@ -523,15 +524,15 @@ row_q_kernel(const float* __restrict__ logits, int V, const float* __restrict__ 
 // The driver's tensor-map encoder, looked up through the runtime so that the
 // library does not link libcuda (it must load on machines without a driver).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {  // looked up once, thread-safely
+    PFN_cuTensorMapEncodeTiled_v12000 found = nullptr;
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      found = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return found;
+  }();
   return fn;
 }
 
@@ -553,12 +554,12 @@ e3_status launch_fuse_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUte
                          int Nw, int Mx, int kb_per_src, int kb_total, int splits, float* out, int32_t* dev_err,
                          cudaStream_t s) {
   using C = TcCfg<BN>;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<bool> attr_done{false};
+  if (!attr_done.load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<BN, kModePartial>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return cuda_status(e, "tc_gemm_kernel smem attribute");
-    attr_done = true;
+    attr_done.store(true, std::memory_order_release);
   }
   const int kb_per_split = (kb_total + splits - 1) / splits;  // callers pass splits with no empty split
   dim3 grid((Mx + BN - 1) / BN, (Nw + BM - 1) / BM, splits);
@@ -636,22 +637,23 @@ e3_status launch_lmhead_bn(const CUtensorMap& a, const CUtensorMap& b, int V, in
                            unsigned long long* best, const float* temp, int32_t* dev_err, cudaStream_t s) {
   using C = LmCfg<BN>;
   static_assert(C::STAGES >= 2, "LM-head ring too small");
-  static bool attr_done = false;
-  static int n_sm = 0;
-  if (!attr_done) {
+  static std::atomic<bool> attr_done{false};
+  static std::atomic<int> n_sm{0};
+  if (!attr_done.load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return cuda_status(e, "lmhead_kernel smem attribute");
     int dev = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-    if (n_sm < 1) n_sm = 1;
-    attr_done = true;
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    n_sm.store(n < 1 ? 1 : n, std::memory_order_relaxed);
+    attr_done.store(true, std::memory_order_release);
   }
   const int n_mt = (M + BN - 1) / BN;
   const int n_vt = (V + BM - 1) / BM;
   const long n_tiles = static_cast<long>(n_mt) * n_vt;
   E3_REQUIRE(n_tiles < (1L << 31), E3_ERR_SHAPE, "lmhead_logits: %ld tiles", n_tiles);
-  const int grid = static_cast<int>(std::min<long>(n_tiles, n_sm));
+  const int grid = static_cast<int>(std::min<long>(n_tiles, n_sm.load(std::memory_order_relaxed)));
   const cudaError_t e = launch_pdl(lmhead_kernel<BN>, dim3(grid), dim3(192), C::SMEM, s, 1, a, b, V, M, kb_total, n_mt,
                                    static_cast<int>(n_tiles), logits, best, temp, dev_err);
   if (e != cudaSuccess) return cuda_status(e, "lmhead_kernel");

@@ -15,6 +15,8 @@
 // log2 domain into the workspace; a merge kernel combines the segments.
 #include <math.h>
 
+#include <atomic>
+
 #include "e3_common.cuh"
 #include "e3_kernels.h"
 
@@ -486,13 +488,13 @@ verify_merge_kernel(e3_kv_layer kv, const int32_t* __restrict__ kv_len, VerifyGe
 }
 
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
+  static const int n_once = [] {  // queried once, thread-safely (152 on GB300 if the query fails)
+    int dev = 0, n = 0;
     cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  }
-  return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+    return n;
+  }();
+  return n_once;
 }
 
 VerifyGeom make_geom(int B, int R, int H, int KVH, int hd, int max_kv_len, bool mma) {
@@ -564,10 +566,10 @@ e3_status launch_verify(const void* Q, const e3_kv_layer& kv, const int32_t* kv_
 #define E3_MMA_CASE(HDV)                                                                           \
   do {                                                                                             \
     const int smem = MmaCfg<HDV>::SMEM;                                                            \
-    static bool attr_done = false;                                                                 \
-    if (!attr_done) {                                                                              \
+    static std::atomic<bool> attr_done{false};                                                     \
+    if (!attr_done.load(std::memory_order_acquire)) {                                              \
       cudaFuncSetAttribute(verify_mma_kernel<HDV>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); \
-      attr_done = true;                                                                            \
+      attr_done.store(true, std::memory_order_release);                                            \
     }                                                                                              \
     verify_mma_kernel<HDV><<<grid, 256, smem, s>>>(static_cast<const __nv_bfloat16*>(Q), kv, kv_len, \
                                                    mask, g, sm_scale, ws_o, ws_ml, dev_err);       \

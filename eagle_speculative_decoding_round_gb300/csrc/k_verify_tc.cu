@@ -36,6 +36,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "e3_common.cuh"
 #include "e3_kernels.h"
 
@@ -937,23 +939,24 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {  // looked up once, thread-safely
+    PFN_cuTensorMapEncodeTiled_v12000 found = nullptr;
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      found = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return found;
+  }();
   return fn;
 }
 
 // How many clusters of S verify CTAs (one per SM) can be resident at once
 // (0 if such clusters cannot be launched).
 int max_active_clusters(int S) {
-  static int cache[17] = {0};  // -1: not launchable
+  static std::atomic<int> cache[17];  // 0: not yet known, -1: not launchable (idempotent entries)
   if (S < 1 || S > 16) return 0;
-  if (cache[S] == 0) {
+  if (cache[S].load(std::memory_order_relaxed) == 0) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S);
     cfg.blockDim = dim3(kThreads);
@@ -966,10 +969,12 @@ int max_active_clusters(int S) {
     cfg.attrs = &at;
     cfg.numAttrs = 1;
     int n = 0;
-    cache[S] = (cudaOccupancyMaxActiveClusters(&n, verify_tc_kernel<true>, &cfg) == cudaSuccess && n > 0) ? n : -1;
+    cache[S].store((cudaOccupancyMaxActiveClusters(&n, verify_tc_kernel<true>, &cfg) == cudaSuccess && n > 0) ? n : -1,
+                   std::memory_order_relaxed);
     cudaGetLastError();
   }
-  return cache[S] > 0 ? cache[S] : 0;
+  const int v = cache[S].load(std::memory_order_relaxed);
+  return v > 0 ? v : 0;
 }
 
 // Segments per cluster: the largest S (<= 16) whose clusters all fit in one wave
@@ -1037,15 +1042,15 @@ e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* 
   g.n_pages = kv.n_pages;
   g.page_table = kv.page_table;
   g.fold_tree = 0;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static std::atomic<bool> attr_done{false};
+  if (!attr_done.load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(verify_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return cuda_status(e, "verify_tc_kernel smem attribute");
     cudaFuncSetAttribute(verify_tc_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaGetLastError();
-    attr_done = true;
+    attr_done.store(true, std::memory_order_release);
   }
   *merged = false;
   const int groups = g.RG * kv.n_kv_heads * B;
