@@ -40,6 +40,10 @@
  *    caller's `dev_err` word (int32, device, nullable) with the E3_DEV_ERR_*
  *    bits; kernels never trap.
  *  - Row-major layouts, innermost dimension last.  bf16 is IEEE bfloat16.
+ *  - Calls may come from several host threads at once: the library's one-time
+ *    setup (kernel attributes, cluster sizes) is thread safe and the error
+ *    message is per thread.  Calls share no device state, except the fixed
+ *    scratch of eagle3_fuse_noalloc (see there).
  */
 #ifndef EAGLE3_H
 #define EAGLE3_H

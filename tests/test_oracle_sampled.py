@@ -73,8 +73,7 @@ def test_exp_variate_is_minus_log_of_the_stream_uniform():
         E = oracle.exp_variate(seed, b, d, f, j)
         assert E >= 0.0
         assert abs(E - (-math.log(U))) <= 4e-7 * max(1.0, -math.log(U)) + 1e-7
-    # U = 1 exactly (top bits all ones) gives E = +0
-    # and the variates have the Exp(1) mean and variance
+    # the variates have the Exp(1) mean and variance
     E = np.array([oracle.exp_variate(11, 0, 1, 0, j) for j in range(20000)])
     assert abs(E.mean() - 1.0) < 0.03 and abs(E.var() - 1.0) < 0.08
 
@@ -111,6 +110,28 @@ def test_sampled_children_are_draws_without_replacement():
     assert stat < chi2.ppf(1 - 1e-3, dof)
     # power: the same draws do not fit the distribution without the removal
     stat, dof = chi_square(np.bincount(ch[sel, 1], minlength=V).astype(float), q)
+    assert stat > chi2.ppf(1 - 1e-3, dof)
+
+
+def test_ordered_pairs_of_draws_follow_the_without_replacement_law():
+    """P(first = a, second = b) = q_a q_b / (1 - q_a) for a != b: chi-square over
+    all 20 ordered pairs of a 5-token row."""
+    V, n = 5, 30000
+    z = np.array([1.2, 0.4, 0.0, -0.6, -1.5], np.float32)
+    q = qprobs(z)
+    ch = draw_children(z, 2, n, seed0=31)
+    pairs = [(a, b) for a in range(V) for b in range(V) if a != b]
+    p = np.array([q[a] * q[b] / (1 - q[a]) for a, b in pairs])
+    assert abs(p.sum() - 1.0) < 1e-12
+    idx = {pr: i for i, pr in enumerate(pairs)}
+    counts = np.bincount([idx[(int(a), int(b))] for a, b in ch], minlength=len(pairs)).astype(float)
+    stat, dof = chi_square(counts, p)
+    assert stat < chi2.ppf(1 - 1e-3, dof)
+    # power: the law that forgets the removal (pairs weighted q_a q_b, renormalised
+    # over a != b) is rejected by the same draws
+    p_wrong = np.array([q[a] * q[b] for a, b in pairs])
+    p_wrong /= p_wrong.sum()
+    stat, dof = chi_square(counts, p_wrong)
     assert stat > chi2.ppf(1 - 1e-3, dof)
 
 
