@@ -5,10 +5,13 @@
 // chosen per expansion, by draft confidence.
 //
 // Kernel 1 (one 16- or 8-CTA cluster per frontier row): each CTA reads its part
-// of the row once into shared memory, then builds a per-thread top-KMAX list
-// (packed (value, id) keys, so ties go to the lower token id); the row maximum,
-// the fixed-point mass Q and the top-k lists are combined through distributed
-// shared memory; CTA 0 writes the k children.
+// of the row once into shared memory and keeps, as packed (value, id) keys (ties
+// go to the lower token id), only the elements that can be among its k best: those
+// not below the smallest warp maximum (or, when k exceeds the warp count or too
+// many qualify, the k-th largest per-thread maximum), ranked exactly.  The row
+// maximum, the fixed-point mass Q and each CTA's k best are combined through
+// distributed shared memory; CTA 0 merges the lists (KMAX-wide per lane) and
+// writes the k children.
 // Kernel 2 (one CTA per request): sort the F*k children by (score desc,
 // candidate index asc) in shared memory and emit the next frontier.
 //
@@ -47,19 +50,6 @@ size_t expand_smem_bytes(int V, bool vec, int k, int CL) {
   const int nvec = vec ? V / 4 : V;
   const int per = (nvec + CL - 1) / CL;
   return static_cast<size_t>(per + 1) * 16 + static_cast<size_t>(expand_cand_cap(V, vec, k, CL)) * 8 + 16;
-}
-
-template <int KMAX>
-__device__ __forceinline__ void topk_insert(uint64_t (&keys)[KMAX], uint64_t key) {
-  if (key <= keys[KMAX - 1]) return;
-#pragma unroll
-  for (int i = KMAX - 1; i > 0; --i) {
-    if (key > keys[i - 1])
-      keys[i] = keys[i - 1];
-    else if (key > keys[i])
-      keys[i] = key;
-  }
-  if (key > keys[0]) keys[0] = key;
 }
 
 // Merge the 32 sorted lists of a warp; lane 0 returns the best k in out[0..k).

@@ -161,41 +161,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 __device__ __forceinline__ void umma_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b)) : "memory");
 }
-// 32 consecutive 32-bit TMEM columns of this thread's lane as 16 register pairs
-// (columns 2i, 2i+1 in v[2i], v[2i+1]), so that paired fp32 operations take them
-// without register moves
-__device__ __forceinline__ void tmem_ld32p(uint32_t taddr, float (&v)[32]) {
-  unsigned long long q[16];
-  asm volatile(
-      "{\n .reg .b32 t<32>;\n"
-      " tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%16];\n"
-      " tcgen05.wait::ld.sync.aligned;\n"
-      " mov.b64 %0, {t0, t1};\n"
-      " mov.b64 %1, {t2, t3};\n"
-      " mov.b64 %2, {t4, t5};\n"
-      " mov.b64 %3, {t6, t7};\n"
-      " mov.b64 %4, {t8, t9};\n"
-      " mov.b64 %5, {t10, t11};\n"
-      " mov.b64 %6, {t12, t13};\n"
-      " mov.b64 %7, {t14, t15};\n"
-      " mov.b64 %8, {t16, t17};\n"
-      " mov.b64 %9, {t18, t19};\n"
-      " mov.b64 %10, {t20, t21};\n"
-      " mov.b64 %11, {t22, t23};\n"
-      " mov.b64 %12, {t24, t25};\n"
-      " mov.b64 %13, {t26, t27};\n"
-      " mov.b64 %14, {t28, t29};\n"
-      " mov.b64 %15, {t30, t31};\n"
-      "}\n"
-      : "=l"(q[0]), "=l"(q[1]), "=l"(q[2]), "=l"(q[3]), "=l"(q[4]), "=l"(q[5]), "=l"(q[6]), "=l"(q[7]), "=l"(q[8]), "=l"(q[9]), "=l"(q[10]), "=l"(q[11]), "=l"(q[12]), "=l"(q[13]), "=l"(q[14]), "=l"(q[15])
-      : "r"(taddr)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    v[2 * i] = __uint_as_float(static_cast<uint32_t>(q[i]));
-    v[2 * i + 1] = __uint_as_float(static_cast<uint32_t>(q[i] >> 32));
-  }
-}
 // 64 consecutive 32-bit TMEM columns of this thread's lane as 32 register pairs,
 // one load instruction and one wait
 __device__ __forceinline__ void tmem_ld64p(uint32_t taddr, float (&v)[64]) {
@@ -300,8 +265,6 @@ __device__ __forceinline__ void st_cluster_v2f(uint32_t a, float x, float y) {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-// TMEM address bits of the lane quarter warp w may access
-__device__ __forceinline__ uint32_t lane_base_of(int w) { return static_cast<uint32_t>((w & 3) * 32) << 16; }
 __device__ __forceinline__ float fmax3f(float a, float b, float c) {
   float y;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
