@@ -42,6 +42,24 @@ def test_library_exports_every_declared_symbol(e3):
     assert e3.QSTAT_BYTES == 24
 
 
+def declared_parameter_counts():
+    """Function name -> number of parameters, from the declarations in the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"E3_API\s+[\w\s\*]+?\b(\w+)\s*\(([^)]*)\)\s*;", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_lists_match_the_header(e3):
+    counts = declared_parameter_counts()
+    assert set(counts) == set(declared_functions())
+    for name, n in counts.items():
+        fn = getattr(e3.lib(), name)
+        assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
+
+
 def test_host_validation_rejects_bad_arguments(e3):
     # every call below fails its host checks before touching the device
     with pytest.raises(e3.E3Error) as ei:
