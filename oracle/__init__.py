@@ -25,7 +25,8 @@ Sources (web pages on EAGLE-3, cited by title and section):
       accepted path's KV).
 
 Parity pins: every function here is pinned by tests in ``tests/test_oracle_*.py``
-against values or identities that do not come from this file.
+against values or identities that do not come from this file.  ``oracle.draft``
+holds the drafter's decoder step (pinned in ``tests/test_oracle_draft.py``).
 """
 from __future__ import annotations
 
