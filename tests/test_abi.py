@@ -60,6 +60,28 @@ def test_binding_argument_lists_match_the_header(e3):
         assert len(fn.argtypes) == n, (name, len(fn.argtypes), n)
 
 
+def test_every_entry_point_rejects_null_arguments_without_a_launch(e3):
+    """Null pointers (host structs included) and zero sizes: each call returns
+    E3_ERR_INVALID_ARG from its host checks and nothing is launched."""
+    n0 = e3.launch_count()
+    statuses = {}
+    for name in e3.SYMBOLS:
+        fn = getattr(e3.lib(), name)
+        if fn.restype is not ctypes.c_int or not fn.argtypes:  # sizes, messages, counters, version
+            continue
+        args = []
+        for t in fn.argtypes:
+            if t is ctypes.c_float:
+                args.append(1.0)
+            elif t in (ctypes.c_int, ctypes.c_size_t, ctypes.c_uint64):
+                args.append(0)
+            else:  # device pointers and pointers to host structs
+                args.append(None)
+        statuses[name] = fn(*args)
+    assert statuses and all(v == 1 for v in statuses.values()), statuses
+    assert e3.launch_count() == n0
+
+
 def test_host_validation_rejects_bad_arguments(e3):
     # every call below fails its host checks before touching the device
     with pytest.raises(e3.E3Error) as ei:
