@@ -98,8 +98,29 @@ def cfg_values(name, seed, layers=None):
 # synthetic workload on the GPU
 # ---------------------------------------------------------------------------
 
+class InputSet:
+    """What differs between the rounds of one configuration: the draft logits of
+    each depth, the root tokens, the per-layer tree Q, and the tree pages of every
+    layer's K/V cache as they are before the round (the round's own tree K/V
+    written at slots P .. P+R-1; compaction changes them, so they are restored
+    before each round)."""
+
+    def __init__(self, drafts, Q, root_tok):
+        self.drafts, self.Q, self.root_tok = drafts, Q, root_tok
+        self.pages = self.snapK = self.snapV = None
+
+
 class Workload:
-    def __init__(self, name, seed=0, device="cuda", layers=None):
+    """Device buffers and synthetic inputs of one configuration.
+
+    ``n_sets`` distinct input sets (trees, roots, draft logits, tree Q/K/V) and
+    ``n_uniform`` uniform sets; round k uses input set k % n_sets and uniform set
+    k % n_uniform.  ``drafts="gpu"`` builds the draft logits with the stand-in
+    below (the library's own verify + LM head on each frontier's mini-tree, plus
+    noise); ``drafts=None`` leaves drafts, trees and tree Q/K/V unset for the
+    caller to fill (``add_set`` / ``finish_set``)."""
+
+    def __init__(self, name, seed=0, device="cuda", layers=None, n_sets=1, n_uniform=1, drafts="gpu"):
         import torch
 
         from eagle_speculative_decoding_round_gb300 import eagle3 as e3
@@ -108,7 +129,7 @@ class Workload:
 
         self.torch, self.e3, self.synth = torch, e3, synth
         c = cfg_values(name, seed, layers)
-        self.name, self.c, self.seed = name, c, seed
+        self.name, self.c, self.seed, self.device = name, c, seed, device
         R = c["N"] + 1
         self.cfg = RoundConfig(B=c["B"], N=c["N"], D=c["D"], k=c["k"], W=c["W"], H=c["H"], KVH=c["KVH"],
                                hd=c["hd"], d=c["d"], V=c["V"], L=c["L"], max_kv_len=max(c["P"]), dtype=c["dtype"],
@@ -136,12 +157,67 @@ class Workload:
         self.Vtab = randn((TAB_ROWS, c["KVH"], c["hd"]), 1.0)
         self.kv_len0 = torch.tensor(c["P"], dtype=torch.int32, device=device)
         b.kv_len.copy_(self.kv_len0)
-        rt = np.random.default_rng(seed + 1).integers(0, c["V"], c["B"]).astype(np.int32)
-        b.root_tok.copy_(torch.from_numpy(rt))
         b.set_temperature(torch.tensor(c["temps"], dtype=torch.float32))
-        b.u_acc.copy_(torch.from_numpy(synth.uniforms(seed, synth.PURPOSE_ACCEPT, c["B"], R).view(np.int32)))
-        b.u_bonus.copy_(torch.from_numpy(synth.uniforms(seed, synth.PURPOSE_BONUS, c["B"], R).view(np.int32)))
-        self.calibrate_and_draft()
+        # pages holding each request's tree slots [P, P + R): restored before every round
+        ps = self.cfg.page_size
+        pg = sorted({int(pt[bb, t // ps]) for bb, P in enumerate(c["P"]) for t in (P, P + R - 1)} |
+                    {int(pt[bb, q]) for bb, P in enumerate(c["P"]) for q in range(P // ps, (P + R - 1) // ps + 1)})
+        self.tree_pages = torch.tensor(pg, dtype=torch.long, device=device)
+        self.uni = []
+        for u in range(max(1, n_uniform)):
+            su = seed if u == 0 else seed * 1000003 + 7919 * u
+            self.uni.append((torch.from_numpy(synth.uniforms(su, synth.PURPOSE_ACCEPT, c["B"], R).view(np.int32))
+                             .to(device),
+                             torch.from_numpy(synth.uniforms(su, synth.PURPOSE_BONUS, c["B"], R).view(np.int32))
+                             .to(device)))
+        self.sets = []
+        if drafts == "gpu":
+            for si in range(max(1, n_sets)):
+                st = self.add_set(si)
+                if si == 0:
+                    self.calibrate()
+                self.draft_on_gpu()
+                from eagle_speculative_decoding_round_gb300.round import build_tree
+                build_tree(b)
+                self.finish_set(st, b.tok.long())
+            self.use(0)
+            torch.cuda.synchronize()
+            assert int(b.dev_err.item()) == 0, "device error during setup"
+
+    # -- input sets --------------------------------------------------------------
+    def root_tokens(self, si):
+        rs = self.seed + 1 if si == 0 else self.seed * 104729 + 31 * si + 1
+        return np.random.default_rng(rs).integers(0, self.c["V"], self.c["B"]).astype(np.int32)
+
+    def add_set(self, si):
+        """Allocate input set si (its draft-logit and Q buffers, root tokens) and make
+        it the current one."""
+        torch, b, c = self.torch, self.bufs, self.cfg
+        drafts = [torch.empty_like(x) for x in b.draft_logits] if self.sets else b.draft_logits
+        Q = [torch.empty_like(x) for x in b.Q] if self.sets else b.Q
+        st = InputSet(drafts, Q, torch.from_numpy(self.root_tokens(si)).to(self.device))
+        self.sets.append(st)
+        self._bind(st)
+        return st
+
+    def finish_set(self, st, toks):
+        """Write the set's tree (toks [B, R]: Q in every layer, K/V at slots P..P+R-1)
+        and snapshot the tree pages of every layer."""
+        b = self.bufs
+        self._bind(st)
+        self.write_nodes(toks, range(self.cfg.L), self.cfg.R)
+        st.pages = self.tree_pages
+        st.snapK = b.K_all.index_select(1, st.pages)
+        st.snapV = b.V_all.index_select(1, st.pages)
+
+    def _bind(self, st):
+        b = self.bufs
+        b.draft_logits, b.Q, b.root_tok = st.drafts, st.Q, st.root_tok
+
+    def use(self, k):
+        """Point the round's buffers at the inputs of round k (no copies)."""
+        self._bind(self.sets[k % len(self.sets)])
+        self.bufs.u_acc, self.bufs.u_bonus = self.uni[k % len(self.uni)]
 
     # -- token-keyed tree Q/K/V of the synthetic target -----------------------
     def write_nodes(self, toks, layers, R):
@@ -190,48 +266,28 @@ class Workload:
                          torch.empty(M, dtype=torch.int32, device="cuda"), b.dev_err, c.dt)
         return z
 
-    def calibrate_and_draft(self):
-        """Draft stand-in: at each depth the frontier nodes' target logits (verify +
-        LM head on the frontier's own mini-tree) plus N(0, noise^2) are the draft
-        logits.  W_lm is first scaled so that target logits have std ~ 4."""
-        from eagle_speculative_decoding_round_gb300.round import build_tree, expand_depth
-        torch, e3, b, c = self.torch, self.e3, self.bufs, self.cfg
-        B = c.B
+    def calibrate(self):
+        """Scale W_lm so that the target logits of the roots have std ~ 4."""
+        b, c = self.bufs, self.cfg
         roots = b.root_tok.cpu().numpy()
-        z = self.target_logits_of(roots[:, None].astype(np.int64), np.full((B, 1), -1), [(bb, 0) for bb in range(B)])
+        z = self.target_logits_of(roots[:, None].astype(np.int64), np.full((c.B, 1), -1),
+                                  [(bb, 0) for bb in range(c.B)])
         scale = 4.0 / float(z.float().std())
         b.W_lm.copy_((b.W_lm.float() * scale).to(c.tdtype))
+
+    def draft_on_gpu(self):
+        """Draft stand-in: at each depth the frontier nodes' target logits (verify +
+        LM head on the frontier's own mini-tree) plus N(0, noise^2) are the draft
+        logits of the current input set."""
+        from eagle_speculative_decoding_round_gb300.round import expand_depth
+        torch, b, c = self.torch, self.bufs, self.cfg
+        B = c.B
+        roots = b.root_tok.cpu().numpy()
         sizes, n_cand = c.frontier_sizes()
         paths = [{-1: [int(roots[bb])]} for bb in range(B)]
         for di, (F, off) in enumerate(sizes):
             fid = b.f_id[di].cpu().numpy()[:, :F]
-            # per request: mini-tree = root + frontier nodes' ancestors + frontier nodes
-            node_lists = []
-            for bb in range(B):
-                nodes = {(): -1}
-                order = [()]
-                for f in fid[bb]:
-                    p = paths[bb][int(f)][1:]
-                    for depth in range(1, len(p) + 1):
-                        key = tuple(p[:depth])
-                        if key not in nodes:
-                            nodes[key] = len(order)
-                            order.append(key)
-                order.sort(key=lambda t: (len(t), t))
-                node_lists.append(order)
-            Rm = max(len(o) for o in node_lists)
-            tok = np.zeros((B, Rm), np.int64)
-            par = np.full((B, Rm), -1, np.int64)
-            rows = []
-            for bb, order in enumerate(node_lists):
-                index = {key: i for i, key in enumerate(order)}
-                for i, key in enumerate(order):
-                    tok[bb, i] = key[-1] if key else roots[bb]
-                    par[bb, i] = index[key[:-1]] if key else -1
-                for i in range(len(order), Rm):  # padding nodes hang off the root
-                    par[bb, i] = 0
-                for f in fid[bb]:
-                    rows.append((bb, index[tuple(paths[bb][int(f)][1:])]))
+            tok, par, rows = mini_trees(paths, fid, roots)
             zt = self.target_logits_of(tok, par, rows).view(B, F, c.V)
             noise = torch.randn(zt.shape, generator=self.gen, device="cuda") * self.c["noise"]
             b.draft_logits[di].copy_(zt + noise)
@@ -240,16 +296,54 @@ class Workload:
             for bb in range(B):
                 for i in range(off, off + F * c.k):
                     paths[bb][i] = paths[bb][int(cp[bb, i])] + [int(ct[bb, i])]
-        # the final tree (same every step) and its Q/K/V in every layer
-        build_tree(b)
-        self.write_nodes(b.tok.long(), range(c.L), c.R)
-        torch.cuda.synchronize()
-        assert int(b.dev_err.item()) == 0, "device error during setup"
 
-    def round(self, stream=None):
+    def round(self, k=0, stream=None, mark=None):
+        """Round k: its inputs bound, request lengths reset, tree pages restored, then
+        the seven steps."""
         from eagle_speculative_decoding_round_gb300.round import run_round
-        self.bufs.kv_len.copy_(self.kv_len0)
-        run_round(self.bufs, stream=stream)
+        b = self.bufs
+        self.use(k)
+        st = self.sets[k % len(self.sets)]
+        b.kv_len.copy_(self.kv_len0)
+        b.K_all.index_copy_(1, st.pages, st.snapK)
+        b.V_all.index_copy_(1, st.pages, st.snapV)
+        run_round(b, stream=stream, mark=mark)
+
+
+def mini_trees(paths, fid, roots):
+    """Per request, the mini-tree of the frontier rows fid [B, F] (candidate ids, -1
+    = root) and their ancestors: tokens [B, R'], parents [B, R'] (flattened by
+    depth, then token path; padding nodes hang off the root) and the (b, node)
+    row of every frontier entry in order.  paths[b][cand] = token path from the
+    root."""
+    B = len(paths)
+    node_lists = []
+    for bb in range(B):
+        nodes = {(): -1}
+        order = [()]
+        for f in fid[bb]:
+            p = paths[bb][int(f)][1:]
+            for depth in range(1, len(p) + 1):
+                key = tuple(p[:depth])
+                if key not in nodes:
+                    nodes[key] = len(order)
+                    order.append(key)
+        order.sort(key=lambda t: (len(t), t))
+        node_lists.append(order)
+    Rm = max(len(o) for o in node_lists)
+    tok = np.zeros((B, Rm), np.int64)
+    par = np.full((B, Rm), -1, np.int64)
+    rows = []
+    for bb, order in enumerate(node_lists):
+        index = {key: i for i, key in enumerate(order)}
+        for i, key in enumerate(order):
+            tok[bb, i] = key[-1] if key else roots[bb]
+            par[bb, i] = index[key[:-1]] if key else -1
+        for i in range(len(order), Rm):
+            par[bb, i] = 0
+        for f in fid[bb]:
+            rows.append((bb, index[tuple(paths[bb][int(f)][1:])]))
+    return tok, par, rows
 
 
 # ---------------------------------------------------------------------------
@@ -332,61 +426,190 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle baseline (bounded sample)
+# CPU oracle baseline: whole rounds of the oracle on the host cores
 # ---------------------------------------------------------------------------
 
-def oracle_sample(w, budget_s=20.0):
-    """Time the oracle on a bounded sample of one round of the same workload and
-    scale to a whole round.  Sample: fusion, all expansion depths, tree build and
-    accept in full; verify attention of request 0 on as many layers as fit about
-    60% of budget_s (at least one; scaled by L over the layers done and by the
-    requests' keys); LM head on a 1/4 slice of the vocabulary (scaled by 4)."""
+class BlasThreads:
+    """Sets the thread count of numpy's OpenBLAS (the oracle's fp64 GEMMs) through
+    its own exported setter, and reads it back; unknown builds are left alone."""
+    NAMES = (("scipy_openblas_set_num_threads64_", "scipy_openblas_get_num_threads64_"),
+             ("scipy_openblas_set_num_threads", "scipy_openblas_get_num_threads"),
+             ("openblas_set_num_threads64_", "openblas_get_num_threads64_"),
+             ("openblas_set_num_threads", "openblas_get_num_threads"))
+
+    def __init__(self):
+        import ctypes
+        np.dot(np.ones((2, 2)), np.ones((2, 2)))  # the BLAS library is loaded
+        self.set = self.get = None
+        try:
+            paths = {ln.split()[-1] for ln in open("/proc/self/maps") if "blas" in ln.lower() and "/" in ln}
+        except OSError:
+            paths = set()
+        for pth in sorted(paths):
+            try:
+                lib = ctypes.CDLL(pth)
+            except OSError:
+                continue
+            for sn, gn in self.NAMES:
+                if hasattr(lib, sn) and hasattr(lib, gn):
+                    self.set, self.get = getattr(lib, sn), getattr(lib, gn)
+                    self.set.argtypes = [ctypes.c_int]
+                    self.get.restype = ctypes.c_int
+                    return
+
+    def threads(self):
+        return int(self.get()) if self.get else None
+
+    def use(self, n):
+        if self.set:
+            self.set(int(n))
+        return self.threads()
+
+
+def whole_round_feasible(w):
+    """A whole oracle round fits the CPU sample budget when its fp64 LM head is at
+    most ~0.2 TFLOP (8B, long, tiny and the chain/sampled variants; not batched or
+    70B)."""
+    c = w.cfg
+    return c.B * c.R * c.V * c.H * c.hd * 2 <= 2.0e11
+
+
+def oracle_round(w, k=0):
+    """One whole round of the oracle on round k's inputs: fusion, expansion and tree
+    build of every request, verify attention of every request on all L layers (the
+    oracle's dense masked form), the LM head of the oracle's own last-layer output,
+    softmax statistics and accept/reject of every request, and the compaction of
+    every layer.  Device data is staged to the host outside the timed parts (one
+    layer's cache at a time); returns seconds per phase."""
     import torch
 
     import oracle
-    try:
-        from threadpoolctl import threadpool_info
-        blas_threads = max([x.get("num_threads", 1) for x in threadpool_info()] or [1])
-    except Exception:
-        blas_threads = os.cpu_count()
+    b, cfg = w.bufs, w.cfg
+    B, R, V, L = cfg.B, cfg.R, cfg.V, cfg.L
+    f = lambda t: t.float().cpu().numpy() if t.dtype == torch.bfloat16 else t.cpu().numpy()  # noqa: E731
+    w.use(k)
+    st = w.sets[k % len(w.sets)]
+    pages = st.pages.cpu().numpy()
+    P = w.kv_len0.cpu().numpy()
+    hs = [f(t) for t in b.h]
+    Wf = f(b.W_f)
+    drafts = [f(x) for x in st.drafts]
+    roots = st.root_tok.cpu().numpy()
+    temps = b.temp.cpu().numpy()
+    ua, ub = b.u_acc.cpu().numpy().view(np.uint32), b.u_bonus.cpu().numpy().view(np.uint32)
+    sizes, n_cand = cfg.frontier_sizes()
+    times = {}
+
+    def layer_cache(l):
+        K, Vc = f(b.K_all[l]), f(b.V_all[l])
+        K[pages] = f(st.snapK[l])
+        Vc[pages] = f(st.snapV[l])
+        return K, Vc
+
+    t = time.perf_counter()
+    oracle.fuse(*hs, Wf)
+    times["fuse"] = time.perf_counter() - t
+    t = time.perf_counter()
+    trees, qrows = [], []
+    for bb in range(B):
+        c = oracle.new_cands(n_cand)
+        fid, fsc = np.array([-1], np.int32), np.zeros(1, np.float32)
+        rows = {}
+        for di, (F, off) in enumerate(sizes):
+            if cfg.sampled:
+                for fr in range(F):
+                    rows[int(fid[fr])] = drafts[di][bb][fr]
+                fid, fsc, _, _ = oracle.expand_sampled(drafts[di][bb][:F], cfg.k, cfg.W, fsc, fid, di + 1, off, c,
+                                                       cfg.draw_seed, bb)
+            else:
+                fid, fsc = oracle.expand(drafts[di][bb][:F], cfg.k, cfg.W, fsc, fid, di + 1, off, c)
+        trees.append(oracle.build_tree(c, n_cand, cfg.N, int(roots[bb]), int(P[bb])))
+        qrows.append(rows)
+    times["expand_build"] = time.perf_counter() - t
+    mask = np.stack([tr["mask"] for tr in trees])
+    sm = 1.0 / math.sqrt(cfg.hd)
+    tv = 0.0
+    O = None
+    for l in range(L):
+        K, Vc = layer_cache(l)
+        Q = f(st.Q[l])
+        t = time.perf_counter()
+        O, _ = oracle.tree_verify_attn_dense(Q, K, Vc, w.pt, P, mask, sm)
+        tv += time.perf_counter() - t
+    times["verify"] = tv
+    Wl = f(b.W_lm)
+    t = time.perf_counter()
+    z = oracle.lmhead_logits(O.reshape(B * R, -1), Wl).astype(np.float32)
+    times["lmhead"] = time.perf_counter() - t
+    t = time.perf_counter()
+    acc, paths = np.zeros(B, np.int32), np.zeros((B, cfg.D + 1), np.int32)
+    for bb in range(B):
+        zb = z[bb * R:(bb + 1) * R]
+        if cfg.sampled:
+            qlog = np.zeros((R, V), np.float32)
+            for u in range(R):
+                key = -1 if u == 0 else int(trees[bb]["node_cand"][u])
+                if key in qrows[bb]:
+                    qlog[u] = qrows[bb][key]
+            a, pth, _ = oracle.accept_sampled(trees[bb], zb, float(temps[bb]), qlog, 1.0, ua[bb], ub[bb], cfg.D)
+        else:
+            a, pth, _ = oracle.accept(trees[bb], zb, float(temps[bb]), ua[bb], ub[bb], cfg.D)
+        acc[bb], paths[bb] = a, pth
+    times["accept"] = time.perf_counter() - t
+    tc = 0.0
+    for l in range(L):
+        K, Vc = layer_cache(l)
+        t = time.perf_counter()
+        oracle.kv_compact([K, Vc], w.pt, P, paths, acc)
+        tc += time.perf_counter() - t
+    times["compact"] = tc
+    return times
+
+
+def oracle_sample(w, budget_s=20.0):
+    """An ESTIMATE of one oracle round for the configurations whose whole round does
+    not fit the budget (batched, 70B): fusion, expansion, tree build and accept of
+    request 0 scaled by B; verify of request 0 (dense form) on as many layers as fit
+    ~60% of budget_s, scaled by L and by the batch's keys; the LM head on 1/4 of the
+    vocabulary, scaled by 4."""
+    import torch
+
+    import oracle
     b, cfg = w.bufs, w.cfg
     f = lambda t: t.float().cpu().numpy() if t.dtype == torch.bfloat16 else t.cpu().numpy()  # noqa: E731
     B, R, V = cfg.B, cfg.R, cfg.V
+    w.use(0)
+    st = w.sets[0]
+    pages = st.pages.cpu().numpy()
     times = {}
-    t0 = time.perf_counter()
     hs = [f(t) for t in b.h]
     Wf = f(b.W_f)
     t = time.perf_counter()
     oracle.fuse(*hs, Wf)
     times["fuse"] = time.perf_counter() - t
     sizes, n_cand = cfg.frontier_sizes()
-    drafts = [f(x) for x in b.draft_logits]
+    drafts = [f(x) for x in st.drafts]
     t = time.perf_counter()
-    trees, qrows = [], []
-    for bb in range(B if B <= 2 else 1):
-        c = oracle.new_cands(n_cand)
-        fid, fsc = np.array([-1], np.int32), np.zeros(1, np.float32)
-        rows = {}  # candidate (root -1) -> the draft row it was expanded with
-        for di, (F, off) in enumerate(sizes):
-            if cfg.sampled:
-                for fr in range(F):
-                    rows[int(fid[fr])] = drafts[di][bb][fr]
-                fid, fsc, _, _ = oracle.expand_sampled(drafts[di][bb], cfg.k, cfg.W, fsc, fid, di + 1, off, c,
-                                                       cfg.draw_seed, bb)
-            else:
-                fid, fsc = oracle.expand(drafts[di][bb], cfg.k, cfg.W, fsc, fid, di + 1, off, c)
-        trees.append(oracle.build_tree(c, n_cand, cfg.N, int(b.root_tok[bb]), int(w.kv_len0[bb])))
-        qrows.append(rows)
-    times["expand_build"] = (time.perf_counter() - t) * (B / len(trees))
+    c = oracle.new_cands(n_cand)
+    fid, fsc = np.array([-1], np.int32), np.zeros(1, np.float32)
+    for di, (F, off) in enumerate(sizes):
+        if cfg.sampled:
+            fid, fsc, _, _ = oracle.expand_sampled(drafts[di][0][:F], cfg.k, cfg.W, fsc, fid, di + 1, off, c,
+                                                   cfg.draw_seed, 0)
+        else:
+            fid, fsc = oracle.expand(drafts[di][0][:F], cfg.k, cfg.W, fsc, fid, di + 1, off, c)
+    tree = oracle.build_tree(c, n_cand, cfg.N, int(st.root_tok[0]), int(w.kv_len0[0]))
+    times["expand_build"] = (time.perf_counter() - t) * B
     p0 = int(w.c["P"][0])
     scale_b = sum(p + R for p in w.c["P"]) / (p0 + R)
     spent, n_layers = 0.0, 0
     for l in range(cfg.L - 1, -1, -1):
-        K, Vc = f(b.K[l]), f(b.Vc[l])
-        Q = f(b.Q[l])[:1]
+        K, Vc = f(b.K_all[l]), f(b.V_all[l])
+        K[pages], Vc[pages] = f(st.snapK[l]), f(st.snapV[l])
+        Q = f(st.Q[l])[:1]
         t = time.perf_counter()
-        oracle.tree_verify_attn(Q, K, Vc, w.pt[:1], w.kv_len0.cpu().numpy()[:1], trees[0]["parent"][None],
-                                1.0 / math.sqrt(cfg.hd))
+        oracle.tree_verify_attn_dense(Q, K, Vc, w.pt[:1], w.kv_len0.cpu().numpy()[:1], tree["mask"][None],
+                                      1.0 / math.sqrt(cfg.hd))
         spent += time.perf_counter() - t
         n_layers += 1
         if spent >= 0.6 * budget_s:
@@ -394,28 +617,65 @@ def oracle_sample(w, budget_s=20.0):
     times["verify"] = spent / n_layers * cfg.L * scale_b
     Wl = f(b.W_lm)
     h = f(b.O[cfg.L - 1]).reshape(B * R, -1)
-    sl = slice(0, V // 4)
     t = time.perf_counter()
-    z = oracle.lmhead_logits(h, Wl[sl])
-    oracle.row_stats(z.astype(np.float32), 1.0)
+    z = oracle.lmhead_logits(h, Wl[:V // 4])
     times["lmhead"] = (time.perf_counter() - t) * 4
-    zl = f(b.logits)
+    del z
+    zl = f(b.logits)[:R]  # full rows (the GPU's logits of the last round): tokens index the whole vocabulary
     t = time.perf_counter()
-    tt = {"tok": b.tok.cpu().numpy()[0], "parent": b.parent.cpu().numpy()[0]}
     ua, ub = b.u_acc.cpu().numpy()[0].view(np.uint32), b.u_bonus.cpu().numpy()[0].view(np.uint32)
     if cfg.sampled:
-        qlog = np.zeros((R, V), np.float32)
-        for u in range(R):
-            key = -1 if u == 0 else int(trees[0]["node_cand"][u])
-            if key in qrows[0]:
-                qlog[u] = qrows[0][key]
-        oracle.accept_sampled(tt, zl[:R], float(w.c["temps"][0]), qlog, 1.0, ua, ub, cfg.D)
+        oracle.accept_sampled(tree, zl, float(w.c["temps"][0]), np.ascontiguousarray(zl), 1.0, ua, ub, cfg.D)
     else:
-        oracle.accept(tt, zl[:R], float(w.c["temps"][0]), ua, ub, cfg.D)
+        oracle.accept(tree, zl, float(w.c["temps"][0]), ua, ub, cfg.D)
     times["accept"] = (time.perf_counter() - t) * B
-    total = sum(times.values())
-    wall = time.perf_counter() - t0
-    return {"round_s": total, "times": times, "cores": blas_threads, "wall_s": wall, "verify_layers": n_layers}
+    return times, n_layers
+
+
+def cpu_baseline(w, budget_s=30.0):
+    """The oracle on the host cores: whole rounds at all cores and at one thread
+    where a whole round fits the budget, else an estimate from a sample."""
+    bt = BlasThreads()
+    n_all = bt.threads() or os.cpu_count()
+    out = {"kind": "oracle", "unit": "rounds/s"}
+    if whole_round_feasible(w):
+        t0 = time.perf_counter()
+        times = oracle_round(w, 0)
+        sec_all = sum(times.values())
+        out.update(value=round(1.0 / sec_all, 6), cores=n_all, seconds_per_round=round(sec_all, 3),
+                   breakdown_s={k: round(v, 3) for k, v in times.items()},
+                   threads_all={"threads": n_all, "rounds_per_s": round(1.0 / sec_all, 6),
+                                "seconds_per_round": round(sec_all, 3)},
+                   sample="one whole round of the same workload (round 0's inputs): fusion, expansion, tree "
+                          "build, verify on all L layers (dense masked form), LM head, statistics and accept "
+                          "of every request, compaction of every layer; device data staged to the host "
+                          "outside the timed parts")
+        if sec_all * 8 <= budget_s and bt.set:
+            one = bt.use(1)
+            try:
+                times1 = oracle_round(w, 0)
+            finally:
+                bt.use(n_all)
+            sec1 = sum(times1.values())
+            out["threads_1"] = {"threads": one, "rounds_per_s": round(1.0 / sec1, 6),
+                                "seconds_per_round": round(sec1, 3),
+                                "breakdown_s": {k: round(v, 3) for k, v in times1.items()}}
+        else:
+            out["threads_1"] = None
+            out["threads_1_note"] = ("BLAS thread control unavailable" if not bt.set else
+                                     f"a one-thread round would exceed the {budget_s:.0f} s sample budget")
+        out["wall_s"] = round(time.perf_counter() - t0, 1)
+    else:
+        times, n_layers = oracle_sample(w, budget_s * 0.6)
+        sec = sum(times.values())
+        out.update(value=round(1.0 / sec, 6), cores=n_all, seconds_per_round=round(sec, 3), estimate=True,
+                   breakdown_s={k: round(v, 3) for k, v in times.items()},
+                   threads_all={"threads": n_all, "rounds_per_s": round(1.0 / sec, 6)}, threads_1=None,
+                   threads_1_note="a whole round does not fit the sample budget at this size",
+                   sample=f"ESTIMATE: request 0's fusion, expansion, tree build and accept scaled by B; verify of "
+                          f"request 0 on {n_layers} of the L layers scaled by L and by the batch's keys; LM head "
+                          f"on 1/4 of the vocabulary scaled by 4")
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -423,11 +683,13 @@ def oracle_sample(w, budget_s=20.0):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=32)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="8b", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--sets", type=int, default=8, help="distinct input sets (trees, roots, drafts) cycled")
+    ap.add_argument("--min-time", type=float, default=2.5, help="seconds of timed graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=None,
@@ -446,73 +708,82 @@ def main():
     if args.impl == "reference":
         return reference_arm(args, rank, world)
     torch.cuda.set_device(local)
-    w = Workload(args.config, seed=args.seed + 1000 * rank, layers=args.layers)
+    K = args.steps
+    n_stat = max(K, 32)
+    w = Workload(args.config, seed=args.seed + 1000 * rank, layers=args.layers, n_sets=args.sets, n_uniform=n_stat)
     cfg = w.cfg
     s = torch.cuda.Stream()
     torch.cuda.synchronize()
+    from eagle_speculative_decoding_round_gb300 import eagle3 as e3
     with torch.cuda.stream(s):
-        for _ in range(args.warmup):
-            w.bufs.kv_len.copy_(w.kv_len0)  # every round starts from the same request lengths
-            w.round()
+        for i in range(args.warmup):
+            w.round(i)
+        # acceptance over n_stat distinct rounds (round k: input set k % sets, uniforms k)
+        hist = torch.empty((n_stat, cfg.B), dtype=torch.int32, device="cuda")
+        for k in range(n_stat):
+            w.round(k)
+            hist[k].copy_(w.bufs.acc_len)
     s.synchronize()
-    accepted = w.bufs.acc_len.cpu().numpy().copy()
+    check_dev_err(w, "warm-up rounds")
+    accepted = hist.cpu().numpy().reshape(-1)
 
-    # The timed region: one graph of K rounds (nothing but the rounds: each round first
-    # resets kv_len).  A second graph of the same rounds with events at the phase
-    # boundaries gives the phase split; it is replayed separately, because an event
-    # between two kernels also cuts the programmatic launch edge between them.
-    K = args.steps
+    # The timed region: one graph of K rounds (round k: its inputs bound, request
+    # lengths reset, tree pages restored, the seven steps), replayed for at least
+    # --min-time seconds, each replay timed alone; the median replay / K is a step.
+    # A second graph of the same rounds with events at the phase boundaries gives
+    # the phase split; it is replayed separately, because an event between two
+    # kernels also cuts the programmatic launch edge between them.
     phases = ["fuse", "expand", "tree", "verify", "lmhead", "accept", "compact"]
     ev = [[graph_event() for _ in range(len(phases) + 1)] for _ in range(K)]
-    from eagle_speculative_decoding_round_gb300 import eagle3 as e3
     graph = torch.cuda.CUDAGraph()
     counts = []  # library launch counter at each phase boundary of the first captured round
     n0 = e3.launch_count()
     with torch.cuda.graph(graph, stream=s):
         for k in range(K):
-            w.bufs.kv_len.copy_(w.kv_len0)
-            run_round_phased(w, None, e3, counts if k == 0 else None)
+            run_round_phased(w, k, None, e3, counts if k == 0 else None)
     launches_timed = e3.launch_count() - n0  # libeagle3 kernels in the K captured rounds
     phase_launches = {p: counts[i + 1] - counts[i] for i, p in enumerate(phases)}
     graph_phased = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph_phased, stream=s):
         for k in range(K):
-            w.bufs.kv_len.copy_(w.kv_len0)
-            run_round_phased(w, ev[k], e3)
+            run_round_phased(w, k, ev[k], e3)
     torch.cuda.synchronize()
     with torch.cuda.stream(s):
-        graph.replay()  # one untimed replay of the captured work
+        graph.replay()  # untimed replays of the captured work
+        graph.replay()
     torch.cuda.synchronize()
+    t = time.perf_counter()
+    with torch.cuda.stream(s):
+        graph.replay()
+    torch.cuda.synchronize()
+    est = max(time.perf_counter() - t, 1e-4)
+    n_rep = max(3, int(math.ceil(args.min_time / est)))
+    marks = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_rep)]
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(s):
-        t0.record(s)
-        graph.replay()
-        t1.record(s)
-    torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    # keep the GPU busy a little longer so the clock sampler sees load
-    extra = 0
-    while extra < 3 and ms * (extra + 1) < 1500:
-        with torch.cuda.stream(s):
+        for a, z in marks:
+            a.record(s)
             graph.replay()
-        extra += 1
+            z.record(s)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    with torch.cuda.stream(s):
-        graph_phased.replay()  # the phase split (not timed as a whole)
-    torch.cuda.synchronize()
+    rep_ms = [a.elapsed_time(z) for a, z in marks]
     check_dev_err(w, "timed rounds")
-    ms = ranks_max(ms, world)
+    ms = ranks_max(statistics.median(rep_ms), world)
     ms_step = ms / K
-    phase_ms = {p: statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K))
-                for i, p in enumerate(phases)}
+    phase_ms = {p: 0.0 for p in phases}
+    n_ph = 3
+    for _ in range(n_ph):
+        with torch.cuda.stream(s):
+            graph_phased.replay()  # the phase split (not timed as a whole)
+        torch.cuda.synchronize()
+        for i, p in enumerate(phases):
+            phase_ms[p] += statistics.mean(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)) / n_ph
     rounds_s = job_rounds_per_s(ms_step, world)
     nodes_s = rounds_s * cfg.B * cfg.N
 
@@ -531,6 +802,7 @@ def main():
                 "achieved": round(ver_gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(ver_gbs / hbm, 4),
                 "traffic": traffic.get("verify"), "algorithmic_bytes": int(wm["verify_bytes"]),
                 "launches_per_layer": ver_launches / cfg.L, "us_per_layer": round(ver_ms * 1e3, 2),
+                "tensor_frac": round(wm["verify_flops"] / (ver_ms * 1e-3) / 1e12 / tflops, 4),
                 "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({src})"}
     lm_ms = phase_ms["lmhead"]
     lm_gbs = wm["lm_bytes"] / (lm_ms * 1e-3) / 1e9
@@ -549,13 +821,7 @@ def main():
     e2e = None if args.no_e2e else e2e_leg(w, s, K, args.warmup, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        o = oracle_sample(w)
-        cpu = {"value": round(1.0 / o["round_s"], 6), "unit": "rounds/s", "cores": o["cores"], "kind": "oracle",
-               "sample": "one round of the same workload: fusion, expansion, tree build, accept in full; verify "
-                         f"of request 0 on {o['verify_layers']} of the L layers, scaled by L and by the batch's keys; "
-                         f"LM head on 1/4 of the vocabulary scaled by 4 (wall {o['wall_s']:.1f} s)",
-               "seconds_per_round": round(o["round_s"], 3),
-               "breakdown_s": {k: round(v, 3) for k, v in o["times"].items()}}
+        cpu = cpu_baseline(w)
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(rounds_s, 3), "unit": "rounds/s", "n_gpus": world, "steps": K,
@@ -563,11 +829,17 @@ def main():
             "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded; random-init weights)",
             "config": {"workload": w.c["workload"], "global_batch": cfg.B * world, "prefix_lens": summarize(w.c["P"]),
                        "nodes": cfg.N, "depth": cfg.D, "topk": cfg.k, "layers": cfg.L,
+                       "input_sets": len(w.sets), "uniform_sets": len(w.uni),
                        "l2": "inputs larger than L2 per step (L distinct per-layer KV caches + 1 LM head)",
+                       "timed": f"median of {n_rep} graph replays of {K} rounds each ({sum(rep_ms) / 1e3:.2f} s); "
+                                "each round restores its tree pages (K/V of the tree slots) from its input set",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "nodes_per_s": round(nodes_s, 1),
-            "accepted_mean": float(np.mean(accepted)),
+            "accepted_mean": round(float(np.mean(accepted)), 4),
+            "accepted_rounds": int(n_stat),
             "accepted_hist": np.bincount(accepted.astype(np.int64), minlength=cfg.D + 1).tolist(),
+            "replay_ms": {"median": round(statistics.median(rep_ms), 4), "min": round(min(rep_ms), 4),
+                          "max": round(max(rep_ms), 4), "n": n_rep},
             "phase_ms": {k: round(v, 4) for k, v in phase_ms.items()},
             "roofline": roofline,
             "roofline_lmhead": lm,
@@ -595,13 +867,11 @@ def summarize(P):
     return P if len(P) <= 4 else {"n": len(P), "min": min(P), "max": max(P), "mean": float(np.mean(P))}
 
 
-def run_round_phased(w, evs, e3, counts=None):
-    """One round (the same calls as Workload.round, through run_round) with a timing
-    event recorded at each of its 8 phase boundaries (none when ``evs`` is None).
-    With ``counts`` (a list), also append the library's launch counter there."""
+def run_round_phased(w, k, evs, e3, counts=None):
+    """Round k (the same calls as Workload.round) with a timing event recorded at each
+    of its 8 phase boundaries (none when ``evs`` is None).  With ``counts`` (a
+    list), also append the library's launch counter there."""
     import torch
-
-    from eagle_speculative_decoding_round_gb300.round import run_round
     s = torch.cuda.current_stream()
 
     def mark(i):
@@ -610,49 +880,103 @@ def run_round_phased(w, evs, e3, counts=None):
         if counts is not None:
             counts.append(e3.launch_count())
 
-    run_round(w.bufs, stream=s, mark=mark)
+    w.round(k, stream=s, mark=mark)
+
+
+class Slot:
+    """One device copy of everything a round reads that changes per step (e2e)."""
+
+    def __init__(self, w, st):
+        b = w.bufs
+        self.h = [t.clone() for t in b.h]
+        self.drafts = [t.clone() for t in st.drafts]
+        self.Q = [t.clone() for t in st.Q]
+        self.u_acc, self.u_bonus = b.u_acc.clone(), b.u_bonus.clone()
+        self.temp, self.temp_rows = b.temp.clone(), b.temp_rows.clone()
+        self.root_tok, self.kv_len0 = st.root_tok.clone(), w.kv_len0.clone()
+        self.snapK, self.snapV = st.snapK.clone(), st.snapV.clone()
+        self.pages = st.pages
+
+    def tensors(self):
+        return [*self.h, *self.drafts, *self.Q, self.u_acc, self.u_bonus, self.temp, self.temp_rows, self.root_tok,
+                self.kv_len0, self.snapK, self.snapV]
+
+    def bind(self, b):
+        b.h, b.draft_logits, b.Q = self.h, self.drafts, self.Q
+        b.u_acc, b.u_bonus, b.temp, b.temp_rows, b.root_tok = (self.u_acc, self.u_bonus, self.temp, self.temp_rows,
+                                                               self.root_tok)
 
 
 def e2e_leg(w, s, K, warmup, world=1):
-    """Same rounds through the C ABI, from pinned HOST buffers: each step copies the
-    round's inputs host->device (fusion inputs, draft logits, per-layer Q, uniforms,
-    temperatures, root tokens, request lengths), runs the round, and copies the
-    result (emitted tokens, path, accepted length) back."""
+    """The same rounds through the C ABI, fed from pinned HOST buffers: every step
+    copies its round's inputs host -> device (fusion inputs, draft logits, per-layer
+    Q, uniforms, temperatures, root tokens, request lengths, the tree pages of every
+    layer's K/V), runs the round and reads its result (emitted tokens, path,
+    accepted length) back.  Two device slots: step i+1's copies run on a second
+    stream while step i computes (events order each slot's reuse)."""
     import torch
+
+    from eagle_speculative_decoding_round_gb300.round import run_round
     b = w.bufs
-    ins = [*b.h, *b.draft_logits, *b.Q, b.u_acc, b.u_bonus, b.temp, b.temp_rows, b.root_tok, b.kv_len]
+    saved = (b.h, b.draft_logits, b.Q, b.u_acc, b.u_bonus, b.temp, b.temp_rows, b.root_tok)
+    n_host = min(len(w.sets), 4)
+    w.use(0)
+    slots = [Slot(w, w.sets[0]) for _ in range(2)]
+    host_sets = []
+    for i in range(n_host):
+        w.use(i)
+        tmp = Slot(w, w.sets[i])
+        host_sets.append([t.detach().cpu().pin_memory() for t in tmp.tensors()])
+        del tmp
     outs = [b.out_tok, b.path, b.acc_len]
-    h_in = [t.detach().cpu().pin_memory() for t in ins[:-1]] + [w.kv_len0.detach().cpu().pin_memory()]
-    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs]
-    bi = sum(t.numel() * t.element_size() for t in ins)
+    h_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs] for _ in range(2)]
+    bi = sum(t.numel() * t.element_size() for t in slots[0].tensors())
     bo = sum(t.numel() * t.element_size() for t in outs)
-    g1 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g1, stream=s):
-        w.round()
+    graphs = []
+    for sl in slots:
+        sl.bind(b)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            b.kv_len.copy_(sl.kv_len0)
+            b.K_all.index_copy_(1, sl.pages, sl.snapK)
+            b.V_all.index_copy_(1, sl.pages, sl.snapV)
+            run_round(b, stream=s)
+        graphs.append(g)
     torch.cuda.synchronize()
+    cs = torch.cuda.Stream()
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        with torch.cuda.stream(s):
-            for d, h in zip(ins, h_in):
+    def step(i):
+        j = i % 2
+        cs.wait_event(free[j])  # the round that last used slot j has finished
+        with torch.cuda.stream(cs):
+            for d, h in zip(slots[j].tensors(), host_sets[i % n_host]):
                 d.copy_(h, non_blocking=True)
-            g1.replay()
-            for h, d in zip(h_out, outs):
+            loaded[j].record(cs)
+        s.wait_event(loaded[j])
+        with torch.cuda.stream(s):
+            graphs[j].replay()
+            for h, d in zip(h_out[j], outs):
                 h.copy_(d, non_blocking=True)
+            free[j].record(s)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     z = torch.cuda.Event(enable_timing=True)
-    a.record(s)
-    for _ in range(K):
-        step()
+    a.record(cs)
+    for i in range(K):
+        step(i)
     z.record(s)
     torch.cuda.synchronize()
     check_dev_err(w, "e2e")
     ms = ranks_max(a.elapsed_time(z) / K, world)
+    (b.h, b.draft_logits, b.Q, b.u_acc, b.u_bonus, b.temp, b.temp_rows, b.root_tok) = saved
     return {"value": round(job_rounds_per_s(ms, world), 3), "unit": "rounds/s", "h2d_bytes_per_step": bi,
-            "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 4)}
+            "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 4),
+            "overlap": "double-buffered: step i+1's host-to-device copies on a second stream during step i"}
 
 
 def check_dev_err(w, where):
@@ -691,24 +1015,30 @@ def load_peaks():
 
 
 def reference_arm(args, rank, world):
-    """The oracle, as it stands, timed on the host cores: each step is a bounded
-    sample of one round of the same workload (see oracle_sample), scaled to a round."""
+    """The oracle, as it stands, on the host cores: every step is one whole oracle
+    round of the same workload (round k's inputs, all BLAS threads), where a whole
+    round fits; otherwise an estimate from a bounded sample, said so in the line."""
     if rank != 0:
         return 0
-    import torch
-    w = Workload(args.config, seed=args.seed)
-    # each step's sample is sized so that the whole run stays near two minutes
-    budget = max(2.0, 120.0 / (args.steps + 1))
-    for _ in range(max(0, min(args.warmup, 1))):
-        oracle_sample(w, budget)
+    w = Workload(args.config, seed=args.seed, n_sets=min(args.sets, 2), n_uniform=max(args.steps, 1))
+    bt = BlasThreads()
+    cores = bt.threads() or os.cpu_count()
+    whole = whole_round_feasible(w)
     per = []
-    cores = 1
-    layers = 1
-    for _ in range(args.steps):
-        o = oracle_sample(w, budget)
-        per.append(o["round_s"])
-        cores = o["cores"]
-        layers = o["verify_layers"]
+    if whole:
+        for i in range(max(0, min(args.warmup, 1))):
+            oracle_round(w, i)
+        for k in range(args.steps):
+            per.append(sum(oracle_round(w, k).values()))
+        sample = "per step: one whole oracle round (round k's inputs) -- fusion, expansion, tree build, verify on " \
+                 "all L layers, LM head, statistics, accept, compaction"
+    else:
+        budget = max(2.0, 120.0 / (args.steps + 1))
+        for _ in range(args.steps):
+            times, n_layers = oracle_sample(w, budget)
+            per.append(sum(times.values()))
+        sample = "ESTIMATE per step: a bounded sample of one round scaled to a whole round (the whole round " \
+                 "does not fit the run's time at this size)"
     sec = float(np.mean(per))
     v = 1.0 / sec
     line = {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "rounds/s", "n_gpus": world,
@@ -717,8 +1047,7 @@ def reference_arm(args, rank, world):
             "data": "synthetic (seeded; random-init weights)",
             "config": {"workload": w.c["workload"], "global_batch": w.cfg.B},
             "cpu_baseline": {"value": round(v, 6), "unit": "rounds/s", "cores": cores, "kind": "oracle",
-                             "sample": f"per step: one round with verify on {layers} of the L layers (scaled by L) "
-                                       "and LM head on 1/4 of the vocabulary (scaled by 4)"},
+                             "sample": sample, "estimate": not whole},
             "e2e": {"value": round(v, 6), "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0

@@ -27,6 +27,8 @@ void set_error(const char* fmt, ...) {
   va_end(ap);
 }
 
+void clear_error() { g_err[0] = 0; }
+
 e3_status cuda_status(cudaError_t e, const char* what) {
   set_error("%s: %s", what, cudaGetErrorString(e));
   return E3_ERR_CUDA;

@@ -14,7 +14,9 @@
 // code its name is only a host-side stand-in, so its device address is looked up
 // with cudaGetSymbolAddress, once per device, with that device current -- the
 // first call on each device does this lookup, so make that first call before any
-// stream capture.  All calls share the one array: calls that overlap on the GPU
+// stream capture.  (The library as a whole serves one device per process: its
+// kernels' one-time attribute setup is per process; only this lookup is kept per
+// device.)  All calls share the one array: calls that overlap on the GPU
 // (different streams, or several host threads) race on it and must be ordered by
 // the caller.  Each call overwrites every scratch element it later reads, so
 // nothing has to start at zero.
@@ -65,6 +67,7 @@ E3_API size_t eagle3_fuse_noalloc_max_scratch_bytes(void) { return kNoAllocScrat
 E3_API e3_status eagle3_fuse_noalloc(const void* h_low, const void* h_mid, const void* h_high, const void* W_f,
                                      const float* bias, void* g, int M, int d, int d_out, e3_dtype dt,
                                      int32_t* dev_err, e3_stream_t stream) {
+  clear_error();
   E3_REQUIRE(h_low && h_mid && h_high && W_f && g, E3_ERR_INVALID_ARG, "eagle3_fuse_noalloc: null pointer");
   E3_REQUIRE(dt == E3_F32 || dt == E3_BF16, E3_ERR_INVALID_ARG, "eagle3_fuse_noalloc: bad dtype");
   E3_REQUIRE(M >= 1 && M <= 65536 && d >= 1 && d_out >= 1, E3_ERR_SHAPE,

@@ -14,6 +14,8 @@ namespace e3 {
 // host-side error reporting
 // ---------------------------------------------------------------------------
 void set_error(const char* fmt, ...);
+// Empties the calling thread's error message (every entry point starts with it).
+void clear_error();
 e3_status cuda_status(cudaError_t e, const char* what);
 
 #define E3_REQUIRE(cond, code, ...)   \

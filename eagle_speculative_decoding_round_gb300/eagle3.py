@@ -22,7 +22,9 @@ STATUS_NAMES = {0: "E3_OK", 1: "E3_ERR_INVALID_ARG", 2: "E3_ERR_SHAPE", 3: "E3_E
 SYMBOLS = ["eagle3_fuse", "eagle3_fuse_workspace_bytes", "eagle3_fuse_noalloc",
            "eagle3_fuse_noalloc_max_scratch_bytes", "eagle3_expand", "eagle3_expand_sampled", "tree_build_mask",
            "tree_verify_attn", "eagle3_verify_workspace_bytes", "lmhead_logits", "spec_accept",
-           "spec_accept_sampled", "kv_compact", "eagle3_last_error", "eagle3_abi_version", "eagle3_launch_count"]
+           "spec_accept_sampled", "kv_compact", "eagle3_budget_init", "eagle3_budget_update", "eagle3_last_error",
+           "eagle3_abi_version", "eagle3_launch_count"]
+MAX_BUDGET_LEVELS = 16
 
 
 class E3Error(RuntimeError):
@@ -50,6 +52,19 @@ class e3_kv_layer(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("dt", ctypes.c_int)]
 
 
+class e3_budget_policy(ctypes.Structure):
+    _fields_ = [("n_levels", ctypes.c_int), ("nodes", ctypes.c_int * MAX_BUDGET_LEVELS),
+                ("depth", ctypes.c_int * MAX_BUDGET_LEVELS), ("min_level", ctypes.c_int), ("max_level", ctypes.c_int),
+                ("base_level", ctypes.c_int), ("alpha", ctypes.c_float), ("low", ctypes.c_float),
+                ("high", ctypes.c_float), ("spread", ctypes.c_float), ("min_spare", ctypes.c_float),
+                ("max_draft_cost", ctypes.c_float), ("cooldown", ctypes.c_int), ("warmup", ctypes.c_int)]
+
+
+class e3_budget_state(ctypes.Structure):
+    _fields_ = [("level", ctypes.c_int32), ("hold", ctypes.c_int32), ("rounds", ctypes.c_int32),
+                ("mean", ctypes.c_float), ("dev", ctypes.c_float)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libeagle3.so is not built ({LIB_PATH}); run "
@@ -71,6 +86,8 @@ def _load() -> ctypes.CDLL:
         "spec_accept": (I, [P, P, I, I, I, P, P, P, P, I, P, P, P, I, P, P, P, P, P]),
         "spec_accept_sampled": (I, [P, P, P, I, I, I, P, P, P, P, I, P, P, I, P, P, P, P, P, P, P]),
         "kv_compact": (I, [ctypes.POINTER(e3_kv_layer), I, I, P, P, I, P, P, P]),
+        "eagle3_budget_init": (I, [ctypes.POINTER(e3_budget_policy), P, I]),
+        "eagle3_budget_update": (I, [ctypes.POINTER(e3_budget_policy), P, I, P, F, F, P]),
         "eagle3_last_error": (ctypes.c_char_p, []),
         "eagle3_abi_version": (I, []),
         "eagle3_launch_count": (ctypes.c_uint64, []),
@@ -122,6 +139,11 @@ def make_kv_layer(k, v, page_table, n_pages, page_size, max_pages, n_kv_heads, h
 
 def abi_version() -> int:
     return _lib.eagle3_abi_version()
+
+
+def last_error() -> str:
+    """The calling thread's last error message ("" after a call that succeeded)."""
+    return _lib.eagle3_last_error().decode()
 
 
 def launch_count() -> int:
@@ -209,3 +231,35 @@ def kv_compact(layers, B, path, acc_len, D, kv_len, dev_err=None, stream=None):
     arr = (e3_kv_layer * len(layers))(*layers)
     _check("kv_compact", _lib.kv_compact(arr, len(layers), B, ptr(path), ptr(acc_len), D, ptr(kv_len),
                                          ptr(dev_err), _stream(stream)))
+
+
+def budget_policy(levels, min_level=0, max_level=None, base_level=0, alpha=0.5, low=0.25, high=0.75, spread=0.25,
+                  min_spare=0.0, max_draft_cost=1.0, cooldown=2, warmup=2) -> e3_budget_policy:
+    """levels: [(N, D), ...] cheapest first."""
+    p = e3_budget_policy()
+    p.n_levels = len(levels)
+    for i, (n, d) in enumerate(levels):
+        p.nodes[i], p.depth[i] = n, d
+    p.min_level, p.max_level = min_level, len(levels) - 1 if max_level is None else max_level
+    p.base_level, p.alpha, p.low, p.high, p.spread = base_level, alpha, low, high, spread
+    p.min_spare, p.max_draft_cost, p.cooldown, p.warmup = min_spare, max_draft_cost, cooldown, warmup
+    return p
+
+
+def eagle3_budget_init(pol: e3_budget_policy, B: int):
+    """A fresh host state array of B entries at the baseline."""
+    st = (e3_budget_state * B)()
+    _check("eagle3_budget_init", _lib.eagle3_budget_init(ctypes.byref(pol), ctypes.addressof(st), B))
+    return st
+
+
+def eagle3_budget_update(pol: e3_budget_policy, st, acc_len, spare=1.0, draft_cost=0.0):
+    """acc_len: host int sequence of len(st); returns the new levels (list)."""
+    import numpy as np
+    B = len(st)
+    a = np.ascontiguousarray(np.asarray(acc_len, np.int32))
+    out = np.zeros(B, np.int32)
+    _check("eagle3_budget_update", _lib.eagle3_budget_update(ctypes.byref(pol), ctypes.addressof(st), B,
+                                                             a.ctypes.data, float(spare), float(draft_cost),
+                                                             out.ctypes.data))
+    return out.tolist()

@@ -88,8 +88,11 @@ class RoundBuffers:
         self.page_table = page_table.to(dev, torch.int32).contiguous()
         self.n_pages = n_pages
         self.max_pages = self.page_table.shape[1]
-        self.K = [torch.empty((n_pages, c.KVH, c.page_size, c.hd), dtype=td, device=dev) for _ in range(c.L)]
-        self.Vc = [torch.empty((n_pages, c.KVH, c.page_size, c.hd), dtype=td, device=dev) for _ in range(c.L)]
+        # one tensor per operand over all layers; layer l's cache is the view [l]
+        self.K_all = torch.empty((c.L, n_pages, c.KVH, c.page_size, c.hd), dtype=td, device=dev)
+        self.V_all = torch.empty((c.L, n_pages, c.KVH, c.page_size, c.hd), dtype=td, device=dev)
+        self.K = list(self.K_all.unbind(0))
+        self.Vc = list(self.V_all.unbind(0))
         self.kv_len = torch.zeros(c.B, **i32)
         # fusion
         self.h = [torch.empty((c.M, c.d), dtype=td, device=dev) for _ in range(3)]

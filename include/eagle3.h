@@ -44,6 +44,9 @@
  *    setup (kernel attributes, cluster sizes) is thread safe and the error
  *    message is per thread.  Calls share no device state, except the fixed
  *    scratch of eagle3_fuse_noalloc (see there).
+ *  - One device per process: that one-time setup (shared-memory and cluster
+ *    attributes of the kernels, occupancy queries) is done once per process, on
+ *    the device current at the first call.  Use one process per GPU.
  */
 #ifndef EAGLE3_H
 #define EAGLE3_H
@@ -347,6 +350,57 @@ E3_API e3_status spec_accept_sampled(const int32_t* tok, const int32_t* parent,
 E3_API e3_status kv_compact(const e3_kv_layer* layers, int L, int B, const int32_t* path,
                      const int32_t* acc_len, int D, int32_t* kv_len, int32_t* dev_err,
                      e3_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Adaptive draft-tree budget for a serving loop (host code only: no device
+ * memory, no stream, no kernel).
+ * "Thinking Budget 与 EAGLE-3", 服务端应怎样联合控制 (the execution controller):
+ * the speculative budget -- never the target's decoding -- is lowered when the
+ * recent accepted length is low or drafting is costly, raised cautiously when
+ * acceptance is stable and verification has spare capacity, always within
+ * bounds, behind a cool-down window and with a fallback baseline.  The budget is
+ * a ladder of tree shapes, cheapest first ("论文专题讲解：EAGLE-3", Draft tree 配置:
+ * a node budget and a depth).
+ *
+ * Per request (state entry b, all host memory, owned by the caller):
+ *   mean <- mean + alpha (a - mean),  dev <- dev + alpha (|a - mean_old| - dev)
+ * with a = acc_len[b] (drafted tokens accepted in the round just run at the
+ * request's level).  While hold > 0 it counts down and the level stays.  Else,
+ * after `warmup` rounds at the level, with D = depth[level]:
+ *   lower one level (not below min_level) if mean < low D or draft_cost > max_draft_cost;
+ *   raise one level (not above max_level) if mean >= high D, dev <= spread D,
+ *     spare >= min_spare and draft_cost <= max_draft_cost;
+ * a change sets hold = cooldown and restarts the round count.  An observation
+ * outside [0, depth[level]] (a finished or failed request) or a state outside the
+ * bounds resets the entry to the baseline (base_level, mean midway between the
+ * thresholds).  spare: the verify step's free capacity as a fraction in [0, 1]
+ * (the caller's measure, e.g. 1 - verify share of the step budget); draft_cost:
+ * the drafting share of the round time.  level[b] receives the new level.
+ * Errors: E3_ERR_INVALID_ARG / E3_ERR_SHAPE for bad policies or pointers.
+ * ------------------------------------------------------------------------- */
+#define E3_MAX_BUDGET_LEVELS 16
+typedef struct {
+  int n_levels;                        /* ladder length, 1 .. E3_MAX_BUDGET_LEVELS */
+  int nodes[E3_MAX_BUDGET_LEVELS];     /* node budget N of each level (non-decreasing) */
+  int depth[E3_MAX_BUDGET_LEVELS];     /* tree depth D of each level (non-decreasing, <= N) */
+  int min_level, max_level;            /* bounds */
+  int base_level;                      /* fallback baseline, within the bounds */
+  float alpha;                         /* weight of the newest round, (0, 1] */
+  float low, high;                     /* 0 <= low <= high <= 1, fractions of the depth */
+  float spread;                        /* stability bound on dev, fraction of the depth */
+  float min_spare;                     /* spare verify capacity needed to raise */
+  float max_draft_cost;                /* drafting share above which the budget falls */
+  int cooldown;                        /* rounds a new level is held (>= 0) */
+  int warmup;                          /* rounds at a level before it may change (>= 1) */
+} e3_budget_policy;
+typedef struct {
+  int32_t level, hold, rounds;
+  float mean, dev;
+} e3_budget_state;
+E3_API e3_status eagle3_budget_init(const e3_budget_policy* pol, e3_budget_state* st, int B);
+E3_API e3_status eagle3_budget_update(const e3_budget_policy* pol, e3_budget_state* st, int B,
+                                      const int32_t* acc_len, float spare, float draft_cost,
+                                      int32_t* level);
 
 /* Last error message of the calling thread ("" if none). */
 E3_API const char* eagle3_last_error(void);

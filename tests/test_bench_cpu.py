@@ -1,6 +1,6 @@
-"""The benchmark's CPU-baseline leg (the oracle timed on a sample of a round)
-runs end to end on a tiny workload held in CPU tensors, for top-k and for
-sampled drafts (no GPU: the sample only reads the workload's buffers)."""
+"""The benchmark's CPU-baseline leg (the oracle timed over a whole round, or on a
+sample of one) runs end to end on a tiny workload held in CPU tensors, for top-k
+and for sampled drafts (no GPU: the oracle only reads the workload's buffers)."""
 import os
 import sys
 import types
@@ -43,22 +43,57 @@ def fake_workload(sampled: bool):
                 fid, fsc = oracle.expand(z, k, W, fsc, fid, di + 1, off, c)
         tr = oracle.build_tree(c, n_cand, cfg.N, 3, P)
         tok[b], par[b] = tr["tok"], tr["parent"]
+    Kall = t(L, npages, KVH, ps, hd)
+    Vall = t(L, npages, KVH, ps, hd)
+    pages = torch.tensor(sorted({int(pt[b, q]) for b in range(B) for q in range(P // ps, (P + R - 1) // ps + 1)}))
     bufs = types.SimpleNamespace(
-        h=[t(cfg.M, cfg.d) for _ in range(3)], W_f=t(cfg.d, 3 * cfg.d), draft_logits=drafts,
-        root_tok=torch.full((B,), 3, dtype=torch.int32), K=[t(npages, KVH, ps, hd) for _ in range(L)],
-        Vc=[t(npages, KVH, ps, hd) for _ in range(L)], Q=[t(B, R, H, hd) for _ in range(L)],
+        h=[t(cfg.M, cfg.d) for _ in range(3)], W_f=t(cfg.d, 3 * cfg.d), K_all=Kall, V_all=Vall,
         O=[t(B, R, H, hd) for _ in range(L)], W_lm=t(V, H * hd), logits=t(B * R, V),
-        tok=torch.from_numpy(tok), parent=torch.from_numpy(par),
-        u_acc=torch.from_numpy(synth.uniforms(1, synth.PURPOSE_ACCEPT, B, R).view(np.int32)),
-        u_bonus=torch.from_numpy(synth.uniforms(1, synth.PURPOSE_BONUS, B, R).view(np.int32)))
-    w = types.SimpleNamespace(bufs=bufs, cfg=cfg, c={"P": [P] * B, "temps": [1.0]}, pt=pt,
-                              kv_len0=torch.full((B,), P, dtype=torch.int32))
+        tok=torch.from_numpy(tok), parent=torch.from_numpy(par), temp=torch.ones(B))
+    st = bench.InputSet(drafts, [t(B, R, H, hd) for _ in range(L)], torch.full((B,), 3, dtype=torch.int32))
+    st.pages, st.snapK, st.snapV = pages, Kall.index_select(1, pages), Vall.index_select(1, pages)
+    uni = [(torch.from_numpy(synth.uniforms(1, synth.PURPOSE_ACCEPT, B, R).view(np.int32)),
+            torch.from_numpy(synth.uniforms(1, synth.PURPOSE_BONUS, B, R).view(np.int32)))]
+
+    class W:
+        pass
+    w = W()
+    w.bufs, w.cfg, w.c, w.pt, w.sets, w.uni = bufs, cfg, {"P": [P] * B, "temps": [1.0]}, pt, [st], uni
+    w.kv_len0 = torch.full((B,), P, dtype=torch.int32)
+
+    def use(k):
+        s_ = w.sets[k % len(w.sets)]
+        bufs.draft_logits, bufs.Q, bufs.root_tok = s_.drafts, s_.Q, s_.root_tok
+        bufs.u_acc, bufs.u_bonus = w.uni[k % len(w.uni)]
+    w.use = use
     return bench, w
 
 
 @pytest.mark.parametrize("sampled", [False, True])
 def test_oracle_sample_runs_on_a_tiny_workload(sampled):
     bench, w = fake_workload(sampled)
-    o = bench.oracle_sample(w, budget_s=0.5)
-    assert o["round_s"] > 0 and o["verify_layers"] >= 1 and o["cores"] >= 1
-    assert set(o["times"]) == {"fuse", "expand_build", "verify", "lmhead", "accept"}
+    times, n_layers = bench.oracle_sample(w, budget_s=0.5)
+    assert n_layers >= 1 and all(v >= 0 for v in times.values())
+    assert set(times) == {"fuse", "expand_build", "verify", "lmhead", "accept"}
+
+
+@pytest.mark.parametrize("sampled", [False, True])
+def test_oracle_whole_round_runs_on_a_tiny_workload(sampled):
+    bench, w = fake_workload(sampled)
+    times = bench.oracle_round(w, 0)
+    assert set(times) == {"fuse", "expand_build", "verify", "lmhead", "accept", "compact"}
+    assert all(v >= 0 for v in times.values())
+    assert bench.whole_round_feasible(w)
+    out = bench.cpu_baseline(w, budget_s=60.0)
+    assert out["value"] > 0 and out["kind"] == "oracle" and out["threads_all"]["threads"] >= 1
+    assert "estimate" not in out
+
+
+def test_blas_thread_control_round_trips():
+    import bench
+    bt = BlasThreads = bench.BlasThreads()
+    n = bt.threads()
+    if n is None:
+        pytest.skip("numpy's BLAS exports no thread setter here")
+    assert BlasThreads.use(1) == 1
+    assert bt.use(n) == n

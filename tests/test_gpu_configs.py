@@ -1,15 +1,20 @@
 """Every benchmarked configuration, one whole round on the GPU in the benchmark's
 own launch configuration (its workload, buffers and round function), checked
-against the oracle:
+against the oracle.  The round's inputs are built without the library under test
+(tests/oracle_workload.py: draft logits = the oracle's fp64 target logits of each
+frontier node + seeded noise; trees from the oracle's expansion):
 
-  fusion        sampled output features, within the dtype tolerance
+  fusion        every output element, within the dtype tolerance
   expansion     every candidate of every request and depth, bit-exact (drawn
                 children for the sampled configurations)
   tree          tokens, parents, depths, positions and mask rows, bit-exact
-  verify        sampled (request, node, head) rows of the first and last layer,
-                within the dtype tolerance (the oracle runs those rows only)
-  LM head       sampled rows on sampled vocabulary columns within tolerance; the
-                softmax statistics of every row bit-exact from the GPU logits
+  verify        the whole O and lse tensors of the last layer (every request,
+                node and head; the 65536-key prefix and the 70B batch included)
+                against the oracle's dense masked form, and sampled rows of the
+                first layer, within the dtype tolerance (norm-wise over the tensor)
+  LM head       whole vocabulary rows (every row up to 64, else 64 sampled rows)
+                within tolerance; the softmax statistics of every row bit-exact
+                from the GPU logits
   accept        accepted length, path and emitted tokens, bit-exact (the
                 min(1, p/q) rule for the sampled configurations)
   compaction    slots P + j of sampled layers hold what slot P + path[j] held
@@ -24,10 +29,10 @@ import torch
 
 import oracle
 from gpu_util import assert_close
+from oracle_workload import oracle_workload
 
 ROOT = os.path.abspath(os.path.join(os.path.dirname(__file__), ".."))
 sys.path.insert(0, ROOT)
-import bench  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -43,7 +48,7 @@ def f32(t):
 @pytest.mark.parametrize("name", ["tiny", "8b", "8b_d8", "8b_chain3", "8b_sampled", "8b_chain3_sampled", "batched",
                                   "long", "70b"])
 def test_round_matches_oracle(name):
-    w = bench.Workload(name, seed=11)
+    w = oracle_workload(name, seed=11)
     b, c = w.bufs, w.cfg
     B, R, L = c.B, c.R, c.L
     rng = np.random.default_rng(7)
@@ -62,10 +67,8 @@ def test_round_matches_oracle(name):
     torch.cuda.synchronize()
     assert int(b.dev_err.item()) == 0
 
-    # fusion: 64 sampled output features of every token row
-    cols = rng.choice(c.d, 64, replace=False)
-    Wf_rows = f32(b.W_f[torch.from_numpy(cols).cuda()])
-    assert_close(f32(b.g)[:, cols], oracle.fuse(hs[0], hs[1], hs[2], Wf_rows), tol, "fusion")
+    # fusion: every output element
+    assert_close(f32(b.g), oracle.fuse(hs[0], hs[1], hs[2], f32(b.W_f)), tol, "fusion")
 
     # expansion and tree, per request
     sizes, n_cand = c.frontier_sizes()
@@ -97,22 +100,23 @@ def test_round_matches_oracle(name):
             assert np.array_equal(host(b.node_cand)[bb], tree["node_cand"]), (name, bb)
         assert np.array_equal(mask[bb].view(np.uint64), tree["mask"]), (name, bb)
 
-    # verify: sampled rows of the first and the last layer
+    # verify: the whole last layer (dense masked form), sampled rows of the first
     sm = 1.0 / math.sqrt(c.hd)
-    for l in layers:
+    Oref, lref = oracle.tree_verify_attn_dense(Qs[L - 1], Kpre[L - 1], Vpre[L - 1], w.pt, P, mask.view(np.uint64), sm)
+    assert_close(f32(b.O[L - 1]), Oref, tol, f"O layer {L - 1} (whole tensor)")
+    assert_close(host(b.lse[L - 1]), lref, tol, f"lse layer {L - 1} (whole tensor)")
+    if L > 1:
         rows = [(int(rng.integers(B)), int(rng.integers(R)), int(rng.integers(c.H))) for _ in range(12)]
-        Oref, lref = oracle.tree_verify_attn_rows(Qs[l], Kpre[l], Vpre[l], w.pt, P, par, sm, rows)
-        Og, lg = f32(b.O[l]), host(b.lse[l])
-        assert_close(np.stack([Og[bb, i, h] for bb, i, h in rows]), Oref, tol, f"O layer {l}")
-        assert_close(np.array([lg[bb, i, h] for bb, i, h in rows]), lref, tol, f"lse layer {l}")
+        Orow, lrow = oracle.tree_verify_attn_rows(Qs[0], Kpre[0], Vpre[0], w.pt, P, par, sm, rows)
+        Og, lg = f32(b.O[0]), host(b.lse[0])
+        assert_close(np.stack([Og[bb, i, h] for bb, i, h in rows]), Orow, tol, "O layer 0")
+        assert_close(np.array([lg[bb, i, h] for bb, i, h in rows]), lrow, tol, "lse layer 0")
 
-    # LM head: sampled rows x sampled vocabulary columns; statistics of every row
+    # LM head: whole vocabulary rows; statistics of every row
     z = host(b.logits)
     hrow = f32(b.O[L - 1]).reshape(B * R, c.H * c.hd)
-    sel = rng.choice(B * R, min(4, B * R), replace=False)
-    vcols = rng.choice(c.V, min(2048, c.V), replace=False)
-    Wl = f32(b.W_lm[torch.from_numpy(vcols).cuda()])
-    assert_close(z[sel][:, vcols], oracle.lmhead_logits(hrow[sel], Wl), tol, "logits")
+    sel = np.arange(B * R) if B * R <= 64 else np.sort(rng.choice(B * R, 64, replace=False))
+    assert_close(z[sel], oracle.lmhead_logits(hrow[sel], f32(b.W_lm)), tol, "logits")
     m, Q, am, bad = oracle.row_stats(z, host(b.temp_rows))
     assert not bad.any()
     assert np.array_equal(host(b.row_max).view(np.uint32), m.view(np.uint32))
