@@ -47,6 +47,7 @@ static e3_status check_kv_layer(const e3_kv_layer* kv, const char* fn) {
   E3_REQUIRE(kv->head_dim >= 32 && kv->head_dim <= 256 && kv->head_dim % 32 == 0, E3_ERR_SHAPE,
              "%s: head_dim %d must be a multiple of 32 in [32, 256]", fn, kv->head_dim);
   E3_REQUIRE(aligned16(kv->k) && aligned16(kv->v), E3_ERR_INVALID_ARG, "%s: k/v not 16-byte aligned", fn);
+  E3_REQUIRE((kv->flags & ~E3_KV_PREFIX_STABLE) == 0, E3_ERR_INVALID_ARG, "%s: unknown kv flags %#x", fn, kv->flags);
   return E3_OK;
 }
 
@@ -58,7 +59,7 @@ extern "C" {
 
 E3_API const char* eagle3_last_error(void) { return g_err; }
 
-E3_API int eagle3_abi_version(void) { return 2; }
+E3_API int eagle3_abi_version(void) { return 3; }
 
 E3_API uint64_t eagle3_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 

@@ -48,6 +48,12 @@ e3_status launch_row_stats(const float* logits, int M, int V, const float* temp,
                            uint64_t* row_Q, int32_t* row_argmax, int32_t* dev_err, cudaStream_t s);
 
 bool tc_gemm_supported(int d_k, int n_rows);
+// Split-K partial sums part[z][m][n] (fp32, z < *splits) of out[m][n] = W[n] . [src_0[m]; ..;
+// src_{n_src-1}[m]] with W [N][n_src*K] and src_i [M][K] bf16 (K % 64 == 0), on the tensor cores.
+int linear_splits(int M, int K_total, int N);
+size_t linear_partial_bytes(int M, int K_total, int N);
+e3_status launch_linear_tc(const void* W, const void* const* src, int n_src, int K, int M, int N, float* part,
+                           int* splits, int32_t* dev_err, cudaStream_t s);
 size_t tc_fuse_workspace_bytes(int M, int d, int d_out);
 e3_status launch_fuse_tc(const void* h_low, const void* h_mid, const void* h_high, const void* W_f, const float* bias,
                          void* g, int M, int d, int d_out, void* ws, size_t ws_bytes, int32_t* dev_err,

@@ -589,9 +589,11 @@ int pick_bn(int Mx) {
   return 256;
 }
 
-int fuse_splits(int M, int d, int d_out) {
-  const int tiles = ((M + pick_bn(M) - 1) / pick_bn(M)) * ((d_out + BM - 1) / BM);
-  const int kb_total = 3 * d / BK;
+// Splits of the K loop: about two CTAs per SM over the (token tile, weight tile) grid,
+// at least four k-blocks per split, at most 16 splits, none empty.
+int linear_splits_impl(int M, int K_total, int N) {
+  const int tiles = ((M + pick_bn(M) - 1) / pick_bn(M)) * ((N + BM - 1) / BM);
+  const int kb_total = K_total / BK;
   int splits = (2 * 148 + tiles - 1) / tiles;  // about two CTAs per SM
   if (splits > kb_total / 4) splits = kb_total / 4;
   if (splits < 1) splits = 1;
@@ -600,7 +602,29 @@ int fuse_splits(int M, int d, int d_out) {
   return (kb_total + per - 1) / per;  // every split owns at least one k-block
 }
 
+int fuse_splits(int M, int d, int d_out) { return linear_splits_impl(M, 3 * d, d_out); }
+
 }  // namespace
+
+int linear_splits(int M, int K_total, int N) { return linear_splits_impl(M, K_total, N); }
+
+size_t linear_partial_bytes(int M, int K_total, int N) {
+  return static_cast<size_t>(linear_splits_impl(M, K_total, N)) * M * N * sizeof(float);
+}
+
+e3_status launch_linear_tc(const void* W, const void* const* src, int n_src, int K, int M, int N, float* part,
+                           int* splits, int32_t* dev_err, cudaStream_t s) {
+  E3_REQUIRE(n_src >= 1 && n_src <= 3 && K % BK == 0 && K >= BK && M >= 1 && N >= 1, E3_ERR_SHAPE,
+             "linear: n_src=%d K=%d M=%d N=%d", n_src, K, M, N);
+  const int bn = pick_bn(M);
+  CUtensorMap a, b[3];
+  bool ok = make_map(&a, W, N, n_src * K, BM);
+  for (int i = 0; i < n_src; ++i) ok = ok && make_map(&b[i], src[i], M, K, bn);
+  E3_REQUIRE(ok, E3_ERR_INVALID_ARG, "linear: cuTensorMapEncodeTiled rejected an operand");
+  for (int i = n_src; i < 3; ++i) b[i] = b[0];
+  *splits = linear_splits_impl(M, n_src * K, N);
+  return dispatch_fuse(bn, a, b[0], b[1], b[2], N, M, K / BK, n_src * K / BK, *splits, part, dev_err, s);
+}
 
 bool tc_gemm_supported(int d_k, int n_rows) { return d_k % BK == 0 && n_rows >= 1; }
 

@@ -301,6 +301,7 @@ __device__ __forceinline__ uint32_t mask_bits32(const uint64_t* row, int words, 
 
 struct TcGeom {
   int B, R, H, KVH, G, n_pre, S, chunk, RG, max_kv_len;
+  int prefix_stable;  // E3_KV_PREFIX_STABLE: prefix K/V, lengths and pages may be read before the wait
   int fold_tree;  // 1: segment S-1 also processes the tree slots (no separate tree segment)
   int page_size, max_pages, n_pages;
   const int32_t* page_table;
@@ -381,9 +382,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   // Launched as a programmatic dependent: everything above touches only this CTA's
-  // shared and tensor memory; nothing in global memory is read or written before
-  // the preceding kernel has completed.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // shared and tensor memory.  Without the prefix-stable promise nothing in global
+  // memory is read before the preceding kernel has completed.  With it (the prefix
+  // K/V, kv_len and the page table are not written by that kernel), the request
+  // lengths and page-table rows are read and the first prefix tiles' K/V loads are
+  // issued before the wait; Q, the mask and the tree slots only after it, and
+  // nothing is written to global memory before it.
+  if (!g.prefix_stable) asm volatile("griddepcontrol.wait;" ::: "memory");
+  auto issue_q = [&](int bq) {
+    bar_expect(q_full, kQBytes);
+    for (int h = 0; h < 2; ++h) tma3d(sQ + h * (kQBytes / 2), &tmQ, h * kHalf, kvh * g.G, bq * g.R + i0, q_full);
+  };
   // Requests are taken in order of decreasing length (ties: lower index first): the
   // CTAs of blockIdx.z = j serve the request of rank j, so that the longest requests
   // are launched first and the short ones fill the last wave.
@@ -403,10 +412,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     __syncthreads();
     b = s_req;
   }
-  if (threadIdx.x == 0) {
-    bar_expect(q_full, kQBytes);
-    for (int h = 0; h < 2; ++h) tma3d(sQ + h * (kQBytes / 2), &tmQ, h * kHalf, kvh * g.G, b * g.R + i0, q_full);
-  }
+  if (!g.prefix_stable && threadIdx.x == 0) issue_q(b);  // Q may be read now: it overlaps the length reads
   // Warp 0 loads, together with the request's length, the page-table entries of
   // this segment's first prefix blocks as they are if the prefix covers the whole
   // segment; after the length is known they are kept where that guess holds.
@@ -422,9 +428,10 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   const int P = kv_len[b];
   const long need = static_cast<long>(P) + g.R;
   if (P < 0 || P > g.max_kv_len || need > static_cast<long>(g.max_pages) * g.page_size) {
+    if (g.prefix_stable) asm volatile("griddepcontrol.wait;" ::: "memory");
     if (threadIdx.x == 0) {
       if (blockIdx.x == 0 && kvh == 0) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
-      bar_wait_timed(q_full, 0);  // the Q load lands before the CTA leaves
+      if (!g.prefix_stable) bar_wait_timed(q_full, 0);  // the Q load lands before the CTA leaves
     }
     // the tensor memory allocated above is released (uniform across the CTA: same request)
     fence_before();
@@ -503,13 +510,27 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       for (int h = 0; h < 2; ++h) tma2d(base + h * (kKVBytes / 2) + blk * kBox, map, h * kHalf, row, bar);
     }
   };
-  if (threadIdx.x == 0 && ntile > 0) {  // the first two tiles' K and V
-    bool okp = true;
-    for (int t = 0; t < ntile && t < 2; ++t) {
-      issue_kv(t, 0, &okp);
-      issue_kv(t, 1, &okp);
+  // The first two tiles' K and V.  Under the prefix-stable promise the prefix
+  // tiles (t < ntA) are requested before the wait: their slots hold the committed
+  // prefix (slots of the tree, which the preceding kernel may be writing, can share
+  // a 64-key block with the prefix's last keys; they are outside [pk0, pk1), so
+  // their scores are never used and their V rows are zeroed below).
+  const int n_first = min(ntile, 2);
+  const int n_early = g.prefix_stable ? min(n_first, ntA) : 0;
+  bool okp0 = true;
+  if (threadIdx.x == 0)
+    for (int t = 0; t < n_early; ++t) {
+      issue_kv(t, 0, &okp0);
+      issue_kv(t, 1, &okp0);
     }
-    if (!okp) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
+  if (g.prefix_stable) asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) {
+    if (g.prefix_stable) issue_q(b);
+    for (int t = n_early; t < n_first; ++t) {
+      issue_kv(t, 0, &okp0);
+      issue_kv(t, 1, &okp0);
+    }
+    if (!okp0) dev_flag(dev_err, E3_DEV_ERR_CAPACITY);
   }
   fence_before();
   __syncthreads();
@@ -1005,6 +1026,7 @@ e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* 
   g.n_pages = kv.n_pages;
   g.page_table = kv.page_table;
   g.fold_tree = 0;
+  g.prefix_stable = (kv.flags & E3_KV_PREFIX_STABLE) ? 1 : 0;
   static std::atomic<bool> attr_done{false};
   if (!attr_done.load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);

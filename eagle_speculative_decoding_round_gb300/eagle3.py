@@ -17,6 +17,7 @@ E3_OK = 0
 E3_F32, E3_BF16 = 0, 1
 E3_DEV_ERR_NONFINITE, E3_DEV_ERR_CAPACITY, E3_DEV_ERR_TIMEOUT = 1, 2, 4
 E3_ACCEPT_TREE_DET, E3_ACCEPT_SAMPLED = 0, 1
+E3_KV_PREFIX_STABLE = 1
 STATUS_NAMES = {0: "E3_OK", 1: "E3_ERR_INVALID_ARG", 2: "E3_ERR_SHAPE", 3: "E3_ERR_UNSUPPORTED",
                 4: "E3_ERR_CAPACITY", 5: "E3_ERR_NONFINITE", 6: "E3_ERR_CUDA", 7: "E3_ERR_TIMEOUT"}
 SYMBOLS = ["eagle3_fuse", "eagle3_fuse_workspace_bytes", "eagle3_fuse_noalloc",
@@ -49,7 +50,8 @@ QSTAT_BYTES = ctypes.sizeof(e3_qstat)  # bytes of one e3_qstat (24)
 class e3_kv_layer(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("page_table", ctypes.c_void_p),
                 ("n_pages", ctypes.c_int), ("page_size", ctypes.c_int), ("max_pages", ctypes.c_int),
-                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("dt", ctypes.c_int)]
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("dt", ctypes.c_int),
+                ("flags", ctypes.c_int)]
 
 
 class e3_budget_policy(ctypes.Structure):
@@ -133,8 +135,9 @@ def make_cand(tok, parent, score, depth, cap: int) -> e3_cand:
     return e3_cand(ptr(tok), ptr(parent), ptr(score), ptr(depth), cap)
 
 
-def make_kv_layer(k, v, page_table, n_pages, page_size, max_pages, n_kv_heads, head_dim, dt) -> e3_kv_layer:
-    return e3_kv_layer(ptr(k), ptr(v), ptr(page_table), n_pages, page_size, max_pages, n_kv_heads, head_dim, dt)
+def make_kv_layer(k, v, page_table, n_pages, page_size, max_pages, n_kv_heads, head_dim, dt, flags=0) -> e3_kv_layer:
+    return e3_kv_layer(ptr(k), ptr(v), ptr(page_table), n_pages, page_size, max_pages, n_kv_heads, head_dim, dt,
+                       flags)
 
 
 def abi_version() -> int:

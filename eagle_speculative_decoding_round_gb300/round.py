@@ -79,7 +79,8 @@ class RoundBuffers:
     """Device buffers for one configuration.  KV caches hold every request's pages
     (prefix + room for the R tree slots) for L layers."""
 
-    def __init__(self, cfg: RoundConfig, page_table: torch.Tensor, n_pages: int, device="cuda"):
+    def __init__(self, cfg: RoundConfig, page_table: torch.Tensor, n_pages: int, device="cuda", kv_cache=None,
+                 W_lm=None):
         c = cfg
         dev = torch.device(device)
         self.cfg = c
@@ -89,8 +90,12 @@ class RoundBuffers:
         self.n_pages = n_pages
         self.max_pages = self.page_table.shape[1]
         # one tensor per operand over all layers; layer l's cache is the view [l]
-        self.K_all = torch.empty((c.L, n_pages, c.KVH, c.page_size, c.hd), dtype=td, device=dev)
-        self.V_all = torch.empty((c.L, n_pages, c.KVH, c.page_size, c.hd), dtype=td, device=dev)
+        # (kv_cache: caches shared with other buffers, e.g. one per tree budget of a serving loop)
+        if kv_cache is not None:
+            self.K_all, self.V_all = kv_cache
+        else:
+            self.K_all = torch.empty((c.L, n_pages, c.KVH, c.page_size, c.hd), dtype=td, device=dev)
+            self.V_all = torch.empty((c.L, n_pages, c.KVH, c.page_size, c.hd), dtype=td, device=dev)
         self.K = list(self.K_all.unbind(0))
         self.Vc = list(self.V_all.unbind(0))
         self.kv_len = torch.zeros(c.B, **i32)
@@ -133,10 +138,12 @@ class RoundBuffers:
         self.lse = [torch.empty((c.B, R, c.H), dtype=torch.float32, device=dev) for _ in range(c.L)]
         self.ws_bytes = e3.eagle3_verify_workspace_bytes(c.B, R, c.H, c.KVH, c.hd, c.max_kv_len, c.dt)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        # the round's verify calls follow tree_build_mask or the previous layer's verify,
+        # neither of which writes the prefix K/V, kv_len or the page table
         self.kv = [e3.make_kv_layer(self.K[l], self.Vc[l], self.page_table, n_pages, c.page_size,
-                                    self.max_pages, c.KVH, c.hd, c.dt) for l in range(c.L)]
+                                    self.max_pages, c.KVH, c.hd, c.dt, e3.E3_KV_PREFIX_STABLE) for l in range(c.L)]
         # logits / accept
-        self.W_lm = torch.empty((c.V, c.H * c.hd), dtype=td, device=dev)
+        self.W_lm = torch.empty((c.V, c.H * c.hd), dtype=td, device=dev) if W_lm is None else W_lm
         self.temp = torch.ones(c.B, dtype=torch.float32, device=dev)
         self.temp_rows = torch.ones(c.B * R, dtype=torch.float32, device=dev)
         self.logits = torch.empty((c.B * R, c.V), dtype=torch.float32, device=dev)
@@ -156,63 +163,74 @@ class RoundBuffers:
         self.temp_rows.copy_(self.temp.repeat_interleave(self.cfg.R))
 
 
-def expand_depth(bufs: RoundBuffers, di: int, stream=None):
-    """Depth di + 1 of the draft tree: expand the frontier rows of bufs.draft_logits[di]."""
+def expand_depth(bufs: RoundBuffers, di: int, stream=None, B=None):
+    """Depth di + 1 of the draft tree: expand the frontier rows of bufs.draft_logits[di]
+    (of the first B requests; all by default)."""
     c = bufs.cfg
+    B = c.B if B is None else B
     F, off = c.frontier_sizes()[0][di]
     if c.sampled:
-        e3.eagle3_expand_sampled(bufs.draft_logits[di], c.B, F, c.V, c.k, c.W, 1.0, bufs.f_score[di], bufs.f_id[di],
+        e3.eagle3_expand_sampled(bufs.draft_logits[di], B, F, c.V, c.k, c.W, 1.0, bufs.f_score[di], bufs.f_id[di],
                                  di + 1, off, bufs.cand, bufs.f_id[di + 1], bufs.f_score[di + 1], c.draw_seed,
                                  bufs.q_stats, bufs.dev_err, stream=stream)
     else:
-        e3.eagle3_expand(bufs.draft_logits[di], c.B, F, c.V, c.k, c.W, 1.0, bufs.f_score[di], bufs.f_id[di],
+        e3.eagle3_expand(bufs.draft_logits[di], B, F, c.V, c.k, c.W, 1.0, bufs.f_score[di], bufs.f_id[di],
                          di + 1, off, bufs.cand, bufs.f_id[di + 1], bufs.f_score[di + 1], bufs.dev_err, stream=stream)
 
 
-def build_tree(bufs: RoundBuffers, stream=None):
+def build_tree(bufs: RoundBuffers, stream=None, B=None):
     c = bufs.cfg
-    e3.tree_build_mask(bufs.cand, c.B, c.n_cand, c.N, bufs.root_tok, bufs.kv_len, bufs.tok, bufs.parent,
+    B = c.B if B is None else B
+    e3.tree_build_mask(bufs.cand, B, c.n_cand, c.N, bufs.root_tok, bufs.kv_len, bufs.tok, bufs.parent,
                        bufs.depth, bufs.pos, bufs.mask, node_cand=bufs.node_cand if c.sampled else None,
                        stream=stream)
 
 
-def run_round(bufs: RoundBuffers, stream=None, write_tree_qkv=None, sm_scale=None, mark=None):
-    """Enqueue one round.  ``write_tree_qkv(bufs)`` (optional) is called after
-    tree_build_mask to write the tree nodes' Q (all layers) and K/V (slots
-    kv_len .. kv_len+R-1); without it the caller has written them beforehand.
-    ``mark(i)`` (optional) is called at the phase boundaries i = 0..7 (before
-    fusion, after fusion, expansion, tree, verify, LM head, accept, compaction)."""
+def run_round(bufs: RoundBuffers, stream=None, write_tree_qkv=None, sm_scale=None, mark=None, B=None, draft=None):
+    """Enqueue one round for the first B requests of the buffers (all by default).
+    ``draft(bufs, di)`` (optional) is called before the expansion of depth di + 1
+    to write that depth's draft logits (the frontier of the previous depth is in
+    bufs.f_id[di]); without it the caller has written every depth's beforehand.
+    ``write_tree_qkv(bufs)`` (optional) is called after tree_build_mask to write
+    the tree nodes' Q (all layers) and K/V (slots kv_len .. kv_len+R-1); without
+    it the caller has written them beforehand.  ``mark(i)`` (optional) is called
+    at the phase boundaries i = 0..7 (before fusion, after fusion, expansion,
+    tree, verify, LM head, accept, compaction)."""
     c = bufs.cfg
+    B = c.B if B is None else B
     R = c.R
     s = stream
     mark = mark or (lambda i: None)
     sm_scale = sm_scale if sm_scale is not None else 1.0 / math.sqrt(c.hd)
     mark(0)
-    e3.eagle3_fuse(bufs.h[0], bufs.h[1], bufs.h[2], bufs.W_f, None, bufs.g, c.M, c.d, c.d, c.dt,
+    M = B * (c.M // c.B)
+    e3.eagle3_fuse(bufs.h[0], bufs.h[1], bufs.h[2], bufs.W_f, None, bufs.g, M, c.d, c.d, c.dt,
                    bufs.fuse_ws, bufs.fuse_ws_bytes, bufs.dev_err, stream=s)
     mark(1)
     for di in range(c.D):
-        expand_depth(bufs, di, stream=s)
+        if draft is not None:
+            draft(bufs, di)
+        expand_depth(bufs, di, stream=s, B=B)
     mark(2)
-    build_tree(bufs, stream=s)
+    build_tree(bufs, stream=s, B=B)
     mark(3)
     if write_tree_qkv is not None:
         write_tree_qkv(bufs)
     for l in range(c.L):
-        e3.tree_verify_attn(bufs.Q[l], bufs.kv[l], bufs.kv_len, bufs.mask, c.B, R, c.H, c.max_kv_len, sm_scale,
+        e3.tree_verify_attn(bufs.Q[l], bufs.kv[l], bufs.kv_len, bufs.mask, B, R, c.H, c.max_kv_len, sm_scale,
                             bufs.O[l], bufs.lse[l], bufs.dev_err, bufs.ws, bufs.ws_bytes, stream=s)
     mark(4)
-    e3.lmhead_logits(bufs.O[c.L - 1], bufs.W_lm, c.B * R, c.H * c.hd, c.V, bufs.temp_rows, bufs.logits,
+    e3.lmhead_logits(bufs.O[c.L - 1], bufs.W_lm, B * R, c.H * c.hd, c.V, bufs.temp_rows, bufs.logits,
                      bufs.row_max, bufs.row_Q, bufs.row_argmax, bufs.dev_err, c.dt, stream=s)
     mark(5)
     if c.sampled:
-        e3.spec_accept_sampled(bufs.tok, bufs.parent, bufs.node_cand, c.B, R, c.D, bufs.logits, bufs.row_max,
+        e3.spec_accept_sampled(bufs.tok, bufs.parent, bufs.node_cand, B, R, c.D, bufs.logits, bufs.row_max,
                                bufs.row_Q, bufs.row_argmax, c.V, bufs.temp, bufs.q_stats, bufs.cap + 1, bufs.u_acc,
                                bufs.u_bonus, bufs.acc_len, bufs.path, bufs.out_tok, bufs.status, stream=s)
     else:
-        e3.spec_accept(bufs.tok, bufs.parent, c.B, R, c.D, bufs.logits, bufs.row_max, bufs.row_Q, bufs.row_argmax,
+        e3.spec_accept(bufs.tok, bufs.parent, B, R, c.D, bufs.logits, bufs.row_max, bufs.row_Q, bufs.row_argmax,
                        c.V, bufs.temp, bufs.u_acc, bufs.u_bonus, e3.E3_ACCEPT_TREE_DET, bufs.acc_len, bufs.path,
                        bufs.out_tok, bufs.status, stream=s)
     mark(6)
-    e3.kv_compact(bufs.kv, c.B, bufs.path, bufs.acc_len, c.D, bufs.kv_len, bufs.dev_err, stream=s)
+    e3.kv_compact(bufs.kv, B, bufs.path, bufs.acc_len, c.D, bufs.kv_len, bufs.dev_err, stream=s)
     mark(7)

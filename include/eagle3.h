@@ -116,7 +116,18 @@ typedef struct {
 
 /* One layer's paged KV cache.  k and v: [n_pages][n_kv_heads][page_size][head_dim]
  * of dtype dt (device).  Logical token t of request b is slot t % page_size of
- * page page_table[b*max_pages + t / page_size]. */
+ * page page_table[b*max_pages + t / page_size].
+ * flags: 0, or E3_KV_PREFIX_STABLE -- a promise about ordering that lets
+ * tree_verify_attn start earlier: the prefix K/V (slots below kv_len[b]),
+ * kv_len and the page table are NOT written by the kernel enqueued immediately
+ * before the tree_verify_attn call on its stream (in a decoder the preceding
+ * kernel is the previous layer's attention or this layer's QKV projection,
+ * which write neither; kv_compact and page allocation happen earlier).  The
+ * kernel then reads the lengths and page table and starts loading prefix K/V
+ * while that preceding kernel is still finishing; Q, the mask and the tree
+ * slots are read only after it has completed.  Breaking the promise can make
+ * the call read stale prefix data.  Other calls ignore the flag. */
+#define E3_KV_PREFIX_STABLE 1
 typedef struct {
   void* k;
   void* v;
@@ -127,6 +138,7 @@ typedef struct {
   int n_kv_heads;
   int head_dim;
   e3_dtype dt;
+  int flags;                 /* 0 or E3_KV_PREFIX_STABLE */
 } e3_kv_layer;
 
 /* ---------------------------------------------------------------------------
@@ -405,7 +417,8 @@ E3_API e3_status eagle3_budget_update(const e3_budget_policy* pol, e3_budget_sta
 /* Last error message of the calling thread ("" if none). */
 E3_API const char* eagle3_last_error(void);
 
-/* ABI version: 2 (1 had no sampled-draft calls and no node_cand output). */
+/* ABI version: 3 (2 had no e3_kv_layer.flags and no budget controller; 1 had no
+ * sampled-draft calls and no node_cand output). */
 E3_API int eagle3_abi_version(void);
 
 /* Diagnostic with no counterpart in the method: the number of kernels this

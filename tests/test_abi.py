@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(e3):
         assert n in exported, n
         assert hasattr(e3.lib(), n)
     assert set(e3.SYMBOLS) == set(declared_functions())
-    assert e3.abi_version() == 2
+    assert e3.abi_version() == 3
     assert e3.QSTAT_BYTES == 24
 
 
@@ -108,6 +108,10 @@ def test_host_validation_rejects_bad_arguments(e3):
     with pytest.raises(e3.E3Error) as ei:
         e3.tree_verify_attn(16, bad, 16, 16, 1, 61, 32, 250, 0.1, 16, 16, None, 16, 1 << 30, stream=0)
     assert ei.value.status == 2
+    odd = e3.make_kv_layer(16, 16, 16, 10, 64, 40, 8, 128, e3.E3_BF16, 6)  # unknown flag bits
+    with pytest.raises(e3.E3Error) as ei:
+        e3.tree_verify_attn(16, odd, 16, 16, 1, 61, 32, 250, 0.1, 16, 16, None, 16, 1 << 30, stream=0)
+    assert ei.value.status == 1 and "flags" in e3.last_error()
     with pytest.raises(e3.E3Error) as ei:  # unknown accept mode
         e3.spec_accept(*([16] * 2), 1, 15, 3, *([16] * 4), 1000, *([16] * 3), 7, *([16] * 4), stream=0)
     assert ei.value.status == 3
@@ -139,3 +143,41 @@ def test_product_path_does_not_reference_the_oracle():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "eagle3_oracle" not in text, f
+
+
+def test_budget_controller_on_the_host(e3):
+    """The adaptive tree budget (host code; "Thinking Budget 与 EAGLE-3", 服务端应怎样联合控制):
+    raise one level at a time when acceptance is high and stable, not during the
+    cool-down, lower on low acceptance or costly drafting, respect the bounds, fall
+    back to the baseline on an invalid observation."""
+    import numpy as np
+    levels = [(6, 2), (14, 3), (30, 4), (60, 6)]
+    pol = e3.budget_policy(levels, min_level=0, max_level=2, base_level=1, alpha=0.5, low=0.25, high=0.75,
+                           spread=0.25, min_spare=0.2, max_draft_cost=0.5, cooldown=2, warmup=2)
+    st = e3.eagle3_budget_init(pol, 3)
+    assert [s.level for s in st] == [1, 1, 1]
+    hist = []
+    for r in range(12):
+        acc = [levels[st[0].level][1], 0, levels[st[2].level][1]]  # full, none, full
+        hist.append(e3.eagle3_budget_update(pol, st, acc, spare=1.0 if r < 6 else 0.0, draft_cost=0.0))
+    lv = np.array(hist)
+    assert lv[:, 0].max() == 2 and lv[:, 0].min() >= 1          # capped at max_level
+    assert lv[-1, 1] == 0                                        # low acceptance: down to the floor
+    assert np.all(np.abs(np.diff(lv, axis=0)) <= 1)              # one level at a time
+    for b in range(3):                                           # a change is held through the cool-down
+        ch = np.nonzero(np.diff(lv[:, b]))[0]
+        assert np.all(np.diff(ch) > pol.cooldown), (b, lv[:, b])
+    # no spare verify capacity: no raise (request 2 kept full acceptance after round 6)
+    st2 = e3.eagle3_budget_init(pol, 1)
+    for r in range(6):
+        out = e3.eagle3_budget_update(pol, st2, [levels[st2[0].level][1]], spare=0.0, draft_cost=0.0)
+    assert out == [1]
+    # costly drafting lowers even a fully accepted request
+    for r in range(6):
+        out = e3.eagle3_budget_update(pol, st2, [levels[st2[0].level][1]], spare=1.0, draft_cost=0.9)
+    assert out == [0]
+    # an invalid observation (request finished / failed) resets to the baseline
+    out = e3.eagle3_budget_update(pol, st2, [-1], spare=1.0, draft_cost=0.0)
+    assert out == [pol.base_level]
+    with pytest.raises(e3.E3Error):  # bounds outside the ladder
+        e3.eagle3_budget_init(e3.budget_policy(levels, max_level=7), 1)

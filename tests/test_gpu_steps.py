@@ -245,7 +245,8 @@ def test_tree_build_page_example():
 
 # ---------------------------------------------------------------- attention ----
 
-def run_gpu_verify(Q, K, Vc, pt, npages, kv_len, mask, H, KVH, hd, page_size, dt, max_kv_len=None, scale=None):
+def run_gpu_verify(Q, K, Vc, pt, npages, kv_len, mask, H, KVH, hd, page_size, dt, max_kv_len=None, scale=None,
+                   flags=0):
     B, R = Q.shape[0], Q.shape[1]
     max_kv_len = int(max(kv_len)) if max_kv_len is None else max_kv_len
     scale = scale or 1.0 / math.sqrt(hd)
@@ -254,7 +255,7 @@ def run_gpu_verify(Q, K, Vc, pt, npages, kv_len, mask, H, KVH, hd, page_size, dt
     Qt = to_dev(Q).to(tdt)
     Kt, Vt = to_dev(K).to(tdt), to_dev(Vc).to(tdt)
     ptt = to_dev(pt)
-    kv = e3.make_kv_layer(Kt, Vt, ptt, npages, page_size, pt.shape[1], KVH, hd, code)
+    kv = e3.make_kv_layer(Kt, Vt, ptt, npages, page_size, pt.shape[1], KVH, hd, code, flags)
     O = torch.full((B, R, H, hd), float("nan"), dtype=tdt, device="cuda")
     lse = torch.full((B, R, H), float("nan"), device="cuda")
     wsb = e3.eagle3_verify_workspace_bytes(B, R, H, KVH, hd, max_kv_len, code)
@@ -293,7 +294,8 @@ def mask_from_parent(par):
     dict(dt="bf16", lens=[12000, 5, 1000], R=61, H=32, KVH=8, hd=128, ps=64, D=6),  # ragged long: empty segments
     dict(dt="bf16", lens=[30000], R=61, H=16, KVH=4, hd=128, ps=64, D=6),       # long: one wave without clusters
 ])
-def test_verify_attention(case):
+@pytest.mark.parametrize("flags", [0, 1])  # 1: E3_KV_PREFIX_STABLE (prefix loads before the grid-dependency wait)
+def test_verify_attention(case, flags):
     dt, lens, R, H, KVH, hd, ps, D = (case[x] for x in ("dt", "lens", "R", "H", "KVH", "hd", "ps", "D"))
     B = len(lens)
     seed = sum(lens) + R
@@ -304,7 +306,7 @@ def test_verify_attention(case):
     rng = np.random.default_rng(seed)
     par = np.stack([random_tree(rng, R, max(D, 1))[0] for _ in range(B)])
     mask = np.stack([mask_from_parent(p) for p in par])
-    O, lse, err = run_gpu_verify(Q, K, Vc, pt, npages, lens, mask, H, KVH, hd, ps, dt)
+    O, lse, err = run_gpu_verify(Q, K, Vc, pt, npages, lens, mask, H, KVH, hd, ps, dt, flags=flags)
     assert err == 0
     Oref, lref = oracle.tree_verify_attn(Q, K, Vc, pt, np.array(lens), par, 1.0 / math.sqrt(hd))
     tol = 2e-2 if dt == "bf16" else 1e-5
