@@ -23,7 +23,8 @@ STATUS_NAMES = {0: "E3_OK", 1: "E3_ERR_INVALID_ARG", 2: "E3_ERR_SHAPE", 3: "E3_E
 SYMBOLS = ["eagle3_fuse", "eagle3_fuse_workspace_bytes", "eagle3_fuse_noalloc",
            "eagle3_fuse_noalloc_max_scratch_bytes", "eagle3_expand", "eagle3_expand_sampled", "tree_build_mask",
            "tree_verify_attn", "eagle3_verify_workspace_bytes", "lmhead_logits", "spec_accept",
-           "spec_accept_sampled", "kv_compact", "eagle3_budget_init", "eagle3_budget_update", "eagle3_last_error",
+           "spec_accept_sampled", "kv_compact", "eagle3_draft_step", "eagle3_draft_workspace_bytes",
+           "eagle3_budget_init", "eagle3_budget_update", "eagle3_last_error",
            "eagle3_abi_version", "eagle3_launch_count"]
 MAX_BUDGET_LEVELS = 16
 
@@ -52,6 +53,15 @@ class e3_kv_layer(ctypes.Structure):
                 ("n_pages", ctypes.c_int), ("page_size", ctypes.c_int), ("max_pages", ctypes.c_int),
                 ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("dt", ctypes.c_int),
                 ("flags", ctypes.c_int)]
+
+
+class e3_drafter(ctypes.Structure):
+    _fields_ = [("emb", ctypes.c_void_p), ("W_in", ctypes.c_void_p), ("norm1", ctypes.c_void_p),
+                ("W_qkv", ctypes.c_void_p), ("W_o", ctypes.c_void_p), ("norm2", ctypes.c_void_p),
+                ("W_gu", ctypes.c_void_p), ("W_down", ctypes.c_void_p), ("norm_f", ctypes.c_void_p),
+                ("W_lm", ctypes.c_void_p), ("d", ctypes.c_int), ("n_heads", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int), ("V", ctypes.c_int),
+                ("rope_base", ctypes.c_float), ("eps", ctypes.c_float)]
 
 
 class e3_budget_policy(ctypes.Structure):
@@ -88,6 +98,9 @@ def _load() -> ctypes.CDLL:
         "spec_accept": (I, [P, P, I, I, I, P, P, P, P, I, P, P, P, I, P, P, P, P, P]),
         "spec_accept_sampled": (I, [P, P, P, I, I, I, P, P, P, P, I, P, P, I, P, P, P, P, P, P, P]),
         "kv_compact": (I, [ctypes.POINTER(e3_kv_layer), I, I, P, P, I, P, P, P]),
+        "eagle3_draft_step": (I, [ctypes.POINTER(e3_drafter), ctypes.POINTER(e3_kv_layer), P, I, I, I, I, P, I, I,
+                                  P, I, I, ctypes.POINTER(e3_cand), P, P, P, P, P, P, P, P, P, S, P, P]),
+        "eagle3_draft_workspace_bytes": (S, [ctypes.POINTER(e3_drafter), I, I, I, I]),
         "eagle3_budget_init": (I, [ctypes.POINTER(e3_budget_policy), P, I]),
         "eagle3_budget_update": (I, [ctypes.POINTER(e3_budget_policy), P, I, P, F, F, P]),
         "eagle3_last_error": (ctypes.c_char_p, []),
@@ -266,3 +279,24 @@ def eagle3_budget_update(pol: e3_budget_policy, st, acc_len, spare=1.0, draft_co
                                                              a.ctypes.data, float(spare), float(draft_cost),
                                                              out.ctypes.data))
     return out.tolist()
+
+
+def make_drafter(emb, W_in, norm1, W_qkv, W_o, norm2, W_gu, W_down, norm_f, W_lm, d, n_heads, n_kv_heads, head_dim,
+                 ffn, V, rope_base=10000.0, eps=1e-6) -> e3_drafter:
+    return e3_drafter(ptr(emb), ptr(W_in), ptr(norm1), ptr(W_qkv), ptr(W_o), ptr(norm2), ptr(W_gu), ptr(W_down),
+                      ptr(norm_f), ptr(W_lm), d, n_heads, n_kv_heads, head_dim, ffn, V, rope_base, eps)
+
+
+def eagle3_draft_workspace_bytes(drafter: e3_drafter, B, F_max, R_slots, max_kv_len) -> int:
+    return int(_lib.eagle3_draft_workspace_bytes(ctypes.byref(drafter), B, F_max, R_slots, max_kv_len))
+
+
+def eagle3_draft_step(drafter: e3_drafter, kv: e3_kv_layer, kv_len, max_kv_len, B, depth, F, frontier, slot_base,
+                      F_prev, frontier_prev, slot_base_prev, R_slots, cands: e3_cand, root_tok, g, a_slots, mask,
+                      logits, row_max, row_Q, row_argmax, ws, ws_bytes, dev_err=None, stream=None):
+    _check("eagle3_draft_step",
+           _lib.eagle3_draft_step(ctypes.byref(drafter), ctypes.byref(kv), ptr(kv_len), max_kv_len, B, depth, F,
+                                  ptr(frontier), slot_base, F_prev, ptr(frontier_prev), slot_base_prev, R_slots,
+                                  ctypes.byref(cands), ptr(root_tok), ptr(g), ptr(a_slots), ptr(mask), ptr(logits),
+                                  ptr(row_max), ptr(row_Q), ptr(row_argmax), ptr(ws), ws_bytes, ptr(dev_err),
+                                  _stream(stream)))

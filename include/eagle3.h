@@ -364,6 +364,69 @@ E3_API e3_status kv_compact(const e3_kv_layer* layers, int L, int B, const int32
                      e3_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * eagle3_draft_step: one step of the drafter -- a single decoder layer -- for
+ * the frontier rows of one depth of the draft tree, B requests at once.
+ * "论文专题讲解：EAGLE-3", 推理流程：多层特征融合 + 单层 draft decoder (one decoder
+ * layer; the first step reads the fused feature g and the token's embedding,
+ * later steps the drafter's own previous output a) and 方法主线：为什么叫
+ * Training-time Test; "SpecForge…", 第二步为什么没有"正确隐藏状态"可用 and 从序列
+ * 到动态草稿树 (a node attends to its ancestors only).
+ * Row f of request b at depth t (1-based), node u = frontier[b][f] (a candidate
+ * index of cands; -1 = the root, the only row at t = 1):
+ *   tok = root_tok[b] (t = 1) or cands->tok[b][u];
+ *   h   = g[b] (t = 1) or a of u's parent (a_slots[b][parent's slot]);
+ *   x = W_in [e(tok); h];  y = RMSNorm(x) norm1;  [q; k; v] = W_qkv y, rotary
+ *   position pos = kv_len[b] + t - 1 applied to q and k (dimension i paired with
+ *   i + hd/2, angle pos * rope_base^(-2i/hd));  o = attention of q over the
+ *   drafter's cache: prefix [0, kv_len[b]) and the tree slots of u's ancestors
+ *   and u (scale 1/sqrt(hd));  x += W_o o;  y = RMSNorm(x) norm2;
+ *   a = x + W_down (silu(W_gate y) * W_up y);
+ *   logits = W_lm (RMSNorm(a) norm_f) with lmhead_logits' row statistics at T = 1.
+ *   RMSNorm(x) = x / sqrt(mean(x^2) + eps).
+ * Slots: u gets tree slot s = slot_base + f: its k and v go to logical position
+ *   kv_len[b] + s of the drafter's cache, its a (fp32) to a_slots[b][s], its mask
+ *   row to mask[b][s] = mask[b][parent's slot] | bit s.  The parent's slot is
+ *   slot_base_prev + f' where frontier_prev[b][f'] = cands->parent[b][u].  At t = 1
+ *   every mask row is reset to its own bit.
+ * Layouts (device; bf16 weights row-major, K innermost):
+ *   drafter (host struct) as e3_drafter; drafter_kv: the drafter's paged cache
+ *   (bf16, head_dim hd, n_kv_heads KVH; pages for kv_len[b] + R_slots tokens);
+ *   frontier [B][F], frontier_prev [B][F_prev] int32; root_tok [B]; g [B][d] bf16;
+ *   a_slots [B][R_slots][d] fp32 and mask [B][R_slots][ceil(R_slots/64)] uint64
+ *   (kept by the caller across the depths of one tree); logits [B][F][V] fp32
+ *   (the rows eagle3_expand reads), row_max/row_Q/row_argmax [B*F].
+ * ws: eagle3_draft_workspace_bytes(drafter, B, F_max, R_slots, max_kv_len) bytes.
+ * Limits: bf16; d, H*hd, ffn multiples of 128; hd even; R_slots <= 256;
+ *   1 <= t <= E3_MAX_DEPTH; slot_base + F <= R_slots; B*F <= 1024.
+ * dev_err: E3_DEV_ERR_CAPACITY (pages, a parent not in the previous frontier),
+ *   E3_DEV_ERR_TIMEOUT.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  const void* emb;      /* [V][d]: token embedding */
+  const void* W_in;     /* [d][2d]: input projection of [e(tok); h] */
+  const float* norm1;   /* [d] */
+  const void* W_qkv;    /* [(H + 2 KVH) hd][d]: rows of W_q, then W_k, then W_v */
+  const void* W_o;      /* [d][H hd] */
+  const float* norm2;   /* [d] */
+  const void* W_gu;     /* [2 ffn][d]: rows of W_gate, then W_up */
+  const void* W_down;   /* [d][ffn] */
+  const float* norm_f;  /* [d] */
+  const void* W_lm;     /* [V][d] */
+  int d, n_heads, n_kv_heads, head_dim, ffn, V;
+  float rope_base, eps;
+} e3_drafter;
+E3_API e3_status eagle3_draft_step(const e3_drafter* drafter, const e3_kv_layer* drafter_kv,
+                                   const int32_t* kv_len, int max_kv_len, int B, int depth, int F,
+                                   const int32_t* frontier, int slot_base, int F_prev,
+                                   const int32_t* frontier_prev, int slot_base_prev, int R_slots,
+                                   const e3_cand* cands, const int32_t* root_tok, const void* g,
+                                   float* a_slots, uint64_t* mask, float* logits, float* row_max,
+                                   uint64_t* row_Q, int32_t* row_argmax, void* ws, size_t ws_bytes,
+                                   int32_t* dev_err, e3_stream_t stream);
+E3_API size_t eagle3_draft_workspace_bytes(const e3_drafter* drafter, int B, int F_max, int R_slots,
+                                           int max_kv_len);
+
+/* ---------------------------------------------------------------------------
  * Adaptive draft-tree budget for a serving loop (host code only: no device
  * memory, no stream, no kernel).
  * "Thinking Budget 与 EAGLE-3", 服务端应怎样联合控制 (the execution controller):
