@@ -692,6 +692,7 @@ def main():
     ap.add_argument("--min-time", type=float, default=2.5, help="seconds of timed graph replays")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-draft", action="store_true", help="skip timing the GPU drafter")
     ap.add_argument("--layers", type=int, default=None,
                     help="profiling only: fewer target layers than the configuration (small ncu captures)")
     args = ap.parse_args()
@@ -819,6 +820,10 @@ def main():
                   peak_source="MEASURED_PEAKS.json bf16_tflops_sustained (of measured)")
     lm["tensor_frac"] = round(lm_tf / tflops, 4)
     e2e = None if args.no_e2e else e2e_leg(w, s, K, args.warmup, world)
+    draft = None if args.no_draft else draft_leg(w, s)
+    if draft is not None:
+        # a round whose draft logits come from the drafter on the GPU: drafting + the round
+        draft["self_contained_rounds_per_s"] = round(1000.0 / (draft["ms"] + ms_step), 3)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w)
@@ -847,6 +852,7 @@ def main():
             "launches_per_round": phase_launches,
             "clocks": clk,
             "e2e": e2e,
+            "drafter": draft,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -977,6 +983,122 @@ def e2e_leg(w, s, K, warmup, world=1):
     return {"value": round(job_rounds_per_s(ms, world), 3), "unit": "rounds/s", "h2d_bytes_per_step": bi,
             "d2h_bytes_per_step": bo, "ms_per_step": round(ms, 4),
             "overlap": "double-buffered: step i+1's host-to-device copies on a second stream during step i"}
+
+
+FFN = {4096: 14336, 8192: 28672}  # MLP width of the target family at each model width
+
+
+def draft_leg(w, s, reps=20):
+    """The drafting phase of a round with the drafter on the GPU: D depths of
+    eagle3_draft_step (one decoder layer with random weights of the target's
+    shape, the target's vocabulary) each followed by eagle3_expand on its logits,
+    for the B requests; captured as one graph and timed by CUDA events.  Reported
+    beside the round (whose draft logits are inputs): per depth, and against HBM
+    for the weights each depth streams."""
+    import torch
+    e3, cfg = w.e3, w.cfg
+    if cfg.dtype != "bf16" or cfg.sampled:
+        return None
+    d, H, KVH, hd, V, B = cfg.d, cfg.H, cfg.KVH, cfg.hd, cfg.V, cfg.B
+    ffn = FFN.get(d, 4 * d)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(99)
+
+    def rnd(shape, std, mean=0.0, dt=torch.bfloat16):
+        return (torch.randn(shape, generator=g, device="cuda") * std + mean).to(dt)
+
+    Wt = dict(emb=rnd((V, d), 1.0), W_in=rnd((d, 2 * d), 0.02), norm1=rnd((d,), 0.02, 1.0, torch.float32),
+              W_qkv=rnd(((H + 2 * KVH) * hd, d), 0.02), W_o=rnd((d, H * hd), 0.02),
+              norm2=rnd((d,), 0.02, 1.0, torch.float32), W_gu=rnd((2 * ffn, d), 0.02), W_down=rnd((d, ffn), 0.02),
+              norm_f=rnd((d,), 0.02, 1.0, torch.float32), W_lm=rnd((V, d), 4.0 / math.sqrt(d)))
+    dr = e3.make_drafter(Wt["emb"], Wt["W_in"], Wt["norm1"], Wt["W_qkv"], Wt["W_o"], Wt["norm2"], Wt["W_gu"],
+                         Wt["W_down"], Wt["norm_f"], Wt["W_lm"], d, H, KVH, hd, ffn, V)
+    sizes, n_cand = cfg.frontier_sizes()
+    bases = [0]
+    for F, _ in sizes:
+        bases.append(bases[-1] + F)
+    R_slots = bases[-1]
+    P = w.c["P"]
+    pt, npages = w.synth.page_table(7, [p + R_slots for p in P], cfg.page_size)
+    Kc, Vc = rnd((npages, KVH, cfg.page_size, hd), 1.0), rnd((npages, KVH, cfg.page_size, hd), 1.0)
+    ptt = torch.from_numpy(pt).cuda()
+    kv = e3.make_kv_layer(Kc, Vc, ptt, npages, cfg.page_size, pt.shape[1], KVH, hd, e3.E3_BF16,
+                          e3.E3_KV_PREFIX_STABLE)
+    kv_len = torch.tensor(P, dtype=torch.int32, device="cuda")
+    gfeat = rnd((B, d), 1.0)
+    roots = torch.randint(0, V, (B,), generator=g, device="cuda", dtype=torch.int32)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    c_tok, c_par = torch.zeros((B, n_cand), **i32), torch.zeros((B, n_cand), **i32)
+    c_sc, c_dep = torch.zeros((B, n_cand), device="cuda"), torch.zeros((B, n_cand), **i32)
+    cands = e3.make_cand(c_tok, c_par, c_sc, c_dep, n_cand)
+    f_id = [torch.full((B, 1), -1, **i32)] + [torch.zeros((B, min(cfg.W, F * cfg.k)), **i32) for F, _ in sizes]
+    f_sc = [torch.zeros((B, 1), device="cuda")] + [torch.zeros((B, min(cfg.W, F * cfg.k)), device="cuda")
+                                                   for F, _ in sizes]
+    a_slots = torch.zeros((B, R_slots, d), device="cuda")
+    mask = torch.zeros((B, R_slots, (R_slots + 63) // 64), dtype=torch.int64, device="cuda")
+    Fmax = max(F for F, _ in sizes)
+    logits = [torch.empty((B, F, V), device="cuda") for F, _ in sizes]
+    rmax, rQ = torch.empty(B * Fmax, device="cuda"), torch.empty(B * Fmax, dtype=torch.int64, device="cuda")
+    ram = torch.empty(B * Fmax, **i32)
+    wsb = e3.eagle3_draft_workspace_bytes(dr, B, Fmax, R_slots, max(P))
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    err = torch.zeros(1, **i32)
+    ev = [graph_event() for _ in range(len(sizes) + 1)]
+
+    def drafting(marks):
+        for di, (F, off) in enumerate(sizes):
+            if marks:
+                ev[di].record(s)
+            prev = f_id[di - 1] if di else f_id[0]
+            e3.eagle3_draft_step(dr, kv, kv_len, max(P), B, di + 1, F, f_id[di], bases[di], prev.shape[1] if di else 0,
+                                 prev if di else None, bases[di - 1] if di else 0, R_slots, cands, roots, gfeat, a_slots,
+                                 mask, logits[di], rmax, rQ, ram, ws, wsb, err, stream=s)
+            e3.eagle3_expand(logits[di], B, F, V, cfg.k, cfg.W, 1.0, f_sc[di], f_id[di], di + 1, off, cands,
+                             f_id[di + 1], f_sc[di + 1], err, stream=s)
+        if marks:
+            ev[-1].record(s)
+
+    with torch.cuda.stream(s):
+        drafting(False)
+    torch.cuda.synchronize()
+    n0 = e3.launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        drafting(False)
+    launches = e3.launch_count() - n0
+    gph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gph, stream=s):
+        drafting(True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        graph.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            a.record(s)
+            graph.replay()
+            z.record(s)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(z))
+    with torch.cuda.stream(s):
+        gph.replay()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"drafting: device error flags {int(err.item()):#x}")
+    per_depth = [ev[i].elapsed_time(ev[i + 1]) for i in range(len(sizes))]
+    # weights each depth streams (the embedding table only by the rows it gathers)
+    wbytes = 2 * (2 * d * d + (H + 2 * KVH) * hd * d + d * H * hd + 3 * ffn * d + V * d)
+    ms = statistics.median(times)
+    peaks = load_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    gbs = wbytes * len(sizes) / (ms * 1e-3) / 1e9
+    return {"what": "drafter on the GPU: D x (eagle3_draft_step + eagle3_expand), random weights of the target's "
+                    f"shape (d={d}, {H}/{KVH} heads x {hd}, MLP {ffn}, vocabulary {V})",
+            "ms": round(ms, 4), "per_depth_ms": [round(x, 4) for x in per_depth], "launches": launches,
+            "weight_bytes_per_depth": wbytes, "achieved_gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / hbm, 4), "self_contained_rounds_per_s": None}
 
 
 def check_dev_err(w, where):
