@@ -47,7 +47,8 @@ static e3_status check_kv_layer(const e3_kv_layer* kv, const char* fn) {
   E3_REQUIRE(kv->head_dim >= 32 && kv->head_dim <= 256 && kv->head_dim % 32 == 0, E3_ERR_SHAPE,
              "%s: head_dim %d must be a multiple of 32 in [32, 256]", fn, kv->head_dim);
   E3_REQUIRE(aligned16(kv->k) && aligned16(kv->v), E3_ERR_INVALID_ARG, "%s: k/v not 16-byte aligned", fn);
-  E3_REQUIRE((kv->flags & ~E3_KV_PREFIX_STABLE) == 0, E3_ERR_INVALID_ARG, "%s: unknown kv flags %#x", fn, kv->flags);
+  E3_REQUIRE((kv->flags & ~(E3_KV_PREFIX_STABLE | E3_KV_SELFTEST_STALL)) == 0, E3_ERR_INVALID_ARG,
+             "%s: unknown kv flags %#x", fn, kv->flags);
   return E3_OK;
 }
 

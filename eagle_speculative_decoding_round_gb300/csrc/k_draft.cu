@@ -378,7 +378,8 @@ E3_API e3_status eagle3_draft_step(const e3_drafter* drafter, const e3_kv_layer*
   E3_REQUIRE(kv->k && kv->v && kv->page_table && kv->dt == E3_BF16 && kv->head_dim == w.head_dim &&
                  kv->n_kv_heads == w.n_kv_heads && kv->page_size > 0 && kv->max_pages > 0 && kv->n_pages > 0,
              E3_ERR_SHAPE, "%s: the drafter's cache must be bf16 with the drafter's head_dim and KV heads", fn);
-  E3_REQUIRE((kv->flags & ~E3_KV_PREFIX_STABLE) == 0, E3_ERR_INVALID_ARG, "%s: unknown kv flags", fn);
+  E3_REQUIRE((kv->flags & ~(E3_KV_PREFIX_STABLE | E3_KV_SELFTEST_STALL)) == 0, E3_ERR_INVALID_ARG,
+             "%s: unknown kv flags", fn);
   E3_REQUIRE(B >= 1 && F >= 1 && B * F <= 1024, E3_ERR_SHAPE, "%s: B=%d F=%d", fn, B, F);
   E3_REQUIRE(depth >= 1 && depth <= E3_MAX_DEPTH, E3_ERR_SHAPE, "%s: depth %d", fn, depth);
   E3_REQUIRE(depth > 1 || (F == 1 && slot_base == 0), E3_ERR_SHAPE, "%s: depth 1 expands the root only (slot 0)", fn);

@@ -302,6 +302,7 @@ __device__ __forceinline__ uint32_t mask_bits32(const uint64_t* row, int words, 
 struct TcGeom {
   int B, R, H, KVH, G, n_pre, S, chunk, RG, max_kv_len;
   int prefix_stable;  // E3_KV_PREFIX_STABLE: prefix K/V, lengths and pages may be read before the wait
+  int stall;          // E3_KV_SELFTEST_STALL: the MMA thread waits on a barrier nothing arrives on
   int fold_tree;  // 1: segment S-1 also processes the tree slots (no separate tree segment)
   int page_size, max_pages, n_pages;
   const int32_t* page_table;
@@ -349,10 +350,12 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   uint64_t* v_empty = bars + 7;    // [2]
   uint64_t* s_full = bars + 9;     // [2]
   uint64_t* p_full = bars + 11;    // [2]
-  uint64_t* o_done = bars + 13;    // PV(t) completed (once per tile); bars + 14, 19 unused
+  uint64_t* o_done = bars + 13;    // PV(t) completed (once per tile); bars + 19 unused
+  uint64_t* stall_bar = bars + 14; // (self-test) never arrived on
   uint64_t* xch = bars + 15;       // [4] exchange among the parts of a row, per lane quarter
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  __shared__ int s_kv_last[4];  // last tile loaded into K stage 0/1 and V stage 0/1 (-1: none)
   float* s_max = reinterpret_cast<float*>(tmem_slot + 4);  // [2 parities][kParts <= 4][128 rows]
   float* s_l = s_max + 8 * kRows;                           // [kParts <= 4][128 rows]
 
@@ -374,6 +377,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
     }
     for (int qq = 0; qq < 4; ++qq) bar_init(&xch[qq], kParts);  // one arrival per part (warp) of a lane quarter
     bar_init(o_done, 1);
+    bar_init(stall_bar, 1);
+    for (int i = 0; i < 4; ++i) s_kv_last[i] = -1;
     *abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -509,6 +514,7 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
       const int row = block_row(2 * t + blk, okp);
       for (int h = 0; h < 2; ++h) tma2d(base + h * (kKVBytes / 2) + blk * kBox, map, h * kHalf, row, bar);
     }
+    s_kv_last[which * 2 + st] = t;  // (written by the issuing thread only; read after the final barrier)
   };
   // The first two tiles' K and V.  Under the prefix-stable promise the prefix
   // tiles (t < ntA) are requested before the wait: their slots hold the committed
@@ -576,7 +582,8 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
         umma_commit(&s_full[bb]);
         umma_commit(&k_empty[bb]);
       };
-      bool ok = bar_wait(q_full, 0, abort);
+      // (self-test: a barrier nothing arrives on, so the bounded wait runs out)
+      bool ok = g.stall ? bar_wait(stall_bar, 0, abort) : bar_wait(q_full, 0, abort);
       for (int t = 0; ok && t < ntile && t < 2; ++t) {
         if (!bar_wait(&k_full[t], 0, abort)) {
           ok = false;
@@ -866,7 +873,17 @@ verify_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant_
   // shared memory is reused or released
   if (threadIdx.x == 0 && !bar_wait_timed(q_full, 0)) *abort = 1;
   fence_before();
-  __syncthreads();
+  if (__syncthreads_or(*abort != 0)) {
+    // After an abort some K/V loads may never have been consumed: every load this CTA
+    // issued lands (bounded by time) before its shared memory is reused or released.
+    // Without an abort every load was waited on by its consumer.
+    if (threadIdx.x == 0)
+      for (int i = 0; i < 4; ++i) {
+        const int t = s_kv_last[i];
+        if (t >= 0) bar_wait_timed(i < 2 ? &k_full[i & 1] : &v_full[i & 1], (t >> 1) & 1);
+      }
+    __syncthreads();
+  }
   if (*abort && threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
   if (CLUSTER && g.S > 1) {
     const int S = g.S;
@@ -1027,6 +1044,7 @@ e3_status launch_verify_tc(const void* Q, const e3_kv_layer& kv, const int32_t* 
   g.page_table = kv.page_table;
   g.fold_tree = 0;
   g.prefix_stable = (kv.flags & E3_KV_PREFIX_STABLE) ? 1 : 0;
+  g.stall = (kv.flags & E3_KV_SELFTEST_STALL) ? 1 : 0;
   static std::atomic<bool> attr_done{false};
   if (!attr_done.load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(verify_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);

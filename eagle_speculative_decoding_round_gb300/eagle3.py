@@ -18,6 +18,7 @@ E3_F32, E3_BF16 = 0, 1
 E3_DEV_ERR_NONFINITE, E3_DEV_ERR_CAPACITY, E3_DEV_ERR_TIMEOUT = 1, 2, 4
 E3_ACCEPT_TREE_DET, E3_ACCEPT_SAMPLED = 0, 1
 E3_KV_PREFIX_STABLE = 1
+E3_KV_SELFTEST_STALL = 0x40000000  # failure-detection self-test only
 STATUS_NAMES = {0: "E3_OK", 1: "E3_ERR_INVALID_ARG", 2: "E3_ERR_SHAPE", 3: "E3_ERR_UNSUPPORTED",
                 4: "E3_ERR_CAPACITY", 5: "E3_ERR_NONFINITE", 6: "E3_ERR_CUDA", 7: "E3_ERR_TIMEOUT"}
 SYMBOLS = ["eagle3_fuse", "eagle3_fuse_workspace_bytes", "eagle3_fuse_noalloc",

@@ -128,6 +128,13 @@ typedef struct {
  * slots are read only after it has completed.  Breaking the promise can make
  * the call read stale prefix data.  Other calls ignore the flag. */
 #define E3_KV_PREFIX_STABLE 1
+/* E3_KV_SELFTEST_STALL: failure-detection self-test, never for production (no
+ * counterpart in the pages).  In tree_verify_attn's tensor-core kernel the MMA
+ * thread waits on a barrier that nothing arrives on: the bounded wait runs out
+ * after about a second, the kernel sets E3_DEV_ERR_TIMEOUT in dev_err, waits for
+ * its own copies in flight, frees its tensor memory and returns; O and lse are not
+ * valid.  Other paths and calls ignore the bit. */
+#define E3_KV_SELFTEST_STALL 0x40000000
 typedef struct {
   void* k;
   void* v;
@@ -138,7 +145,7 @@ typedef struct {
   int n_kv_heads;
   int head_dim;
   e3_dtype dt;
-  int flags;                 /* 0 or E3_KV_PREFIX_STABLE */
+  int flags;                 /* 0, E3_KV_PREFIX_STABLE, E3_KV_SELFTEST_STALL */
 } e3_kv_layer;
 
 /* ---------------------------------------------------------------------------
