@@ -137,6 +137,7 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
   __shared__ float s_nmax[kMaxR];  // every node's row statistics, loaded in parallel
   __shared__ int s_nam[kMaxR];
   __shared__ unsigned long long s_nQ[kMaxR];
+  __shared__ uint32_t s_ua[kMaxR];  // every child's acceptance uniform (the walk is serial)
 
   pdl_wait();
   pdl_trigger();
@@ -149,6 +150,7 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
     s_nmax[i] = row_max[rb + i];
     s_nam[i] = row_argmax[rb + i];
     s_nQ[i] = row_Q[rb + i];
+    s_ua[i] = u_acc[rb + i];
   }
   __syncthreads();
   // children lists in CSR form (children in ascending flat order) and child masses
@@ -210,7 +212,7 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
         }
         if (t < 0 || t >= V) continue;
         const uint64_t q = s_qc[c];
-        if (mulhi32(u_acc[rb + c], Rm) < q) {
+        if (mulhi32(s_ua[c], Rm) < q) {
           accepted = c;
           break;
         }
