@@ -297,14 +297,19 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 DraftWs draft_ws(const e3_drafter& w, int B, int F_max, int R_slots, int max_kv_len) {
   const int M = B * F_max;
   const int H = w.n_heads, KVH = w.n_kv_heads, hd = w.head_dim, d = w.d;
+  // The largest split-K partial of any of the five GEMMs at any row count up to M.  Between
+  // the row counts where the token tiling steps (16, 32, 64, 128, then multiples of 256)
+  // the split count is fixed and the partial grows with the rows, so the step ends suffice.
   size_t part = 0;
-  for (int mm = 1; mm <= M; ++mm) {  // the largest split-K partial of any GEMM at any row count
+  auto part_at = [&](int mm) {
     part = std::max(part, linear_partial_bytes(mm, 2 * d, d));
     part = std::max(part, linear_partial_bytes(mm, d, (H + 2 * KVH) * hd));
     part = std::max(part, linear_partial_bytes(mm, H * hd, d));
     part = std::max(part, linear_partial_bytes(mm, d, 2 * w.ffn));
     part = std::max(part, linear_partial_bytes(mm, w.ffn, d));
-  }
+  };
+  for (int mm : {16, 32, 64, 128}) part_at(std::min(mm, M));
+  for (int mm = 256; mm < M + 256; mm += 256) part_at(std::min(mm, M));
   DraftWs r{};
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -392,8 +397,8 @@ E3_API e3_status eagle3_draft_step(const e3_drafter* drafter, const e3_kv_layer*
   E3_REQUIRE(max_kv_len >= 0 && static_cast<long>(max_kv_len) + R_slots <= static_cast<long>(kv->max_pages) * kv->page_size,
              E3_ERR_CAPACITY, "%s: max_kv_len + R_slots exceeds the drafter cache's pages", fn);
   const DraftWs L = draft_ws(w, B, F, R_slots, max_kv_len);
-  const size_t need = draft_ws(w, B, F, R_slots, max_kv_len).total;
-  E3_REQUIRE(ws_bytes >= need, E3_ERR_CAPACITY, "%s: workspace of %zu bytes needed, %zu given", fn, need, ws_bytes);
+  E3_REQUIRE(ws_bytes >= L.total, E3_ERR_CAPACITY, "%s: workspace of %zu bytes needed, %zu given", fn, L.total,
+             ws_bytes);
   E3_REQUIRE(aligned16(ws) && aligned16(g) && aligned16(w.emb) && aligned16(a_slots) && aligned16(logits), E3_ERR_INVALID_ARG,
              "%s: ws, g, emb, a_slots, logits must be 16-byte aligned", fn);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -413,8 +418,7 @@ E3_API e3_status eagle3_draft_step(const e3_drafter* drafter, const e3_kv_layer*
   cudaError_t e = launch_pdl(draft_prep_kernel, dim3(M), dim3(kThreads), 0, s, 1, pa);
   if (e != cudaSuccess) return cuda_status(e, "draft_prep_kernel");
 
-  auto norm = [&](int K_in, const float* resid, const float* wn, float* slot_out) {
-    (void)K_in;
+  auto norm = [&](const float* resid, const float* wn, float* slot_out) {
     NormArgs na{part, splits, M, d, resid, f32(L.x), wn, w.eps, bf(L.y), slot_out, i32(L.row_slot), F, R_slots};
     const cudaError_t e2 = launch_pdl(draft_norm_kernel, dim3(M), dim3(kThreads), static_cast<size_t>(d) * 4, s, 1, na);
     return e2 == cudaSuccess ? E3_OK : cuda_status(e2, "draft_norm_kernel");
@@ -423,7 +427,7 @@ E3_API e3_status eagle3_draft_step(const e3_drafter* drafter, const e3_kv_layer*
   const void* in_src[2] = {bf(L.e_rows), bf(L.h_rows)};
   st = launch_linear_tc(w.W_in, in_src, 2, d, M, d, part, &splits, dev_err, s);
   if (st != E3_OK) return st;
-  if ((st = norm(2 * d, nullptr, w.norm1, nullptr)) != E3_OK) return st;
+  if ((st = norm(nullptr, w.norm1, nullptr)) != E3_OK) return st;
   // q, k, v with rotary positions; k, v into the cache at the rows' tree slots
   const void* y_src[1] = {bf(L.y)};
   st = launch_linear_tc(w.W_qkv, y_src, 1, d, M, (H + 2 * KVH) * hd, part, &splits, dev_err, s);
@@ -444,7 +448,7 @@ E3_API e3_status eagle3_draft_step(const e3_drafter* drafter, const e3_kv_layer*
   const void* o_src[1] = {bf(L.o_rows)};
   st = launch_linear_tc(w.W_o, o_src, 1, H * hd, M, d, part, &splits, dev_err, s);
   if (st != E3_OK) return st;
-  if ((st = norm(H * hd, f32(L.x), w.norm2, nullptr)) != E3_OK) return st;
+  if ((st = norm(f32(L.x), w.norm2, nullptr)) != E3_OK) return st;
   // SwiGLU MLP
   st = launch_linear_tc(w.W_gu, y_src, 1, d, M, 2 * w.ffn, part, &splits, dev_err, s);
   if (st != E3_OK) return st;
@@ -459,7 +463,7 @@ E3_API e3_status eagle3_draft_step(const e3_drafter* drafter, const e3_kv_layer*
   const void* m_src[1] = {bf(L.mlp)};
   st = launch_linear_tc(w.W_down, m_src, 1, w.ffn, M, d, part, &splits, dev_err, s);
   if (st != E3_OK) return st;
-  if ((st = norm(w.ffn, f32(L.x), w.norm_f, a_slots)) != E3_OK) return st;
+  if ((st = norm(f32(L.x), w.norm_f, a_slots)) != E3_OK) return st;
   // draft logits and their statistics (temperature 1)
   return launch_lmhead_tc(bf(L.y), w.W_lm, M, d, w.V, f32(L.ones), logits, row_max, row_Q, row_argmax, dev_err, s);
 }
