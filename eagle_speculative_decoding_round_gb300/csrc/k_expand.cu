@@ -10,8 +10,8 @@
 // not below the smallest warp maximum (or, when k exceeds the warp count or too
 // many qualify, the k-th largest per-thread maximum), ranked exactly.  The row
 // maximum, the fixed-point mass Q and each CTA's k best are combined through
-// distributed shared memory; CTA 0 merges the lists (KMAX-wide per lane) and
-// writes the k children.
+// distributed shared memory; CTA 0 ranks the lists' keys and writes the k
+// children.
 // Kernel 2 (one CTA per request): sort the F*k children by (score desc,
 // candidate index asc) in shared memory and emit the next frontier.
 //
@@ -74,16 +74,16 @@ __device__ __forceinline__ uint32_t cl_addr(const void* p, uint32_t rank) {
                : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void cl_st64(uint32_t a, uint64_t v) {
-  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+// asynchronous store into a peer's shared memory (cluster address a), completing
+// its byte count on the peer's mbarrier at cluster address bar: the sender does
+// not wait for the store to land
+__device__ __forceinline__ void cl_st_async64(uint32_t a, uint64_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(a), "l"(v), "r"(bar)
+               : "memory");
 }
-__device__ __forceinline__ void cl_st32(uint32_t a, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
-}
-// arrive (release at cluster scope: this thread's earlier stores to the peer are
-// visible to whoever observes the phase) on the mbarrier at cluster address a
-__device__ __forceinline__ void cl_arrive(uint32_t a) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(a) : "memory");
+__device__ __forceinline__ void cl_st_async32(uint32_t a, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(a), "r"(v), "r"(bar)
+               : "memory");
 }
 __device__ __forceinline__ void mb_init(uint64_t* b, uint32_t n) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(b))),
@@ -114,10 +114,11 @@ __device__ __forceinline__ bool mb_wait0(uint64_t* b) {
 // smallest of the 16 warp maxima (at least 16 >= k elements qualify, typically a
 // few dozen), ranked exactly; if more than fit, the exact threshold (k-th largest
 // per-thread maximum, which admits at most k * per-thread elements) is used.
-// Exchanges go through the peers' shared memory with mbarrier arrivals: every CTA
-// sends its maximum key and non-finite flag to every CTA (each then knows the row
-// maximum m), and its mass and top-k list to CTA 0, which merges and writes the
-// k children.
+// Exchanges are asynchronous stores into the peers' shared memory that complete
+// on the receivers' mbarriers (st.async, transaction bytes): every CTA sends its
+// maximum key and non-finite flag to every CTA (each then knows the row maximum
+// m), and its mass and top-k list to CTA 0, which ranks the CL lists' keys and
+// writes the k children.
 //
 // SAMPLED: the children are drawn from the row's draft distribution instead of
 // taken as its top k.  Once the row maximum m is known, each CTA makes one pass
@@ -162,11 +163,26 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   const int e0 = vec ? 4 * v0 : v0;  // token id of chunk[0]
   const int n_local = vec ? 4 * (v1 - v0) : (v1 - v0);
   pdl_wait();  // the previous depth's frontier (parent ids and scores) is complete
+  // the row's parent (id and score), needed by CTA 0's writers at the end: requested now
+  float ps_row = 0.0f;
+  int pid_row = -1;
+  if (rank == 0 && threadIdx.x < k) {
+    ps_row = parent_score[row];
+    pid_row = parent_id[row];
+  }
   if (threadIdx.x == 0) {
-    mb_init(&mx_bar, CL);
-    mb_init(&fin_bar, CL);
+    mb_init(&mx_bar, 1);  // completed by the peers' asynchronous stores: 12 bytes from each
+    mb_init(&fin_bar, 1);  // (CTA 0) completed by every CTA's mass and k keys: 8 (k + 1) bytes each
     mb_init(&ld_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(&mx_bar))),
+                 "r"(static_cast<uint32_t>(CL) * 12u)
+                 : "memory");
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(&fin_bar))),
+                 "r"(static_cast<uint32_t>(CL) * 8u * static_cast<uint32_t>(k + 1))
+                 : "memory");
     if (vec) {  // the chunk: bulk copies of 16-byte aligned row pieces
       const uint32_t bar = static_cast<uint32_t>(__cvta_generic_to_shared(&ld_bar));
       const uint32_t bytes = static_cast<uint32_t>(v1 - v0) * 16u;
@@ -233,9 +249,9 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   if (threadIdx.x < CL) {
     uint64_t lbest = 0ull;
     for (int w = 0; w < kExpandThreads / 32; ++w) lbest = max(lbest, s_wmax[w]);
-    cl_st64(cl_addr(&s_pmax[rank], threadIdx.x), lbest);
-    cl_st32(cl_addr(&s_pbad[rank], threadIdx.x), static_cast<uint32_t>(bad));
-    cl_arrive(cl_addr(&mx_bar, threadIdx.x));
+    const uint32_t bar = cl_addr(&mx_bar, threadIdx.x);
+    cl_st_async64(cl_addr(&s_pmax[rank], threadIdx.x), lbest, bar);
+    cl_st_async32(cl_addr(&s_pbad[rank], threadIdx.x), static_cast<uint32_t>(bad), bar);
   }
   // each thread visits the chunk elements it staged: float4 slots q - v0 (vec) or j - v0
   auto for_own = [&](auto&& fn) {
@@ -311,6 +327,7 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     for (int i = threadIdx.x; i < ncand; i += blockDim.x) {
       const uint64_t key = cand[i];
       int rnk = 0;
+#pragma unroll 8
       for (int j = 0; j < ncand; ++j) rnk += cand[j] > key;
       if (rnk < k) ltop[rnk] = key;
     }
@@ -379,10 +396,14 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     for_own([&](float v, uint32_t) { Q += fx_mass(v, m); });
   }
   Q = block_reduce(Q, SumU64(), red64);  // also orders ltop[] before thread 0 reads it
-  if (threadIdx.x == 0) {  // mass and top-k list to CTA 0
-    cl_st64(cl_addr(&s_pQ[rank], 0), Q);
-    for (int i = 0; i < k; ++i) cl_st64(cl_addr(&s_ptop[rank * k + i], 0), ltop[i]);
-    cl_arrive(cl_addr(&fin_bar, 0));
+  // mass (thread 0) and top-k list (threads 1..k) to CTA 0, as asynchronous stores
+  // completing on its fin_bar (register values: nothing of this CTA is read later)
+  if (threadIdx.x <= k) {
+    const uint32_t bar = cl_addr(&fin_bar, 0);
+    if (threadIdx.x == 0)
+      cl_st_async64(cl_addr(&s_pQ[rank], 0), Q, bar);
+    else
+      cl_st_async64(cl_addr(&s_ptop[rank * k + threadIdx.x - 1], 0), ltop[threadIdx.x - 1], bar);
   }
   if (rank != 0) return;  // nothing reads this CTA's shared memory any more
   const bool fin = mb_wait0(&fin_bar);
@@ -390,13 +411,17 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     if (threadIdx.x == 0) dev_flag(dev_err, E3_DEV_ERR_TIMEOUT);
     return;
   }
-  // every CTA's list is sorted (best first, zero-padded): warp 0 merges them, one
-  // list per lane
-  if (warp == 0) {
-    uint64_t lk[KMAX];
-#pragma unroll
-    for (int i = 0; i < KMAX; ++i) lk[i] = (lane < CL && i < k) ? s_ptop[lane * k + i] : 0ull;
-    warp_merge_topk(lk, k, top);
+  // the row's k best of the CL lists (distinct keys, zero-padded): each key's rank
+  // among all CL * k of them
+  if (threadIdx.x < k) top[threadIdx.x] = 0ull;
+  __syncthreads();
+  for (int i = threadIdx.x; i < CL * k; i += blockDim.x) {
+    const uint64_t key = s_ptop[i];
+    if (key == 0ull) continue;
+    int rnk = 0;
+#pragma unroll 8
+    for (int j = 0; j < CL * k; ++j) rnk += s_ptop[j] > key;
+    if (rnk < k) top[rnk] = key;
   }
   __shared__ uint64_t s_Qt;
   if (threadIdx.x == 0) {
@@ -406,7 +431,7 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
   }
   __syncthreads();
   if (SAMPLED && threadIdx.x == 0) {
-    const int pid = parent_id[row];
+    const int pid = pid_row;
     if (pid >= -1 && pid < c.cap) {
       e3_qstat st;
       st.row = z;
@@ -422,10 +447,10 @@ expand_rows_kernel(const float* __restrict__ logits, int F, int V, int k, float 
     const uint32_t t = packed_id(top[r]);
     const float sc = SAMPLED ? (t < static_cast<uint32_t>(V) ? __fmul_rn(__ldg(z + t), it) : -INFINITY)
                              : unord_f32(static_cast<uint32_t>(top[r] >> 32));
-    const float ps = parent_score[row];
+    const float ps = ps_row;
     const size_t ci = static_cast<size_t>(b) * c.cap + cand_offset + f * k + r;
     c.tok[ci] = static_cast<int32_t>(t);
-    c.parent[ci] = parent_id[row];
+    c.parent[ci] = pid_row;
     c.score[ci] = __fsub_rn(__fadd_rn(ps, __fsub_rn(sc, m)), ell);
     c.depth[ci] = depth;
   }
@@ -495,10 +520,13 @@ expand_frontier_kernel(int n, int Wn, int cand_offset, e3_cand c, int32_t* next_
   pdl_wait();
   pdl_trigger();
   __shared__ uint64_t keys[2048];
+  __shared__ float sc[1024];
   const int b = blockIdx.x;
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
     const int ci = cand_offset + i;
-    keys[i] = pack_best(c.score[static_cast<size_t>(b) * c.cap + ci], static_cast<uint32_t>(ci));
+    const float v = c.score[static_cast<size_t>(b) * c.cap + ci];
+    keys[i] = pack_best(v, static_cast<uint32_t>(ci));
+    if (n <= 1024) sc[i] = v;
   }
   __syncthreads();
   if (n <= 1024) {
@@ -506,11 +534,11 @@ expand_frontier_kernel(int n, int Wn, int cand_offset, e3_cand c, int32_t* next_
     for (int i = threadIdx.x; i < n; i += blockDim.x) {
       const uint64_t key = keys[i];
       int rank = 0;
+#pragma unroll 8
       for (int j = 0; j < n; ++j) rank += keys[j] > key;
       if (rank < Wn) {
-        const uint32_t ci = packed_id(key);
-        next_id[static_cast<size_t>(b) * Wn + rank] = static_cast<int32_t>(ci);
-        next_score[static_cast<size_t>(b) * Wn + rank] = c.score[static_cast<size_t>(b) * c.cap + ci];
+        next_id[static_cast<size_t>(b) * Wn + rank] = static_cast<int32_t>(cand_offset + i);
+        next_score[static_cast<size_t>(b) * Wn + rank] = sc[i];
       }
     }
     return;
