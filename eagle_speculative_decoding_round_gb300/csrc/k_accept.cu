@@ -14,13 +14,14 @@
 // child accepted, the bonus (correction) token is drawn from the residual.
 //
 // One cluster of CL CTAs per request (16 where allowed, else 8).  Every CTA
-// builds the children lists and each child's fixed-point mass in parallel and
-// then walks the tree (integer work only).  For the bonus draw, CTA r owns a
-// contiguous chunk of the vocabulary: it computes the residual masses of its
-// chunk into shared memory; every CTA pushes its chunk sum into all CTAs'
-// shared memory; the CTA whose chunk holds the target finds the token (warp
-// sums, then one warp scan over per-lane pieces) and writes the request's
-// outputs.
+// builds the children lists (warp ballots) and each child's fixed-point mass in
+// parallel, and its warp 0 walks the tree, testing a node's children as one warp
+// (integer work only).  For the bonus draw, CTA r owns a contiguous chunk of the
+// vocabulary, staged by a bulk copy (the root's row is staged speculatively while
+// the tree is walked): it computes the residual masses of its chunk into shared
+// memory; every CTA sends its chunk sum to all CTAs as asynchronous stores; the
+// CTA whose chunk holds the target finds the token (warp sums, then one warp scan
+// over per-lane pieces) and writes the request's outputs.
 //
 // accept_sampled_kernel (spec_accept_sampled) serves children that were drawn
 // from the draft distribution: the acceptance probability is the page's
@@ -115,6 +116,108 @@ __device__ int cluster_inverse_cdf(cg::cluster_group& cluster, const unsigned lo
   return found < 0 ? 0 : found;
 }
 
+// Children lists in CSR form, children of u (the nodes c > u with parent u) in
+// ascending flat order: counts by warp ballots (warp w takes nodes w, w + nw, ...),
+// offsets by one warp scan, then the lists.  Every thread of the CTA calls it;
+// s_par is complete and visible on entry, the lists are on return.
+__device__ void build_children(int R, const int* s_par, int* s_nch, int* s_first, int* s_child) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int u = warp; u < R; u += nw) {
+    int cnt = 0;
+    for (int c0 = 0; c0 < R; c0 += 32) {
+      const int c = c0 + lane;
+      cnt += __popc(__ballot_sync(0xFFFFFFFFu, c < R && c > u && s_par[c] == u));
+    }
+    if (lane == 0) s_nch[u] = cnt;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0;
+    for (int u0 = 0; u0 < R; u0 += 32) {
+      const int u = u0 + lane;
+      const int v = u < R ? s_nch[u] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (u < R) s_first[u] = run + incl - v;
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) s_first[R] = run;
+  }
+  __syncthreads();
+  for (int u = warp; u < R; u += nw) {
+    int base = s_first[u];
+    for (int c0 = 0; c0 < R; c0 += 32) {
+      const int c = c0 + lane;
+      const bool is = c < R && c > u && s_par[c] == u;
+      const unsigned bal = __ballot_sync(0xFFFFFFFFu, is);
+      if (is) s_child[base + __popc(bal & ((1u << lane) - 1u))] = c;
+      base += __popc(bal);
+    }
+  }
+  __syncthreads();
+}
+
+// Shared-memory and cluster helpers of accept_kernel.
+__device__ __forceinline__ uint32_t sh_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void acc_bar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sh_addr(b)), "r"(n));
+}
+__device__ __forceinline__ void acc_bar_expect(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sh_addr(b)), "r"(bytes) : "memory");
+}
+// bounded wait (acquire at cluster scope) for the phase of parity par of a local mbarrier
+__device__ __forceinline__ bool acc_bar_wait(uint64_t* b, uint32_t par) {
+  uint64_t t0 = 0;
+  for (int i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(sh_addr(b)), "r"(par)
+        : "memory");
+    if (ok) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    if (i == 0) t0 = t;
+    if (t - t0 > 1000000000ull) return false;
+  }
+}
+// 8 bytes into CTA `rank`'s shared memory at the same offset as p, completing on
+// that CTA's mbarrier at the same offset as bar (the sender does not wait)
+__device__ __forceinline__ void acc_st_async64(const void* p, uint64_t v, const uint64_t* bar, uint32_t rank) {
+  uint32_t a, m;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(sh_addr(p)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(m) : "r"(sh_addr(bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(a), "l"(v), "r"(m)
+               : "memory");
+}
+
+// Dynamic shared memory of accept_kernel for chunks of `per` tokens: residual
+// masses (u64), the bonus row's logits (fp32) and a removed-token bit per token.
+size_t accept_smem_bytes(int per) {
+  const size_t q = (static_cast<size_t>(per) * 8 + 15) & ~static_cast<size_t>(15);
+  const size_t z = (static_cast<size_t>(per) * 4 + 15) & ~static_cast<size_t>(15);
+  return q + z + static_cast<size_t>((per + 31) / 32) * 4 + 16;
+}
+
+// One cluster of CL CTAs per request; CTA r owns vocabulary chunk r.
+//   1. The tree, every node's statistics and uniforms go to shared memory; each
+//      child's mass under its parent's row is fetched (one load per child); the
+//      children lists are built with warp ballots.  While this happens, a bulk
+//      copy stages the root row's chunk (the bonus row when nothing is accepted).
+//   2. Warp 0 walks the tree.  At node u the children are tested in order as one
+//      warp: child c is accepted iff (u_acc[c] * Rm_c) >> 32 < q_c with Rm_c = Q_u
+//      minus the masses of the valid siblings before it (they were rejected); the
+//      first passing child wins, so the serial rule is reproduced exactly.
+//   3. Sampled rows: the bonus row's chunk (staged, re-staged if the walk left the
+//      root) becomes residual masses (removed tokens zero), summed per warp; the
+//      chunk sums travel to every CTA as asynchronous stores; the CTA and warp
+//      whose tokens hold x find the token.
 __global__ void __launch_bounds__(kAcceptThreads)
 accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ parent, int R, int D,
               const float* __restrict__ logits, const float* __restrict__ row_max,
@@ -126,24 +229,61 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
   const int b = blockIdx.x / CL;
-  extern __shared__ unsigned long long qbuf[];  // residual masses of this CTA's chunk
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int per = (V + CL - 1) / CL;
+  const int j0 = min(V, rank * per), j1 = min(V, j0 + per);
+  const int n = j1 - j0;
+  const int nwords = (per + 31) >> 5;
+  extern __shared__ __align__(16) unsigned char acc_dyn[];
+  unsigned long long* qbuf = reinterpret_cast<unsigned long long*>(acc_dyn);  // [per] residual masses
+  float* zbuf = reinterpret_cast<float*>(acc_dyn + ((static_cast<size_t>(per) * 8 + 15) & ~static_cast<size_t>(15)));
+  uint32_t* rbits = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(zbuf) +
+                                                ((static_cast<size_t>(per) * 4 + 15) & ~static_cast<size_t>(15)));
   __shared__ int s_tok[kMaxR], s_par[kMaxR], s_nch[kMaxR], s_first[kMaxR + 1], s_child[kMaxR];
   __shared__ unsigned long long s_qc[kMaxR];  // mass of child c under its parent's row
+  __shared__ unsigned long long s_nQ[kMaxR];
+  __shared__ float s_nmax[kMaxR];
+  __shared__ int s_nam[kMaxR];
+  __shared__ uint32_t s_ua[kMaxR], s_ub[kMaxR];
   __shared__ int s_removed[kMaxR];
   __shared__ int s_path[E3_MAX_DEPTH + 1];
   __shared__ int s_nrem, s_u, s_acc, s_err, s_bonus;
   __shared__ unsigned long long s_x, s_sums[kMaxCluster];
   __shared__ unsigned long long s_wsum[kAcceptThreads / 32];
-  __shared__ float s_nmax[kMaxR];  // every node's row statistics, loaded in parallel
-  __shared__ int s_nam[kMaxR];
-  __shared__ unsigned long long s_nQ[kMaxR];
-  __shared__ uint32_t s_ua[kMaxR];  // every child's acceptance uniform (the walk is serial)
+  __shared__ uint64_t ld_bar, sum_bar;
 
+  if (threadIdx.x == 0) {
+    acc_bar_init(&ld_bar, 1);
+    acc_bar_init(&sum_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    acc_bar_expect(&sum_bar, static_cast<uint32_t>(CL) * 8u);  // every CTA's chunk sum
+  }
+  __syncthreads();
+  // the peers' mbarriers are initialized before anyone stores to them (waited for
+  // just before the first asynchronous store)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
   pdl_wait();
   pdl_trigger();
   const size_t rb = static_cast<size_t>(b) * R;
   const float T = temp[b];
   const float it = inv_temp(T);
+  // chunk staging: bulk copies of 16-byte multiples when the rows allow it (the last
+  // n % 4 logits, or all of them otherwise, by plain loads)
+  const bool bulk = (V % 4) == 0 && (per % 4) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0;
+  const uint32_t bulk_bytes = bulk ? static_cast<uint32_t>(n / 4) * 16u : 0u;
+  auto stage_row = [&](int u) {  // thread 0: chunk of row u into zbuf, completing on ld_bar
+    acc_bar_expect(&ld_bar, bulk_bytes);
+    const unsigned char* src = reinterpret_cast<const unsigned char*>(logits + (rb + u) * V + j0);
+    for (uint32_t off = 0; off < bulk_bytes; off += 32768u) {
+      const uint32_t nb = min(32768u, bulk_bytes - off);
+      asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                       sh_addr(reinterpret_cast<unsigned char*>(zbuf) + off)),
+                   "l"(src + off), "r"(nb), "r"(sh_addr(&ld_bar))
+                   : "memory");
+    }
+  };
+  const bool spec_root = T > 0.0f && bulk && bulk_bytes > 0;
+  if (threadIdx.x == 0 && spec_root) stage_row(0);
   for (int i = threadIdx.x; i < R; i += blockDim.x) {
     s_tok[i] = tok[rb + i];
     s_par[i] = parent[rb + i];
@@ -151,131 +291,221 @@ accept_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ paren
     s_nam[i] = row_argmax[rb + i];
     s_nQ[i] = row_Q[rb + i];
     s_ua[i] = u_acc[rb + i];
+    s_ub[i] = u_bonus[rb + i];
   }
-  __syncthreads();
-  // children lists in CSR form (children in ascending flat order) and child masses
-  for (int u = threadIdx.x; u < R; u += blockDim.x) {
-    int n = 0;
-    for (int c = u + 1; c < R; ++c) n += (s_par[c] == u);
-    s_nch[u] = n;
-  }
-  __syncthreads();
+  for (int w = threadIdx.x; w < nwords; w += blockDim.x) rbits[w] = 0u;
   if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int u = 0; u < R; ++u) {
-      s_first[u] = acc;
-      acc += s_nch[u];
-    }
-    s_first[R] = acc;
-    s_err = 0;
     s_bonus = -1;
     s_path[0] = 0;
   }
   __syncthreads();
-  for (int c = threadIdx.x; c < R; c += blockDim.x) {
-    const int p = s_par[c];
-    s_qc[c] = 0ull;
-    if (c == 0 || p < 0 || p >= c) continue;  // root, or not a forward edge
-    int rk = 0;
-    for (int c2 = p + 1; c2 < c; ++c2) rk += (s_par[c2] == p);
-    s_child[s_first[p] + rk] = c;
-    const int t = s_tok[c];
-    if (T > 0.0f && t >= 0 && t < V) {
-      const size_t prow = rb + p;
-      s_qc[c] = fx_mass(__fmul_rn(logits[prow * V + t], it), s_nmax[p]);
-    }
-  }
+  // each child's mass under its parent's row: thread c requests its logit now (one
+  // global load per child, R <= blockDim.x) and uses it after the children lists
+  const int c_me = threadIdx.x;
+  const int p_me = c_me < R ? s_par[c_me] : -1;
+  const int t_me = c_me < R ? s_tok[c_me] : -1;
+  const bool has_q = c_me > 0 && c_me < R && p_me >= 0 && p_me < c_me && T > 0.0f && t_me >= 0 && t_me < V;
+  const float z_me = has_q ? logits[(rb + p_me) * V + t_me] : 0.0f;
+  build_children(R, s_par, s_nch, s_first, s_child);
+  if (c_me < R) s_qc[c_me] = has_q ? fx_mass(__fmul_rn(z_me, it), s_nmax[p_me]) : 0ull;
   __syncthreads();
-  // the walk (every CTA of the cluster does it; integer work only)
-  if (threadIdx.x == 0) {
-    int u = 0, a = 0, nrem = 0;
+  // the walk (warp 0 of every CTA; integer work only)
+  if (warp == 0) {
+    int u = 0, a = 0, nrem = 0, err = 0, bonus = -1;
     uint64_t Rm = 0;
     for (;;) {
       const float m = s_nmax[u];
       const int am = s_nam[u];
       if (am < 0 || !isfinite(m)) {
-        s_err = E3_DEV_ERR_NONFINITE;
+        err = E3_DEV_ERR_NONFINITE;
         break;
       }
       Rm = s_nQ[u];
       nrem = 0;
       int accepted = -1;
-      for (int e = s_first[u]; e < s_first[u] + s_nch[u]; ++e) {
-        const int c = s_child[e];
-        const int t = s_tok[c];
+      const int e0 = s_first[u], ne = s_nch[u];
+      for (int eb = 0; eb < ne; eb += 32) {  // the children in order, 32 at a time
+        const int e = eb + lane;
+        const bool in = e < ne;
+        const int c = in ? s_child[e0 + e] : 0;
+        const int t = in ? s_tok[c] : -1;
+        bool pass, valid = false;
+        uint64_t q = 0ull;
         if (T <= 0.0f) {
-          if (t == am) {
-            accepted = c;
-            break;
+          pass = in && t == am;
+        } else {
+          valid = in && t >= 0 && t < V;
+          q = valid ? s_qc[c] : 0ull;
+          uint64_t incl = q;  // masses of the valid children up to this one
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
           }
-          continue;
+          pass = valid && mulhi32(s_ua[c], Rm - (incl - q)) < q;
         }
-        if (t < 0 || t >= V) continue;
-        const uint64_t q = s_qc[c];
-        if (mulhi32(s_ua[c], Rm) < q) {
-          accepted = c;
+        const unsigned pb = __ballot_sync(0xFFFFFFFFu, pass);
+        const int first = pb ? __ffs(pb) - 1 : 32;
+        // the valid children before the first acceptance were rejected: they leave
+        // the residual
+        const bool rej = valid && lane < first;
+        const unsigned rb_mask = __ballot_sync(0xFFFFFFFFu, rej);
+        if (rej) s_removed[nrem + __popc(rb_mask & ((1u << lane) - 1u))] = t;
+        Rm -= warp_reduce(rej ? q : 0ull, SumU64());
+        nrem += __popc(rb_mask);
+        if (pb) {
+          accepted = __shfl_sync(0xFFFFFFFFu, c, first);
           break;
         }
-        Rm -= q;
-        s_removed[nrem++] = t;
       }
       if (accepted >= 0 && a < D) {
         ++a;
-        s_path[a] = accepted;
+        if (lane == 0) s_path[a] = accepted;
         u = accepted;
         continue;
       }
-      if (T <= 0.0f) s_bonus = am;
+      if (T <= 0.0f) bonus = am;
       break;
     }
-    s_u = u;
-    s_acc = a;
-    s_nrem = nrem;
-    s_x = (T > 0.0f) ? mulhi32(u_bonus[rb + u], Rm) : 0ull;
+    if (lane == 0) {
+      s_u = u;
+      s_acc = a;
+      s_nrem = nrem;
+      s_err = err;
+      if (bonus >= 0) s_bonus = bonus;
+      s_x = (T > 0.0f) ? mulhi32(s_ub[u], Rm) : 0ull;
+    }
   }
   __syncthreads();
   const int err = s_err;
   int writer = 0;  // the CTA that writes this request's outputs
   const bool sampled = !err && T > 0.0f;  // uniform across the cluster
+  bool ok = true;
   if (sampled) {
     const int u = s_u;
     const uint64_t x = s_x;
-    const size_t row = rb + u;
     const float m = s_nmax[u];
-    const float* z = logits + row * V;
-    const int per = (V + CL - 1) / CL;
-    const int j0 = min(V, rank * per), j1 = min(V, j0 + per);
-    const int n = j1 - j0;
-    // residual masses of the chunk (removed tokens zeroed) and the chunk sum
-#pragma unroll 4
-    for (int j = threadIdx.x; j < n; j += blockDim.x) qbuf[j] = fx_mass(__fmul_rn(z[j0 + j], it), m);
+    const int nrem = s_nrem;
+    for (int i = threadIdx.x; i < nrem; i += blockDim.x) {
+      const int t = s_removed[i];
+      if (t >= j0 && t < j1) atomicOr(&rbits[(t - j0) >> 5], 1u << ((t - j0) & 31));
+    }
+    // the bonus row's chunk: the staged root row, or row u staged now
+    if (bulk && bulk_bytes > 0) {
+      if (threadIdx.x == 0 && u != 0) {
+        ok = acc_bar_wait(&ld_bar, 0);  // the root row's copy has landed before zbuf is reused
+        stage_row(u);
+      }
+      ok = __syncthreads_and(ok) && acc_bar_wait(&ld_bar, u != 0 ? 1u : 0u);
+    }
+    const float* z = logits + (rb + u) * V + j0;
+    for (int j = static_cast<int>(bulk_bytes / 4) + threadIdx.x; j < n; j += blockDim.x) zbuf[j] = z[j];
+    ok = __syncthreads_and(ok);
+    // residual masses of warp w's contiguous segment of the chunk, two tokens at a time
+    const int wseg = (n + nw - 1) / nw;
+    const int a0 = min(n, warp * wseg), a1 = min(n, a0 + wseg);
+    uint64_t local = 0;
+    for (int j = a0 + lane; j < a1; j += 128) {  // four tokens per lane and step, two exponentials at a time
+      float x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[i] = j + 32 * i < a1 ? __fsub_rn(__fmul_rn(zbuf[j + 32 * i], it), m) : -INFINITY;
+      const float2 e01 = fx_exp_x2(make_float2(x[0], x[1])), e23 = fx_exp_x2(make_float2(x[2], x[3]));
+      const float e[4] = {e01.x, e01.y, e23.x, e23.y};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int jj = j + 32 * i;
+        if (jj < a1) {
+          const uint64_t q = ((rbits[jj >> 5] >> (jj & 31)) & 1u) ? 0ull : fx_scale40_floor(e[i]);
+          qbuf[jj] = q;
+          local += q;
+        }
+      }
+    }
+    local = warp_reduce(local, SumU64());
+    if (lane == 0) s_wsum[warp] = local;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int i = 0; i < s_nrem; ++i) {
-        const int t = s_removed[i];
-        if (t >= j0 && t < j1) qbuf[t - j0] = 0ull;
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // the peers' mbarriers are initialized
+    if (warp == 0) {
+      uint64_t tot = lane < nw ? s_wsum[lane] : 0ull;
+      tot = warp_reduce(tot, SumU64());
+      if (lane < CL) acc_st_async64(&s_sums[rank], tot, &sum_bar, static_cast<uint32_t>(lane));
+    }
+    ok = acc_bar_wait(&sum_bar, 0) && ok;
+    // the chunk sums partition [0, total): the CTA, then the warp, then the lane
+    // piece whose masses hold x
+    uint64_t excl = 0;
+    int found = -1;
+    for (int r = 0; r < CL; ++r) {
+      const uint64_t sr = s_sums[r];
+      if (found < 0 && x >= excl && x < excl + sr) found = r;
+      excl += sr;
+    }
+    if (ok && found == rank) {
+      uint64_t wex = 0;
+      for (int r = 0; r < rank; ++r) wex += s_sums[r];
+      for (int i = 0; i < warp; ++i) wex += s_wsum[i];
+      if (x >= wex && x < wex + s_wsum[warp]) {  // uniform within the warp
+        // lane pieces of the segment: the piece holding x by one warp scan of the
+        // piece sums, then the token by one warp scan of that piece's masses (in
+        // steps of 32 tokens)
+        const int sub = (a1 - a0 + 31) >> 5;
+        const int b0 = min(a1, a0 + lane * sub), b1 = min(a1, b0 + sub);
+        uint64_t part = 0;
+#pragma unroll 4
+        for (int j = b0; j < b1; ++j) part += qbuf[j];
+        uint64_t incl = part;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const unsigned hit = __ballot_sync(0xFFFFFFFFu, wex + incl > x);
+        if (hit) {
+          const int L = __ffs(hit) - 1;
+          const int pb0 = __shfl_sync(0xFFFFFFFFu, b0, L), pb1 = __shfl_sync(0xFFFFFFFFu, b1, L);
+          uint64_t cum = __shfl_sync(0xFFFFFFFFu, wex + incl - part, L);  // mass before the piece
+          for (int q0 = pb0; q0 < pb1; q0 += 32) {
+            const int j = q0 + lane;
+            const uint64_t v = j < pb1 ? qbuf[j] : 0ull;
+            uint64_t ci = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+              if (lane >= o) ci += y;
+            }
+            const unsigned h2 = __ballot_sync(0xFFFFFFFFu, j < pb1 && cum + ci > x);
+            if (h2) {
+              if (lane == __ffs(h2) - 1) s_bonus = j0 + j;
+              break;
+            }
+            cum += __shfl_sync(0xFFFFFFFFu, ci, 31);
+          }
+        }
       }
     }
     __syncthreads();
-    writer = cluster_inverse_cdf(cluster, qbuf, n, j0, x, s_wsum, s_sums, &s_bonus);
+    writer = found < 0 ? 0 : found;
+  } else {
+    if (spec_root && threadIdx.x == 0) ok = acc_bar_wait(&ld_bar, 0);  // the root copy lands before exit
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
   }
   if (rank == writer && threadIdx.x == 0) {
-    const int a = err ? 0 : s_acc;
+    const int e = err ? err : (ok ? 0 : E3_DEV_ERR_TIMEOUT);
+    const int a = e ? 0 : s_acc;
     const size_t o = static_cast<size_t>(b) * (D + 1);
     for (int j = 0; j <= D; ++j) {
-      path[o + j] = (!err && j <= a) ? s_path[j] : -1;
+      path[o + j] = (!e && j <= a) ? s_path[j] : -1;
       out_tok[o + j] = -1;
     }
-    if (err) {
+    if (e) {
       path[o] = 0;
     } else {
       for (int j = 1; j <= a; ++j) out_tok[o + j - 1] = s_tok[s_path[j]];
       out_tok[o + a] = s_bonus;
     }
     acc_len[b] = a;
-    status[b] = err;
+    status[b] = e;
   }
-  cluster.sync();  // peers may still read this CTA's chunk sum
 }
 
 // Children drawn from the draft distribution q (eagle3_expand_sampled): accept
@@ -356,33 +586,14 @@ accept_sampled_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict
   for (int w = threadIdx.x; w < nwords; w += blockDim.x) rbits[w] = 0u;
   __syncthreads();
   // children lists in CSR form, children in ascending flat order (= draw order)
-  for (int u = threadIdx.x; u < R; u += blockDim.x) {
-    int cnt = 0;
-    for (int c = u + 1; c < R; ++c) cnt += (s_par[c] == u);
-    s_nch[u] = cnt;
-  }
-  __syncthreads();
   if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int u = 0; u < R; ++u) {
-      s_first[u] = acc;
-      acc += s_nch[u];
-    }
-    s_first[R] = acc;
     s_err = 0;
     s_bonus = -1;
     s_path[0] = 0;
     s_u = 0;
     s_a = 0;
   }
-  __syncthreads();
-  for (int c = threadIdx.x; c < R; c += blockDim.x) {
-    const int p = s_par[c];
-    if (c == 0 || p < 0 || p >= c) continue;
-    int rk = 0;
-    for (int c2 = p + 1; c2 < c; ++c2) rk += (s_par[c2] == p);
-    s_child[s_first[p] + rk] = c;
-  }
+  build_children(R, s_par, s_nch, s_first, s_child);
   for (int c = threadIdx.x; c < R; c += blockDim.x) {
     s_Dc[c] = 0ull;
     s_Rc[c] = 0ull;
@@ -582,14 +793,20 @@ accept_sampled_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict
   cluster.sync();  // peers may still read this CTA's shared memory
 }
 
-int accept_cluster_size() {
-  static const int cl_once = [] {  // computed once, thread-safely
-    int cl = 8;
+// 16-CTA clusters of accept_kernel where the GPU allows them (for this vocabulary's
+// shared memory), else 8.
+int accept_cluster_size(int V) {
+  static std::mutex mu;  // the cache below is read and refreshed as a unit
+  const std::lock_guard<std::mutex> lock(mu);
+  static int cached_v = -1, cl = 8;
+  if (cached_v != V) {
+    cl = 8;
+    cached_v = V;
     if (cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(16);
       cfg.blockDim = dim3(kAcceptThreads);
-      cfg.dynamicSmemBytes = 72 * 1024;
+      cfg.dynamicSmemBytes = accept_smem_bytes((V + 15) / 16);
       cudaLaunchAttribute at;
       at.id = cudaLaunchAttributeClusterDimension;
       at.val.clusterDim.x = 16;
@@ -601,9 +818,8 @@ int accept_cluster_size() {
       if (cudaOccupancyMaxActiveClusters(&n, accept_kernel, &cfg) == cudaSuccess && n > 0) cl = 16;
     }
     cudaGetLastError();
-    return cl;
-  }();
-  return cl_once;
+  }
+  return cl;
 }
 
 // 16-CTA clusters of accept_sampled_kernel where the GPU allows them, else 8.
@@ -667,8 +883,8 @@ e3_status launch_accept(const int32_t* tok, const int32_t* parent, int B, int R,
   static const bool attr_done =
       (cudaFuncSetAttribute(accept_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024), true);
   (void)attr_done;
-  const int CL = accept_cluster_size();
-  const size_t smem = static_cast<size_t>((V + CL - 1) / CL) * sizeof(unsigned long long) + 16;
+  const int CL = accept_cluster_size(V);
+  const size_t smem = accept_smem_bytes((V + CL - 1) / CL);
   E3_REQUIRE(smem <= 200 * 1024, E3_ERR_SHAPE, "spec_accept: V=%d too large", V);
   E3_REQUIRE(static_cast<long>(B) * CL < (1L << 31), E3_ERR_SHAPE, "spec_accept: B=%d too large", B);
   cudaError_t e = launch_pdl(accept_kernel, dim3(B * CL), dim3(kAcceptThreads), smem, s, static_cast<unsigned>(CL), tok,
