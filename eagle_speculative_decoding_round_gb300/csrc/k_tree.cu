@@ -74,8 +74,18 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
   if (i < E3_MAX_DEPTH + 2) cnt[i] = 0;
   const int P = kv_len[b];
   uint64_t top;  // (thread i < N) the i-th best candidate key
+  // (one key per thread) this thread's candidate's depth, parent and token, requested
+  // with its score and kept in registers through the sort; after it, the kept nodes
+  // read them from shared memory instead of global memory
+  int pre_d = 0, pre_p = -1, pre_t = 0;
   if (per_thread) {
-    const uint64_t v = i < n_cand ? pack_best(c.score[cb + i], static_cast<uint32_t>(i)) : 0ull;
+    uint64_t v = 0ull;
+    if (i < n_cand) {
+      v = pack_best(c.score[cb + i], static_cast<uint32_t>(i));
+      pre_d = c.depth[cb + i];
+      pre_p = c.parent[cb + i];
+      pre_t = c.tok[cb + i];
+    }
     top = bitonic_desc_thread(v, keys);
   } else {
     for (int q = i; q < np; q += blockDim.x)
@@ -84,13 +94,30 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
     block_bitonic_desc(keys, np);
     top = i < np ? keys[i] : 0ull;
   }
-  // the kept nodes' candidate data, loaded once
+  // the kept nodes' candidate data: staged in shared memory by the candidates' own
+  // threads (per-thread sort: the exchange buffers are free again), else from global
+  int* cdat = reinterpret_cast<int*>(keys);  // [3][n_cand] (needs 12 n_cand <= 16 max(np, blockDim) bytes)
+  if (per_thread) {
+    __syncthreads();  // every thread is done with the sort's exchange buffers
+    if (i < n_cand) {
+      cdat[i] = pre_d;
+      cdat[n_cand + i] = pre_p;
+      cdat[2 * n_cand + i] = pre_t;
+    }
+    __syncthreads();
+  }
   int my_c = -1, my_d = 0, my_p = -1, my_tok = 0;
   if (i < N) {
     my_c = static_cast<int>(packed_id(top));
-    my_d = c.depth[cb + my_c];
-    my_p = c.parent[cb + my_c];
-    my_tok = c.tok[cb + my_c];
+    if (per_thread) {
+      my_d = cdat[my_c];
+      my_p = cdat[n_cand + my_c];
+      my_tok = cdat[2 * n_cand + my_c];
+    } else {
+      my_d = c.depth[cb + my_c];
+      my_p = c.parent[cb + my_c];
+      my_tok = c.tok[cb + my_c];
+    }
     if (my_p >= n_cand) my_p = -1;  // malformed parent: hang the node off the root
     if (my_d < 1) my_d = 1;
     if (my_d > E3_MAX_DEPTH) my_d = E3_MAX_DEPTH;
@@ -125,6 +152,7 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
     if (i < N && my_d == d) {
       const int mine = (my_pf << 12) | my_c;
       int rank = 0;
+#pragma unroll 8
       for (int j = 0; j < N; ++j) rank += kkey[j] < mine;
       my_fl = base[d] + rank;
       flat_of[my_c] = static_cast<int16_t>(my_fl);
