@@ -377,6 +377,52 @@ def test_accept_bitexact(B, R, D, V):
         assert host(st)[b] == 0
 
 
+def test_accept_wide_nodes():
+    """Nodes with more children than a warp has lanes (the walk tests a node's children 32
+    at a time): the root has 40 children (the first the most likely token, the rest from
+    the least to the most likely of the next 39), its first child 33 children (from the
+    least to the most likely, so the greedy match is the 33rd, beyond the first 32).
+    Bit-exact against the oracle."""
+    R, D, V = 1 + 40 + 33 + 3, 3, 2000
+    parent = np.full(R, -1, np.int32)
+    parent[1:41] = 0
+    parent[41:74] = 1
+    parent[74:77] = 41
+    B = 16
+    temps = np.array([[0.0, 1.0, 0.7, 1.5][b % 4] for b in range(B)], np.float32)
+    rng = np.random.default_rng(31)
+    z = (rng.standard_normal((B * R, V)) * 2.0).astype(np.float32)
+    toks = np.zeros((B, R), np.int32)
+    for b in range(B):
+        zb = z[b * R:(b + 1) * R]
+        for u in range(R):
+            kids = [c for c in range(R) if parent[c] == u]
+            if kids:
+                top = np.argsort(-zb[u], kind="stable")[:len(kids)]
+                order = np.concatenate([top[:1], top[1:][::-1]]) if u == 0 else top[::-1]
+                for c, t in zip(kids, order):
+                    toks[b, c] = t
+    par = np.tile(parent, (B, 1))
+    logits, rmax, rQ, ram, err = gpu_stats(z, np.arange(B * R), np.repeat(temps, R))
+    ua = synth.uniforms(B + R + 1, synth.PURPOSE_ACCEPT, B, R)
+    ub = synth.uniforms(B + R + 1, synth.PURPOSE_BONUS, B, R)
+    acc, path, out, st = i32(B), i32((B, D + 1)), i32((B, D + 1)), i32(B)
+    e3.spec_accept(to_dev(toks), to_dev(par), B, R, D, logits, rmax, rQ, ram, V, to_dev(temps),
+                   to_dev(ua.view(np.int32)), to_dev(ub.view(np.int32)), e3.E3_ACCEPT_TREE_DET, acc, path, out, st)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    zl = host(logits)
+    deep = 0
+    for b in range(B):
+        a, pth, o = oracle.accept({"tok": toks[b], "parent": par[b]}, zl[b * R:(b + 1) * R], temps[b], ua[b], ub[b], D)
+        assert host(acc)[b] == a, b
+        assert np.array_equal(host(path)[b], pth), b
+        assert np.array_equal(host(out)[b], o), b
+        assert host(st)[b] == 0
+        deep += a >= 2
+    assert deep > 0  # the greedy walks accept node 1's 33rd child
+
+
 def test_accept_sampling_lossless_on_gpu():
     """Chi-square losslessness run on the GPU: 200k independent requests with the
     same tree and logits, fresh uniforms each."""
