@@ -7,13 +7,17 @@
 // "SpecForge…", 从序列到动态草稿树: the node budget goes to the most confident
 // candidates.
 //
-// One CTA per request: bitonic sort of the candidate keys (score desc, index
-// asc), one key per thread in registers (shuffles within a warp, shared memory
-// across warps); the first N are kept.  Flat indices are assigned depth by
-// depth with a parallel rank count on (parent's flat index, candidate index);
-// each mask row is the OR of the bits on its ancestor walk.  Optionally the
-// candidate index of every flat node is written (node_cand), which is how the
-// sampled accept finds the draft row a node's children were drawn from.
+// One CTA per request.  Selection: with one key per thread (up to 1024
+// candidates) each warp sorts its 32 keys (score desc, index asc) through
+// shuffles, and a key's rank among all candidates is its lane plus, for every
+// other warp's sorted list, a binary-searched count of the keys above it; the
+// keys of rank < N are kept.  Beyond 1024 candidates a shared-memory bitonic
+// sort over 1024 threads orders them.  Flattening runs depth by depth on the
+// warps that hold the N kept nodes: each level's nodes (bucketed by depth) are
+// ranked by (parent's flat index, candidate index), and each node's mask row is
+// its parent's row plus its own bit.  Optionally the candidate index of every
+// flat node is written (node_cand), which is how the sampled accept finds the
+// draft row a node's children were drawn from.
 #include <algorithm>
 
 #include "e3_common.cuh"
@@ -25,30 +29,36 @@ namespace {
 
 constexpr int kTreeThreads = 256;  // at least E3_MAX_NODES + 1 (one thread per flat row)
 
-// Descending bitonic sort of n = blockDim.x keys (a power of two, <= 1024), one
-// key per thread: partners within a warp exchange through shuffles, the others
-// through two alternating shared-memory buffers (one barrier per such step).
-__device__ __forceinline__ uint64_t bitonic_desc_thread(uint64_t v, uint64_t* buf /* [2][n] */) {
-  const int n = blockDim.x, tid = threadIdx.x;
-  int flip = 0;
-  for (int kk = 2; kk <= n; kk <<= 1) {
+// Descending bitonic sort of the 32 keys of a warp, one per lane, through shuffles.
+__device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
     for (int j = kk >> 1; j > 0; j >>= 1) {
-      uint64_t o;
-      if (j >= 32) {
-        uint64_t* b = buf + flip * n;
-        b[tid] = v;
-        __syncthreads();
-        o = b[tid ^ j];
-        flip ^= 1;
-      } else {
-        o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
-      }
-      const bool lower = (tid & j) == 0;  // the lower index of the pair keeps the larger key...
-      const bool desc = (tid & kk) == 0;  // ...in the descending halves of the merge
+      const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
+      const bool lower = (lane & j) == 0;  // the lower lane of the pair keeps the larger key...
+      const bool desc = (lane & kk) == 0;  // ...in the descending halves of the merge
       v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
     }
   }
   return v;
+}
+
+// Number of keys above x in a descending list of 32 (binary search: the keys above
+// x form a prefix of the list).
+__device__ __forceinline__ int count_above32(const uint64_t* L, uint64_t x) {
+  int c = L[15] > x ? 16 : 0;
+  c += L[c + 7] > x ? 8 : 0;
+  c += L[c + 3] > x ? 4 : 0;
+  c += L[c + 1] > x ? 2 : 0;
+  c += L[c] > x ? 1 : 0;
+  c += (c == 31 && L[31] > x) ? 1 : 0;
+  return c;
+}
+
+__device__ __forceinline__ void sync_first(int nthreads) {  // barrier 1 over the first nthreads threads
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
 __global__ void __launch_bounds__(1024)
@@ -56,118 +66,122 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
                   const int32_t* __restrict__ kv_len, int32_t* tok, int32_t* parent, int32_t* depth,
                   int32_t* pos, uint64_t* mask, int32_t* node_cand) {
   extern __shared__ uint64_t sh[];
-  uint64_t* keys = sh;  // [2 * max(np, blockDim.x)]: the two exchange buffers, or the in-place sort
+  __shared__ int sel[E3_MAX_NODES];                      // candidate of the r-th best key
+  __shared__ int nd_c[E3_MAX_NODES], nd_p[E3_MAX_NODES];  // kept node r: candidate, parent candidate
+  __shared__ int nd_t[E3_MAX_NODES], lvl[E3_MAX_NODES];   // token; kept nodes bucketed by depth
+  __shared__ int lkey[E3_MAX_NODES];                      // one level's (parent flat, candidate) keys
+  __shared__ uint64_t rows[E3_MAX_NODES + 1][4];          // ancestor-or-self bit rows by flat index
+  __shared__ int cnt[E3_MAX_DEPTH + 2], base[E3_MAX_DEPTH + 2];
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
+  const int i = threadIdx.x, warp = i >> 5, lane = i & 31;
   int np = 1;
   while (np < n_cand) np <<= 1;
-  const bool per_thread = np <= static_cast<int>(blockDim.x);  // then blockDim.x == np
-  int16_t* flat_of = reinterpret_cast<int16_t*>(keys + 2 * max(np, static_cast<int>(blockDim.x)));  // [n_cand]
-  __shared__ int kkey[E3_MAX_NODES];  // per level: (parent flat index, candidate index) of its nodes
-  __shared__ int pflat[E3_MAX_NODES + 1];
-  __shared__ int cnt[E3_MAX_DEPTH + 2], base[E3_MAX_DEPTH + 2];
-
+  const bool per_thread = np <= static_cast<int>(blockDim.x);  // one key per thread
+  uint64_t* keys = sh;                                          // [max(np, blockDim.x)]
+  int* cdat = reinterpret_cast<int*>(keys + max(np, static_cast<int>(blockDim.x)));  // [3][n_cand] (per_thread)
+  int16_t* flat_of = reinterpret_cast<int16_t*>(cdat + (per_thread ? 3 * n_cand : 0));  // [n_cand]
   const size_t cb = static_cast<size_t>(b) * c.cap;
-  const int i = threadIdx.x;
   for (int q = i; q < n_cand; q += blockDim.x) flat_of[q] = -1;
   if (i < E3_MAX_DEPTH + 2) cnt[i] = 0;
   const int P = kv_len[b];
-  uint64_t top;  // (thread i < N) the i-th best candidate key
-  // (one key per thread) this thread's candidate's depth, parent and token, requested
-  // with its score and kept in registers through the sort; after it, the kept nodes
-  // read them from shared memory instead of global memory
-  int pre_d = 0, pre_p = -1, pre_t = 0;
   if (per_thread) {
-    uint64_t v = 0ull;
+    uint64_t v = 0ull;  // padding keys (0) rank below every candidate's key
     if (i < n_cand) {
       v = pack_best(c.score[cb + i], static_cast<uint32_t>(i));
-      pre_d = c.depth[cb + i];
-      pre_p = c.parent[cb + i];
-      pre_t = c.tok[cb + i];
+      cdat[i] = c.depth[cb + i];
+      cdat[n_cand + i] = c.parent[cb + i];
+      cdat[2 * n_cand + i] = c.tok[cb + i];
     }
-    top = bitonic_desc_thread(v, keys);
+    v = warp_sort_desc(v);
+    keys[i] = v;
+    __syncthreads();
+    if (v != 0ull && lane < N) {
+      const int nl = (n_cand + 31) >> 5;  // warps holding candidates
+      int rank = lane;
+#pragma unroll 4
+      for (int q = 0; q < nl; ++q)
+        if (q != warp) rank += count_above32(keys + 32 * q, v);
+      if (rank < N) sel[rank] = static_cast<int>(packed_id(v));
+    }
   } else {
     for (int q = i; q < np; q += blockDim.x)
       keys[q] = q < n_cand ? pack_best(c.score[cb + q], static_cast<uint32_t>(q)) : 0ull;
     __syncthreads();
     block_bitonic_desc(keys, np);
-    top = i < np ? keys[i] : 0ull;
-  }
-  // the kept nodes' candidate data: staged in shared memory by the candidates' own
-  // threads (per-thread sort: the exchange buffers are free again), else from global
-  int* cdat = reinterpret_cast<int*>(keys);  // [3][n_cand] (needs 12 n_cand <= 16 max(np, blockDim) bytes)
-  if (per_thread) {
-    __syncthreads();  // every thread is done with the sort's exchange buffers
-    if (i < n_cand) {
-      cdat[i] = pre_d;
-      cdat[n_cand + i] = pre_p;
-      cdat[2 * n_cand + i] = pre_t;
-    }
-    __syncthreads();
-  }
-  int my_c = -1, my_d = 0, my_p = -1, my_tok = 0;
-  if (i < N) {
-    my_c = static_cast<int>(packed_id(top));
-    if (per_thread) {
-      my_d = cdat[my_c];
-      my_p = cdat[n_cand + my_c];
-      my_tok = cdat[2 * n_cand + my_c];
-    } else {
-      my_d = c.depth[cb + my_c];
-      my_p = c.parent[cb + my_c];
-      my_tok = c.tok[cb + my_c];
-    }
-    if (my_p >= n_cand) my_p = -1;  // malformed parent: hang the node off the root
-    if (my_d < 1) my_d = 1;
-    if (my_d > E3_MAX_DEPTH) my_d = E3_MAX_DEPTH;
-    atomicAdd(&cnt[my_d], 1);
+    if (i < N) sel[i] = static_cast<int>(packed_id(keys[i]));
   }
   __syncthreads();
+  // from here on only the warps of the N kept nodes and the root row take part
+  const int nthr = ((N + 1 + 31) >> 5) << 5;
+  if (i >= nthr) return;
+  int my_d = 0, lpos = 0;
+  if (i < N) {
+    const int cc = sel[i];
+    int d, p, t;
+    if (per_thread) {
+      d = cdat[cc];
+      p = cdat[n_cand + cc];
+      t = cdat[2 * n_cand + cc];
+    } else {
+      d = c.depth[cb + cc];
+      p = c.parent[cb + cc];
+      t = c.tok[cb + cc];
+    }
+    if (p >= n_cand) p = -1;  // malformed parent: hang the node off the root
+    my_d = min(max(d, 1), E3_MAX_DEPTH);
+    nd_c[i] = cc;
+    nd_p[i] = p;
+    nd_t[i] = t;
+    lpos = atomicAdd(&cnt[my_d], 1);  // position within the level (any order: levels are ranked below)
+  }
+  sync_first(nthr);
   if (i == 0) {
     int acc = 1;
     for (int d = 1; d <= E3_MAX_DEPTH; ++d) {
       base[d] = acc;
       acc += cnt[d];
     }
-    pflat[0] = -1;
+    rows[0][0] = 1ull;
+    rows[0][1] = rows[0][2] = rows[0][3] = 0ull;
   }
-  __syncthreads();
-  // flat indices depth by depth: rank among the level's nodes by (parent's flat
-  // index, candidate index), packed into one integer key (both below 2^12)
-  int my_fl = 0, my_pf = 0;
+  sync_first(nthr);
+  if (i < N) lvl[base[my_d] - 1 + lpos] = i;
+  sync_first(nthr);
+  const int R = N + 1;
+  const int words = (R + 63) >> 6;
+  // flat indices level by level: rank among the level's nodes by (parent's flat
+  // index, candidate index), packed into one integer key (both below 2^12); a
+  // parent not yet flattened (not kept, or not at a smaller depth) counts as the root
   for (int d = 1; d <= E3_MAX_DEPTH; ++d) {
-    if (cnt[d] == 0) continue;  // uniform across the block
-    if (i < N) {
-      int key = 0x7FFFFFFF;
-      if (my_d == d) {
-        int pf = my_p < 0 ? 0 : flat_of[my_p];
-        if (pf < 0) pf = 0;  // parent not kept: cannot happen for expansion scores
-        my_pf = pf;
-        key = (pf << 12) | my_c;
-      }
-      kkey[i] = key;
+    const int n = cnt[d];
+    if (n == 0) continue;  // uniform across the threads taking part
+    int r = 0, pf = 0, key = 0;
+    if (i < n) {
+      r = lvl[base[d] - 1 + i];
+      const int p = nd_p[r];
+      pf = p < 0 ? 0 : flat_of[p];
+      if (pf < 0) pf = 0;
+      key = (pf << 12) | nd_c[r];
+      lkey[i] = key;
     }
-    __syncthreads();
-    if (i < N && my_d == d) {
-      const int mine = (my_pf << 12) | my_c;
+    sync_first(nthr);
+    if (i < n) {
       int rank = 0;
 #pragma unroll 8
-      for (int j = 0; j < N; ++j) rank += kkey[j] < mine;
-      my_fl = base[d] + rank;
-      flat_of[my_c] = static_cast<int16_t>(my_fl);
-      pflat[my_fl] = my_pf;
+      for (int q = 0; q < n; ++q) rank += lkey[q] < key;
+      const int f = base[d] + rank;
+      flat_of[nd_c[r]] = static_cast<int16_t>(f);
+      for (int w = 0; w < words; ++w) rows[f][w] = rows[pf][w] | (w == (f >> 6) ? 1ull << (f & 63) : 0ull);
+      const size_t o = static_cast<size_t>(b) * R + f;
+      tok[o] = nd_t[r];
+      parent[o] = pf;
+      depth[o] = d;
+      pos[o] = P + d;
+      if (node_cand) node_cand[o] = nd_c[r];
     }
-    __syncthreads();
-  }
-  const int R = N + 1;
-  if (i < N) {
-    const size_t o = static_cast<size_t>(b) * R + my_fl;
-    tok[o] = my_tok;
-    parent[o] = my_pf;
-    depth[o] = my_d;
-    pos[o] = P + my_d;
-    if (node_cand) node_cand[o] = my_c;
+    sync_first(nthr);
   }
   if (i == 0) {
     const size_t o = static_cast<size_t>(b) * R;
@@ -177,17 +191,9 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
     pos[o] = P;
     if (node_cand) node_cand[o] = -1;
   }
-  // ancestor-or-self bit rows
-  const int words = (R + 63) >> 6;
   if (i < R) {
-    uint64_t w[4] = {0ull, 0ull, 0ull, 0ull};
-    int j = i;
-    for (int step = 0; step <= E3_MAX_DEPTH && j >= 0; ++step) {
-      w[j >> 6] |= 1ull << (j & 63);
-      j = pflat[j];
-    }
     uint64_t* row = mask + (static_cast<size_t>(b) * R + i) * words;
-    for (int q = 0; q < words; ++q) row[q] = w[q];
+    for (int w = 0; w < words; ++w) row[w] = rows[i][w];
   }
 }
 
@@ -198,11 +204,15 @@ e3_status launch_tree_build(const e3_cand& c, int B, int n_cand, int N, const in
                             int32_t* pos, uint64_t* mask, int32_t* node_cand, cudaStream_t s) {
   int np = 1;
   while (np < n_cand) np <<= 1;
-  // one thread per sort key up to 1024 keys (sorted in registers and shuffles),
-  // else 1024 threads over a shared-memory sort
+  // one thread per key up to 1024 keys (warp sorts and ranks), else 1024 threads
+  // over a shared-memory sort
   const int threads = std::max(kTreeThreads, std::min(np, 1024));
-  const size_t smem = static_cast<size_t>(std::max(np, threads)) * 16 + static_cast<size_t>(n_cand) * 2 + 16;
-  if (smem > 48 * 1024) {
+  const bool per_thread = np <= threads;
+  const size_t smem = static_cast<size_t>(std::max(np, threads)) * 8 + (per_thread ? static_cast<size_t>(n_cand) * 12 : 0) +
+                      static_cast<size_t>(n_cand) * 2 + 16;
+  // the kernel's static arrays: node tables, level keys, ancestor rows, depth counts
+  constexpr size_t kStatic = 6 * sizeof(int) * E3_MAX_NODES + 32 * (E3_MAX_NODES + 1) + 8 * (E3_MAX_DEPTH + 2);
+  if (smem + kStatic > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_status(e, "tree_build_kernel smem attribute");
