@@ -13,9 +13,9 @@
 // other warp's sorted list, a binary-searched count of the keys above it; the
 // keys of rank < N are kept.  Beyond 1024 candidates a shared-memory bitonic
 // sort over 1024 threads orders them.  Flattening runs depth by depth on the
-// warps that hold the N kept nodes: each level's nodes (bucketed by depth) are
-// ranked by (parent's flat index, candidate index), and each node's mask row is
-// its parent's row plus its own bit.  Optionally the candidate index of every
+// warps that hold the N kept nodes, each node on its own thread: a level's nodes
+// are ranked by (parent's flat index, candidate index), and each node's mask row
+// is its parent's row plus its own bit.  Optionally the candidate index of every
 // flat node is written (node_cand), which is how the sampled accept finds the
 // draft row a node's children were drawn from.
 #include <algorithm>
@@ -66,10 +66,8 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
                   const int32_t* __restrict__ kv_len, int32_t* tok, int32_t* parent, int32_t* depth,
                   int32_t* pos, uint64_t* mask, int32_t* node_cand) {
   extern __shared__ uint64_t sh[];
-  __shared__ int sel[E3_MAX_NODES];                      // candidate of the r-th best key
-  __shared__ int nd_c[E3_MAX_NODES], nd_p[E3_MAX_NODES];  // kept node r: candidate, parent candidate
-  __shared__ int nd_t[E3_MAX_NODES], lvl[E3_MAX_NODES];   // token; kept nodes bucketed by depth
-  __shared__ int lkey[E3_MAX_NODES];                      // one level's (parent flat, candidate) keys
+  __shared__ int sel[E3_MAX_NODES];              // candidate of the r-th best key
+  __shared__ int lkey[E3_MAX_NODES];             // one level's (parent flat, candidate) keys
   __shared__ uint64_t rows[E3_MAX_NODES + 1][4];          // ancestor-or-self bit rows by flat index
   __shared__ int cnt[E3_MAX_DEPTH + 2], base[E3_MAX_DEPTH + 2];
   pdl_wait();
@@ -97,14 +95,18 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
     v = warp_sort_desc(v);
     keys[i] = v;
     __syncthreads();
-    if (v != 0ull && lane < N) {
-      const int nl = (n_cand + 31) >> 5;  // warps holding candidates
-      int rank = lane;
-#pragma unroll 4
-      for (int q = 0; q < nl; ++q)
-        if (q != warp) rank += count_above32(keys + 32 * q, v);
-      if (rank < N) sel[rank] = static_cast<int>(packed_id(v));
+    // lists in order; a lane stops once its rank reaches N (candidates of the first
+    // depths, which hold most of the best keys, come first), the warp once all its lanes have
+    const int nl = (n_cand + 31) >> 5;  // warps holding candidates
+    int rank = lane;
+    bool live = v != 0ull && lane < N;
+    for (int q = 0; q < nl && __any_sync(0xFFFFFFFFu, live); ++q) {
+      if (live && q != warp) {
+        rank += count_above32(keys + 32 * q, v);
+        live = rank < N;
+      }
     }
+    if (v != 0ull && rank < N) sel[rank] = static_cast<int>(packed_id(v));
   } else {
     for (int q = i; q < np; q += blockDim.x)
       keys[q] = q < n_cand ? pack_best(c.score[cb + q], static_cast<uint32_t>(q)) : 0ull;
@@ -116,70 +118,68 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
   // from here on only the warps of the N kept nodes and the root row take part
   const int nthr = ((N + 1 + 31) >> 5) << 5;
   if (i >= nthr) return;
-  int my_d = 0, lpos = 0;
+  int my_d = 0, lpos = 0, my_c = 0, my_p = -1, my_t = 0;
   if (i < N) {
-    const int cc = sel[i];
-    int d, p, t;
+    my_c = sel[i];
+    int d;
     if (per_thread) {
-      d = cdat[cc];
-      p = cdat[n_cand + cc];
-      t = cdat[2 * n_cand + cc];
+      d = cdat[my_c];
+      my_p = cdat[n_cand + my_c];
+      my_t = cdat[2 * n_cand + my_c];
     } else {
-      d = c.depth[cb + cc];
-      p = c.parent[cb + cc];
-      t = c.tok[cb + cc];
+      d = c.depth[cb + my_c];
+      my_p = c.parent[cb + my_c];
+      my_t = c.tok[cb + my_c];
     }
-    if (p >= n_cand) p = -1;  // malformed parent: hang the node off the root
+    if (my_p >= n_cand) my_p = -1;  // malformed parent: hang the node off the root
     my_d = min(max(d, 1), E3_MAX_DEPTH);
-    nd_c[i] = cc;
-    nd_p[i] = p;
-    nd_t[i] = t;
     lpos = atomicAdd(&cnt[my_d], 1);  // position within the level (any order: levels are ranked below)
   }
   sync_first(nthr);
   if (i == 0) {
-    int acc = 1;
+    int acc = 1, top = 0;
     for (int d = 1; d <= E3_MAX_DEPTH; ++d) {
       base[d] = acc;
       acc += cnt[d];
+      if (cnt[d] > 0) top = d;
     }
+    cnt[0] = top;  // the deepest level
     rows[0][0] = 1ull;
     rows[0][1] = rows[0][2] = rows[0][3] = 0ull;
   }
   sync_first(nthr);
-  if (i < N) lvl[base[my_d] - 1 + lpos] = i;
-  sync_first(nthr);
   const int R = N + 1;
   const int words = (R + 63) >> 6;
-  // flat indices level by level: rank among the level's nodes by (parent's flat
-  // index, candidate index), packed into one integer key (both below 2^12); a
-  // parent not yet flattened (not kept, or not at a smaller depth) counts as the root
-  for (int d = 1; d <= E3_MAX_DEPTH; ++d) {
+  const int maxd = cnt[0];
+  // flat indices level by level, each node handled by the thread that holds it:
+  // rank among the level's nodes by (parent's flat index, candidate index), packed
+  // into one integer key (both below 2^12); a parent not yet flattened (not kept,
+  // or not at a smaller depth) counts as the root
+  for (int d = 1; d <= maxd; ++d) {
     const int n = cnt[d];
     if (n == 0) continue;  // uniform across the threads taking part
-    int r = 0, pf = 0, key = 0;
-    if (i < n) {
-      r = lvl[base[d] - 1 + i];
-      const int p = nd_p[r];
-      pf = p < 0 ? 0 : flat_of[p];
+    const bool mine = i < N && my_d == d;
+    int pf = 0, key = 0;
+    if (mine) {
+      pf = my_p < 0 ? 0 : flat_of[my_p];
       if (pf < 0) pf = 0;
-      key = (pf << 12) | nd_c[r];
-      lkey[i] = key;
+      key = (pf << 12) | my_c;
+      lkey[lpos] = key;
     }
     sync_first(nthr);
-    if (i < n) {
+    if (mine) {
       int rank = 0;
 #pragma unroll 8
       for (int q = 0; q < n; ++q) rank += lkey[q] < key;
       const int f = base[d] + rank;
-      flat_of[nd_c[r]] = static_cast<int16_t>(f);
+      flat_of[my_c] = static_cast<int16_t>(f);
       for (int w = 0; w < words; ++w) rows[f][w] = rows[pf][w] | (w == (f >> 6) ? 1ull << (f & 63) : 0ull);
       const size_t o = static_cast<size_t>(b) * R + f;
-      tok[o] = nd_t[r];
+      tok[o] = my_t;
       parent[o] = pf;
       depth[o] = d;
       pos[o] = P + d;
-      if (node_cand) node_cand[o] = nd_c[r];
+      if (node_cand) node_cand[o] = my_c;
     }
     sync_first(nthr);
   }
@@ -211,7 +211,7 @@ e3_status launch_tree_build(const e3_cand& c, int B, int n_cand, int N, const in
   const size_t smem = static_cast<size_t>(std::max(np, threads)) * 8 + (per_thread ? static_cast<size_t>(n_cand) * 12 : 0) +
                       static_cast<size_t>(n_cand) * 2 + 16;
   // the kernel's static arrays: node tables, level keys, ancestor rows, depth counts
-  constexpr size_t kStatic = 6 * sizeof(int) * E3_MAX_NODES + 32 * (E3_MAX_NODES + 1) + 8 * (E3_MAX_DEPTH + 2);
+  constexpr size_t kStatic = 2 * sizeof(int) * E3_MAX_NODES + 32 * (E3_MAX_NODES + 1) + 8 * (E3_MAX_DEPTH + 2);
   if (smem + kStatic > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
