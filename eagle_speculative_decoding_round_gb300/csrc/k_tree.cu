@@ -69,7 +69,7 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
   __shared__ int sel[E3_MAX_NODES];              // candidate of the r-th best key
   __shared__ int lkey[E3_MAX_NODES];             // one level's (parent flat, candidate) keys
   __shared__ uint64_t rows[E3_MAX_NODES + 1][4];          // ancestor-or-self bit rows by flat index
-  __shared__ int cnt[E3_MAX_DEPTH + 2], base[E3_MAX_DEPTH + 2];
+  __shared__ int cnt[E3_MAX_DEPTH + 2];
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
@@ -95,14 +95,24 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
     v = warp_sort_desc(v);
     keys[i] = v;
     __syncthreads();
-    // lists in order; a lane stops once its rank reaches N (candidates of the first
-    // depths, which hold most of the best keys, come first), the warp once all its lanes have
+    // lists in order, eight searches at a time (independent chains of loads, taken
+    // without branches: a search outside the lists or of the warp's own list reads a
+    // valid list and counts 0); a lane stops once its rank reaches N (candidates of the
+    // first depths, which hold most of the best keys, come first), the warp once all
+    // its lanes have
     const int nl = (n_cand + 31) >> 5;  // warps holding candidates
     int rank = lane;
     bool live = v != 0ull && lane < N;
-    for (int q = 0; q < nl && __any_sync(0xFFFFFFFFu, live); ++q) {
-      if (live && q != warp) {
-        rank += count_above32(keys + 32 * q, v);
+    for (int q0 = 0; q0 < nl && __any_sync(0xFFFFFFFFu, live); q0 += 8) {
+      if (live) {
+        int add = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int q = q0 + u;
+          const int cq = count_above32(keys + 32 * min(q, nl - 1), v);
+          add += (q < nl && q != warp) ? cq : 0;
+        }
+        rank += add;
         live = rank < N;
       }
     }
@@ -137,43 +147,55 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
   }
   sync_first(nthr);
   if (i == 0) {
-    int acc = 1, top = 0;
-    for (int d = 1; d <= E3_MAX_DEPTH; ++d) {
-      base[d] = acc;
-      acc += cnt[d];
-      if (cnt[d] > 0) top = d;
-    }
-    cnt[0] = top;  // the deepest level
     rows[0][0] = 1ull;
     rows[0][1] = rows[0][2] = rows[0][3] = 0ull;
+  }
+  // the level sizes (each below 2^8), packed eight to a register so that the level
+  // loop reads none of them from shared memory
+  uint64_t lv_lo = 0ull, lv_hi = 0ull;
+  int maxd = 0;
+#pragma unroll
+  for (int d = 1; d <= E3_MAX_DEPTH; ++d) {
+    const uint64_t n = static_cast<uint64_t>(cnt[d]);
+    if (d <= 8)
+      lv_lo |= n << (8 * (d - 1));
+    else
+      lv_hi |= n << (8 * (d - 9));
+    if (n > 0) maxd = d;
   }
   sync_first(nthr);
   const int R = N + 1;
   const int words = (R + 63) >> 6;
-  const int maxd = cnt[0];
   // flat indices level by level, each node handled by the thread that holds it:
   // rank among the level's nodes by (parent's flat index, candidate index), packed
   // into one integer key (both below 2^12); a parent not yet flattened (not kept,
   // or not at a smaller depth) counts as the root
+  int base = 1;  // flat index of the level's first node
   for (int d = 1; d <= maxd; ++d) {
-    const int n = cnt[d];
+    const int n = static_cast<int>(((d <= 8 ? lv_lo : lv_hi) >> (8 * ((d - 1) & 7))) & 0xFFu);
     if (n == 0) continue;  // uniform across the threads taking part
     const bool mine = i < N && my_d == d;
     int pf = 0, key = 0;
+    uint64_t prow[4] = {0ull, 0ull, 0ull, 0ull};
     if (mine) {
       pf = my_p < 0 ? 0 : flat_of[my_p];
       if (pf < 0) pf = 0;
       key = (pf << 12) | my_c;
       lkey[lpos] = key;
+#pragma unroll
+      for (int w = 0; w < 4; ++w)  // final: pf is on an earlier level
+        if (w < words) prow[w] = rows[pf][w];
     }
     sync_first(nthr);
     if (mine) {
       int rank = 0;
 #pragma unroll 8
       for (int q = 0; q < n; ++q) rank += lkey[q] < key;
-      const int f = base[d] + rank;
+      const int f = base + rank;
       flat_of[my_c] = static_cast<int16_t>(f);
-      for (int w = 0; w < words; ++w) rows[f][w] = rows[pf][w] | (w == (f >> 6) ? 1ull << (f & 63) : 0ull);
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        if (w < words) rows[f][w] = prow[w] | (w == (f >> 6) ? 1ull << (f & 63) : 0ull);
       const size_t o = static_cast<size_t>(b) * R + f;
       tok[o] = my_t;
       parent[o] = pf;
@@ -181,6 +203,7 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
       pos[o] = P + d;
       if (node_cand) node_cand[o] = my_c;
     }
+    base += n;
     sync_first(nthr);
   }
   if (i == 0) {
@@ -211,7 +234,7 @@ e3_status launch_tree_build(const e3_cand& c, int B, int n_cand, int N, const in
   const size_t smem = static_cast<size_t>(std::max(np, threads)) * 8 + (per_thread ? static_cast<size_t>(n_cand) * 12 : 0) +
                       static_cast<size_t>(n_cand) * 2 + 16;
   // the kernel's static arrays: node tables, level keys, ancestor rows, depth counts
-  constexpr size_t kStatic = 2 * sizeof(int) * E3_MAX_NODES + 32 * (E3_MAX_NODES + 1) + 8 * (E3_MAX_DEPTH + 2);
+  constexpr size_t kStatic = 2 * sizeof(int) * E3_MAX_NODES + 32 * (E3_MAX_NODES + 1) + 4 * (E3_MAX_DEPTH + 2);
   if (smem + kStatic > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(tree_build_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
