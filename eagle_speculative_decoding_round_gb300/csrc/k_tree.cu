@@ -45,15 +45,16 @@ __device__ __forceinline__ uint64_t warp_sort_desc(uint64_t v) {
   return v;
 }
 
-// Number of keys above x in a descending list of 32 (binary search: the keys above
-// x form a prefix of the list).
-__device__ __forceinline__ int count_above32(const uint64_t* L, uint64_t x) {
-  int c = L[15] > x ? 16 : 0;
-  c += L[c + 7] > x ? 8 : 0;
-  c += L[c + 3] > x ? 4 : 0;
-  c += L[c + 1] > x ? 2 : 0;
-  c += L[c] > x ? 1 : 0;
-  c += (c == 31 && L[31] > x) ? 1 : 0;
+// Number of high words above xh in a descending list of 32 keys' high words (binary
+// search: those words form a prefix of the list).  Keys whose high word equals xh
+// follow that prefix, ordered by their low words.
+__device__ __forceinline__ int count_hi_above32(const uint32_t* H, uint32_t xh) {
+  int c = H[15] > xh ? 16 : 0;
+  c += H[c + 7] > xh ? 8 : 0;
+  c += H[c + 3] > xh ? 4 : 0;
+  c += H[c + 1] > xh ? 2 : 0;
+  c += H[c] > xh ? 1 : 0;
+  c += (c == 31 && H[31] > xh) ? 1 : 0;
   return c;
 }
 
@@ -77,8 +78,9 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
   int np = 1;
   while (np < n_cand) np <<= 1;
   const bool per_thread = np <= static_cast<int>(blockDim.x);  // one key per thread
-  uint64_t* keys = sh;                                          // [max(np, blockDim.x)]
-  int* cdat = reinterpret_cast<int*>(keys + max(np, static_cast<int>(blockDim.x)));  // [3][n_cand] (per_thread)
+  uint64_t* keys = sh;  // [max(np, blockDim.x)]: sorted warp lists, or the whole sort
+  uint32_t* whi = reinterpret_cast<uint32_t*>(keys + max(np, static_cast<int>(blockDim.x)));  // [blockDim.x] (per_thread)
+  int* cdat = reinterpret_cast<int*>(whi + (per_thread ? blockDim.x : 0));  // [3][n_cand] (per_thread)
   int16_t* flat_of = reinterpret_cast<int16_t*>(cdat + (per_thread ? 3 * n_cand : 0));  // [n_cand]
   const size_t cb = static_cast<size_t>(b) * c.cap;
   for (int q = i; q < n_cand; q += blockDim.x) flat_of[q] = -1;
@@ -94,6 +96,7 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
     }
     v = warp_sort_desc(v);
     keys[i] = v;
+    whi[i] = static_cast<uint32_t>(v >> 32);
     __syncthreads();
     // lists in order, eight searches at a time (independent chains of loads, taken
     // without branches: a search outside the lists or of the warp's own list reads a
@@ -103,15 +106,32 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
     const int nl = (n_cand + 31) >> 5;  // warps holding candidates
     int rank = lane;
     bool live = v != 0ull && lane < N;
+    const uint32_t vh = static_cast<uint32_t>(v >> 32);
     for (int q0 = 0; q0 < nl && __any_sync(0xFFFFFFFFu, live); q0 += 8) {
       if (live) {
-        int add = 0;
+        // counts over the high words (32-bit loads); a list whose next high word
+        // equals vh holds a score tie, settled on the full keys
+        int cs[8];
+        bool tie = false;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) cs[u] = count_hi_above32(whi + 32 * min(q0 + u, nl - 1), vh);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           const int q = q0 + u;
-          const int cq = count_above32(keys + 32 * min(q, nl - 1), v);
-          add += (q < nl && q != warp) ? cq : 0;
+          const bool valid = q < nl && q != warp;
+          tie |= valid && cs[u] < 32 && whi[32 * min(q, nl - 1) + min(cs[u], 31)] == vh;
         }
+        if (tie) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int q = q0 + u;
+            if (q < nl && q != warp)
+              while (cs[u] < 32 && keys[32 * q + cs[u]] > v) ++cs[u];
+          }
+        }
+        int add = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) add += (q0 + u < nl && q0 + u != warp) ? cs[u] : 0;
         rank += add;
         live = rank < N;
       }
@@ -231,7 +251,8 @@ e3_status launch_tree_build(const e3_cand& c, int B, int n_cand, int N, const in
   // over a shared-memory sort
   const int threads = std::max(kTreeThreads, std::min(np, 1024));
   const bool per_thread = np <= threads;
-  const size_t smem = static_cast<size_t>(std::max(np, threads)) * 8 + (per_thread ? static_cast<size_t>(n_cand) * 12 : 0) +
+  const size_t smem = static_cast<size_t>(std::max(np, threads)) * 8 +
+                      (per_thread ? static_cast<size_t>(threads) * 4 + static_cast<size_t>(n_cand) * 12 : 0) +
                       static_cast<size_t>(n_cand) * 2 + 16;
   // the kernel's static arrays: node tables, level keys, ancestor rows, depth counts
   constexpr size_t kStatic = 2 * sizeof(int) * E3_MAX_NODES + 32 * (E3_MAX_NODES + 1) + 4 * (E3_MAX_DEPTH + 2);

@@ -243,6 +243,47 @@ def test_tree_build_page_example():
     assert not (row >> flat.index("x_2")) & 1
 
 
+@pytest.mark.parametrize("n_cand,N,B,levels", [(510, 60, 2, 3), (1000, 255, 1, 2), (300, 100, 3, 40),
+                                               (2000, 200, 1, 4)])
+def test_tree_build_score_ties(n_cand, N, B, levels):
+    """Candidate sets whose scores take only a few values: the rank of a key among
+    equal scores is settled by the candidate index (score descending, index
+    ascending), bit-exact against the oracle."""
+    rng = np.random.default_rng(n_cand + N)
+    C = n_cand
+    cands = {x: np.zeros((B, C), t) for x, t in (("tok", np.int32), ("parent", np.int32), ("score", np.float32),
+                                                 ("depth", np.int32))}
+    for b in range(B):
+        for i in range(C):
+            # a parent earlier in the list, scores that never rise along a path and
+            # repeat across the set
+            p = -1 if i < 8 or rng.random() < 0.1 else int(rng.integers(0, i))
+            d = 1 if p < 0 else min(cands["depth"][b, p] + 1, 16)
+            if d > 1 and cands["depth"][b, p] >= 16:
+                p, d = -1, 1
+            ps = 0.0 if p < 0 else float(cands["score"][b, p])
+            cands["parent"][b, i] = p
+            cands["depth"][b, i] = d
+            cands["score"][b, i] = ps - float(rng.integers(0, levels))
+            cands["tok"][b, i] = int(rng.integers(0, 1 << 20))
+    ct, cp, cs, cd = (to_dev(cands[x]) for x in ("tok", "parent", "score", "depth"))
+    cand = e3.make_cand(ct, cp, cs, cd, C)
+    R = N + 1
+    kvl = rng.integers(0, 5000, B).astype(np.int32)
+    root = rng.integers(0, 1000, B).astype(np.int32)
+    out = {x: i32((B, R), -9) for x in ("tok", "parent", "depth", "pos", "node_cand")}
+    mask = torch.zeros((B, R, (R + 63) // 64), dtype=torch.int64, device="cuda")
+    e3.tree_build_mask(cand, B, C, N, to_dev(root), to_dev(kvl), out["tok"], out["parent"], out["depth"],
+                       out["pos"], mask, node_cand=out["node_cand"])
+    torch.cuda.synchronize()
+    for b in range(B):
+        cb = {x: np.ascontiguousarray(cands[x][b]) for x in ("tok", "parent", "score", "depth")}
+        ref = oracle.build_tree(cb, C, N, int(root[b]), int(kvl[b]))
+        for x in ("tok", "parent", "depth", "pos", "node_cand"):
+            assert np.array_equal(host(out[x])[b], ref[x]), (x, b)
+        assert np.array_equal(host(mask)[b].view(np.uint64), ref["mask"]), ("mask", b)
+
+
 # ---------------------------------------------------------------- attention ----
 
 def run_gpu_verify(Q, K, Vc, pt, npages, kv_len, mask, H, KVH, hd, page_size, dt, max_kv_len=None, scale=None,
