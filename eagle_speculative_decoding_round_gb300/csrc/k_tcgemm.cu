@@ -22,7 +22,6 @@
 
 #include <algorithm>
 #include <atomic>
-#include <cfloat>
 
 #include "e3_common.cuh"
 #include "e3_kernels.h"
@@ -490,22 +489,22 @@ row_q_kernel(const float* __restrict__ logits, int V, const float* __restrict__ 
   // pipe busy): z * 0 + acc stays 0 for finite z and turns NaN for an infinity or NaN
   float2 nf = make_float2(0.0f, 0.0f);
   const float2 zero2 = make_float2(0.0f, 0.0f);
-  // eight loads in flight per thread, then their masses (a slot past the chunk reads
-  // -FLT_MAX: finite, and of mass 0)
+  auto add4 = [&](const float4& v) {
+    nf = __ffma2_rn(make_float2(v.x, v.y), zero2, nf);
+    nf = __ffma2_rn(make_float2(v.z, v.w), zero2, nf);
+    Q += fx_mass_x2(__fmul_rn(v.x, it), __fmul_rn(v.y, it), mx) + fx_mass_x2(__fmul_rn(v.z, it), __fmul_rn(v.w, it), mx);
+  };
+  // eight loads in flight per thread, then the masses of those inside the chunk
   for (int q8 = q0 + threadIdx.x; q8 < q1; q8 += 8 * kRowQThreads) {
     float4 v[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int q = q8 + u * kRowQThreads;
-      v[u] = q < q1 ? z4[q] : make_float4(-FLT_MAX, -FLT_MAX, -FLT_MAX, -FLT_MAX);
+      v[u] = q < q1 ? z4[q] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      nf = __ffma2_rn(make_float2(v[u].x, v[u].y), zero2, nf);
-      nf = __ffma2_rn(make_float2(v[u].z, v[u].w), zero2, nf);
-      Q += fx_mass_x2(__fmul_rn(v[u].x, it), __fmul_rn(v[u].y, it), mx) +
-           fx_mass_x2(__fmul_rn(v[u].z, it), __fmul_rn(v[u].w, it), mx);
-    }
+    for (int u = 0; u < 8; ++u)
+      if (q8 + u * kRowQThreads < q1) add4(v[u]);
   }
   int bad = (nf.x != nf.x) | (nf.y != nf.y);
   Q = block_reduce(Q, SumU64(), red64);

@@ -93,6 +93,31 @@ def test_lmhead_logits_and_stats(M, d, V, dt):
     assert np.array_equal(host(ram), am)
 
 
+def test_lmhead_stats_extreme_temperatures():
+    """Temperatures whose inverse is 0, denormal or huge: the statistics pass sums the
+    masses of the row's tokens only (every CTA chunk of the full vocabulary ends in a
+    partial group of loads), bit-exact against the oracle."""
+    M, d, V = 6, 64, 128256
+    h = synth.normal(11, "h", (M, d), 1.0)
+    W = synth.normal(11, "W", (V, d), 0.125)
+    temps = np.array([np.inf, 1e30, 3e38, 1e-30, 0.5, 1.0], np.float32)
+    ht, h = bf16_dev(h)
+    Wt, W = bf16_dev(W)
+    logits = torch.empty((M, V), dtype=torch.float32, device="cuda")
+    rmax = torch.empty(M, dtype=torch.float32, device="cuda")
+    rQ = torch.empty(M, dtype=torch.int64, device="cuda")
+    ram = i32(M)
+    err = i32(1)
+    e3.lmhead_logits(ht, Wt, M, d, V, to_dev(temps), logits, rmax, rQ, ram, err, e3.E3_BF16)
+    torch.cuda.synchronize()
+    m, Q, am, bad = oracle.row_stats(host(logits), temps)
+    assert not bad.any() and int(err.item()) == 0
+    assert np.array_equal(host(rmax).view(np.uint32), m.view(np.uint32))
+    assert np.array_equal(host(rQ).view(np.uint64), Q)
+    assert np.array_equal(host(ram), am)
+    assert int(Q[0]) == V << 40  # 1/T = 0: every token has mass 2^40
+
+
 def test_lmhead_flags_nonfinite():
     M, d, V = 4, 64, 256
     h = synth.normal(3, "h", (M, d), 1.0)
