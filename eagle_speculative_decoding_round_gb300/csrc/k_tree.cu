@@ -67,10 +67,10 @@ tree_build_kernel(e3_cand c, int n_cand, int N, const int32_t* __restrict__ root
                   const int32_t* __restrict__ kv_len, int32_t* tok, int32_t* parent, int32_t* depth,
                   int32_t* pos, uint64_t* mask, int32_t* node_cand) {
   extern __shared__ uint64_t sh[];
-  __shared__ int sel[E3_MAX_NODES];              // candidate of the r-th best key
-  __shared__ int lkey[E3_MAX_NODES];             // one level's (parent flat, candidate) keys
-  __shared__ uint64_t rows[E3_MAX_NODES + 1][4];          // ancestor-or-self bit rows by flat index
-  __shared__ int cnt[E3_MAX_DEPTH + 2];
+  __shared__ int sel[E3_MAX_NODES];               // candidate of the r-th best key
+  __shared__ int lkey[E3_MAX_NODES];              // one level's (parent flat, candidate) keys
+  __shared__ uint64_t rows[E3_MAX_NODES + 1][4];  // ancestor-or-self bit rows by flat index
+  __shared__ int cnt[E3_MAX_DEPTH + 2];           // kept nodes per depth (1 .. E3_MAX_DEPTH)
   pdl_wait();
   pdl_trigger();
   const int b = blockIdx.x;
